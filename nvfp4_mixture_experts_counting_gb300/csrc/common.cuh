@@ -1,0 +1,107 @@
+// Device helpers shared by the ftmoe kernels: NVFP4 encode/decode through the
+// sm_100-family conversion instructions, bf16 conversions, warp reductions and
+// the device status word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace ftmoe {
+
+constexpr int kBlock = 16;           // NVFP4 scale block (elements)
+constexpr float kE2M1Max = 6.0f;
+constexpr float kWeightGlobalDiv = 2688.0f;  // 448 * 6
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- NVFP4 codes
+
+// E4M3 ("fn") byte of a non-negative fp32 value: round to nearest even,
+// saturating at 448 (cvt .satfinite).
+__device__ __forceinline__ uint8_t e4m3_encode(float u) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(u));
+  return (uint8_t)(r & 0xFF);
+}
+
+// fp32 value of an E4M3 byte (exact).
+__device__ __forceinline__ float e4m3_decode(uint8_t c) {
+  uint32_t r;
+  uint16_t in = c;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+  __half2 h = *reinterpret_cast<__half2*>(&r);
+  return __low2float(h);
+}
+
+// Two E2M1 codes (low nibble = a, high nibble = b) of fp32 values, round to
+// nearest even, saturating at 6; a zero magnitude gets sign bit 0.
+__device__ __forceinline__ uint8_t e2m1x2_encode(float a, float b) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+      : "=r"(r) : "f"(b), "f"(a));
+  uint32_t lo = r & 0xF, hi = (r >> 4) & 0xF;
+  if ((lo & 7) == 0) lo = 0;
+  if ((hi & 7) == 0) hi = 0;
+  return (uint8_t)(lo | (hi << 4));
+}
+
+// Exact half2 of a byte holding two E2M1 codes (x = low nibble).
+__device__ __forceinline__ __half2 e2m1x2_to_half2(uint32_t byte) {
+  uint32_t r;
+  uint16_t in = (uint16_t)(byte & 0xFF);
+  asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "h"(in));
+  return *reinterpret_cast<__half2*>(&r);
+}
+
+// Quantise one 16-element block of fp32 values with row global g (1.0 for
+// activations).  Writes 8 code bytes and returns the scale byte.
+// Steps: t = fp32(amax/6); u = fp32(t/g); s = E4M3(u); d = fp32(dec(s)*g);
+// code_i = E2M1(fp32(v_i/d)); g == 0, s == 0 or d == 0 give zero codes.
+__device__ __forceinline__ uint8_t quantize_block16(const float v[16], float g, uint8_t codes[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  uint8_t s = 0;
+  if (g != 0.f) {
+    float t = __fdiv_rn(amax, kE2M1Max);
+    float u = __fdiv_rn(t, g);
+    s = e4m3_encode(u);
+  }
+  float d = __fmul_rn(e4m3_decode(s), g);
+  if (s == 0 || d == 0.f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) codes[i] = 0;
+    return 0;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) codes[i] = e2m1x2_encode(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d));
+  return s;
+}
+
+// ---------------------------------------------------------------- misc
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace ftmoe

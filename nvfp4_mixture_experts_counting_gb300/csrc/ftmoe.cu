@@ -1,0 +1,477 @@
+// Host side of the ftmoe C ABI: handle, validation, bank loading (window
+// slicing), workspace, forward orchestration, stats and status.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/ftmoe.h"
+#include "kernels.h"
+
+namespace ftmoe {
+cudaError_t route_set_smem_limits(int H, int E);
+cudaError_t experts_set_smem_limits(int H, int I);
+}  // namespace ftmoe
+
+using namespace ftmoe;
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  char buf[256];
+  snprintf(buf, sizeof buf, "%s: %s", what, cudaGetErrorString(e));
+  g_last_cuda_error = buf;
+  return FTMOE_ERR_CUDA;
+}
+
+#define CK(call)                                          \
+  do {                                                    \
+    cudaError_t _e = (call);                              \
+    if (_e != cudaSuccess) return cuda_fail(_e, #call);   \
+  } while (0)
+
+// Host-side fault injection: FTMOE_FAULT is a comma-separated list of names.
+bool fault(const char* name) {
+  const char* f = getenv("FTMOE_FAULT");
+  if (!f || !*f) return false;
+  std::string s(f);
+  size_t pos = 0;
+  while (pos <= s.size()) {
+    size_t c = s.find(',', pos);
+    if (c == std::string::npos) c = s.size();
+    if (s.compare(pos, c - pos, name) == 0) return true;
+    pos = c + 1;
+  }
+  return false;
+}
+
+inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+struct Layer {
+  bool loaded = false;
+  int li0 = 0, lIw = 0;    // loaded routed window
+  int sli0 = 0, slIw = 0;  // loaded shared window
+  RecLayout lay{};
+  float* router_w = nullptr;
+  float* router_bias = nullptr;
+  uint8_t* bank = nullptr;  // E records
+  uint8_t** rec_dev = nullptr;  // [E] record pointers (device)
+  uint16_t* sh_gu = nullptr;
+  uint16_t* sh_dn = nullptr;
+  uint16_t* sh_gate = nullptr;
+  int last_T = 0;
+  int last_I_loc = 0;
+};
+
+}  // namespace
+
+struct ftmoe_handle {
+  ftmoe_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  std::vector<Layer> layers;
+  // workspace
+  unsigned char* ws = nullptr;
+  size_t ws_bytes = 0;
+  RouteArgs r{};  // workspace pointers for routing (inputs filled per call)
+  uint16_t* hs = nullptr;
+  uint8_t* hq_codes = nullptr;
+  uint8_t* hq_scales = nullptr;
+  float* Y = nullptr;
+  float* S = nullptr;
+  float* stack_y = nullptr;
+  uint16_t* stack_x[2] = {nullptr, nullptr};
+  uint32_t* status = nullptr;
+  uint32_t last_status = 0;
+};
+
+namespace ftmoe {
+RecLayout make_rec_layout(int H, int Iw) {
+  RecLayout L{};
+  int64_t o = 0;
+  L.gu_codes = o;  o = align_up(o + (int64_t)2 * Iw * (H / 2), 256);
+  L.gu_scales = o; o = align_up(o + (int64_t)2 * Iw * (H / 16), 256);
+  L.dn_codes = o;  o = align_up(o + (int64_t)H * (Iw / 2), 256);
+  L.dn_scales = o; o = align_up(o + (int64_t)H * (Iw / 16), 256);
+  L.gu_global = o; o = align_up(o + (int64_t)2 * Iw * 4, 256);
+  L.dn_global = o; o = align_up(o + (int64_t)H * 4, 256);
+  L.bytes = o;
+  return L;
+}
+}  // namespace ftmoe
+
+namespace {
+
+void free_layer(Layer& L) {
+  cudaFree(L.router_w);
+  cudaFree(L.router_bias);
+  cudaFree(L.bank);
+  cudaFree(L.rec_dev);
+  cudaFree(L.sh_gu);
+  cudaFree(L.sh_dn);
+  cudaFree(L.sh_gate);
+  L = Layer{};
+}
+
+int validate_config(const ftmoe_config* c) {
+  if (!c || c->abi_version != FTMOE_ABI_VERSION) return FTMOE_ERR_INVALID_ARG;
+  if (c->H <= 0 || c->I <= 0 || c->E <= 0 || c->top_k <= 0 || c->num_layers <= 0 ||
+      c->max_tokens < 0 || c->I_shared < 0)
+    return FTMOE_ERR_INVALID_ARG;
+  if (c->H % 16 || c->I % 16 || c->I_shared % 16) return FTMOE_ERR_ALIGNMENT;
+  if (c->H > 8192 || c->I > 8192 || c->I_shared > 4096 || c->E > 1024 || c->top_k > 32 ||
+      c->top_k > c->E || c->max_tokens > (1 << 20))
+    return FTMOE_ERR_INVALID_ARG;
+  if (c->hbm_slot_bytes < 0) return FTMOE_ERR_INVALID_ARG;
+  if (c->hbm_slot_bytes > 0) return FTMOE_ERR_INVALID_ARG;  // offload mode: not in this build yet
+  return FTMOE_OK;
+}
+
+// Shared window for a routed window (I_s may differ from I).
+bool shared_window(const ftmoe_config& c, int i0, int I_loc, int* si0, int* sI) {
+  if (c.I_shared == 0) { *si0 = 0; *sI = 0; return true; }
+  if (c.I_shared == c.I) { *si0 = i0; *sI = I_loc; return true; }
+  int64_t a = (int64_t)i0 * c.I_shared, b = (int64_t)I_loc * c.I_shared;
+  if (a % c.I || b % c.I) return false;
+  *si0 = (int)(a / c.I);
+  *sI = (int)(b / c.I);
+  return (*si0 % 16 == 0) && (*sI % 16 == 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ftmoe_error_string(int code) {
+  switch (code) {
+    case FTMOE_OK: return "ok";
+    case FTMOE_ERR_INVALID_ARG: return "invalid argument";
+    case FTMOE_ERR_ALIGNMENT: return "misaligned size or pointer (sizes and windows must be multiples of 16, pointers 16-byte aligned)";
+    case FTMOE_ERR_NOT_LOADED: return "layer bank not loaded";
+    case FTMOE_ERR_SLICE_OUT_OF_RANGE: return "forward window is not inside the loaded window";
+    case FTMOE_ERR_OOM: return "out of memory";
+    case FTMOE_ERR_CUDA: return "CUDA runtime error";
+    case FTMOE_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case FTMOE_ERR_FAULT_INJECTED: return "fault injected (FTMOE_FAULT)";
+    case FTMOE_ERR_DEVICE: return "no usable device (needs compute capability 10.3)";
+    case FTMOE_ERR_DEVICE_CHECK: return "an in-kernel range check failed";
+    default: return "unknown status";
+  }
+}
+
+const char* ftmoe_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
+  if (!out) return FTMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate_config(config);
+  if (rc) return rc;
+  if (fault("oom")) return FTMOE_ERR_OOM;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return FTMOE_ERR_DEVICE;
+  }
+  cudaDeviceProp prop;
+  CK(cudaGetDeviceProperties(&prop, device));
+  if (prop.major != 10 || prop.minor != 3) return FTMOE_ERR_DEVICE;
+  CK(cudaSetDevice(device));
+  auto* h = new ftmoe_handle();
+  h->cfg = *config;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  h->layers.resize(config->num_layers);
+  const ftmoe_config& c = *config;
+  const int64_t T = c.max_tokens > 0 ? c.max_tokens : 1;
+  const int64_t P = T * c.top_k;
+  // workspace carve-up
+  struct Part { void** p; int64_t bytes; };
+  std::vector<Part> parts = {
+      {(void**)&h->r.logits, T * c.E * 4},   {(void**)&h->r.err, T * c.E * 4},
+      {(void**)&h->r.topk_idx, P * 4},       {(void**)&h->r.topk_w, P * 4},
+      {(void**)&h->r.xq_codes, T * c.H / 2}, {(void**)&h->r.xq_scales, T * c.H / 16},
+      {(void**)&h->r.sigma, T * 4},          {(void**)&h->r.offsets, (int64_t)(c.E + 1) * 4},
+      {(void**)&h->r.perm, P * 4},           {(void**)&h->r.inv, P * 4},
+      {(void**)&h->r.touched, (int64_t)c.E * 4}, {(void**)&h->r.n_touched, 16},
+      {(void**)&h->hs, T * (c.I_shared > 0 ? c.I_shared : 16) * 2},
+      {(void**)&h->hq_codes, P * c.I / 2},   {(void**)&h->hq_scales, P * c.I / 16},
+      {(void**)&h->Y, P * c.H * 4},          {(void**)&h->S, T * c.H * 4},
+      {(void**)&h->stack_y, T * c.H * 4},    {(void**)&h->stack_x[0], T * c.H * 2},
+      {(void**)&h->stack_x[1], T * c.H * 2}, {(void**)&h->status, 16},
+  };
+  int64_t total = 0;
+  for (auto& p : parts) total += align_up(p.bytes, 256);
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return FTMOE_ERR_OOM;
+  }
+  h->ws_bytes = total;
+  int64_t off = 0;
+  for (auto& p : parts) {
+    *p.p = h->ws + off;
+    off += align_up(p.bytes, 256);
+  }
+  cudaError_t e = cudaMemset(h->ws, 0, total);
+  if (e == cudaSuccess) e = route_set_smem_limits(c.H, c.E);
+  if (e == cudaSuccess) e = experts_set_smem_limits(c.H, c.I > c.I_shared ? c.I : c.I_shared);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "create");
+    cudaFree(h->ws);
+    delete h;
+    return FTMOE_ERR_CUDA;
+  }
+  h->r.status = h->status;
+  *out = h;
+  return FTMOE_OK;
+}
+
+int ftmoe_destroy(ftmoe_handle* h) {
+  if (!h) return FTMOE_OK;
+  cudaSetDevice(h->device);
+  for (auto& L : h->layers) free_layer(L);
+  cudaFree(h->ws);
+  delete h;
+  return FTMOE_OK;
+}
+
+int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0, int I_loc,
+                    ftmoe_stream_t stream) {
+  if (!h || !d || layer < 0 || layer >= h->cfg.num_layers) return FTMOE_ERR_INVALID_ARG;
+  const ftmoe_config& c = h->cfg;
+  if (i0 % 16 || I_loc % 16) return FTMOE_ERR_ALIGNMENT;
+  if (I_loc <= 0 || i0 < 0 || i0 + I_loc > c.I) return FTMOE_ERR_INVALID_ARG;
+  int si0, sI;
+  if (!shared_window(c, i0, I_loc, &si0, &sI)) return FTMOE_ERR_ALIGNMENT;
+  if (!d->router_w || !d->gu_codes || !d->gu_scales || !d->gu_global || !d->dn_codes ||
+      !d->dn_scales || !d->dn_global)
+    return FTMOE_ERR_INVALID_ARG;
+  if ((c.has_router_bias != 0) != (d->router_bias != nullptr)) return FTMOE_ERR_INVALID_ARG;
+  if (c.I_shared > 0 && (!d->sh_gate_up || !d->sh_down || !d->sh_gate)) return FTMOE_ERR_INVALID_ARG;
+  if (fault("bad_bank")) return FTMOE_ERR_FAULT_INJECTED;
+  CK(cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  Layer& L = h->layers[layer];
+  free_layer(L);
+  const int H = c.H, E = c.E, I = c.I, Iw = I_loc;
+  L.lay = make_rec_layout(H, Iw);
+  const int64_t bank_bytes = L.lay.bytes * E;
+  if (cudaMalloc(&L.bank, bank_bytes) != cudaSuccess || cudaMalloc(&L.rec_dev, E * sizeof(void*)) != cudaSuccess ||
+      cudaMalloc(&L.router_w, (size_t)E * H * 4) != cudaSuccess) {
+    cudaGetLastError();
+    free_layer(L);
+    return FTMOE_ERR_OOM;
+  }
+  const cudaMemcpyKind K = cudaMemcpyDefault;
+  CK(cudaMemcpyAsync(L.router_w, d->router_w, (size_t)E * H * 4, K, s));
+  if (d->router_bias) {
+    if (cudaMalloc(&L.router_bias, E * 4) != cudaSuccess) { free_layer(L); return FTMOE_ERR_OOM; }
+    CK(cudaMemcpyAsync(L.router_bias, d->router_bias, E * 4, K, s));
+  }
+  const int64_t gcb = H / 2, gsb = H / 16;  // gate_up row bytes (codes, scales)
+  for (int e = 0; e < E; ++e) {
+    uint8_t* rec = L.bank + L.lay.bytes * e;
+    const int64_t r_gate = (int64_t)e * 2 * I + i0, r_up = (int64_t)e * 2 * I + I + i0;
+    CK(cudaMemcpyAsync(rec + L.lay.gu_codes, d->gu_codes + r_gate * gcb, Iw * gcb, K, s));
+    CK(cudaMemcpyAsync(rec + L.lay.gu_codes + Iw * gcb, d->gu_codes + r_up * gcb, Iw * gcb, K, s));
+    CK(cudaMemcpyAsync(rec + L.lay.gu_scales, d->gu_scales + r_gate * gsb, Iw * gsb, K, s));
+    CK(cudaMemcpyAsync(rec + L.lay.gu_scales + Iw * gsb, d->gu_scales + r_up * gsb, Iw * gsb, K, s));
+    CK(cudaMemcpyAsync(rec + L.lay.gu_global, d->gu_global + r_gate, Iw * 4, K, s));
+    CK(cudaMemcpyAsync(rec + L.lay.gu_global + Iw * 4, d->gu_global + r_up, Iw * 4, K, s));
+    CK(cudaMemcpy2DAsync(rec + L.lay.dn_codes, Iw / 2, d->dn_codes + (int64_t)e * H * (I / 2) + i0 / 2, I / 2,
+                         Iw / 2, H, K, s));
+    CK(cudaMemcpy2DAsync(rec + L.lay.dn_scales, Iw / 16, d->dn_scales + (int64_t)e * H * (I / 16) + i0 / 16,
+                         I / 16, Iw / 16, H, K, s));
+    CK(cudaMemcpyAsync(rec + L.lay.dn_global, d->dn_global + (int64_t)e * H, H * 4, K, s));
+  }
+  std::vector<uint8_t*> ptrs(E);
+  for (int e = 0; e < E; ++e) ptrs[e] = L.bank + L.lay.bytes * e;
+  CK(cudaMemcpyAsync(L.rec_dev, ptrs.data(), E * sizeof(void*), cudaMemcpyHostToDevice, s));
+  if (c.I_shared > 0) {
+    if (cudaMalloc(&L.sh_gu, (size_t)2 * sI * H * 2) != cudaSuccess ||
+        cudaMalloc(&L.sh_dn, (size_t)H * sI * 2) != cudaSuccess || cudaMalloc(&L.sh_gate, (size_t)H * 2) != cudaSuccess) {
+      cudaGetLastError();
+      free_layer(L);
+      return FTMOE_ERR_OOM;
+    }
+    const int Is = c.I_shared;
+    CK(cudaMemcpyAsync(L.sh_gu, d->sh_gate_up + (int64_t)si0 * H, (size_t)sI * H * 2, K, s));
+    CK(cudaMemcpyAsync(L.sh_gu + (int64_t)sI * H, d->sh_gate_up + (int64_t)(Is + si0) * H, (size_t)sI * H * 2, K, s));
+    CK(cudaMemcpy2DAsync(L.sh_dn, sI * 2, d->sh_down + si0, (size_t)Is * 2, sI * 2, H, K, s));
+    CK(cudaMemcpyAsync(L.sh_gate, d->sh_gate, (size_t)H * 2, K, s));
+  }
+  CK(cudaStreamSynchronize(s));
+  L.li0 = i0;
+  L.lIw = Iw;
+  L.sli0 = si0;
+  L.slIw = sI;
+  L.loaded = true;
+  return FTMOE_OK;
+}
+
+static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags, int i0,
+                        int I_loc, const ftmoe_aux* aux, cudaStream_t s) {
+  const ftmoe_config& c = h->cfg;
+  Layer& L = h->layers[layer];
+  RouteArgs r = h->r;
+  r.x = (const uint16_t*)x;
+  r.router_w = L.router_w;
+  r.router_bias = L.router_bias;
+  r.sh_gate = c.I_shared > 0 ? L.sh_gate : nullptr;
+  r.T = T;
+  r.H = c.H;
+  r.E = c.E;
+  r.top_k = c.top_k;
+  r.norm_topk_prob = c.norm_topk_prob;
+  CK(launch_route(r, s));
+  ExpertArgs a{};
+  a.r = r;
+  a.rec = L.rec_dev;
+  a.lay = L.lay;
+  a.win.row0 = i0 - L.li0;
+  a.win.I_loc = I_loc;
+  a.win.Iw = L.lIw;
+  a.H = c.H;
+  a.T = T;
+  a.top_k = c.top_k;
+  if (c.I_shared > 0) {
+    int si0 = 0, sI = 0;
+    shared_window(c, i0, I_loc, &si0, &sI);
+    a.sh_gate_up = L.sh_gu;
+    a.sh_down = L.sh_dn;
+    a.s_row0 = si0 - L.sli0;
+    a.s_I_loc = sI;
+    a.s_Iw = L.slIw;
+  }
+  a.hs = h->hs;
+  a.hq_codes = h->hq_codes;
+  a.hq_scales = h->hq_scales;
+  a.Y = h->Y;
+  a.S = h->S;
+  a.out = out;
+  a.out_flags = out_flags;
+  a.num_sms = h->num_sms;
+  CK(launch_experts(a, s));
+  if (aux) {
+    const int64_t P = (int64_t)T * c.top_k;
+    if (aux->topk_idx) CK(cudaMemcpyAsync(aux->topk_idx, r.topk_idx, P * 4, cudaMemcpyDeviceToDevice, s));
+    if (aux->topk_w) CK(cudaMemcpyAsync(aux->topk_w, r.topk_w, P * 4, cudaMemcpyDeviceToDevice, s));
+    if (aux->offsets) CK(cudaMemcpyAsync(aux->offsets, r.offsets, (c.E + 1) * 4, cudaMemcpyDeviceToDevice, s));
+    if (aux->perm) CK(cudaMemcpyAsync(aux->perm, r.perm, P * 4, cudaMemcpyDeviceToDevice, s));
+    if (aux->inv) CK(cudaMemcpyAsync(aux->inv, r.inv, P * 4, cudaMemcpyDeviceToDevice, s));
+  }
+  L.last_T = T;
+  L.last_I_loc = I_loc;
+  return FTMOE_OK;
+}
+
+int ftmoe_forward(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags, int i0, int I_loc,
+                  const ftmoe_aux* aux, ftmoe_stream_t stream) {
+  if (!h || layer < 0 || layer >= h->cfg.num_layers) return FTMOE_ERR_INVALID_ARG;
+  const ftmoe_config& c = h->cfg;
+  if (T < 0 || T > c.max_tokens) return FTMOE_ERR_INVALID_ARG;
+  const int otype = out_flags & 0xff;
+  if ((out_flags & ~0x1ff) || otype > FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  if ((out_flags & FTMOE_OUT_ACCUMULATE) && otype != FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  Layer& L = h->layers[layer];
+  if (!L.loaded) return FTMOE_ERR_NOT_LOADED;
+  if (i0 % 16 || I_loc % 16) return FTMOE_ERR_ALIGNMENT;
+  if (I_loc <= 0 || i0 < L.li0 || i0 + I_loc > L.li0 + L.lIw) return FTMOE_ERR_SLICE_OUT_OF_RANGE;
+  int si0, sI;
+  if (!shared_window(c, i0, I_loc, &si0, &sI)) return FTMOE_ERR_ALIGNMENT;
+  if (T == 0) return FTMOE_OK;
+  if (!x || !out || x == out) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return FTMOE_ERR_ALIGNMENT;
+  if (fault("forward")) return FTMOE_ERR_FAULT_INJECTED;
+  CK(cudaSetDevice(h->device));
+  return forward_impl(h, layer, x, T, out, out_flags, i0, I_loc, aux, (cudaStream_t)stream);
+}
+
+int ftmoe_forward_stack(ftmoe_handle* h, const void* x, int T, void* out, ftmoe_stream_t stream) {
+  if (!h) return FTMOE_ERR_INVALID_ARG;
+  const ftmoe_config& c = h->cfg;
+  if (T < 0 || T > c.max_tokens) return FTMOE_ERR_INVALID_ARG;
+  for (auto& L : h->layers)
+    if (!L.loaded) return FTMOE_ERR_NOT_LOADED;
+  if (T == 0) return FTMOE_OK;
+  if (!x || !out || x == out) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return FTMOE_ERR_ALIGNMENT;
+  CK(cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  const void* cur = x;
+  for (int l = 0; l < c.num_layers; ++l) {
+    Layer& L = h->layers[l];
+    const bool last = l == c.num_layers - 1;
+    int rc = forward_impl(h, l, cur, T, last ? out : (void*)h->stack_y, last ? FTMOE_OUT_BF16 : FTMOE_OUT_FP32,
+                          L.li0, L.lIw, nullptr, s);
+    if (rc) return rc;
+    if (!last) {
+      uint16_t* nx = h->stack_x[l & 1];
+      CK(launch_rms_renorm(h->stack_y, nx, T, c.H, s));
+      cur = nx;
+    }
+  }
+  return FTMOE_OK;
+}
+
+int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out) {
+  if (!h || !out || layer < 0 || layer >= h->cfg.num_layers) return FTMOE_ERR_INVALID_ARG;
+  CK(cudaSetDevice(h->device));
+  CK(cudaDeviceSynchronize());
+  memset(out, 0, sizeof *out);
+  Layer& L = h->layers[layer];
+  int32_t nt = 0;
+  CK(cudaMemcpy(&nt, h->r.n_touched, 4, cudaMemcpyDeviceToHost));
+  out->touched_experts = L.last_T > 0 ? nt : 0;
+  const int H = h->cfg.H, W = L.last_I_loc;
+  const int64_t per_expert = (int64_t)2 * W * (H / 2 + H / 16 + 4) + (int64_t)H * (W / 2 + W / 16) + (int64_t)H * 4;
+  out->touched_bytes = out->touched_experts * per_expert;
+  out->resident_slots = h->cfg.E;
+  out->residency = 1.0;
+  out->device_status = (int32_t)h->last_status;
+  return FTMOE_OK;
+}
+
+int ftmoe_check_status(ftmoe_handle* h, ftmoe_stream_t stream) {
+  if (!h) return FTMOE_ERR_INVALID_ARG;
+  CK(cudaSetDevice(h->device));
+  CK(cudaStreamSynchronize((cudaStream_t)stream));
+  uint32_t st = 0;
+  CK(cudaMemcpy(&st, h->status, 4, cudaMemcpyDeviceToHost));
+  CK(cudaMemset(h->status, 0, 4));
+  h->last_status = st;
+  if (st & kStatusTimeout) return FTMOE_ERR_TIMEOUT;
+  if (st & kStatusRange) return FTMOE_ERR_DEVICE_CHECK;
+  return FTMOE_OK;
+}
+
+int ftmoe_quantize_weights(const float* w, int64_t rows, int K, uint8_t* codes, uint8_t* scales, float* globals,
+                           ftmoe_stream_t stream) {
+  if (rows < 0 || K <= 0) return FTMOE_ERR_INVALID_ARG;
+  if (K % 16) return FTMOE_ERR_ALIGNMENT;
+  if (rows == 0) return FTMOE_OK;
+  if (!w || !codes || !scales || !globals) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(w) || ((uintptr_t)codes & 7)) return FTMOE_ERR_ALIGNMENT;
+  CK(launch_quantize_weights(w, rows, K, codes, scales, globals, (cudaStream_t)stream));
+  return FTMOE_OK;
+}
+
+int ftmoe_quantize_activations(const void* a, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
+                               ftmoe_stream_t stream) {
+  if (rows < 0 || K <= 0) return FTMOE_ERR_INVALID_ARG;
+  if (K % 16) return FTMOE_ERR_ALIGNMENT;
+  if (rows == 0) return FTMOE_OK;
+  if (!a || !codes || !scales) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || ((uintptr_t)codes & 7)) return FTMOE_ERR_ALIGNMENT;
+  CK(launch_quantize_act_bf16((const uint16_t*)a, rows, K, codes, scales, (cudaStream_t)stream));
+  return FTMOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Host-side declarations of the ftmoe kernel launchers (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ftmoe {
+
+// Device status word bits (set with atomicOr, read by ftmoe_check_status).
+constexpr uint32_t kStatusRange = 1u;    // an in-kernel range check failed
+constexpr uint32_t kStatusTimeout = 2u;  // a bounded wait ran out
+
+// Byte offsets of the sections of one expert record (one expert's bank
+// restricted to a loaded window of width Iw).  Sections are 256-byte aligned.
+struct RecLayout {
+  int64_t gu_codes, gu_scales, gu_global;  // [2Iw][H/2], [2Iw][H/16], [2Iw] fp32
+  int64_t dn_codes, dn_scales, dn_global;  // [H][Iw/2], [H][Iw/16], [H] fp32
+  int64_t bytes;                           // record size (multiple of 256)
+};
+RecLayout make_rec_layout(int H, int Iw);
+
+// Window of a forward relative to the loaded records.
+struct Window {
+  int row0;   // first intermediate index of the window inside the loaded window
+  int I_loc;  // window width
+  int Iw;     // loaded window width (row pitch of down codes is Iw/2)
+};
+
+struct RouteArgs {
+  const uint16_t* x;      // [T][H] bf16
+  const float* router_w;  // [E][H]
+  const float* router_bias;  // [E] or null
+  const uint16_t* sh_gate;   // [H] bf16 or null
+  int T, H, E, top_k, norm_topk_prob;
+  // workspace outputs
+  float* logits;     // [T][E]
+  float* err;        // [T][E]
+  int32_t* topk_idx; // [T][k]
+  float* topk_w;     // [T][k]
+  uint8_t* xq_codes; // [T][H/2]
+  uint8_t* xq_scales;  // [T][H/16]
+  float* sigma;      // [T]
+  int32_t* offsets;  // [E+1]
+  int32_t* perm;     // [P]
+  int32_t* inv;      // [P]
+  int32_t* touched;  // [E] touched experts, increasing
+  int32_t* n_touched;  // [1]
+  uint32_t* status;
+};
+
+cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, uint8_t* codes,
+                                    uint8_t* scales, float* globals, cudaStream_t s);
+cudaError_t launch_quantize_act_bf16(const uint16_t* a, int64_t rows, int K, uint8_t* codes,
+                                     uint8_t* scales, cudaStream_t s);
+
+// x quantisation + shared gate, router logits, top-k, counting sort.
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+
+struct ExpertArgs {
+  RouteArgs r;  // routing workspace and inputs (by value: kernels read it)
+  const uint8_t* const* rec;  // [E] device pointers to expert records
+  RecLayout lay;
+  Window win;
+  int H, T, top_k;
+  // shared expert (null sh_gate_up => none)
+  const uint16_t* sh_gate_up;  // [2*sIw][H] bf16 (loaded window)
+  const uint16_t* sh_down;     // [H][sIw] bf16
+  int s_row0, s_I_loc, s_Iw;
+  // workspace
+  uint16_t* hs;        // [T][s_I_loc] bf16 shared intermediate
+  uint8_t* hq_codes;   // [P][I_loc/2]
+  uint8_t* hq_scales;  // [P][I_loc/16]
+  float* Y;            // [P][H] fp32, rows in sorted order
+  float* S;            // [T][H] fp32
+  void* out;
+  int out_flags;
+  int num_sms;
+};
+
+cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s);
+
+// y fp32 [T][H] -> bf16(y / sqrt(mean(y^2) + eps)) [T][H]
+cudaError_t launch_rms_renorm(const float* y, uint16_t* x, int T, int H, cudaStream_t s);
+
+}  // namespace ftmoe
