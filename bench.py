@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Throughput of the routed NVFP4 MoE layer on GB300, through libftmoe.so.
+
+python bench.py --gpus N --steps K --warmup W [--impl reference]
+
+A step is one forward of one MoE layer (router, top-k, counting sort,
+activation quantisation, gate_up + SwiGLU, down, shared expert, combine) over
+a batch of T tokens.  The default workload is the decode-shaped layer
+(H=2560, I=I_s=640, E=256, top_k=8, T=16, the whole of I).  Each step uses the
+next of 8 independently seeded layers, so the banks the steps read (8 x 712
+MB) are far larger than L2.  All inputs are synthetic and seeded.
+
+Under torchrun each rank runs the same workload on its own tokens (weak
+scaling, no collective on the data path); the printed value is the sum over
+ranks divided by the slowest rank's time.
+
+--impl reference times the CPU oracle (the fp64 numpy restatement used by the
+tests) on the host cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+KERNEL_SOURCES = {
+    "k_gate_up": "experts.cu", "k_down": "experts.cu", "k_shared_gate_up": "experts.cu",
+    "k_shared_down": "experts.cu", "k_combine": "experts.cu", "k_router_logits": "route.cu",
+    "k_topk": "route.cu", "k_sort": "route.cu", "k_xquant_sigma": "route.cu",
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="decode")
+    p.add_argument("--T", type=int, default=16)
+    p.add_argument("--layers", type=int, default=8, help="independently seeded layers rotated per step")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ small helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(kernel: str) -> str:
+    src = os.path.join(ROOT, "nvfp4_mixture_experts_counting_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
+    h = hashlib.sha256()
+    for path in (src, os.path.join(ROOT, "nvfp4_mixture_experts_counting_gb300", "csrc", "common.cuh")):
+        if os.path.exists(path):
+            h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tab = json.load(f)
+        ent = tab[kernel][workload_key]
+        if ent.get("source_digest") != source_digest(kernel):
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside:
+            # the timed region was shorter than the sampling period: take the
+            # samples nearest to it
+            near = sorted(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[:3]
+            inside = [p for (_, p) in near]
+            note = "timed region shorter than the 100 ms sampling period; nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for n, v in zip(names, p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------------ oracle timing (CPU)
+
+def _oracle_steps(workload: str, T: int, tokens_per_step: int, max_steps: int, budget_s: float,
+                  threads: int):
+    """Runs in a spawned process.  Each step times the oracle layer on the
+    next tokens_per_step tokens of a seeded batch of T tokens; the experts
+    those tokens route to are quantised by the oracle beforehand (untimed,
+    as bank loading is on the GPU side).  Stops after max_steps steps or
+    once budget_s seconds of timed work are spent.  Returns the step times."""
+    os.environ["OMP_NUM_THREADS"] = str(threads)
+    os.environ["OPENBLAS_NUM_THREADS"] = str(threads)
+    import numpy as np
+    from nvfp4_mixture_experts_counting_gb300 import workloads as W
+    from oracle import moe
+    wl = W.WORKLOADS[workload]
+    x = W.hidden(wl, T).float().numpy()
+    rw = W.router_weight(wl).numpy()
+    b = W.router_bias(wl)
+    b = None if b is None else b.numpy()
+    sgu, sdn, sg = [t.float().numpy() for t in W.shared_weights(wl)]
+    idx, _ = moe.select_topk(moe.router_logits(x, rw, b), wl.top_k)
+    banks = {}
+    times = []
+    spent = 0.0
+    s = 0
+    while s < max_steps and spent < budget_s:
+        toks = np.array([(s * tokens_per_step + j) % T for j in range(tokens_per_step)])
+        for e in sorted(set(idx[toks].reshape(-1).tolist())):
+            if e not in banks:
+                g, d = W.expert_masters(wl, e)
+                banks[e] = moe.quantize_expert(g.numpy(), d.numpy())
+        t0 = time.perf_counter()
+        moe.moe_layer(x, rw, b, lambda e: banks[e], sgu, sdn, sg, I=wl.I, I_s=wl.I_s,
+                      top_k=wl.top_k, tokens=toks)
+        dt = time.perf_counter() - t0
+        times.append(dt)
+        spent += dt
+        s += 1
+    return times
+
+
+def oracle_times(workload: str, T: int, tokens_per_step: int, max_steps: int, budget_s: float,
+                 threads: int):
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(1) as pool:
+        return pool.apply(_oracle_steps, (workload, T, tokens_per_step, max_steps, budget_s, threads))
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def build_layers(wl, n_layers, max_tokens, dev):
+    import torch
+    from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
+    cfg = ftmoe.make_config(H=wl.H, I=wl.I, E=wl.E, top_k=wl.top_k, I_shared=wl.I_s,
+                            num_layers=n_layers, max_tokens=max_tokens,
+                            norm_topk_prob=wl.norm_topk_prob, has_router_bias=wl.router_bias)
+    layer = ftmoe.Layer(cfg, torch.cuda.current_device())
+    E, I, H = wl.E, wl.I, wl.H
+    for l in range(n_layers):
+        gu = torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev)
+        dn = torch.empty((E, H, I), dtype=torch.float32, device=dev)
+        for e in range(E):
+            g, d = W.expert_masters(wl, e, l, device=dev)
+            gu[e].copy_(g)
+            dn[e].copy_(d)
+        q = {
+            "gu_codes": torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=dev),
+            "gu_scales": torch.empty((E, 2 * I, H // 16), dtype=torch.uint8, device=dev),
+            "gu_global": torch.empty((E, 2 * I), dtype=torch.float32, device=dev),
+            "dn_codes": torch.empty((E, H, I // 2), dtype=torch.uint8, device=dev),
+            "dn_scales": torch.empty((E, H, I // 16), dtype=torch.uint8, device=dev),
+            "dn_global": torch.empty((E, H), dtype=torch.float32, device=dev),
+        }
+        ftmoe.ftmoe_quantize_weights(gu, E * 2 * I, H, q["gu_codes"], q["gu_scales"], q["gu_global"])
+        ftmoe.ftmoe_quantize_weights(dn, E * H, I, q["dn_codes"], q["dn_scales"], q["dn_global"])
+        del gu, dn
+        rw = W.router_weight(wl, l, device=dev)
+        rb = W.router_bias(wl, l, device=dev)
+        sgu, sdn, sg = W.shared_weights(wl, l, device=dev)
+        desc = ftmoe.bank_desc(rw, rb, q["gu_codes"], q["gu_scales"], q["gu_global"], q["dn_codes"],
+                               q["dn_scales"], q["dn_global"], sgu, sdn, sg, on_device=True)
+        layer.load_bank(l, desc)
+        del q
+        torch.cuda.synchronize()
+    return layer
+
+
+def _barrier_and_sync(ws):
+    import torch
+    import torch.distributed as dist
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def _max_over_ranks(ws, v: float) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    from nvfp4_mixture_experts_counting_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if ws > 1:
+        dist.barrier()
+    from nvfp4_mixture_experts_counting_gb300 import accounting as A
+    from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
+
+    wl = W.WORKLOADS[args.workload]
+    T, L, K, Wm = args.T, args.layers, args.steps, max(args.warmup, 3)
+    dev = "cuda"
+    layer = build_layers(wl, L, T, dev)
+    I_loc, sI_loc = wl.I, wl.I_s
+    NX = 8
+    xs = [W.hidden(wl, T, step=s + 100 * rank, device=dev) for s in range(NX)]
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, o=out, x=None):
+        layer.forward(i % L, xs[i % NX] if x is None else x, o, stream=stream)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region (per-kernel events recorded on the launch stream)
+    ftmoe.ftmoe_profile_enable(layer.handle, True)
+    ftmoe.ftmoe_profile_read(layer.handle)          # drop warm-up records
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    _barrier_and_sync(ws)
+    t_wall0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(K):
+        step(i)
+    ev1.record(stream)
+    _barrier_and_sync(ws)
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ktimes = ftmoe.ftmoe_profile_read(layer.handle)
+    ftmoe.ftmoe_profile_enable(layer.handle, False)
+    ms_max = _max_over_ranks(ws, ms)
+    value = ws * T * K / (ms_max / 1e3)
+
+    # ---- untimed: touched experts of every (layer, x) combination used above
+    offs = torch.empty((wl.E + 1,), dtype=torch.int32, device=dev)
+    aux = ftmoe.Aux(None, None, offs.data_ptr(), None, None)
+    touched = {}
+    for li in range(L):
+        for xi in range(NX):
+            layer.forward(li, xs[xi], out, aux=aux, stream=stream)
+            o = offs.cpu()
+            touched[(li, xi)] = int(((o[1:] - o[:-1]) > 0).sum())
+    per_step_touched = [touched[(i % L, i % NX)] for i in range(K)]
+    mean_touched = sum(per_step_touched) / K
+    bytes_step = sum(A.layer_touched_bytes(wl.H, wl.E, I_loc, sI_loc, T, tt) for tt in per_step_touched) / K
+    routed_bytes_step = mean_touched * A.expert_window_bytes(wl.H, I_loc)
+
+    # ---- dominant kernel roofline
+    peak, peak_kind = load_peaks()
+    total_k = sum(v[1] for v in ktimes.values()) or 1.0
+    dom = max(ktimes.items(), key=lambda kv: kv[1][1])[0] if ktimes else None
+    roof = None
+    if dom:
+        launches, kms = ktimes[dom]
+        avg_s = kms / launches / 1e3
+        unit_bytes, unit = A.kernel_unit_bytes(dom, wl.H, I_loc, sI_loc)
+        if unit_bytes is not None:
+            units = mean_touched if unit.startswith("touched") else 1.0
+            alg = unit_bytes * units
+            achieved = alg / avg_s / 1e9
+            roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": ncu_traffic(dom, f"{args.workload}_T{T}"),
+                    "algorithmic_bytes_per_launch": int(alg), "unit_bytes": unit_bytes,
+                    "units_per_launch": round(units, 2), "units": unit,
+                    "avg_launch_us": round(avg_s * 1e6, 2),
+                    "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+    shares = {k: {"launches": v[0], "ms": round(v[1], 3), "share": round(v[1] / total_k, 4)}
+              for k, v in ktimes.items()}
+
+    # ---- end to end through the C ABI with host buffers
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(xs[0])
+    for i in range(Wm):
+        xd.copy_(xh[i % NX], non_blocking=True)
+        step(i, out, xd)
+        oh.copy_(out, non_blocking=True)
+    _barrier_and_sync(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        xd.copy_(xh[i % NX], non_blocking=True)
+        step(i, out, xd)
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    _barrier_and_sync(ws)
+    e2e_ms = _max_over_ranks(ws, e0.elapsed_time(e1))
+    e2e_value = ws * T * K / (e2e_ms / 1e3)
+
+    # ---- GPU launch count inside the timed region
+    launches_total = sum(v[0] for v in ktimes.values())
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n_tok = 4
+        th = cpu_threads()
+        try:
+            secs = sum(oracle_times(args.workload, T, n_tok, 1, 1e9, th))
+            cpu = {"value": round(n_tok / secs, 4), "unit": "tokens/s", "cores": th, "kind": "oracle",
+                   "sample": f"{n_tok} tokens of one seeded T={T} batch of the {args.workload} layer "
+                             f"(their experts' banks quantised beforehand, untimed); numpy fp64, "
+                             f"BLAS threads={th}"}
+        except Exception as ex:  # the baseline is reported, never required
+            cpu = {"value": None, "unit": "tokens/s", "cores": th, "kind": "oracle", "sample": f"failed: {ex}"}
+
+    if rank == 0:
+        cl = clocks.summary(t_wall0, t_wall1)
+        line = {
+            "metric": "MoE-layer tokens/s at 1 GB300 (decode: % of HBM peak over touched bytes)",
+            "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+            "ms_per_step": round(ms_max / K, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate); bf16 shared expert",
+            "data": "synthetic, seeded",
+            "config": {"workload": f"{args.workload} layer: H={wl.H} I={wl.I} I_s={wl.I_s} E={wl.E} "
+                                   f"top_k={wl.top_k}, T={T}, full I window",
+                       "global_batch": T * ws, "layers_rotated": L,
+                       "l2": f"inputs larger than L2: {L} independently seeded layers rotated per step "
+                             f"({L} x {A.expert_window_bytes(wl.H, I_loc) * wl.E / 1e6:.0f} MB of banks)",
+                       "parallelism": f"replicas x{ws} (token-parallel, no collective)"},
+            "touched_experts_per_step": round(mean_touched, 2),
+            "touched_bytes_per_step": int(bytes_step),
+            "layer_hbm_frac": round(bytes_step / (ms_max / K / 1e3) / 1e9 / peak, 4),
+            "layer_hbm_gbs": round(bytes_step / (ms_max / K / 1e3) / 1e9, 1),
+            "routed_only_gbs": round(routed_bytes_step / (ms_max / K / 1e3) / 1e9, 1),
+            "roofline": roof,
+            "kernel_shares": shares,
+            "gpu_launches": launches_total,
+            "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": T * wl.H * 2,
+                    "d2h_bytes_per_step": T * wl.H * 2},
+            "clocks": cl,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from nvfp4_mixture_experts_counting_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    th = cpu_threads()
+    K, Wm = args.steps, args.warmup
+    # one token of the batch per step; stop running steps once the budget is
+    # spent so the whole run stays within a few minutes
+    budget_s = 120.0
+    times = oracle_times(args.workload, args.T, 1, K, budget_s, th)
+    n = max(len(times), 1)
+    tot = sum(times)
+    value = n / tot
+    line = {
+        "impl": "reference",
+        "metric": "MoE-layer tokens/s at 1 GB300 (decode: % of HBM peak over touched bytes)",
+        "value": round(value, 4), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+        "ms_per_step": round(1e3 * tot / n, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic, seeded",
+        "config": {"workload": f"{args.workload} layer: H={wl.H} I={wl.I} I_s={wl.I_s} E={wl.E} "
+                               f"top_k={wl.top_k}, T={args.T}, full I window"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": th, "kind": "oracle",
+                         "sample": f"one token of a seeded T={args.T} batch per step; {n} of {K} steps "
+                                   f"run within a {budget_s:.0f} s budget"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -193,6 +193,21 @@ int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out);
  * DEVICE_CHECK or TIMEOUT. */
 int ftmoe_check_status(ftmoe_handle* h, ftmoe_stream_t stream);
 
+/* Per-kernel timing.  While enabled, every kernel the handle launches is
+ * bracketed by two CUDA events recorded on its launch stream.  Reading
+ * synchronises those events, returns one entry per kernel name (launches,
+ * summed event time in ms) in first-launch order, and clears the record.
+ * Recording stays off by default; the events cost a few microseconds of host
+ * time per launch.  n_out receives the number of entries (<= max_entries). */
+typedef struct {
+  char name[48];
+  int64_t launches;
+  double total_ms;
+} ftmoe_kernel_time;
+
+int ftmoe_profile_enable(ftmoe_handle* h, int enable);
+int ftmoe_profile_read(ftmoe_handle* h, ftmoe_kernel_time* out, int max_entries, int* n_out);
+
 /* NVFP4-quantise fp32 weight rows on the device (a load-time tool; the same
  * block arithmetic the forward applies to activations):
  *   g = fp32(row_amax / 2688); per 16-block s = E4M3(fp32(fp32(amax / 6) / g));

@@ -1,0 +1,57 @@
+"""Algorithmic byte and flop counts of the MoE layer, for roofline reporting.
+
+Byte counts are those of the bank format itself (packed E2M1 codes, one E4M3
+scale per 16 elements, one fp32 global per row), restricted to the
+intermediate window a forward uses, with no padding.
+"""
+
+from __future__ import annotations
+
+
+def gate_up_window_bytes(H: int, I_loc: int) -> int:
+    """gate_up rows of one expert in a window: 2*I_loc rows of H/2 code bytes,
+    H/16 scale bytes and a 4-byte global."""
+    return 2 * I_loc * (H // 2 + H // 16 + 4)
+
+
+def down_window_bytes(H: int, I_loc: int) -> int:
+    """down of one expert in a window: H rows of I_loc/2 code bytes and
+    I_loc/16 scale bytes, plus all H row globals."""
+    return H * (I_loc // 2 + I_loc // 16 + 4)
+
+
+def expert_window_bytes(H: int, I_loc: int) -> int:
+    return gate_up_window_bytes(H, I_loc) + down_window_bytes(H, I_loc)
+
+
+def shared_window_bytes(H: int, sI_loc: int) -> int:
+    """bf16 shared expert: gate and up rows (2*sI_loc x H) and down columns
+    (H x sI_loc), plus the bf16 gate vector."""
+    return 2 * sI_loc * H * 2 + H * sI_loc * 2 + H * 2
+
+
+def layer_touched_bytes(H: int, E: int, I_loc: int, sI_loc: int, T: int, touched: int,
+                        out_bytes_per_elem: int = 2) -> int:
+    """HBM bytes one forward must move at least: the touched experts' window
+    bytes, the shared expert, the fp32 router, x in and out."""
+    return (touched * expert_window_bytes(H, I_loc) + shared_window_bytes(H, sI_loc)
+            + E * H * 4 + T * H * 2 + T * H * out_bytes_per_elem)
+
+
+def routed_flops(H: int, I_loc: int, pairs: int) -> int:
+    """Multiply-adds x 2 of the routed experts: gate_up (2*I_loc x H) and down
+    (H x I_loc) per token-expert pair."""
+    return pairs * (2 * H * 2 * I_loc + 2 * I_loc * H)
+
+
+#: per kernel: (bytes per unit, unit name), where units are touched experts
+def kernel_unit_bytes(kernel: str, H: int, I_loc: int, sI_loc: int):
+    if kernel == "k_gate_up":
+        return gate_up_window_bytes(H, I_loc), "touched expert (gate_up window)"
+    if kernel == "k_down":
+        return down_window_bytes(H, I_loc), "touched expert (down window)"
+    if kernel == "k_shared_gate_up":
+        return 2 * sI_loc * H * 2, "launch (shared gate_up rows)"
+    if kernel == "k_shared_down":
+        return H * sI_loc * 2, "launch (shared down columns)"
+    return None, None

@@ -14,11 +14,55 @@
 namespace ftmoe {
 cudaError_t route_set_smem_limits(int H, int E);
 cudaError_t experts_set_smem_limits(int H, int I);
+thread_local Profiler* g_prof = nullptr;
 }  // namespace ftmoe
 
 using namespace ftmoe;
 
 namespace {
+
+// Records a pair of CUDA events around each launch; events are pooled.
+class EventProfiler final : public Profiler {
+ public:
+  struct Rec { std::string name; cudaEvent_t a, b; };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  std::string pending;
+  cudaEvent_t pending_ev = nullptr;
+
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void begin(const char* name, cudaStream_t s) override {
+    pending = name;
+    pending_ev = get();
+    cudaEventRecord(pending_ev, s);
+  }
+  void end(cudaStream_t s) override {
+    cudaEvent_t b = get();
+    cudaEventRecord(b, s);
+    recs.push_back({pending, pending_ev, b});
+    pending_ev = nullptr;
+  }
+  ~EventProfiler() override {
+    for (auto& r : recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+// Sets the thread's profiler for the duration of one entry-point call.
+struct ProfScope {
+  Profiler* saved;
+  explicit ProfScope(Profiler* p) : saved(g_prof) { g_prof = p; }
+  ~ProfScope() { g_prof = saved; }
+};
 
 thread_local std::string g_last_cuda_error;
 
@@ -90,6 +134,7 @@ struct ftmoe_handle {
   uint16_t* stack_x[2] = {nullptr, nullptr};
   uint32_t* status = nullptr;
   uint32_t last_status = 0;
+  EventProfiler* prof = nullptr;  // non-null while per-kernel timing is enabled
 };
 
 namespace ftmoe {
@@ -237,6 +282,7 @@ int ftmoe_destroy(ftmoe_handle* h) {
   if (!h) return FTMOE_OK;
   cudaSetDevice(h->device);
   for (auto& L : h->layers) free_layer(L);
+  delete h->prof;
   cudaFree(h->ws);
   delete h;
   return FTMOE_OK;
@@ -391,6 +437,7 @@ int ftmoe_forward(ftmoe_handle* h, int layer, const void* x, int T, void* out, i
   if (!aligned16(x) || !aligned16(out)) return FTMOE_ERR_ALIGNMENT;
   if (fault("forward")) return FTMOE_ERR_FAULT_INJECTED;
   CK(cudaSetDevice(h->device));
+  ProfScope ps(h->prof);
   return forward_impl(h, layer, x, T, out, out_flags, i0, I_loc, aux, (cudaStream_t)stream);
 }
 
@@ -405,6 +452,7 @@ int ftmoe_forward_stack(ftmoe_handle* h, const void* x, int T, void* out, ftmoe_
   if (!aligned16(x) || !aligned16(out)) return FTMOE_ERR_ALIGNMENT;
   CK(cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
+  ProfScope ps(h->prof);
   const void* cur = x;
   for (int l = 0; l < c.num_layers; ++l) {
     Layer& L = h->layers[l];
@@ -449,6 +497,49 @@ int ftmoe_check_status(ftmoe_handle* h, ftmoe_stream_t stream) {
   h->last_status = st;
   if (st & kStatusTimeout) return FTMOE_ERR_TIMEOUT;
   if (st & kStatusRange) return FTMOE_ERR_DEVICE_CHECK;
+  return FTMOE_OK;
+}
+
+int ftmoe_profile_enable(ftmoe_handle* h, int enable) {
+  if (!h) return FTMOE_ERR_INVALID_ARG;
+  CK(cudaSetDevice(h->device));
+  if (enable && !h->prof) h->prof = new EventProfiler();
+  if (!enable && h->prof) {
+    CK(cudaDeviceSynchronize());
+    delete h->prof;
+    h->prof = nullptr;
+  }
+  return FTMOE_OK;
+}
+
+int ftmoe_profile_read(ftmoe_handle* h, ftmoe_kernel_time* out, int max_entries, int* n_out) {
+  if (!h || !n_out || max_entries < 0 || (max_entries > 0 && !out)) return FTMOE_ERR_INVALID_ARG;
+  *n_out = 0;
+  if (!h->prof) return FTMOE_OK;
+  CK(cudaSetDevice(h->device));
+  EventProfiler& P = *h->prof;
+  std::vector<std::string> names;
+  std::vector<ftmoe_kernel_time> acc;
+  for (auto& r : P.recs) {
+    CK(cudaEventSynchronize(r.b));
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, r.a, r.b));
+    size_t i = 0;
+    while (i < names.size() && names[i] != r.name) ++i;
+    if (i == names.size()) {
+      names.push_back(r.name);
+      ftmoe_kernel_time kt{};
+      snprintf(kt.name, sizeof kt.name, "%s", r.name.c_str());
+      acc.push_back(kt);
+    }
+    acc[i].launches += 1;
+    acc[i].total_ms += ms;
+  }
+  for (auto& r : P.recs) { P.pool.push_back(r.a); P.pool.push_back(r.b); }
+  P.recs.clear();
+  const int n = (int)acc.size() < max_entries ? (int)acc.size() : max_entries;
+  for (int i = 0; i < n; ++i) out[i] = acc[i];
+  *n_out = n;
   return FTMOE_OK;
 }
 

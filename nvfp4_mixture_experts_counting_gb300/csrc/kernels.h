@@ -10,6 +10,19 @@ namespace ftmoe {
 constexpr uint32_t kStatusRange = 1u;    // an in-kernel range check failed
 constexpr uint32_t kStatusTimeout = 2u;  // a bounded wait ran out
 
+// Optional per-launch timing: when set for the calling thread, launchers
+// bracket each kernel with begin/end (CUDA events on the launch stream).
+struct Profiler {
+  virtual void begin(const char* name, cudaStream_t s) = 0;
+  virtual void end(cudaStream_t s) = 0;
+  virtual ~Profiler() = default;
+};
+extern thread_local Profiler* g_prof;
+#define FTMOE_PROF_BEGIN(name, s) \
+  do { if (::ftmoe::g_prof) ::ftmoe::g_prof->begin(name, s); } while (0)
+#define FTMOE_PROF_END(s) \
+  do { if (::ftmoe::g_prof) ::ftmoe::g_prof->end(s); } while (0)
+
 // Byte offsets of the sections of one expert record (one expert's bank
 // restricted to a loaded window of width Iw).  Sections are 256-byte aligned.
 struct RecLayout {

@@ -431,8 +431,10 @@ cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, uint8_t
                                     uint8_t* scales, float* globals, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const int wpb = 8;
+  FTMOE_PROF_BEGIN("k_quantize_weights", s);
   k_quantize_weights<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, s>>>(w, rows, K, codes, scales,
                                                                             globals);
+  FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
 
@@ -440,7 +442,9 @@ cudaError_t launch_quantize_act_bf16(const uint16_t* a, int64_t rows, int K, uin
                                      uint8_t* scales, cudaStream_t s) {
   const int64_t nb = rows * (K / kBlock);
   if (nb == 0) return cudaSuccess;
+  FTMOE_PROF_BEGIN("k_quantize_act", s);
   k_quantize_act<<<(unsigned)((nb + 255) / 256), 256, 0, s>>>(a, nb, K, codes, scales);
+  FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
 
@@ -448,23 +452,31 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   cudaError_t err;
   {
     const int wpb = 8;
+    FTMOE_PROF_BEGIN("k_xquant_sigma", s);
     k_xquant_sigma<<<(a.T + wpb - 1) / wpb, wpb * 32, 0, s>>>(a);
+    FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {
     dim3 grid((a.E + kRouterWarps - 1) / kRouterWarps, (a.T + kRouterTT - 1) / kRouterTT);
     size_t smem = (size_t)kRouterTT * a.H * 2;
+    FTMOE_PROF_BEGIN("k_router_logits", s);
     k_router_logits<<<grid, kRouterWarps * 32, smem, s>>>(a);
+    FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {
     size_t smem = (size_t)kTopkWarps * a.E * (4 + 4 + 8);
+    FTMOE_PROF_BEGIN("k_topk", s);
     k_topk<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, smem, s>>>(a);
+    FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {
     size_t smem = (size_t)kSortWarps * a.E * 4;
+    FTMOE_PROF_BEGIN("k_sort", s);
     k_sort<<<1, kSortThreads, smem, s>>>(a);
+    FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   return cudaSuccess;

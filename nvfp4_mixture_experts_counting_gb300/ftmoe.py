@@ -58,6 +58,10 @@ class Stats(C.Structure):
                 ("h2d_bytes", C.c_int64), ("residency", C.c_double), ("device_status", C.c_int32)]
 
 
+class KernelTime(C.Structure):
+    _fields_ = [("name", C.c_char * 48), ("launches", C.c_int64), ("total_ms", C.c_double)]
+
+
 _lib = None
 
 #: every symbol the header declares, with its argument and result types
@@ -72,6 +76,8 @@ SIGNATURES = {
     "ftmoe_last_cuda_error": ([], C.c_char_p),
     "ftmoe_get_stats": ([C.c_void_p, C.c_int, C.POINTER(Stats)], C.c_int),
     "ftmoe_check_status": ([C.c_void_p, C.c_void_p], C.c_int),
+    "ftmoe_profile_enable": ([C.c_void_p, C.c_int], C.c_int),
+    "ftmoe_profile_read": ([C.c_void_p, C.POINTER(KernelTime), C.c_int, C.POINTER(C.c_int)], C.c_int),
     "ftmoe_quantize_weights": ([C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p], C.c_int),
     "ftmoe_quantize_activations": ([C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p],
@@ -163,6 +169,18 @@ def ftmoe_get_stats(h: int, layer: int) -> Stats:
 
 def ftmoe_check_status(h: int, stream=None) -> int:
     return lib().ftmoe_check_status(h, _stream(stream))
+
+
+def ftmoe_profile_enable(h: int, enable: bool):
+    _check(lib().ftmoe_profile_enable(h, int(enable)), "ftmoe_profile_enable")
+
+
+def ftmoe_profile_read(h: int, max_entries: int = 64) -> dict:
+    """{kernel name: (launches, total ms)} recorded since the last read."""
+    arr = (KernelTime * max_entries)()
+    n = C.c_int()
+    _check(lib().ftmoe_profile_read(h, arr, max_entries, C.byref(n)), "ftmoe_profile_read")
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}
 
 
 def ftmoe_quantize_weights(w, rows: int, K: int, codes, scales, globals_, stream=None):
