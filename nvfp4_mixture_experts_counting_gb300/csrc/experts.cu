@@ -362,18 +362,23 @@ __global__ void k_rms_renorm(const float* __restrict__ y, uint16_t* __restrict__
 
 // ------------------------------------------------------------------ launchers
 
+// Per-function maxima shared by every handle in the process: always the
+// request of the largest accepted sizes (H, I <= 8192, I_shared <= 4096).
 cudaError_t experts_set_smem_limits(int H, int I) {
+  (void)H;
+  (void)I;
+  const int Hm = 8192, Im = 8192, Ism = 4096;
   cudaError_t e;
-  const int gu = kMT * (H / 2) * 4 + kMT * (H / kBlock) * 4 + kMT * 32 * 4;
+  const int gu = kMT * (Hm / 2) * 4 + kMT * (Hm / kBlock) * 4 + kMT * 32 * 4;
   if ((e = cudaFuncSetAttribute(k_gate_up, cudaFuncAttributeMaxDynamicSharedMemorySize, gu)) != cudaSuccess)
     return e;
-  const int dn = kMT * (I / 2) * 4 + kMT * (I / kBlock) * 4;
+  const int dn = kMT * (Im / 2) * 4 + kMT * (Im / kBlock) * 4;
   if ((e = cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, dn)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_shared_gate_up, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kMT * H * 2)) != cudaSuccess)
+                                kMT * Hm * 2)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(k_shared_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kMT * I * 4);
+  return cudaFuncSetAttribute(k_shared_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kMT * Ism * 4);
 }
 
 cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s) {

@@ -483,15 +483,20 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
 }
 
 // Opt the kernels that need more than 48 KB of dynamic shared memory in.
+// The limit is a per-function maximum shared by every handle in the process,
+// so it is always set to what the largest accepted sizes (H <= 8192,
+// E <= 1024) can request; the arguments only have to stay within those.
 cudaError_t route_set_smem_limits(int H, int E) {
+  (void)H;
+  (void)E;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kRouterTT * H * 2)) != cudaSuccess)
+                                kRouterTT * 8192 * 2)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kTopkWarps * E * 16)) != cudaSuccess)
+                                kTopkWarps * 1024 * 16)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(k_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortWarps * E * 4);
+  return cudaFuncSetAttribute(k_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortWarps * 1024 * 4);
 }
 
 }  // namespace ftmoe
