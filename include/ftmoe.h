@@ -65,7 +65,8 @@ typedef enum {
   FTMOE_ERR_TIMEOUT = -7,          /* a bounded device-side wait ran out */
   FTMOE_ERR_FAULT_INJECTED = -8,   /* FTMOE_FAULT selected this call to fail */
   FTMOE_ERR_DEVICE = -9,           /* no device, or not a compute capability 10.3 device */
-  FTMOE_ERR_DEVICE_CHECK = -10     /* an in-kernel range check failed (see ftmoe_check_status) */
+  FTMOE_ERR_DEVICE_CHECK = -10,    /* an in-kernel range check failed (see ftmoe_check_status) */
+  FTMOE_ERR_TOO_LARGE = -11        /* sizes exceed the fixed scratch of ftmoe_route_static */
 } ftmoe_status;
 
 /* out_flags of ftmoe_forward: the output type, optionally OR-ed with ACCUMULATE */
@@ -218,6 +219,32 @@ int ftmoe_profile_read(ftmoe_handle* h, ftmoe_kernel_time* out, int max_entries,
  * Asynchronous on `stream`. */
 int ftmoe_quantize_weights(const float* w, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
                            float* globals, ftmoe_stream_t stream);
+
+/* Routing that allocates nothing.  The pages have no counterpart to this
+ * entry point; it exists for callers that cannot call cudaMalloc when they
+ * route: a serving runtime that has given all free device memory to its KV
+ * cache and graph pools up front, a host that forbids device allocations
+ * from plugins, or code running while a CUDA graph is captured.
+ *
+ * It runs the same router, top-k and counting-sort kernels as ftmoe_forward
+ * and returns what ftmoe_forward's aux outputs return, with no handle.  All
+ * pointers are device memory of the current device:
+ *   x:        bf16 [T, H] (16-byte aligned), H a multiple of 16
+ *   router_w: fp32 [E, H] (16-byte aligned); router_bias: fp32 [E] or NULL
+ *   topk_idx [T, top_k], topk_w [T, top_k], offsets [E + 1],
+ *   perm [T*top_k], inv [T*top_k]: outputs, as in ftmoe_aux.
+ * Its scratch is one fixed array in the library's device image (287 KB per
+ * device that loads the library, held until the process exits),
+ * which bounds the sizes: T <= 1024, E <= 1024, T*E <= 16384,
+ * T*H <= 262144 and H <= 8192; larger problems return FTMOE_ERR_TOO_LARGE.
+ * The first call on a device looks up that array's device address (and sets
+ * the kernels' shared-memory limits); make that first call before any stream
+ * capture.  Every call shares the one array, so calls whose kernels overlap
+ * on the GPU (different streams, or several threads) race: serialise them.
+ * Asynchronous on `stream`; calls no allocating routine. */
+int ftmoe_route_static(const void* x, int T, int H, const float* router_w, const float* router_bias, int E,
+                       int top_k, int norm_topk_prob, int32_t* topk_idx, float* topk_w, int32_t* offsets,
+                       int32_t* perm, int32_t* inv, ftmoe_stream_t stream);
 
 /* NVFP4-quantise bf16 activation rows with the global fixed at 1.0 (the
  * forward's own activation quantiser, exposed for testing):

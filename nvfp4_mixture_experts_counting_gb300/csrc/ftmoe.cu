@@ -207,6 +207,7 @@ const char* ftmoe_error_string(int code) {
     case FTMOE_ERR_FAULT_INJECTED: return "fault injected (FTMOE_FAULT)";
     case FTMOE_ERR_DEVICE: return "no usable device (needs compute capability 10.3)";
     case FTMOE_ERR_DEVICE_CHECK: return "an in-kernel range check failed";
+    case FTMOE_ERR_TOO_LARGE: return "sizes exceed the fixed scratch of the allocation-free routing entry point";
     default: return "unknown status";
   }
 }

@@ -23,6 +23,7 @@ OUT_BF16, OUT_FP32, OUT_ACCUMULATE = 0, 1, 0x100
 STATUS = {
     0: "OK", -1: "INVALID_ARG", -2: "ALIGNMENT", -3: "NOT_LOADED", -4: "SLICE_OUT_OF_RANGE",
     -5: "OOM", -6: "CUDA", -7: "TIMEOUT", -8: "FAULT_INJECTED", -9: "DEVICE", -10: "DEVICE_CHECK",
+    -11: "TOO_LARGE",
 }
 
 
@@ -78,6 +79,8 @@ SIGNATURES = {
     "ftmoe_check_status": ([C.c_void_p, C.c_void_p], C.c_int),
     "ftmoe_profile_enable": ([C.c_void_p, C.c_int], C.c_int),
     "ftmoe_profile_read": ([C.c_void_p, C.POINTER(KernelTime), C.c_int, C.POINTER(C.c_int)], C.c_int),
+    "ftmoe_route_static": ([C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "ftmoe_quantize_weights": ([C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p], C.c_int),
     "ftmoe_quantize_activations": ([C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p],
@@ -181,6 +184,14 @@ def ftmoe_profile_read(h: int, max_entries: int = 64) -> dict:
     n = C.c_int()
     _check(lib().ftmoe_profile_read(h, arr, max_entries, C.byref(n)), "ftmoe_profile_read")
     return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}
+
+
+def ftmoe_route_static(x, T: int, H: int, router_w, router_bias, E: int, top_k: int, norm_topk_prob: bool,
+                       topk_idx, topk_w, offsets, perm, inv, stream=None):
+    """Routing with no device allocation (scratch in a fixed device array)."""
+    _check(lib().ftmoe_route_static(_ptr(x), T, H, _ptr(router_w), _ptr(router_bias), E, top_k,
+                                    int(norm_topk_prob), _ptr(topk_idx), _ptr(topk_w), _ptr(offsets),
+                                    _ptr(perm), _ptr(inv), _stream(stream)), "ftmoe_route_static")
 
 
 def ftmoe_quantize_weights(w, rows: int, K: int, codes, scales, globals_, stream=None):
