@@ -39,9 +39,12 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
 KERNEL_SOURCES = {
-    "k_gate_up": "experts.cu", "k_down": "experts.cu", "k_shared_gate_up": "experts.cu",
-    "k_shared_down": "experts.cu", "k_combine": "experts.cu", "k_router_logits": "route.cu",
-    "k_topk": "route.cu", "k_sort": "route.cu", "k_xquant_sigma": "route.cu",
+    "k_dec_route": ("decode_route.cu", "decode_common.cuh", "tma.cuh"),
+    "k_dec_gate_up": ("decode_gate_up.cu", "decode_common.cuh", "tma.cuh"),
+    "k_dec_down": ("decode_down.cu", "decode_common.cuh", "tma.cuh"),
+    "k_gate_up": ("experts.cu",), "k_down": ("experts.cu",), "k_shared_gate_up": ("experts.cu",),
+    "k_shared_down": ("experts.cu",), "k_combine": ("experts.cu",), "k_router_logits": ("route.cu",),
+    "k_topk": ("route.cu",), "k_sort": ("route.cu",), "k_xquant_sigma": ("route.cu",),
 }
 
 
@@ -77,9 +80,11 @@ def load_peaks():
 
 
 def source_digest(kernel: str) -> str:
-    src = os.path.join(ROOT, "nvfp4_mixture_experts_counting_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
+    """Digest of the sources a kernel is compiled from (its files + common.cuh)."""
+    csrc = os.path.join(ROOT, "nvfp4_mixture_experts_counting_gb300", "csrc")
     h = hashlib.sha256()
-    for path in (src, os.path.join(ROOT, "nvfp4_mixture_experts_counting_gb300", "csrc", "common.cuh")):
+    for name in (*KERNEL_SOURCES.get(kernel, ()), "common.cuh"):
+        path = os.path.join(csrc, name)
         if os.path.exists(path):
             h.update(open(path, "rb").read())
     return h.hexdigest()[:16]
@@ -319,6 +324,7 @@ def run_gpu(args):
     # ---- timed region (per-kernel events recorded on the launch stream)
     ftmoe.ftmoe_profile_enable(layer.handle, True)
     ftmoe.ftmoe_profile_read(layer.handle)          # drop warm-up records
+    rerank0 = layer.stats(0).reranked_tokens
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -335,6 +341,7 @@ def run_gpu(args):
     clocks.stop()
     ms = ev0.elapsed_time(ev1)
     ktimes = ftmoe.ftmoe_profile_read(layer.handle)
+    reranked = layer.stats(0).reranked_tokens - rerank0
     ftmoe.ftmoe_profile_enable(layer.handle, False)
     ms_max = _max_over_ranks(ws, ms)
     value = ws * T * K / (ms_max / 1e3)
@@ -361,10 +368,10 @@ def run_gpu(args):
     if dom:
         launches, kms = ktimes[dom]
         avg_s = kms / launches / 1e3
-        unit_bytes, unit = A.kernel_unit_bytes(dom, wl.H, I_loc, sI_loc)
+        unit_bytes, unit, fixed = A.kernel_unit_bytes(dom, wl.H, I_loc, sI_loc, wl.E)
         if unit_bytes is not None:
             units = mean_touched if unit.startswith("touched") else 1.0
-            alg = unit_bytes * units
+            alg = unit_bytes * units + fixed
             achieved = alg / avg_s / 1e9
             roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -427,6 +434,7 @@ def run_gpu(args):
                              f"({L} x {A.expert_window_bytes(wl.H, I_loc) * wl.E / 1e6:.0f} MB of banks)",
                        "parallelism": f"replicas x{ws} (token-parallel, no collective)"},
             "touched_experts_per_step": round(mean_touched, 2),
+            "reranked_tokens_per_step": round(reranked / K, 4),
             "touched_bytes_per_step": int(bytes_step),
             "layer_hbm_frac": round(bytes_step / (ms_max / K / 1e3) / 1e9 / peak, 4),
             "layer_hbm_gbs": round(bytes_step / (ms_max / K / 1e3) / 1e9, 1),

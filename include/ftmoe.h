@@ -25,9 +25,10 @@
  *     are quantised in 16-blocks with E4M3 scale = RNE(amax / 6) and a global
  *     of 1.0, so each expert contraction is W4A4 with exact block products.
  *   - Top-k ties go to the lower expert index; slots are ordered by logit
- *     descending.  Indices are those of the exact (fp64) logits: the kernel
+ *     descending.  Indices are those of the exact logits: the kernel
  *     ranks fp32 logits, certifies the ranking with a rigorous error bound,
- *     and re-ranks uncertain candidates from fp64 sums.
+ *     and re-ranks uncertain candidates from compensated double-fp32 sums
+ *     (about 2^-48 relative error).
  *   - Reductions are in a fixed order with no atomics on values, so results
  *     are bit-identical run to run ([PR385] "Correctness" traces run-to-run
  *     divergence to bf16 atomics in the expert kernels).
@@ -128,6 +129,7 @@ typedef struct {
   int64_t h2d_bytes;        /* offload mode: cumulative host->device expert bytes of this layer */
   double residency;         /* offload mode: resident slots / E; resident mode: 1.0 */
   int32_t device_status;    /* last device status word read by ftmoe_check_status */
+  int64_t reranked_tokens;  /* cumulative tokens (all layers) whose top-k needed re-ranking */
 } ftmoe_stats;
 
 /* Create a handle on CUDA device `device` for layers of the given shape.

@@ -44,14 +44,22 @@ def routed_flops(H: int, I_loc: int, pairs: int) -> int:
     return pairs * (2 * H * 2 * I_loc + 2 * I_loc * H)
 
 
-#: per kernel: (bytes per unit, unit name), where units are touched experts
-def kernel_unit_bytes(kernel: str, H: int, I_loc: int, sI_loc: int):
-    if kernel == "k_gate_up":
-        return gate_up_window_bytes(H, I_loc), "touched expert (gate_up window)"
+def kernel_unit_bytes(kernel: str, H: int, I_loc: int, sI_loc: int, E: int = 0):
+    """(bytes per unit, unit name, fixed bytes per launch) of a kernel's
+    algorithmic HBM traffic; units are touched experts where named so."""
+    if kernel in ("k_gate_up", "k_dec_gate_up"):
+        return gate_up_window_bytes(H, I_loc), "touched expert (gate_up window)", 0
     if kernel == "k_down":
-        return down_window_bytes(H, I_loc), "touched expert (down window)"
+        return down_window_bytes(H, I_loc), "touched expert (down window)", 0
+    if kernel == "k_dec_down":
+        # routed down rows of every touched expert, plus the shared expert's
+        # bf16 down columns (one launch streams both)
+        return down_window_bytes(H, I_loc), "touched expert (down window), + shared down", H * sI_loc * 2
+    if kernel == "k_dec_route":
+        # fp32 router and the shared expert's bf16 gate_up rows
+        return 0, "launch (router + shared gate_up)", E * H * 4 + 2 * sI_loc * H * 2
     if kernel == "k_shared_gate_up":
-        return 2 * sI_loc * H * 2, "launch (shared gate_up rows)"
+        return 0, "launch (shared gate_up rows)", 2 * sI_loc * H * 2
     if kernel == "k_shared_down":
-        return H * sI_loc * 2, "launch (shared down columns)"
-    return None, None
+        return 0, "launch (shared down columns)", H * sI_loc * 2
+    return None, None, None

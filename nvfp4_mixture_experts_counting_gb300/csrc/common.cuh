@@ -104,4 +104,66 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// ---------------------------------------------------------------- double-fp32
+
+// A number hi + lo held as two fp32 values.  Built from error-free
+// transformations (two-sum of Knuth, FMA two-product), so a router logit is
+// carried to about twice fp32's precision on the fp32 pipes.  The explicit
+// _rn intrinsics keep the compiler from fusing the steps.
+struct df32 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ df32 df_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float z = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+  return {s, e};
+}
+
+__device__ __forceinline__ df32 df_add(df32 a, df32 b) {
+  const df32 s = df_two_sum(a.hi, b.hi);
+  return df_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+// Strict order of logits: larger value first (hi, then lo), then lower index.
+__device__ __forceinline__ bool df_before(df32 a, int ea, df32 b, int eb) {
+  if (a.hi != b.hi) return a.hi > b.hi;
+  if (a.lo != b.lo) return a.lo > b.lo;
+  return ea < eb;
+}
+
+// Compensated router logit of one token (bf16 row x) and one expert (fp32 row
+// w), + bias, by a warp: every product is split exactly (x*w = p + pe) and
+// accumulated with two-sum, lane sums are combined in double-fp32.  The
+// absolute error is a few units of 2^-48 times sum |x*w|.
+__device__ __forceinline__ df32 logit_df32(const uint16_t* x, const float* w, int H, float bias, int lane) {
+  float s = 0.f, c = 0.f;
+  const uint2* x4 = reinterpret_cast<const uint2*>(x);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll 4
+  for (int i = lane; i < H / 4; i += 32) {
+    const uint2 xv = __ldg(x4 + i);
+    const float4 wv = __ldg(w4 + i);
+    const float xs[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xffff0000u),
+                         __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xffff0000u)};
+    const float ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float p = __fmul_rn(xs[k], ws[k]);
+      const float pe = __fmaf_rn(xs[k], ws[k], -p);
+      const df32 t = df_two_sum(s, p);
+      s = t.hi;
+      c = __fadd_rn(c, __fadd_rn(t.lo, pe));
+    }
+  }
+  df32 v = df_two_sum(s, c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const df32 u = {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+    v = df_add(v, u);
+  }
+  return df_add(v, {bias, 0.f});
+}
+
 }  // namespace ftmoe

@@ -1,0 +1,485 @@
+// k_dec_route: routing for the decode path.  Router CTAs compute the fp32
+// logits of 2 experts each (H split over 4 warps) with a rigorous error
+// bound; other CTAs run the shared expert's gate_up + SwiGLU and the x
+// quantisation with the shared gate; the last router CTA to finish stages
+// every logit and bound in shared memory, runs top-k (certified, with compensated
+// re-ranking of uncertain candidates) and the counting sort.
+//
+// Pages: PR #385 "feat(qwen4_exp): tensor parallelism for Qwen3.8-Flash-Next
+// (offload backend)", "What this adds" (replicated router; shared expert and
+// its sigmoid gate); Issue #62 "Offloaded MoE ignores tensor parallelism ...",
+// first comment (norm_topk_prob defaults to True).
+#include "decode_common.cuh"
+
+namespace ftmoe {
+
+__device__ __forceinline__ bool key_before(float la, int ea, float lb, int eb) {
+  return la > lb || (la == lb && ea < eb);
+}
+// Top-k of token t by one warp, from logits lg and bounds er in shared
+// memory.  The fp32 ranking is certified with the error bounds (every chosen
+// expert's interval lies above the next one's and above every unchosen
+// expert's); if it is not, every expert that could belong to the top-k is
+// re-ranked from compensated double-fp32 sums (about 2^-48 relative; FP64 is
+// far slower on this GPU).  Ties go to the lower index.
+__device__ void dec_topk_token(const DecodeArgs& a, int t, int lane, const float* lg, const float* er,
+                               uint8_t* ch, int* cand, df32* l64, int* s_idx) {
+  const int E = a.r.E, k = a.r.top_k;
+  for (int e = lane; e < E; e += 32) ch[e] = 0;
+  __syncwarp();
+  int my_idx = 0;  // lane j keeps slot j
+  float my_l = 0.f;
+  float lmax = -INFINITY;
+  bool certified = true;
+  float prev_lo = INFINITY, lmin_lo = INFINITY;
+  for (int j = 0; j < k; ++j) {
+    float bl = -INFINITY;
+    int be = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      const float v = lg[e];
+      if (!ch[e] && key_before(v, e, bl, be)) { bl = v; be = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (key_before(ol, oe, bl, be)) { bl = ol; be = oe; }
+    }
+    if (lane == j) { my_idx = be; my_l = bl; }
+    if (j == 0) lmax = bl;
+    const float eb = er[be];
+    const float lo = bl - eb, hi = bl + eb;
+    if (!(hi < prev_lo)) certified = false;
+    prev_lo = lo;
+    lmin_lo = fminf(lmin_lo, lo);
+    __syncwarp();
+    if (lane == 0) ch[be] = 1;
+    __syncwarp();
+  }
+  bool reach = false;
+  for (int e = lane; e < E; e += 32)
+    if (!ch[e] && lg[e] + er[e] >= lmin_lo) reach = true;
+  if (__any_sync(0xffffffffu, reach)) certified = false;
+  if (!certified) {
+    if (lane == 0 && a.r.n_rerank) atomicAdd(a.r.n_rerank, 1ull);  // telemetry only
+    int nc = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      bool c = false;
+      if (e < E) c = ch[e] || (lg[e] + er[e] >= lmin_lo);
+      const unsigned m = __ballot_sync(0xffffffffu, c);
+      if (c) cand[nc + __popc(m & ((1u << lane) - 1))] = e;
+      nc += __popc(m);
+    }
+    __syncwarp();
+    const uint16_t* xrow = a.r.x + (int64_t)t * a.r.H;
+    for (int c = 0; c < nc; ++c) {
+      const int e = cand[c];
+      const df32 v = logit_df32(xrow, a.r.router_w + (int64_t)e * a.r.H, a.r.H,
+                                a.r.router_bias ? a.r.router_bias[e] : 0.f, lane);
+      if (lane == 0) l64[c] = v;
+    }
+    __syncwarp();
+    const df32 none = {-INFINITY, 0.f};
+    for (int j = 0; j < k; ++j) {
+      df32 bl = none;
+      int be = 0x7fffffff, bc = -1;
+      for (int c = lane; c < nc; c += 32) {
+        const df32 v = l64[c];
+        const int e = cand[c];
+        if (v.hi != -INFINITY && df_before(v, e, bl, be)) { bl = v; be = e; bc = c; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const df32 ol = {__shfl_xor_sync(0xffffffffu, bl.hi, o), __shfl_xor_sync(0xffffffffu, bl.lo, o)};
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        if (df_before(ol, oe, bl, be)) { bl = ol; be = oe; bc = oc; }
+      }
+      if (lane == j) { my_idx = be; my_l = bl.hi; }
+      if (j == 0) lmax = bl.hi;
+      __syncwarp();
+      if (lane == 0) l64[bc] = none;
+      __syncwarp();
+    }
+  }
+  // routing weights: softmax over the chosen (norm_topk_prob) or over all
+  const float ex = (lane < k) ? expf(my_l - lmax) : 0.f;
+  float den;
+  if (a.r.norm_topk_prob) {
+    den = warp_sum(ex);
+  } else {
+    float s = 0.f;
+    for (int e = lane; e < E; e += 32) s += expf(lg[e] - lmax);
+    den = warp_sum(s);
+  }
+  if (lane < k) {
+    a.r.topk_idx[(int64_t)t * k + lane] = my_idx;
+    a.r.topk_w[(int64_t)t * k + lane] = ex / den;
+    s_idx[t * k + lane] = my_idx;
+  }
+}
+
+// Counting sort of P <= 1024 pairs by the 256 threads of one CTA: per-warp
+// chunk histograms, a scan over experts, then each warp scatters its chunk in
+// order, so every expert's pairs come out in increasing pair id.
+__device__ void dec_sort(const DecodeArgs& a, const int* s_idx, int* hist /*[8][E]*/, int* scan /*[32]*/) {
+  const int E = a.r.E, P = a.T * a.top_k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 8 * E; i += kRtThreads) hist[i] = 0;
+  __syncthreads();
+  const int CH = (P + 7) / 8;
+  const int c0 = min(P, warp * CH), c1 = min(P, c0 + CH);
+  for (int p = c0 + lane; p < c1; p += 32) {
+    int e = s_idx[p];
+    if ((unsigned)e >= (unsigned)E) { set_status(a.r.status, kStatusRange); e = 0; }
+    atomicAdd(&hist[warp * E + e], 1);
+  }
+  __syncthreads();
+  // each thread owns experts [e0, e1): totals, then a block scan of them
+  const int per = (E + kRtThreads - 1) / kRtThreads;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int cnt = 0, tcnt = 0;
+  for (int e = e0; e < e1; ++e) {
+    int c = 0;
+    for (int w = 0; w < 8; ++w) c += hist[w * E + e];
+    cnt += c;
+    tcnt += c > 0;
+  }
+  int inc = cnt, tinc = tcnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o), tn = __shfl_up_sync(0xffffffffu, tinc, o);
+    if (lane >= o) { inc += n; tinc += tn; }
+  }
+  if (lane == 31) { scan[warp] = inc; scan[16 + warp] = tinc; }
+  __syncthreads();
+  int wbase = 0, twbase = 0;
+  for (int w = 0; w < warp; ++w) { wbase += scan[w]; twbase += scan[16 + w]; }
+  int off = wbase + inc - cnt, toff = twbase + tinc - tcnt;
+  for (int e = e0; e < e1; ++e) {
+    int c = 0;
+    for (int w = 0; w < 8; ++w) {
+      const int h = hist[w * E + e];
+      hist[w * E + e] = off + c;
+      c += h;
+    }
+    a.r.offsets[e] = off;
+    if (c > 0) a.r.touched[toff++] = e;
+    off += c;
+  }
+  if (tid == kRtThreads - 1) {
+    a.r.offsets[E] = P;
+    a.r.n_touched[0] = toff;
+  }
+  __syncthreads();
+  for (int p0 = c0; p0 < c1; p0 += 32) {
+    const int p = p0 + lane;
+    const bool valid = p < c1;
+    int e = valid ? s_idx[p] : -1 - lane;
+    if (valid && (unsigned)e >= (unsigned)E) e = 0;
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(mask & ((1u << lane) - 1));
+    int pos = 0;
+    if (valid) pos = hist[warp * E + e] + rank;
+    __syncwarp();
+    if (valid) {
+      a.r.perm[pos] = p;
+      a.r.inv[p] = pos;
+      if (rank == 0) hist[warp * E + e] += __popc(mask);
+    }
+    __syncwarp();
+  }
+}
+
+// Work split of k_dec_gate_up over its CTAs (one per SM), balanced by cost.
+// An item (touched expert j, 16-wide block) costs kItemCost units of weight
+// work plus one unit per pair of the expert.  gu_split[b] is the first item
+// whose cost interval starts at or after b * C / G (C the total cost, G the
+// number of CTAs), so CTA b takes items [gu_split[b], gu_split[b+1]).
+// Runs in the CTA that did the sort; pre[] holds nt + 1 ints of scratch.
+constexpr int kItemCost = 2;
+__device__ void dec_split(const DecodeArgs& a, int* pre, int* scan) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nt = __ldcg(a.r.n_touched), n_ib = a.win.I_loc / kBlock, G = a.num_sms;
+  // exclusive prefix of per-expert costs, 4 consecutive experts per thread
+  const int j0 = tid * 4;
+  int c[4], sum = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = j0 + q;
+    int cj = 0;
+    if (j < nt) {
+      const int e = __ldcg(a.r.touched + j);
+      cj = n_ib * (kItemCost + __ldcg(a.r.offsets + e + 1) - __ldcg(a.r.offsets + e));
+    }
+    c[q] = cj;
+    sum += cj;
+  }
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) scan[warp] = inc;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += scan[w];
+  int run = base + inc - sum;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (j0 + q <= nt) pre[j0 + q] = run;
+    run += c[q];
+  }
+  __syncthreads();
+  const int64_t C = pre[nt];
+  for (int b = tid; b <= G; b += kRtThreads) {
+    int item;
+    if (b == G || nt == 0) {
+      item = nt * n_ib;
+    } else {
+      const int64_t X = C * b / G;
+      int lo = 0, hi = nt - 1;  // last expert whose prefix is <= X
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= X) lo = mid; else hi = mid - 1;
+      }
+      const int per_item = (pre[lo + 1] - pre[lo]) / n_ib;
+      const int64_t into = (X - pre[lo] + per_item - 1) / per_item;
+      item = lo * n_ib + (int)(into < n_ib ? into : n_ib);
+    }
+    a.gu_split[b] = item;
+  }
+}
+
+__global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  __shared__ int s_last;
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = a.r.H, T = a.T, E = a.r.E;
+  const int b = blockIdx.x;
+  if (b < a.n_router_ctas) {
+    // ---- router: experts 2b (warps 0-3) and 2b+1 (warps 4-7), H in quarters
+    float* part = reinterpret_cast<float*>(sm);  // [8 warps][T][2]
+    const int e = 2 * b + (warp >> 2);
+    const int q = warp & 3;
+    const int Hq = H / 4;
+    if (e < E) {
+      const float4* wr = reinterpret_cast<const float4*>(a.r.router_w + (int64_t)e * H + q * Hq);
+      const int nq = Hq / 4;  // float4 chunks of the quarter row
+      for (int t0 = 0; t0 < T; t0 += 8) {
+        float acc[8], ab[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) { acc[m] = 0.f; ab[m] = 0.f; }
+        for (int g0 = 0; g0 < nq; g0 += 8 * 32) {
+          // all of this lane's chunks of the group in flight at once
+          float4 wv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c = g0 + lane + 32 * j;
+            wv[j] = c < nq ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c = g0 + lane + 32 * j;
+            if (c < nq) {
+              const float4 w = wv[j];
+#pragma unroll
+              for (int m = 0; m < 8; ++m) {
+                if (t0 + m < T) {
+                  const uint2 xv =
+                      __ldg(reinterpret_cast<const uint2*>(a.r.x + (int64_t)(t0 + m) * H + q * Hq) + c);
+                  const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xffff0000u);
+                  const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xffff0000u);
+                  acc[m] = fmaf(x0, w.x, acc[m]);
+                  acc[m] = fmaf(x1, w.y, acc[m]);
+                  acc[m] = fmaf(x2, w.z, acc[m]);
+                  acc[m] = fmaf(x3, w.w, acc[m]);
+                  ab[m] = fmaf(fabsf(x0), fabsf(w.x), ab[m]);
+                  ab[m] = fmaf(fabsf(x1), fabsf(w.y), ab[m]);
+                  ab[m] = fmaf(fabsf(x2), fabsf(w.z), ab[m]);
+                  ab[m] = fmaf(fabsf(x3), fabsf(w.w), ab[m]);
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float s = warp_sum(acc[m]);
+          const float bb = warp_sum(ab[m]);
+          if (lane == 0 && t0 + m < T) {
+            part[(warp * T + t0 + m) * 2] = s;
+            part[(warp * T + t0 + m) * 2 + 1] = bb;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    // combine the quarters in a fixed order.  The sequential roundings of a
+    // logit: 4*ceil(H/512) FMAs per lane, 5 butterfly levels, 3 quarter adds
+    // and the bias, so |l - exact| <= (D+1) u A (1.01 covers A's own error)
+    const int n_seq = 4 * ((Hq / 4 + 31) / 32);
+    const float gamma = (float)((double)(n_seq + 10) * 5.9604644775390625e-8 * 1.01);
+    for (int i = tid; i < 2 * T; i += kRtThreads) {
+      const int ex = i / T, t = i % T;
+      const int ee = 2 * b + ex;
+      if (ee < E) {
+        const int w0 = ex * 4;
+        float s = part[(w0 * T + t) * 2];
+        float bb = part[(w0 * T + t) * 2 + 1];
+        for (int qq = 1; qq < 4; ++qq) {
+          s += part[((w0 + qq) * T + t) * 2];
+          bb += part[((w0 + qq) * T + t) * 2 + 1];
+        }
+        const float l = s + (a.r.router_bias ? a.r.router_bias[ee] : 0.f);
+        a.r.logits[(int64_t)t * E + ee] = l;
+        a.r.err[(int64_t)t * E + ee] = gamma * bb + 1.2e-7f * fabsf(l) + 1e-30f;
+      }
+    }
+    // the last router CTA to arrive runs top-k and the sort
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(a.counter, 1) == a.n_router_ctas - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const RtSmem L = rt_smem_layout(T, E, a.top_k);
+    float* s_lg = reinterpret_cast<float*>(sm + L.logits_off) + warp * E;  // one token row per warp
+    float* s_er = reinterpret_cast<float*>(sm + L.err_off) + warp * E;
+    uint8_t* ch = sm + L.ch_off + warp * E;
+    int* cand = reinterpret_cast<int*>(sm + L.cand_off) + warp * E;
+    df32* l64 = reinterpret_cast<df32*>(sm + L.l64_off) + warp * E;
+    int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
+    for (int t = warp; t < T; t += 8) {
+      for (int e = lane; e < E; e += 32) {
+        s_lg[e] = __ldcg(a.r.logits + (int64_t)t * E + e);
+        s_er[e] = __ldcg(a.r.err + (int64_t)t * E + e);
+      }
+      __syncwarp();
+      dec_topk_token(a, t, lane, s_lg, s_er, ch, cand, l64, s_idx);
+      __syncwarp();
+    }
+    __syncthreads();
+    int* hist = reinterpret_cast<int*>(sm + L.hist_off);
+    int* scan = reinterpret_cast<int*>(sm + L.scan_off);
+    dec_sort(a, s_idx, hist, scan);
+    __syncthreads();
+    dec_split(a, hist, scan);
+    if (tid == 0) *a.counter = 0;  // ready for the next launch
+    return;
+  }
+  if (b < a.n_router_ctas + a.n_shared_ctas) {
+    // ---- shared expert gate_up + SwiGLU: two window indices per CTA, a
+    // quarter of H per warp (warps 0-3 index 2b', warps 4-7 index 2b'+1);
+    // the quarters' partial sums add in a fixed order
+    float* part = reinterpret_cast<float*>(sm);  // [8 warps][T][2]
+    const int i = (b - a.n_router_ctas) * 2 + (warp >> 2);
+    const int q = warp & 3;
+    const int Hq = H / 4, nq = Hq / 8;  // uint4 chunks (8 bf16) of a quarter row
+    if (i < a.s_I_loc) {
+      const uint4* g_row = reinterpret_cast<const uint4*>(a.sh_gate_up + (int64_t)(a.s_row0 + i) * H + q * Hq);
+      const uint4* u_row =
+          reinterpret_cast<const uint4*>(a.sh_gate_up + (int64_t)(a.s_Iw + a.s_row0 + i) * H + q * Hq);
+      for (int t0 = 0; t0 < T; t0 += 8) {
+        float ag[8], au[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) { ag[m] = 0.f; au[m] = 0.f; }
+        for (int g0 = 0; g0 < nq; g0 += 4 * 32) {
+          uint4 gv[4], uv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = g0 + lane + 32 * j;
+            gv[j] = c < nq ? __ldg(g_row + c) : make_uint4(0, 0, 0, 0);
+            uv[j] = c < nq ? __ldg(u_row + c) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = g0 + lane + 32 * j;
+            if (c < nq) {
+              const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+              const uint32_t uw[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
+#pragma unroll
+              for (int m = 0; m < 8; ++m) {
+                if (t0 + m < T) {
+                  const uint4 xv =
+                      __ldg(reinterpret_cast<const uint4*>(a.r.x + (int64_t)(t0 + m) * H + q * Hq) + c);
+                  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                  for (int qq = 0; qq < 4; ++qq) {
+                    const float x0 = __uint_as_float(xw[qq] << 16), x1 = __uint_as_float(xw[qq] & 0xffff0000u);
+                    ag[m] = fmaf(x0, __uint_as_float(gw[qq] << 16), ag[m]);
+                    ag[m] = fmaf(x1, __uint_as_float(gw[qq] & 0xffff0000u), ag[m]);
+                    au[m] = fmaf(x0, __uint_as_float(uw[qq] << 16), au[m]);
+                    au[m] = fmaf(x1, __uint_as_float(uw[qq] & 0xffff0000u), au[m]);
+                  }
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float g = warp_sum(ag[m]), u = warp_sum(au[m]);
+          if (lane == 0 && t0 + m < T) {
+            part[(warp * T + t0 + m) * 2] = g;
+            part[(warp * T + t0 + m) * 2 + 1] = u;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    for (int k2 = tid; k2 < 2 * T; k2 += kRtThreads) {
+      const int ii = k2 / T, t = k2 % T;
+      const int idx = (b - a.n_router_ctas) * 2 + ii;
+      if (idx < a.s_I_loc) {
+        const int w0 = ii * 4;
+        float g = part[(w0 * T + t) * 2], u = part[(w0 * T + t) * 2 + 1];
+        for (int qq = 1; qq < 4; ++qq) {
+          g += part[((w0 + qq) * T + t) * 2];
+          u += part[((w0 + qq) * T + t) * 2 + 1];
+        }
+        const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * u);
+        a.hs[(int64_t)t * a.s_I_loc + idx] = *reinterpret_cast<const uint16_t*>(&hb);
+      }
+    }
+    return;
+  }
+  // ---- x quantisation (global 1.0) and sigma_t = sigmoid(g . x_t)
+  const int nb = H / kBlock;
+  for (int t = warp; t < T; t += 8) {
+    float z = 0.f;
+    for (int bb = lane; bb < nb; bb += 32) {
+      const int64_t blk = (int64_t)t * nb + bb;
+      float v[16];
+      const uint4* p = reinterpret_cast<const uint4*>(a.r.x + blk * kBlock);
+      const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+      const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) {
+        v[2 * qq] = __uint_as_float(words[qq] << 16);
+        v[2 * qq + 1] = __uint_as_float(words[qq] & 0xffff0000u);
+      }
+      if (a.r.sh_gate) {
+        const uint4* gp = reinterpret_cast<const uint4*>(a.r.sh_gate + bb * kBlock);
+        const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          z = fmaf(v[2 * qq], __uint_as_float(gw[qq] << 16), z);
+          z = fmaf(v[2 * qq + 1], __uint_as_float(gw[qq] & 0xffff0000u), z);
+        }
+      }
+      uint8_t c[8];
+      const uint8_t s = quantize_block16(v, 1.0f, c);
+      *reinterpret_cast<uint2*>(a.r.xq_codes + blk * 8) = pack8(c);
+      a.r.xq_scales[blk] = s;
+    }
+    z = warp_sum(z);
+    if (lane == 0) a.r.sigma[t] = a.r.sh_gate ? 1.0f / (1.0f + expf(-z)) : 0.f;
+  }
+}
+
+}  // namespace ftmoe

@@ -133,6 +133,8 @@ struct ftmoe_handle {
   float* stack_y = nullptr;
   uint16_t* stack_x[2] = {nullptr, nullptr};
   uint32_t* status = nullptr;
+  int* counter = nullptr;  // arrival counter of the decode routing kernel
+  int* gu_split = nullptr;  // decode gate_up work split, one entry per SM + 1
   uint32_t last_status = 0;
   EventProfiler* prof = nullptr;  // non-null while per-kernel timing is enabled
 };
@@ -247,10 +249,13 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
       {(void**)&h->r.perm, P * 4},           {(void**)&h->r.inv, P * 4},
       {(void**)&h->r.touched, (int64_t)c.E * 4}, {(void**)&h->r.n_touched, 16},
       {(void**)&h->hs, T * (c.I_shared > 0 ? c.I_shared : 16) * 2},
-      {(void**)&h->hq_codes, P * c.I / 2},   {(void**)&h->hq_scales, P * c.I / 16},
+      // intermediate rows padded to 16 bytes (the decode path copies them in bulk)
+      {(void**)&h->hq_codes, P * align_up(c.I * 2, 16)}, {(void**)&h->hq_scales, P * align_up(c.I / 16 * 4, 16)},
       {(void**)&h->Y, P * c.H * 4},          {(void**)&h->S, T * c.H * 4},
       {(void**)&h->stack_y, T * c.H * 4},    {(void**)&h->stack_x[0], T * c.H * 2},
       {(void**)&h->stack_x[1], T * c.H * 2}, {(void**)&h->status, 16},
+      {(void**)&h->counter, 16},             {(void**)&h->r.n_rerank, 16},
+      {(void**)&h->gu_split, (int64_t)(prop.multiProcessorCount + 1) * 4},
   };
   int64_t total = 0;
   for (auto& p : parts) total += align_up(p.bytes, 256);
@@ -268,6 +273,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
   cudaError_t e = cudaMemset(h->ws, 0, total);
   if (e == cudaSuccess) e = route_set_smem_limits(c.H, c.E);
   if (e == cudaSuccess) e = experts_set_smem_limits(c.H, c.I > c.I_shared ? c.I : c.I_shared);
+  if (e == cudaSuccess) e = decode_set_smem_limits();
   if (e != cudaSuccess) {
     cuda_fail(e, "create");
     cudaFree(h->ws);
@@ -377,9 +383,7 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
   r.E = c.E;
   r.top_k = c.top_k;
   r.norm_topk_prob = c.norm_topk_prob;
-  CK(launch_route(r, s));
   ExpertArgs a{};
-  a.r = r;
   a.rec = L.rec_dev;
   a.lay = L.lay;
   a.win.row0 = i0 - L.li0;
@@ -405,7 +409,38 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
   a.out = out;
   a.out_flags = out_flags;
   a.num_sms = h->num_sms;
-  CK(launch_experts(a, s));
+  if (decode_supported(c.H, c.E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T, c.top_k)) {
+    // decode sizes: routing, streamed gate_up, fused down + combine
+    DecodeArgs d{};
+    d.r = r;
+    d.rec = a.rec;
+    d.lay = a.lay;
+    d.win = a.win;
+    d.H = c.H;
+    d.T = T;
+    d.top_k = c.top_k;
+    d.sh_gate_up = a.sh_gate_up;
+    d.sh_down = a.sh_down;
+    d.s_row0 = a.s_row0;
+    d.s_I_loc = a.s_I_loc;
+    d.s_Iw = a.s_Iw;
+    d.hs = h->hs;
+    d.hq_codes = h->hq_codes;
+    d.hq_scales = h->hq_scales;
+    d.hq_cpitch = decode_hq_cpitch(I_loc);
+    d.hq_spitch = decode_hq_spitch(I_loc);
+    d.out = out;
+    d.out_flags = out_flags;
+    d.counter = h->counter;
+    d.gu_split = h->gu_split;
+    d.num_sms = h->num_sms;
+    d.pdl = 1;
+    CK(launch_decode(d, s));
+  } else {
+    CK(launch_route(r, s));
+    a.r = r;
+    CK(launch_experts(a, s));
+  }
   if (aux) {
     const int64_t P = (int64_t)T * c.top_k;
     if (aux->topk_idx) CK(cudaMemcpyAsync(aux->topk_idx, r.topk_idx, P * 4, cudaMemcpyDeviceToDevice, s));
@@ -485,6 +520,9 @@ int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out) {
   out->resident_slots = h->cfg.E;
   out->residency = 1.0;
   out->device_status = (int32_t)h->last_status;
+  unsigned long long nr = 0;
+  CK(cudaMemcpy(&nr, h->r.n_rerank, 8, cudaMemcpyDeviceToHost));
+  out->reranked_tokens = (int64_t)nr;
   return FTMOE_OK;
 }
 

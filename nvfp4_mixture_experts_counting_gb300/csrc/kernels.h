@@ -58,6 +58,7 @@ struct RouteArgs {
   int32_t* inv;      // [P]
   int32_t* touched;  // [E] touched experts, increasing
   int32_t* n_touched;  // [1]
+  unsigned long long* n_rerank;  // [1] cumulative count of fp64 re-ranked tokens (may be null)
   uint32_t* status;
 };
 
@@ -91,6 +92,40 @@ struct ExpertArgs {
 };
 
 cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s);
+
+// Decode path (T <= 32): routing kernel, streamed gate_up, fused down+combine.
+struct DecodeArgs {
+  RouteArgs r;
+  const uint8_t* const* rec;  // [E] device pointers to expert records
+  RecLayout lay;
+  Window win;
+  int H, T, top_k;
+  const uint16_t* sh_gate_up;  // null => no shared expert
+  const uint16_t* sh_down;
+  int s_row0, s_I_loc, s_Iw;
+  uint16_t* hs;        // [T][s_I_loc] bf16
+  // The quantised SwiGLU output, stored decoded: each E2M1 code as its half
+  // value ([P][I_loc] half, pitch hq_cpitch bytes) and each block's E4M3
+  // scale as fp32 ([P][I_loc/16], pitch hq_spitch bytes); pitches are
+  // multiples of 16 bytes.
+  uint8_t* hq_codes;
+  uint8_t* hq_scales;
+  int hq_cpitch, hq_spitch;
+  void* out;
+  int out_flags;
+  int* counter;        // arrival counter of the router CTAs (zero between launches)
+  int* gu_split;       // [num_sms + 1] first gate_up work item of each CTA (cost-balanced)
+  int n_router_ctas, n_shared_ctas;
+  int num_sms;
+  int pdl;             // chain the kernels with programmatic dependent launch
+};
+
+int decode_hq_cpitch(int I_loc);
+int decode_hq_spitch(int I_loc);
+bool decode_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, int s_Iw, int s_row0, int T,
+                      int top_k);
+cudaError_t decode_set_smem_limits();
+cudaError_t launch_decode(DecodeArgs a, cudaStream_t s);
 
 // y fp32 [T][H] -> bf16(y / sqrt(mean(y^2) + eps)) [T][H]
 cudaError_t launch_rms_renorm(const float* y, uint16_t* x, int T, int H, cudaStream_t s);

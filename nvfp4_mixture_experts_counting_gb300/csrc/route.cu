@@ -1,5 +1,5 @@
 // Routing kernels: activation quantisation + shared gate, router logits with
-// a certified error bound, top-k with fp64 re-ranking of uncertain
+// a certified error bound, top-k with compensated re-ranking of uncertain
 // candidates, and the counting-sort permutation.
 //
 // Pages: PR #385 "feat(qwen4_exp): tensor parallelism for Qwen3.8-Flash-Next
@@ -182,24 +182,9 @@ constexpr int kTopkWarps = 8;
 __device__ __forceinline__ bool before(float la, int ea, float lb, int eb) {
   return la > lb || (la == lb && ea < eb);
 }
-__device__ __forceinline__ bool before_d(double la, int ea, double lb, int eb) {
-  return la > lb || (la == lb && ea < eb);
-}
-
-// fp64 logit of (t, e): exact products, fp64 sum (lanes stride h), + bias.
-__device__ double logit_fp64(const RouteArgs& a, int t, int e, int lane) {
-  const uint16_t* x = a.x + (int64_t)t * a.H;
-  const float* w = a.router_w + (int64_t)e * a.H;
-  double s = 0.0;
-  for (int h = lane; h < a.H; h += 32)
-    s = fma((double)bf16_bits_to_float(x[h]), (double)w[h], s);
-  s = warp_sum_d(s);
-  if (a.router_bias) s += (double)a.router_bias[e];
-  return s;
-}
-
 // One warp per token.  Select the k best by fp32 logit; certify the set and
-// its order with the error bounds; if not certified, recompute fp64 logits
+// its order with the error bounds; if not certified, recompute compensated
+// double-fp32 logits (about 2^-48 relative; FP64 is far slower on this GPU)
 // for every expert that could belong to the top-k and select among those.
 __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
@@ -207,7 +192,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* lw = reinterpret_cast<float*>(sm) + warp * E;                // working logits
   int* cand = reinterpret_cast<int*>(sm) + kTopkWarps * E + warp * E;  // candidate list
-  double* l64 = reinterpret_cast<double*>(sm + (size_t)kTopkWarps * E * 8) + warp * E;
+  df32* l64 = reinterpret_cast<df32*>(sm + (size_t)kTopkWarps * E * 8) + warp * E;
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= a.T) return;
   const float* lg = a.logits + (int64_t)t * E;
@@ -249,8 +234,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
     if (lw[e] != -INFINITY && lg[e] + er[e] >= lmin_lo) reach = true;
   if (__any_sync(0xffffffffu, reach)) certified = false;
 
-  double w64[32];
+  float w64[32];
   if (!certified) {
+    if (lane == 0 && a.n_rerank) atomicAdd(a.n_rerank, 1ull);  // telemetry only
     // candidates: the chosen plus every unchosen expert that may outrank one
     int nc = 0;
     for (int base = 0; base < E; base += 32) {
@@ -262,34 +248,38 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
       nc += __popc(m);
     }
     __syncwarp();
+    const uint16_t* xrow = a.x + (int64_t)t * a.H;
     for (int c = 0; c < nc; ++c) {
-      double v = logit_fp64(a, t, cand[c], lane);
+      const int e = cand[c];
+      const df32 v = logit_df32(xrow, a.router_w + (int64_t)e * a.H, a.H,
+                                a.router_bias ? a.router_bias[e] : 0.f, lane);
       if (lane == 0) l64[c] = v;
     }
     __syncwarp();
-    // select k among the candidates by (fp64 logit desc, index asc)
+    // select k among the candidates by (compensated logit desc, index asc)
+    const df32 none = {-INFINITY, 0.f};
     for (int j = 0; j < k; ++j) {
-      double bl = -INFINITY;
+      df32 bl = none;
       int be = 0x7fffffff, bc = -1;
       for (int c = lane; c < nc; c += 32) {
-        double v = l64[c];
-        int e = cand[c];
-        if (v != -INFINITY && before_d(v, e, bl, be)) { bl = v; be = e; bc = c; }
+        const df32 v = l64[c];
+        const int e = cand[c];
+        if (v.hi != -INFINITY && df_before(v, e, bl, be)) { bl = v; be = e; bc = c; }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        double ol = __shfl_xor_sync(0xffffffffu, bl, o);
-        int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-        if (before_d(ol, oe, bl, be)) { bl = ol; be = oe; bc = oc; }
+        const df32 ol = {__shfl_xor_sync(0xffffffffu, bl.hi, o), __shfl_xor_sync(0xffffffffu, bl.lo, o)};
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        if (df_before(ol, oe, bl, be)) { bl = ol; be = oe; bc = oc; }
       }
       chosen[j] = be;
-      w64[j] = bl;
+      w64[j] = bl.hi;
       __syncwarp();
-      if (lane == 0) l64[bc] = -INFINITY;
+      if (lane == 0) l64[bc] = none;
       __syncwarp();
     }
-    lmax = (float)w64[0];
+    lmax = w64[0];
   }
   // routing weights
   float wt[32];

@@ -56,7 +56,8 @@ class Aux(C.Structure):
 class Stats(C.Structure):
     _fields_ = [("touched_experts", C.c_int32), ("resident_slots", C.c_int32),
                 ("touched_bytes", C.c_int64), ("hits", C.c_int64), ("misses", C.c_int64),
-                ("h2d_bytes", C.c_int64), ("residency", C.c_double), ("device_status", C.c_int32)]
+                ("h2d_bytes", C.c_int64), ("residency", C.c_double), ("device_status", C.c_int32),
+                ("reranked_tokens", C.c_int64)]
 
 
 class KernelTime(C.Structure):

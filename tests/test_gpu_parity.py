@@ -73,7 +73,7 @@ def tiny():
     return wl, bank, layer
 
 
-@pytest.mark.parametrize("T", [4, 1, 3, 37, 64])
+@pytest.mark.parametrize("T", [4, 1, 3, 32, 33, 37, 64])
 def test_tiny_layer_matches_oracle(tiny, T):
     wl, bank, layer = tiny
     x = W.hidden(wl, T, device=DEV)
@@ -222,7 +222,7 @@ def decode():
     return wl, bank, layer
 
 
-@pytest.mark.parametrize("T", [1, 8, 16])
+@pytest.mark.parametrize("T", [1, 8, 16, 32, 40])
 def test_decode_layer_matches_oracle(decode, T):
     wl, bank, layer = decode
     x = W.hidden(wl, T, device=DEV)
