@@ -381,38 +381,38 @@ cudaError_t experts_set_smem_limits(int H, int I) {
   return cudaFuncSetAttribute(k_shared_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kMT * Ism * 4);
 }
 
-cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s) {
+cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s, int parts) {
   cudaError_t err;
   const int grid = a.num_sms * 4;
-  if (a.sh_gate_up) {
+  if ((parts & kPartSharedGateUp) && a.sh_gate_up) {
     dim3 g1((a.s_I_loc + 7) / 8, (a.T + kMT - 1) / kMT);
     FTMOE_PROF_BEGIN("k_shared_gate_up", s);
     k_shared_gate_up<<<g1, 256, (size_t)kMT * a.H * 2, s>>>(a);
     FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  {
+  if (parts & kPartRouted) {
     const size_t smem = (size_t)kMT * (a.H / 2) * 4 + kMT * (a.H / kBlock) * 4 + kMT * 32 * 4;
     FTMOE_PROF_BEGIN("k_gate_up", s);
     k_gate_up<<<grid, 256, smem, s>>>(a);
     FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  {
+  if (parts & kPartRouted) {
     const size_t smem = (size_t)kMT * (a.win.I_loc / 2) * 4 + kMT * (a.win.I_loc / kBlock) * 4;
     FTMOE_PROF_BEGIN("k_down", s);
     k_down<<<grid, 256, smem, s>>>(a);
     FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  if (a.sh_gate_up) {
+  if ((parts & kPartTail) && a.sh_gate_up) {
     dim3 g2((a.H + 31) / 32, (a.T + kMT - 1) / kMT);
     FTMOE_PROF_BEGIN("k_shared_down", s);
     k_shared_down<<<g2, 256, (size_t)kMT * a.s_I_loc * 4, s>>>(a);
     FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  {
+  if (parts & kPartTail) {
     const int64_t n = (int64_t)a.T * a.H;
     int64_t nblk = (n + 255) / 256;
     if (nblk > (int64_t)a.num_sms * 16) nblk = (int64_t)a.num_sms * 16;

@@ -135,6 +135,14 @@ struct ftmoe_handle {
   uint32_t* status = nullptr;
   int* counter = nullptr;  // arrival counter of the decode routing kernel
   int* gu_split = nullptr;  // decode gate_up work split, one entry per SM + 1
+  // prefill (tensor-core) path buffers, present when the shapes allow it
+  int64_t pf_pad_max = 0;
+  int32_t* pf_pad_off = nullptr;
+  uint8_t* pf_xg = nullptr;
+  uint8_t* pf_xg_sf = nullptr;
+  uint8_t* pf_hq = nullptr;
+  uint8_t* pf_hq_sf = nullptr;
+  bool pf_enabled = false;
   uint32_t last_status = 0;
   EventProfiler* prof = nullptr;  // non-null while per-kernel timing is enabled
 };
@@ -149,6 +157,11 @@ RecLayout make_rec_layout(int H, int Iw) {
   L.dn_scales = o; o = align_up(o + (int64_t)H * (Iw / 16), 256);
   L.gu_global = o; o = align_up(o + (int64_t)2 * Iw * 4, 256);
   L.dn_global = o; o = align_up(o + (int64_t)H * 4, 256);
+  if (H % 256 == 0 && Iw % 64 == 0) {
+    L.gu_sf_bytes = (int64_t)2 * Iw * (H / 16);
+    L.gu_sf = o; o = align_up(o + L.gu_sf_bytes, 256);
+    L.dn_sf = o; o = align_up(o + (int64_t)H * (Iw / 16), 256);
+  }
   L.bytes = o;
   return L;
 }
@@ -257,6 +270,18 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
       {(void**)&h->counter, 16},             {(void**)&h->r.n_rerank, 16},
       {(void**)&h->gu_split, (int64_t)(prop.multiProcessorCount + 1) * 4},
   };
+  // tensor-core prefill buffers (padded pair order), for shapes it accepts
+  const char* no_tc = getenv("FTMOE_NO_TC");
+  if (c.max_tokens > 32 && c.H % 256 == 0 && c.I % 64 == 0 && c.E <= 1024 && !(no_tc && no_tc[0] == '1')) {
+    h->pf_enabled = true;
+    h->pf_pad_max = pf_pad_max(P, c.E);
+    const int64_t R = h->pf_pad_max;
+    parts.push_back({(void**)&h->pf_pad_off, (int64_t)(c.E + 1) * 4});
+    parts.push_back({(void**)&h->pf_xg, R * c.H / 2});
+    parts.push_back({(void**)&h->pf_xg_sf, R * c.H / 16});
+    parts.push_back({(void**)&h->pf_hq, R * align_up(c.I / 2, 16)});
+    parts.push_back({(void**)&h->pf_hq_sf, R * (c.I / 16)});
+  }
   int64_t total = 0;
   for (auto& p : parts) total += align_up(p.bytes, 256);
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
@@ -274,6 +299,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
   if (e == cudaSuccess) e = route_set_smem_limits(c.H, c.E);
   if (e == cudaSuccess) e = experts_set_smem_limits(c.H, c.I > c.I_shared ? c.I : c.I_shared);
   if (e == cudaSuccess) e = decode_set_smem_limits();
+  if (e == cudaSuccess) e = prefill_set_smem_limits();
   if (e != cudaSuccess) {
     cuda_fail(e, "create");
     cudaFree(h->ws);
@@ -344,6 +370,7 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0
                          I / 16, Iw / 16, H, K, s));
     CK(cudaMemcpyAsync(rec + L.lay.dn_global, d->dn_global + (int64_t)e * H, H * 4, K, s));
   }
+  CK(launch_repack_sf(L.bank, L.lay, H, Iw, E, s));
   std::vector<uint8_t*> ptrs(E);
   for (int e = 0; e < E; ++e) ptrs[e] = L.bank + L.lay.bytes * e;
   CK(cudaMemcpyAsync(L.rec_dev, ptrs.data(), E * sizeof(void*), cudaMemcpyHostToDevice, s));
@@ -436,6 +463,37 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     d.num_sms = h->num_sms;
     d.pdl = 1;
     CK(launch_decode(d, s));
+  } else if (h->pf_enabled && T > 32 && L.lay.gu_sf_bytes &&
+             prefill_supported(c.H, c.E, I_loc, L.lIw, a.win.row0)) {
+    // prefill sizes: routing, then the routed GEMMs on the tensor cores
+    CK(launch_route(r, s));
+    a.r = r;
+    CK(launch_experts(a, s, kPartSharedGateUp));
+    PfArgs p{};
+    p.offsets = r.offsets;
+    p.perm = r.perm;
+    p.xq_codes = r.xq_codes;
+    p.xq_scales = r.xq_scales;
+    p.bank = L.bank;
+    p.lay = L.lay;
+    p.win = a.win;
+    p.H = c.H;
+    p.T = T;
+    p.E = c.E;
+    p.top_k = c.top_k;
+    p.P_pad_max = (int)h->pf_pad_max;
+    p.pad_off = h->pf_pad_off;
+    p.xg = h->pf_xg;
+    p.xg_sf = h->pf_xg_sf;
+    p.hq = h->pf_hq;
+    p.hq_sf = h->pf_hq_sf;
+    p.hq_pitch = (int)align_up(I_loc / 2, 16);
+    p.Y = h->Y;
+    p.status = h->status;
+    PfMaps maps;
+    CK(prefill_make_maps(p, &maps));
+    CK(launch_prefill_routed(p, maps, h->num_sms, s));
+    CK(launch_experts(a, s, kPartTail));
   } else {
     CK(launch_route(r, s));
     a.r = r;

@@ -1,6 +1,7 @@
 // Host-side declarations of the ftmoe kernel launchers (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,6 +29,12 @@ extern thread_local Profiler* g_prof;
 struct RecLayout {
   int64_t gu_codes, gu_scales, gu_global;  // [2Iw][H/2], [2Iw][H/16], [2Iw] fp32
   int64_t dn_codes, dn_scales, dn_global;  // [H][Iw/2], [H][Iw/16], [H] fp32
+  // The same scales in 512-byte blocks for the tensor-core path (present
+  // when H % 256 == 0 and Iw % 64 == 0, else gu_sf_bytes == 0):
+  //   gu_sf [Iw/64][H/64][512]: tile j = gate rows [64j, 64j+64) then the
+  //                             matching up rows, 64-element K steps
+  //   dn_sf [H/128][Iw/64][512]: tile j = rows [128j, 128j+128)
+  int64_t gu_sf, dn_sf, gu_sf_bytes;
   int64_t bytes;                           // record size (multiple of 256)
 };
 RecLayout make_rec_layout(int H, int Iw);
@@ -91,7 +98,10 @@ struct ExpertArgs {
   int num_sms;
 };
 
-cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s);
+// Parts of the any-T expert stage: shared gate_up; routed gate_up + down on
+// CUDA cores; shared down + combine.
+constexpr int kPartSharedGateUp = 1, kPartRouted = 2, kPartTail = 4, kPartAll = 7;
+cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s, int parts = kPartAll);
 
 // Decode path (T <= 32): routing kernel, streamed gate_up, fused down+combine.
 struct DecodeArgs {
@@ -126,6 +136,39 @@ bool decode_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, in
                       int top_k);
 cudaError_t decode_set_smem_limits();
 cudaError_t launch_decode(DecodeArgs a, cudaStream_t s);
+
+// Prefill path: grouped block-scaled NVFP4 GEMMs on tcgen05 (prefill.cu).
+// Pairs are regrouped in a padded order where expert e owns rows
+// [pad_off[e], pad_off[e] + round128(m_e)).
+struct PfArgs {
+  const int32_t* offsets;     // [E+1] sorted-position starts
+  const int32_t* perm;        // [P]
+  const uint8_t* xq_codes;    // [T][H/2]
+  const uint8_t* xq_scales;   // [T][H/16]
+  const uint8_t* bank;        // expert records, lay.bytes apart
+  RecLayout lay;
+  Window win;
+  int H, T, E, top_k;
+  int P_pad_max;              // rows of the padded buffers (multiple of 128)
+  int32_t* pad_off;           // [E+1]
+  uint8_t* xg;                // [P_pad_max][H/2] activation codes, padded order
+  uint8_t* xg_sf;             // [P_pad_max/128][H/64][512] activation scale blocks
+  uint8_t* hq;                // [P_pad_max][hq_pitch] intermediate codes (I_loc/2 used)
+  uint8_t* hq_sf;             // [P_pad_max/128][I_loc/64][512]
+  int hq_pitch;
+  float* Y;                   // [P][H] fp32, rows in sorted order
+  uint32_t* status;
+};
+struct PfMaps {
+  CUtensorMap xg, gu, hq, dn;
+};
+
+int64_t pf_pad_max(int64_t P, int E);
+bool prefill_supported(int H, int E, int I_loc, int Iw, int row0);
+cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m);
+cudaError_t prefill_set_smem_limits();
+cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw, int E, cudaStream_t s);
+cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
 
 // y fp32 [T][H] -> bf16(y / sqrt(mean(y^2) + eps)) [T][H]
 cudaError_t launch_rms_renorm(const float* y, uint16_t* x, int T, int H, cudaStream_t s);

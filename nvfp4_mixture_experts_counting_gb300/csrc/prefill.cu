@@ -1,0 +1,460 @@
+// Prefill path: routed gate_up and down as grouped block-scaled NVFP4 GEMMs
+// on the fifth-generation tensor cores.
+//
+// For every touched expert e with m_e pairs (sorted positions
+// [off_e, off_e + m_e)), the pairs are laid out in a padded order: expert e
+// owns rows [pad_e, pad_e + round128(m_e)), so each 128-row tile belongs to
+// one expert.
+//   gate_up: G[pair][r] = sum_k xq[pair][k] * W_gu[r][k] over r in 64 gate
+//            rows and the matching 64 up rows of the window (Issue #62
+//            "Offloaded MoE ignores tensor parallelism ...", "What it
+//            touches": gate and up rows split as two disjoint row ranges);
+//            the epilogue applies the row globals, SwiGLU and the NVFP4
+//            quantisation of the intermediate (global 1.0).
+//   down:    Y[pair][h] = sum_k hq[pair][k] * W_dn[h][window k] over the
+//            window's columns, times the down row global.
+// Both are D = A * B^T with the pairs as the 128-row A operand and 128
+// weight rows as B: E2M1 codes in shared memory (TMA, 128-byte swizzle),
+// E4M3 16-block scales copied into TMEM, fp32 accumulators in TMEM.  The
+// products of E2M1 values are exact; scaling and accumulation are fp32.
+//
+// Kernel roles (one persistent CTA per SM): warp 0 issues TMA, warp 1 owns
+// TMEM and issues the MMAs, warps 2-5 drain the accumulators.  Two TMEM
+// accumulators let the epilogue of one tile run under the next tile's MMAs.
+// Every mbarrier wait is bounded; a wait that runs out stops every role,
+// drains what is in flight and frees TMEM.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace ftmoe {
+
+namespace {
+
+constexpr int kPfStages = 5;
+constexpr int kPfThreads = 192;
+constexpr int kTile = 16384;        // one 128 x 128-byte operand tile
+constexpr int kSfStage = 2048;      // four 512-byte scale blocks
+constexpr int kPfOffA = 0;
+constexpr int kPfOffB = kPfStages * kTile;
+constexpr int kPfOffSfa = 2 * kPfStages * kTile;
+constexpr int kPfOffSfb = kPfOffSfa + kPfStages * kSfStage;
+constexpr int kPfOffBar = kPfOffSfb + kPfStages * kSfStage;
+constexpr int kPfOffTab = kPfOffBar + 256;
+constexpr int kPfMaxE = 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256;   // scale-factor columns start after the two accumulators
+
+__host__ __device__ inline int pf_smem_bytes(int E) { return 1024 + kPfOffTab + 3 * 4 * (E + 1); }
+
+// Exclusive scan over n values val(i) by one warp: out[i] = sum_{j<i} val(j),
+// out[n] = the total.
+template <class F>
+__device__ void warp_excl_scan(int n, F val, int* out) {
+  const int lane = threadIdx.x & 31;
+  const int c = (n + 31) / 32, i0 = lane * c, i1 = min(n, i0 + c);
+  int s = 0;
+  for (int i = i0; i < i1; ++i) s += val(i);
+  int inc = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  int run = inc - s;
+  for (int i = i0; i < i1; ++i) {
+    out[i] = run;
+    run += val(i);
+  }
+  if (lane == 31) out[n] = inc;
+}
+
+// Largest index i in [0, n] with tab[i] <= v (tab non-decreasing, tab[0] <= v).
+__device__ __forceinline__ int find_le(const int* tab, int n, int v) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tab[mid] <= v) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Byte offset of row r's 4 scale bytes inside a 512-byte scale block of 128
+// rows: rows r, r+32, r+64, r+96 share a 16-byte line (the order tcgen05.cp
+// .32x128b.warpx4 places into TMEM lanes r % 32, columns r / 32).
+__host__ __device__ constexpr int sf_slot(int r) { return (r & 31) * 16 + ((r & 127) >> 5) * 4; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ weight scale repack
+
+// Row-major weight scales -> 512-byte blocks for the MMA, per expert:
+//   gate_up: tile j = window gate rows [64j, 64j+64) then the matching up
+//            rows; blocks [tile][H/64]
+//   down:    tile j = rows [128j, 128j+128); blocks [tile][Iw/64]
+__global__ void k_repack_sf(uint8_t* bank, RecLayout lay, int H, int Iw, int E) {
+  const int gtiles = Iw / 64, gks = H / 64, dtiles = H / 128, dks = Iw / 64;
+  const int64_t n_gu = (int64_t)gtiles * gks * 128, n_dn = (int64_t)dtiles * dks * 128;
+  const int64_t per = n_gu + n_dn, total = per * E;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / per);
+    int64_t k = i % per;
+    uint8_t* rec = bank + lay.bytes * e;
+    if (k < n_gu) {
+      const int n = (int)(k % 128), ks = (int)((k / 128) % gks), j = (int)(k / (128 * gks));
+      const int row = n < 64 ? 64 * j + n : Iw + 64 * j + (n - 64);
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + lay.gu_scales + (int64_t)row * (H / 16) + 4 * ks);
+      *reinterpret_cast<uint32_t*>(rec + lay.gu_sf + ((int64_t)j * gks + ks) * 512 + sf_slot(n)) = w;
+    } else {
+      k -= n_gu;
+      const int n = (int)(k % 128), ks = (int)((k / 128) % dks), j = (int)(k / (128 * dks));
+      const int row = 128 * j + n;
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + lay.dn_scales + (int64_t)row * (Iw / 16) + 4 * ks);
+      *reinterpret_cast<uint32_t*>(rec + lay.dn_sf + ((int64_t)j * dks + ks) * 512 + sf_slot(n)) = w;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ prep
+
+// Padded group starts, and every padded row's activation codes and scale
+// blocks in padded order (padding rows get zero scales).
+__global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
+  __shared__ int s_off[kPfMaxE + 1], s_pad[kPfMaxE + 1];
+  const int E = a.E, H = a.H;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = a.offsets[e];
+  __syncthreads();
+  if (threadIdx.x < 32) warp_excl_scan(E, [&](int e) { return (s_off[e + 1] - s_off[e] + 127) & ~127; }, s_pad);
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) a.pad_off[e] = s_pad[e];
+  const int total = s_pad[E], hc = H / 2, nks = H / 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int pp = blockIdx.x * nw + warp; pp < total; pp += gridDim.x * nw) {
+    const int e = find_le(s_pad, E, pp);
+    const int local = pp - s_pad[e], m = s_off[e + 1] - s_off[e];
+    uint8_t* sfrow = a.xg_sf + (int64_t)(pp >> 7) * nks * 512 + sf_slot(pp);
+    if (local < m) {
+      const int t = a.perm[s_off[e] + local] / a.top_k;
+      const uint4* src = reinterpret_cast<const uint4*>(a.xq_codes + (int64_t)t * hc);
+      uint4* dst = reinterpret_cast<uint4*>(a.xg + (int64_t)pp * hc);
+      for (int i = lane; i < hc / 16; i += 32) dst[i] = src[i];
+      const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.xq_scales + (int64_t)t * (H / 16));
+      for (int ks = lane; ks < nks; ks += 32) *reinterpret_cast<uint32_t*>(sfrow + (int64_t)ks * 512) = ssrc[ks];
+    } else {
+      for (int ks = lane; ks < nks; ks += 32) *reinterpret_cast<uint32_t*>(sfrow + (int64_t)ks * 512) = 0u;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ grouped GEMM
+
+// MODE 0: gate_up + SwiGLU + quantisation.  MODE 1: down -> Y.
+template <int MODE>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    k_pf_mma(const __grid_constant__ PfArgs a, const __grid_constant__ CUtensorMap mapA,
+             const __grid_constant__ CUtensorMap mapB) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPfOffBar);
+  uint64_t* empty = full + kPfStages;
+  uint64_t* acc_full = empty + kPfStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(sm + kPfOffTab);
+  const int E = a.E, H = a.H;
+  int* s_pad = s_off + (E + 1);
+  int* s_up = s_pad + (E + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int I_loc = a.win.I_loc, row0 = a.win.row0, Iw = a.win.Iw;
+  const int J = MODE == 0 ? I_loc / 64 : H / 128;          // weight tiles per pair tile
+  const int nks_all = MODE == 0 ? H / 64 : I_loc / 64;     // 64-element K steps
+  const int nkt = (nks_all + 3) / 4;                        // 256-element K tiles
+
+  if (tid == 0) {
+    for (int s = 0; s < kPfStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 4); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  for (int e = tid; e <= E; e += kPfThreads) {
+    s_off[e] = a.offsets[e];
+    s_pad[e] = a.pad_off[e];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) warp_excl_scan(E, [&](int e) { return ((s_pad[e + 1] - s_pad[e]) >> 7) * J; }, s_up);
+  __syncthreads();
+  const uint32_t tmem = *tmem_slot;
+  const int n_units = s_up[E];
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int k = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+        const int e = find_le(s_up, E, u), r = u - s_up[e];
+        const int nt = r / J, j = r % J;
+        const int pp0 = s_pad[e] + nt * 128;
+        const uint8_t* rec = a.bank + a.lay.bytes * e;
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kPfStages;
+          if (k >= kPfStages && !mbar_wait(&empty[s], ((k / kPfStages) - 1) & 1, a.status)) {
+            *abort_flag = 1;
+            break;
+          }
+          const int nks = min(4, nks_all - 4 * kt);
+          unsigned char* sa = sm + kPfOffA + s * kTile;
+          unsigned char* sb = sm + kPfOffB + s * kTile;
+          unsigned char* sfa = sm + kPfOffSfa + s * kSfStage;
+          unsigned char* sfb = sm + kPfOffSfb + s * kSfStage;
+          mbar_arrive_expect_tx(&full[s], 2 * kTile + 2 * nks * 512);
+          if (MODE == 0) {
+            tma_load_2d(sa, &mapA, kt * 128, pp0, &full[s]);
+            tma_load_3d(sb, &mapB, kt * 128, row0 + 64 * j, e, &full[s]);
+            tma_load_3d(sb + kTile / 2, &mapB, kt * 128, Iw + row0 + 64 * j, e, &full[s]);
+            bulk_g2s(sfa, a.xg_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
+            bulk_g2s(sfb, rec + a.lay.gu_sf + ((int64_t)(row0 / 64 + j) * nks_all + 4 * kt) * 512, nks * 512,
+                     &full[s]);
+          } else {
+            tma_load_2d(sa, &mapA, kt * 128, pp0, &full[s]);
+            tma_load_3d(sb, &mapB, row0 / 2 + kt * 128, 128 * j, e, &full[s]);
+            bulk_g2s(sfa, a.hq_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
+            bulk_g2s(sfb, rec + a.lay.dn_sf + ((int64_t)j * (Iw / 64) + row0 / 64 + 4 * kt) * 512, nks * 512,
+                     &full[s]);
+          }
+        }
+      }
+      // nothing may still be landing when the CTA exits
+      for (int q = k - kPfStages > 0 ? k - kPfStages : 0; q < k; ++q)
+        mbar_wait(&full[q % kPfStages], (q / kPfStages) & 1, a.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_nvf4(128, 128);
+      int k = 0, ui = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
+        const int buf = ui & 1;
+        if (ui >= 2 && !mbar_wait(&acc_empty[buf], ((ui >> 1) - 1) & 1, a.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * 128;
+        bool ok = true;
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kPfStages;
+          if (!mbar_wait(&full[s], (k / kPfStages) & 1, a.status)) { *abort_flag = 1; ok = false; break; }
+          tc_fence_after();
+          const int nks = min(4, nks_all - 4 * kt);
+          const uint32_t sfa_col = tmem + kSfCol0 + s * 32, sfb_col = sfa_col + 16;
+          const uint32_t sfa_smem = smem_u32(sm + kPfOffSfa + s * kSfStage);
+          const uint32_t sfb_smem = smem_u32(sm + kPfOffSfb + s * kSfStage);
+          for (int ks = 0; ks < nks; ++ks) {
+            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
+            tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sfb_smem + 512 * ks));
+          }
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + kPfOffA + s * kTile));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + kPfOffB + s * kTile));
+          for (int ks = 0; ks < nks; ++ks)
+            tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, idesc, sfa_col + 4 * ks, sfb_col + 4 * ks,
+                        (kt | ks) != 0);
+          tc_commit(&empty[s]);  // stage free once these MMAs have read it
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+      }
+      // every MMA and scale copy this thread issued has completed before
+      // TMEM is released
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.status);
+    }
+  } else {
+    // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ...
+    const int q = warp & 3;
+    int ui = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
+      const int buf = ui & 1;
+      if (!mbar_wait(&acc_full[buf], (ui >> 1) & 1, a.status)) { *abort_flag = 1; break; }
+      tc_fence_after();
+      const int e = find_le(s_up, E, u), r = u - s_up[e];
+      const int nt = r / J, j = r % J;
+      const int pp0 = s_pad[e] + nt * 128;
+      const int local = nt * 128 + 32 * q + lane;
+      const bool valid = local < s_off[e + 1] - s_off[e];
+      const uint8_t* rec = a.bank + a.lay.bytes * e;
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 128;
+      if (MODE == 0) {
+        const float* gglob = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * j;
+        const float* uglob = gglob + Iw;
+        const int pp = pp0 + 32 * q + lane;
+        uint32_t sfw = 0;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          uint32_t g[16], v[16];
+          tc_ld16(taddr + 16 * b, g);
+          tc_ld16(taddr + 64 + 16 * b, v);
+          tc_wait16x2(g, v);
+          float h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float gg = __ldg(gglob + 16 * b + i), ug = __ldg(uglob + 16 * b + i);
+            h[i] = silu(__uint_as_float(g[i]) * gg) * (__uint_as_float(v[i]) * ug);
+          }
+          uint8_t codes[8];
+          const uint8_t sc = quantize_block16(h, 1.0f, codes);
+          sfw |= (uint32_t)sc << (8 * b);
+          if (valid) {
+            uint2 pk;
+            pk.x = codes[0] | (codes[1] << 8) | (codes[2] << 16) | ((uint32_t)codes[3] << 24);
+            pk.y = codes[4] | (codes[5] << 8) | (codes[6] << 16) | ((uint32_t)codes[7] << 24);
+            *reinterpret_cast<uint2*>(a.hq + (int64_t)pp * a.hq_pitch + 32 * j + 8 * b) = pk;
+          }
+        }
+        *reinterpret_cast<uint32_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4) =
+            valid ? sfw : 0u;
+      } else {
+        const float* gd = reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j;
+        const int64_t pos = s_off[e] + local;
+        float* yrow = a.Y + pos * H + 128 * j;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tc_ld16(taddr + 16 * c, v);
+          tc_wait16(v);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              float4 o;
+              o.x = __uint_as_float(v[i]) * __ldg(gd + 16 * c + i);
+              o.y = __uint_as_float(v[i + 1]) * __ldg(gd + 16 * c + i + 1);
+              o.z = __uint_as_float(v[i + 2]) * __ldg(gd + 16 * c + i + 2);
+              o.w = __uint_as_float(v[i + 3]) * __ldg(gd + 16 * c + i + 3);
+              *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+int64_t pf_pad_max(int64_t P, int E) {
+  const int64_t groups = P < E ? P : E;
+  return ((P + 127 * groups) + 127) / 128 * 128;
+}
+
+bool prefill_supported(int H, int E, int I_loc, int Iw, int row0) {
+  if (E > kPfMaxE || H % 256 || H > 16384) return false;
+  if (I_loc % 64 || row0 % 64 || Iw % 64) return false;
+  // every operand row is at least one 128-byte TMA box wide
+  if (I_loc < 256 || Iw < 256) return false;
+  return pf_smem_bytes(E) <= 227 * 1024;
+}
+
+static cudaError_t encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                          const uint32_t* box) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return cudaErrorNotSupported;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides[i];
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d, st, b, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m) {
+  cudaError_t e;
+  const int H = a.H, Iw = a.win.Iw, I_loc = a.win.I_loc;
+  {
+    const uint64_t dims[2] = {(uint64_t)H / 2, (uint64_t)a.P_pad_max}, st[1] = {(uint64_t)H / 2};
+    const uint32_t box[2] = {128, 128};
+    if ((e = encode(&m->xg, a.xg, 2, dims, st, box)) != cudaSuccess) return e;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)H / 2, (uint64_t)2 * Iw, (uint64_t)a.E};
+    const uint64_t st[2] = {(uint64_t)H / 2, (uint64_t)a.lay.bytes};
+    const uint32_t box[3] = {128, 64, 1};
+    if ((e = encode(&m->gu, a.bank + a.lay.gu_codes, 3, dims, st, box)) != cudaSuccess) return e;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)I_loc / 2, (uint64_t)a.P_pad_max}, st[1] = {(uint64_t)a.hq_pitch};
+    const uint32_t box[2] = {128, 128};
+    if ((e = encode(&m->hq, a.hq, 2, dims, st, box)) != cudaSuccess) return e;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)Iw / 2, (uint64_t)H, (uint64_t)a.E};
+    const uint64_t st[2] = {(uint64_t)Iw / 2, (uint64_t)a.lay.bytes};
+    const uint32_t box[3] = {128, 128, 1};
+    if ((e = encode(&m->dn, a.bank + a.lay.dn_codes, 3, dims, st, box)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t prefill_set_smem_limits() {
+  cudaError_t e;
+  const int bytes = pf_smem_bytes(kPfMaxE);
+  if ((e = cudaFuncSetAttribute(k_pf_mma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw, int E, cudaStream_t s) {
+  if (!lay.gu_sf_bytes) return cudaSuccess;
+  k_repack_sf<<<1024, 256, 0, s>>>(bank, lay, H, Iw, E);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
+  cudaError_t err;
+  {
+    int64_t blocks = (a.P_pad_max + 7) / 8;
+    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    FTMOE_PROF_BEGIN("k_pf_prep", s);
+    k_pf_prep<<<(int)blocks, 256, 0, s>>>(a);
+    FTMOE_PROF_END(s);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  const int smem = pf_smem_bytes(a.E);
+  FTMOE_PROF_BEGIN("k_pf_gate_up", s);
+  k_pf_mma<0><<<num_sms, kPfThreads, smem, s>>>(a, m.xg, m.gu);
+  FTMOE_PROF_END(s);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  FTMOE_PROF_BEGIN("k_pf_down", s);
+  k_pf_mma<1><<<num_sms, kPfThreads, smem, s>>>(a, m.hq, m.dn);
+  FTMOE_PROF_END(s);
+  return cudaGetLastError();
+}
+
+}  // namespace ftmoe

@@ -7,6 +7,9 @@ the CUDA library and to the CPU oracle; the benchmark feeds it to the library.
 Workloads (all synthetic; no dataset or trained weights exist for this path):
 
 * ``tiny``      T=4, H=256, E=8, top_k=2, I=I_s=64.
+* ``mid``       H=512, I=I_s=256, E=16, top_k=4, T in {33, 100, 600}: the
+                smallest layer whose shapes take the tensor-core path, small
+                enough for the oracle to check every token.
 * ``decode``    H=2560, I=I_s=640, E=256, top_k=8, T in {1, 8, 16}.
 * ``stack48``   the decode layer as 48 layers of independent weights.
 * ``prefill``   the decode layer's sizes, T in {1024, 4096, 16384}, with a
@@ -52,6 +55,7 @@ class Workload:
 WORKLOADS = {
     "tiny": Workload("tiny", H=256, I=64, E=8, top_k=2, I_s=64, tokens=(4,),
                      slices=((0, 16), (16, 48))),
+    "mid": Workload("mid", H=512, I=256, E=16, top_k=4, I_s=256, tokens=(33, 100, 600)),
     "decode": Workload("decode", H=2560, I=640, E=256, top_k=8, I_s=640, tokens=(1, 8, 16),
                        slices=((0, 320), (320, 320))),
     "stack48": Workload("stack48", H=2560, I=640, E=256, top_k=8, I_s=640, tokens=(1, 8, 16),
