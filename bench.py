@@ -42,6 +42,8 @@ KERNEL_SOURCES = {
     "k_dec_route": ("decode_route.cu", "decode_common.cuh", "tma.cuh"),
     "k_dec_gate_up": ("decode_gate_up.cu", "decode_common.cuh", "tma.cuh"),
     "k_dec_down": ("decode_down.cu", "decode_common.cuh", "tma.cuh"),
+    "k_pf_gate_up": ("prefill.cu", "tc_common.cuh", "tma.cuh"), "k_pf_down": ("prefill.cu", "tc_common.cuh", "tma.cuh"),
+    "k_pf_prep": ("prefill.cu",),
     "k_gate_up": ("experts.cu",), "k_down": ("experts.cu",), "k_shared_gate_up": ("experts.cu",),
     "k_shared_down": ("experts.cu",), "k_combine": ("experts.cu",), "k_router_logits": ("route.cu",),
     "k_topk": ("route.cu",), "k_sort": ("route.cu",), "k_xquant_sigma": ("route.cu",),
@@ -56,7 +58,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="decode")
     p.add_argument("--T", type=int, default=16)
-    p.add_argument("--layers", type=int, default=8, help="independently seeded layers rotated per step")
+    p.add_argument("--layers", type=int, default=0,
+                   help="independently seeded layers rotated per step (default: 8 for decode, 2 for prefill)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -77,6 +80,23 @@ def load_peaks():
         return float(pk["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+FP32_ALU_SOURCE = "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (nominal)"
+FP4_PER_BF16 = 13.5 / 2.25  # nominal dense NVFP4 / BF16 tensor rates
+
+
+def load_fp4_peak():
+    """Dense NVFP4 peak: the measured cuBLAS bf16 burst rate x the nominal
+    FP4/BF16 ratio (6), else the 1.9 PFLOP/s bf16 fallback x 6."""
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]) * FP4_PER_BF16, "measured cuBLAS bf16 burst x nominal NVFP4/BF16 ratio 6"
+    except Exception:
+        return 1900.0 * FP4_PER_BF16, "fallback bf16 1.9 PFLOP/s x nominal NVFP4/BF16 ratio 6"
 
 
 def source_digest(kernel: str) -> str:
@@ -305,7 +325,8 @@ def run_gpu(args):
     from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
 
     wl = W.WORKLOADS[args.workload]
-    T, L, K, Wm = args.T, args.layers, args.steps, max(args.warmup, 3)
+    T, K, Wm = args.T, args.steps, max(args.warmup, 3)
+    L = args.layers or (8 if T <= 32 else 2)
     dev = "cuda"
     layer = build_layers(wl, L, T, dev)
     I_loc, sI_loc = wl.I, wl.I_s
@@ -362,6 +383,8 @@ def run_gpu(args):
 
     # ---- dominant kernel roofline
     peak, peak_kind = load_peaks()
+    fp4_peak, fp4_kind = load_fp4_peak()
+    pairs = T * wl.top_k
     total_k = sum(v[1] for v in ktimes.values()) or 1.0
     dom = max(ktimes.items(), key=lambda kv: kv[1][1])[0] if ktimes else None
     roof = None
@@ -369,7 +392,21 @@ def run_gpu(args):
         launches, kms = ktimes[dom]
         avg_s = kms / launches / 1e3
         unit_bytes, unit, fixed = A.kernel_unit_bytes(dom, wl.H, I_loc, sI_loc, wl.E)
-        if unit_bytes is not None:
+        unit_flops, funit, path = A.kernel_unit_flops(dom, wl.H, I_loc, sI_loc, wl.E)
+        if unit_flops is not None:
+            units = pairs if funit == "pair" else T
+            achieved = unit_flops * units / avg_s / 1e12
+            if path.startswith("nvfp4"):
+                pk, pk_src, bound = fp4_peak, fp4_kind, "tensor"
+            else:
+                pk, pk_src, bound = FP32_ALU_TFLOPS, FP32_ALU_SOURCE, "alu"
+            roof = {"bound": bound, "kernel": dom, "achieved": round(achieved, 1), "peak": round(pk, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
+                    "traffic": ncu_traffic(dom, f"{args.workload}_T{T}"),
+                    "algorithmic_flops_per_launch": int(unit_flops * units), "unit_flops": unit_flops,
+                    "units_per_launch": units, "units": funit, "datapath": path,
+                    "avg_launch_us": round(avg_s * 1e6, 2), "peak_source": pk_src}
+        elif unit_bytes is not None:
             units = mean_touched if unit.startswith("touched") else 1.0
             alg = unit_bytes * units + fixed
             achieved = alg / avg_s / 1e9
@@ -428,7 +465,8 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate); bf16 shared expert",
             "data": "synthetic, seeded",
             "config": {"workload": f"{args.workload} layer: H={wl.H} I={wl.I} I_s={wl.I_s} E={wl.E} "
-                                   f"top_k={wl.top_k}, T={T}, full I window",
+                                   f"top_k={wl.top_k}, T={T}, full I window"
+                                   + (", Zipf(1.1) router bias" if wl.router_bias else ""),
                        "global_batch": T * ws, "layers_rotated": L,
                        "l2": f"inputs larger than L2: {L} independently seeded layers rotated per step "
                              f"({L} x {A.expert_window_bytes(wl.H, I_loc) * wl.E / 1e6:.0f} MB of banks)",
@@ -440,6 +478,9 @@ def run_gpu(args):
             "layer_hbm_gbs": round(bytes_step / (ms_max / K / 1e3) / 1e9, 1),
             "routed_only_gbs": round(routed_bytes_step / (ms_max / K / 1e3) / 1e9, 1),
             "roofline": roof,
+            "routed_fp4_tflops": round(A.routed_flops(wl.H, I_loc, pairs) / (ms_max / K / 1e3) / 1e12, 2),
+            "routed_frac_of_fp4_peak": round(A.routed_flops(wl.H, I_loc, pairs) / (ms_max / K / 1e3) / 1e12
+                                             / fp4_peak, 4),
             "kernel_shares": shares,
             "gpu_launches": launches_total,
             "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": T * wl.H * 2,

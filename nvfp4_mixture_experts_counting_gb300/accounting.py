@@ -63,3 +63,21 @@ def kernel_unit_bytes(kernel: str, H: int, I_loc: int, sI_loc: int, E: int = 0):
     if kernel == "k_shared_down":
         return 0, "launch (shared down columns)", H * sI_loc * 2
     return None, None, None
+
+
+def kernel_unit_flops(kernel: str, H: int, I_loc: int, sI_loc: int, E: int = 0):
+    """(flops per unit, unit name, datapath) of a contraction kernel, or
+    (None, None, None).  Units are token-expert pairs for the routed GEMMs
+    and tokens for the shared expert and the router; flops = 2 x
+    multiply-adds of the contraction as defined, no padding counted."""
+    if kernel == "k_pf_gate_up":
+        return 2 * H * 2 * I_loc, "pair", "nvfp4 tensor"
+    if kernel == "k_pf_down":
+        return 2 * I_loc * H, "pair", "nvfp4 tensor"
+    if kernel == "k_shared_gate_up":
+        return 2 * H * 2 * sI_loc, "token", "fp32 CUDA cores"
+    if kernel == "k_shared_down":
+        return 2 * sI_loc * H, "token", "fp32 CUDA cores"
+    if kernel == "k_router_logits":
+        return 2 * H * E, "token", "fp32 CUDA cores"
+    return None, None, None

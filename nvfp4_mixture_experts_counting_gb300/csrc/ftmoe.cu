@@ -465,10 +465,12 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     CK(launch_decode(d, s));
   } else if (h->pf_enabled && T > 32 && L.lay.gu_sf_bytes &&
              prefill_supported(c.H, c.E, I_loc, L.lIw, a.win.row0)) {
-    // prefill sizes: routing, then the routed GEMMs on the tensor cores
+    // prefill sizes: routing, then the routed GEMMs on the tensor cores;
+    // the shared expert too when its window fits them, its down product
+    // fused with the combine
     CK(launch_route(r, s));
     a.r = r;
-    CK(launch_experts(a, s, kPartSharedGateUp));
+    const bool tc_shared = a.sh_gate_up && prefill_shared_supported(c.H, a.s_I_loc, a.s_Iw, a.s_row0, c.top_k);
     PfArgs p{};
     p.offsets = r.offsets;
     p.perm = r.perm;
@@ -490,10 +492,27 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     p.hq_pitch = (int)align_up(I_loc / 2, 16);
     p.Y = h->Y;
     p.status = h->status;
+    if (tc_shared) {
+      p.x = (const uint16_t*)x;
+      p.sh_gu = a.sh_gate_up;
+      p.sh_dn = a.sh_down;
+      p.s_row0 = a.s_row0;
+      p.s_I_loc = a.s_I_loc;
+      p.s_Iw = a.s_Iw;
+      p.hs = h->hs;
+      p.inv = r.inv;
+      p.topk_w = r.topk_w;
+      p.sigma = r.sigma;
+      p.out = out;
+      p.out_flags = out_flags;
+    }
     PfMaps maps;
     CK(prefill_make_maps(p, &maps));
+    if (tc_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
+    else CK(launch_experts(a, s, kPartSharedGateUp));
     CK(launch_prefill_routed(p, maps, h->num_sms, s));
-    CK(launch_experts(a, s, kPartTail));
+    if (tc_shared) CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
+    else CK(launch_experts(a, s, kPartTail));
   } else {
     CK(launch_route(r, s));
     a.r = r;

@@ -158,13 +158,28 @@ struct PfArgs {
   int hq_pitch;
   float* Y;                   // [P][H] fp32, rows in sorted order
   uint32_t* status;
+  // shared expert on the tensor cores, fused with the combine
+  const uint16_t* x;          // [T][H] bf16
+  const uint16_t* sh_gu;      // [2*s_Iw][H] bf16 (loaded window: gate rows, then up rows)
+  const uint16_t* sh_dn;      // [H][s_Iw] bf16
+  int s_row0, s_I_loc, s_Iw;
+  uint16_t* hs;               // [T][s_I_loc] bf16 shared intermediate
+  const int32_t* inv;         // [P]
+  const float* topk_w;        // [P]
+  const float* sigma;         // [T]
+  void* out;
+  int out_flags;
 };
 struct PfMaps {
-  CUtensorMap xg, gu, hq, dn;
+  CUtensorMap xg, gu, hq, dn;   // routed operands
+  CUtensorMap x, sgu, hs, sdn;  // shared-expert operands
 };
 
 int64_t pf_pad_max(int64_t P, int E);
 bool prefill_supported(int H, int E, int I_loc, int Iw, int row0);
+bool prefill_shared_supported(int H, int s_I_loc, int s_Iw, int s_row0, int top_k);
+cudaError_t launch_prefill_shared_gate_up(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
 cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m);
 cudaError_t prefill_set_smem_limits();
 cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw, int E, cudaStream_t s);

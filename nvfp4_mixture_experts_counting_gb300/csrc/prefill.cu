@@ -44,6 +44,7 @@ constexpr int kPfOffSfb = kPfOffSfa + kPfStages * kSfStage;
 constexpr int kPfOffBar = kPfOffSfb + kPfStages * kSfStage;
 constexpr int kPfOffTab = kPfOffBar + 256;
 constexpr int kPfMaxE = 1024;
+constexpr int kPfMaxK = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;   // scale-factor columns start after the two accumulators
 
@@ -151,11 +152,24 @@ __global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
 
 // ------------------------------------------------------------------ grouped GEMM
 
-// MODE 0: gate_up + SwiGLU + quantisation.  MODE 1: down -> Y.
+// One kernel body, four problems (all D = A * B^T, A = 128 token or pair
+// rows, B = 128 weight rows, K-major operands in 128-byte swizzled tiles):
+//   MODE 0  routed gate_up, NVFP4, grouped by expert; epilogue: row globals,
+//           SwiGLU, NVFP4 quantisation of the intermediate (padded order)
+//   MODE 1  routed down, NVFP4, grouped; epilogue: down row global -> Y
+//   MODE 2  shared gate_up, bf16, one group of T tokens; epilogue: SwiGLU,
+//           rounded to bf16 -> hs
+//   MODE 3  shared down, bf16; epilogue: the combine
+//           out_t = sum_j w_tj * Y[inv(t, j)] + sigma_t * S_t in slot order
+//           (PR #385 "feat(qwen4_exp): tensor parallelism for
+//           Qwen3.8-Flash-Next (offload backend)", "What this adds")
+// A K step is 32 bytes of a row (64 E2M1 or 16 bf16 elements), a K tile 4
+// steps (one 128-byte swizzle row).
 template <int MODE>
 __global__ void __launch_bounds__(kPfThreads, 1)
     k_pf_mma(const __grid_constant__ PfArgs a, const __grid_constant__ CUtensorMap mapA,
              const __grid_constant__ CUtensorMap mapB) {
+  constexpr bool kF4 = MODE < 2;
   extern __shared__ unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPfOffBar);
@@ -165,15 +179,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int E = kF4 ? a.E : 1, H = a.H;
   int* s_off = reinterpret_cast<int*>(sm + kPfOffTab);
-  const int E = a.E, H = a.H;
   int* s_pad = s_off + (E + 1);
   int* s_up = s_pad + (E + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int I_loc = a.win.I_loc, row0 = a.win.row0, Iw = a.win.Iw;
-  const int J = MODE == 0 ? I_loc / 64 : H / 128;          // weight tiles per pair tile
-  const int nks_all = MODE == 0 ? H / 64 : I_loc / 64;     // 64-element K steps
-  const int nkt = (nks_all + 3) / 4;                        // 256-element K tiles
+  const int kbytes = MODE == 0 ? H / 2 : MODE == 1 ? I_loc / 2 : MODE == 2 ? 2 * H : 2 * a.s_I_loc;
+  const int nks_all = kbytes / 32;
+  const int nkt = (nks_all + 3) / 4;
+  const int J = MODE == 0 ? I_loc / 64 : MODE == 2 ? a.s_I_loc / 64 : H / 128;  // weight tiles per row tile
 
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -187,9 +202,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tma_prefetch_desc(&mapB);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
-  for (int e = tid; e <= E; e += kPfThreads) {
-    s_off[e] = a.offsets[e];
-    s_pad[e] = a.pad_off[e];
+  if (kF4) {
+    for (int e = tid; e <= E; e += kPfThreads) {
+      s_off[e] = a.offsets[e];
+      s_pad[e] = a.pad_off[e];
+    }
+  } else if (tid == 0) {
+    s_off[0] = 0;
+    s_off[1] = a.T;
+    s_pad[0] = 0;
+    s_pad[1] = (a.T + 127) & ~127;
   }
   tc_fence_before();
   __syncthreads();
@@ -207,7 +229,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int e = find_le(s_up, E, u), r = u - s_up[e];
         const int nt = r / J, j = r % J;
         const int pp0 = s_pad[e] + nt * 128;
-        const uint8_t* rec = a.bank + a.lay.bytes * e;
+        const uint8_t* rec = kF4 ? a.bank + a.lay.bytes * e : nullptr;
         for (int kt = 0; kt < nkt; ++kt, ++k) {
           const int s = k % kPfStages;
           if (k >= kPfStages && !mbar_wait(&empty[s], ((k / kPfStages) - 1) & 1, a.status)) {
@@ -219,20 +241,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           unsigned char* sb = sm + kPfOffB + s * kTile;
           unsigned char* sfa = sm + kPfOffSfa + s * kSfStage;
           unsigned char* sfb = sm + kPfOffSfb + s * kSfStage;
-          mbar_arrive_expect_tx(&full[s], 2 * kTile + 2 * nks * 512);
+          mbar_arrive_expect_tx(&full[s], 2 * kTile + (kF4 ? 2 * nks * 512 : 0));
+          tma_load_2d(sa, &mapA, kt * 128, pp0, &full[s]);
           if (MODE == 0) {
-            tma_load_2d(sa, &mapA, kt * 128, pp0, &full[s]);
             tma_load_3d(sb, &mapB, kt * 128, row0 + 64 * j, e, &full[s]);
             tma_load_3d(sb + kTile / 2, &mapB, kt * 128, Iw + row0 + 64 * j, e, &full[s]);
             bulk_g2s(sfa, a.xg_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
             bulk_g2s(sfb, rec + a.lay.gu_sf + ((int64_t)(row0 / 64 + j) * nks_all + 4 * kt) * 512, nks * 512,
                      &full[s]);
-          } else {
-            tma_load_2d(sa, &mapA, kt * 128, pp0, &full[s]);
+          } else if (MODE == 1) {
             tma_load_3d(sb, &mapB, row0 / 2 + kt * 128, 128 * j, e, &full[s]);
             bulk_g2s(sfa, a.hq_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
             bulk_g2s(sfb, rec + a.lay.dn_sf + ((int64_t)j * (Iw / 64) + row0 / 64 + 4 * kt) * 512, nks * 512,
                      &full[s]);
+          } else if (MODE == 2) {
+            tma_load_2d(sb, &mapB, kt * 128, a.s_row0 + 64 * j, &full[s]);
+            tma_load_2d(sb + kTile / 2, &mapB, kt * 128, a.s_Iw + a.s_row0 + 64 * j, &full[s]);
+          } else {
+            tma_load_2d(sb, &mapB, 2 * a.s_row0 + kt * 128, 128 * j, &full[s]);
           }
         }
       }
@@ -243,7 +269,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_nvf4(128, 128);
+      const uint32_t idesc = kF4 ? idesc_nvf4(128, 128) : idesc_bf16(128, 128);
       int k = 0, ui = 0;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
         const int buf = ui & 1;
@@ -256,18 +282,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (!mbar_wait(&full[s], (k / kPfStages) & 1, a.status)) { *abort_flag = 1; ok = false; break; }
           tc_fence_after();
           const int nks = min(4, nks_all - 4 * kt);
-          const uint32_t sfa_col = tmem + kSfCol0 + s * 32, sfb_col = sfa_col + 16;
-          const uint32_t sfa_smem = smem_u32(sm + kPfOffSfa + s * kSfStage);
-          const uint32_t sfb_smem = smem_u32(sm + kPfOffSfb + s * kSfStage);
-          for (int ks = 0; ks < nks; ++ks) {
-            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
-            tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sfb_smem + 512 * ks));
-          }
           const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + kPfOffA + s * kTile));
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + kPfOffB + s * kTile));
-          for (int ks = 0; ks < nks; ++ks)
-            tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, idesc, sfa_col + 4 * ks, sfb_col + 4 * ks,
-                        (kt | ks) != 0);
+          if (kF4) {
+            const uint32_t sfa_col = tmem + kSfCol0 + s * 32, sfb_col = sfa_col + 16;
+            const uint32_t sfa_smem = smem_u32(sm + kPfOffSfa + s * kSfStage);
+            const uint32_t sfb_smem = smem_u32(sm + kPfOffSfb + s * kSfStage);
+            for (int ks = 0; ks < nks; ++ks) {
+              tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
+              tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sfb_smem + 512 * ks));
+            }
+            for (int ks = 0; ks < nks; ++ks)
+              tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, idesc, sfa_col + 4 * ks, sfb_col + 4 * ks,
+                          (kt | ks) != 0);
+          } else {
+            for (int ks = 0; ks < nks; ++ks) tc_mma_bf16(d, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kt | ks) != 0);
+          }
           tc_commit(&empty[s]);  // stage free once these MMAs have read it
         }
         if (!ok) break;
@@ -291,9 +321,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int pp0 = s_pad[e] + nt * 128;
       const int local = nt * 128 + 32 * q + lane;
       const bool valid = local < s_off[e + 1] - s_off[e];
-      const uint8_t* rec = a.bank + a.lay.bytes * e;
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 128;
       if (MODE == 0) {
+        const uint8_t* rec = a.bank + a.lay.bytes * e;
         const float* gglob = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * j;
         const float* uglob = gglob + Iw;
         const int pp = pp0 + 32 * q + lane;
@@ -322,7 +352,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         *reinterpret_cast<uint32_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4) =
             valid ? sfw : 0u;
-      } else {
+      } else if (MODE == 1) {
+        const uint8_t* rec = a.bank + a.lay.bytes * e;
         const float* gd = reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j;
         const int64_t pos = s_off[e] + local;
         float* yrow = a.Y + pos * H + 128 * j;
@@ -340,6 +371,89 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               o.z = __uint_as_float(v[i + 2]) * __ldg(gd + 16 * c + i + 2);
               o.w = __uint_as_float(v[i + 3]) * __ldg(gd + 16 * c + i + 3);
               *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
+            }
+          }
+        }
+      } else if (MODE == 2) {
+        const int t = local;
+        uint16_t* hrow = a.hs + (int64_t)t * a.s_I_loc + 64 * j;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          uint32_t g[16], v[16];
+          tc_ld16(taddr + 16 * b, g);
+          tc_ld16(taddr + 64 + 16 * b, v);
+          tc_wait16x2(g, v);
+          if (valid) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(v[2 * i]);
+              const float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+              pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(hrow + 16 * b);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else {
+        // combine for token t over output rows [128 j, 128 j + 128)
+        const int t = local;
+        const int k = a.top_k;
+        const int32_t* pos = a.inv + (int64_t)t * k;
+        const float* w = a.topk_w + (int64_t)t * k;
+        const float sig = valid ? a.sigma[t] : 0.f;
+        const int64_t obase = (int64_t)t * H + 128 * j;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tc_ld16(taddr + 16 * c, v);
+          tc_wait16(v);
+          if (valid) {
+            float o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = 0.f;
+            for (int jj = 0; jj < k; ++jj) {
+              const float wj = __ldg(w + jj);
+              const float4* yp = reinterpret_cast<const float4*>(a.Y + (int64_t)__ldg(pos + jj) * H + 128 * j + 16 * c);
+#pragma unroll
+              for (int i4 = 0; i4 < 4; ++i4) {
+                const float4 y = yp[i4];
+                o[4 * i4] = fmaf(wj, y.x, o[4 * i4]);
+                o[4 * i4 + 1] = fmaf(wj, y.y, o[4 * i4 + 1]);
+                o[4 * i4 + 2] = fmaf(wj, y.z, o[4 * i4 + 2]);
+                o[4 * i4 + 3] = fmaf(wj, y.w, o[4 * i4 + 3]);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = fmaf(sig, __uint_as_float(v[i]), o[i]);
+            const int64_t oi = obase + 16 * c;
+            if ((a.out_flags & 0xff) == 0) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const __nv_bfloat162 hb = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+                pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + oi);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi);
+              const bool accum = (a.out_flags & 0x100) != 0;
+#pragma unroll
+              for (int i4 = 0; i4 < 4; ++i4) {
+                float4 val = make_float4(o[4 * i4], o[4 * i4 + 1], o[4 * i4 + 2], o[4 * i4 + 3]);
+                if (accum) {
+                  const float4 prev = dst[i4];
+                  val.x += prev.x;
+                  val.y += prev.y;
+                  val.z += prev.z;
+                  val.w += prev.w;
+                }
+                dst[i4] = val;
+              }
             }
           }
         }
@@ -394,8 +508,36 @@ static cudaError_t encode(CUtensorMap* m, const void* base, int rank, const uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+bool prefill_shared_supported(int H, int s_I_loc, int s_Iw, int s_row0, int top_k) {
+  // bf16 rows of at least one 128-byte box, windows in 64-element tiles
+  return H % 128 == 0 && s_I_loc % 64 == 0 && s_row0 % 64 == 0 && s_Iw % 64 == 0 && top_k <= kPfMaxK;
+}
+
 cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m) {
   cudaError_t e;
+  if (a.sh_gu) {
+    const int H = a.H;
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * H, (uint64_t)a.T}, st[1] = {(uint64_t)2 * H};
+      const uint32_t box[2] = {128, 128};
+      if ((e = encode(&m->x, a.x, 2, dims, st, box)) != cudaSuccess) return e;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * H, (uint64_t)2 * a.s_Iw}, st[1] = {(uint64_t)2 * H};
+      const uint32_t box[2] = {128, 64};
+      if ((e = encode(&m->sgu, a.sh_gu, 2, dims, st, box)) != cudaSuccess) return e;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * a.s_I_loc, (uint64_t)a.T}, st[1] = {(uint64_t)2 * a.s_I_loc};
+      const uint32_t box[2] = {128, 128};
+      if ((e = encode(&m->hs, a.hs, 2, dims, st, box)) != cudaSuccess) return e;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * a.s_Iw, (uint64_t)H}, st[1] = {(uint64_t)2 * a.s_Iw};
+      const uint32_t box[2] = {128, 128};
+      if ((e = encode(&m->sdn, a.sh_dn, 2, dims, st, box)) != cudaSuccess) return e;
+    }
+  }
   const int H = a.H, Iw = a.win.Iw, I_loc = a.win.I_loc;
   {
     const uint64_t dims[2] = {(uint64_t)H / 2, (uint64_t)a.P_pad_max}, st[1] = {(uint64_t)H / 2};
@@ -427,7 +569,11 @@ cudaError_t prefill_set_smem_limits() {
   const int bytes = pf_smem_bytes(kPfMaxE);
   if ((e = cudaFuncSetAttribute(k_pf_mma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if ((e = cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_pf_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_pf_mma<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw, int E, cudaStream_t s) {
@@ -453,6 +599,20 @@ cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms,
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   FTMOE_PROF_BEGIN("k_pf_down", s);
   k_pf_mma<1><<<num_sms, kPfThreads, smem, s>>>(a, m.hq, m.dn);
+  FTMOE_PROF_END(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_shared_gate_up(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
+  FTMOE_PROF_BEGIN("k_pf_shared_gate_up", s);
+  k_pf_mma<2><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.x, m.sgu);
+  FTMOE_PROF_END(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
+  FTMOE_PROF_BEGIN("k_pf_shared_down_combine", s);
+  k_pf_mma<3><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.hs, m.sdn);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
