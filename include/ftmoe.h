@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define FTMOE_ABI_VERSION 1
+#define FTMOE_ABI_VERSION 2
 
 typedef void* ftmoe_stream_t; /* a cudaStream_t */
 
@@ -119,6 +119,8 @@ typedef struct {
   int32_t* offsets;   /* [E + 1] first sorted position of each expert; offsets[E] = T*top_k */
   int32_t* perm;      /* [T*top_k] pair id p = t*top_k + j at each sorted position */
   int32_t* inv;       /* [T*top_k] sorted position of each pair id */
+  float* logits;      /* [T, E] router logits (bias included) as the fast pass computed them,
+                         before any re-rank of uncertain tokens */
 } ftmoe_aux;
 
 typedef struct {

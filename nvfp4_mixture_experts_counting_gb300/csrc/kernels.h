@@ -60,6 +60,7 @@ struct RouteArgs {
   uint8_t* xq_codes; // [T][H/2]
   uint8_t* xq_scales;  // [T][H/16]
   float* sigma;      // [T]
+  float* xnorm;      // [T] upper bound of ||x_t||_2 (may be null)
   int32_t* offsets;  // [E+1]
   int32_t* perm;     // [P]
   int32_t* inv;      // [P]
@@ -74,8 +75,10 @@ cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, uint8_t
 cudaError_t launch_quantize_act_bf16(const uint16_t* a, int64_t rows, int K, uint8_t* codes,
                                      uint8_t* scales, cudaStream_t s);
 
-// x quantisation + shared gate, router logits, top-k, counting sort.
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+// x quantisation + shared gate, router logits, top-k, counting sort (parts
+// selectable so another router-logit kernel can take the second's place).
+constexpr int kRouteXq = 1, kRouteLogits = 2, kRouteTopk = 4, kRouteSort = 8, kRouteAll = 15;
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int parts = kRouteAll);
 
 struct ExpertArgs {
   RouteArgs r;  // routing workspace and inputs (by value: kernels read it)
@@ -169,15 +172,27 @@ struct PfArgs {
   const float* sigma;         // [T]
   void* out;
   int out_flags;
+  // router logits on the tensor cores: W = W1 + W2 + W3 exactly (bf16 parts)
+  const uint16_t* wcat;       // [E][3H] bf16: W1 | W2 | W3
+  const float* wnorm;         // [E] upper bound of ||w_e||_2
+  const float* xnorm;         // [T] upper bound of ||x_t||_2
+  const float* router_bias;   // [E] or null
+  float* logits;              // [T][E]
+  float* err;                 // [T][E] bound on |logit - exact|
+  float kappa;                // err = kappa * ||x|| * ||w|| + 2^-22 |logit|
 };
 struct PfMaps {
   CUtensorMap xg, gu, hq, dn;   // routed operands
   CUtensorMap x, sgu, hs, sdn;  // shared-expert operands
+  CUtensorMap wr;               // router parts
 };
 
 int64_t pf_pad_max(int64_t P, int E);
 bool prefill_supported(int H, int E, int I_loc, int Iw, int row0);
 bool prefill_shared_supported(int H, int s_I_loc, int s_Iw, int s_row0, int top_k);
+bool prefill_router_supported(int H, int E);
+cudaError_t launch_router_split(const float* w, int E, int H, uint16_t* wcat, float* wnorm, cudaStream_t s);
+cudaError_t launch_prefill_router(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill_shared_gate_up(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
 cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m);

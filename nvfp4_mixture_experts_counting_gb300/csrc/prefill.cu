@@ -19,7 +19,7 @@
 // products of E2M1 values are exact; scaling and accumulation are fp32.
 //
 // Kernel roles (one persistent CTA per SM): warp 0 issues TMA, warp 1 owns
-// TMEM and issues the MMAs, warps 2-5 drain the accumulators.  Two TMEM
+// TMEM and issues the MMAs, warps 2-9 drain the accumulators.  Two TMEM
 // accumulators let the epilogue of one tile run under the next tile's MMAs.
 // Every mbarrier wait is bounded; a wait that runs out stops every role,
 // drains what is in flight and frees TMEM.
@@ -34,7 +34,8 @@ namespace ftmoe {
 namespace {
 
 constexpr int kPfStages = 5;
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 320;    // producer, MMA, 8 epilogue warps
+constexpr int kPfEpiWarps = 8;
 constexpr int kTile = 16384;        // one 128 x 128-byte operand tile
 constexpr int kSfStage = 2048;      // four 512-byte scale blocks
 constexpr int kPfOffA = 0;
@@ -42,7 +43,8 @@ constexpr int kPfOffB = kPfStages * kTile;
 constexpr int kPfOffSfa = 2 * kPfStages * kTile;
 constexpr int kPfOffSfb = kPfOffSfa + kPfStages * kSfStage;
 constexpr int kPfOffBar = kPfOffSfb + kPfStages * kSfStage;
-constexpr int kPfOffTab = kPfOffBar + 256;
+constexpr int kPfOffGlob = kPfOffBar + 256;  // per epilogue warp: 128 row globals
+constexpr int kPfOffTab = kPfOffGlob + kPfEpiWarps * 512;
 constexpr int kPfMaxE = 1024;
 constexpr int kPfMaxK = 32;
 constexpr uint32_t kTmemCols = 512;
@@ -86,6 +88,31 @@ __device__ __forceinline__ int find_le(const int* tab, int n, int v) {
 // rows: rows r, r+32, r+64, r+96 share a 16-byte line (the order tcgen05.cp
 // .32x128b.warpx4 places into TMEM lanes r % 32, columns r / 32).
 __host__ __device__ constexpr int sf_slot(int r) { return (r & 31) * 16 + ((r & 127) >> 5) * 4; }
+
+// SiLU with the fast exponential and division (the epilogue's result is
+// quantised to E2M1 right after; the approximation changes h by a few ulp).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// NVFP4 quantisation of 16 activation values with global 1.0: scale =
+// E4M3(amax / 6), codes = E2M1(v * (1 / scale)).  Multiplying by the
+// reciprocal can move a value sitting exactly on an E2M1 rounding boundary
+// by one ulp, which the parity tolerance absorbs.
+__device__ __forceinline__ uint8_t quantize_act16_fast(const float v[16], uint8_t codes[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint8_t s = e4m3_encode(__fdiv_rn(amax, kE2M1Max));
+  const float d = e4m3_decode(s);
+  if (s == 0 || d == 0.f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) codes[i] = 0;
+    return 0;
+  }
+  const float r = __frcp_rn(d);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) codes[i] = e2m1x2_encode(v[2 * i] * r, v[2 * i + 1] * r);
+  return s;
+}
 
 }  // namespace
 
@@ -163,6 +190,9 @@ __global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
 //           out_t = sum_j w_tj * Y[inv(t, j)] + sigma_t * S_t in slot order
 //           (PR #385 "feat(qwen4_exp): tensor parallelism for
 //           Qwen3.8-Flash-Next (offload backend)", "What this adds")
+//   MODE 4  router logits, bf16: x . (W1 + W2 + W3) with K = 3H (the three
+//           exact bf16 parts of the fp32 router rows, x repeated along K);
+//           epilogue: bias and the error bound the top-k certificate uses
 // A K step is 32 bytes of a row (64 E2M1 or 16 bf16 elements), a K tile 4
 // steps (one 128-byte swizzle row).
 template <int MODE>
@@ -185,14 +215,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   int* s_up = s_pad + (E + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int I_loc = a.win.I_loc, row0 = a.win.row0, Iw = a.win.Iw;
-  const int kbytes = MODE == 0 ? H / 2 : MODE == 1 ? I_loc / 2 : MODE == 2 ? 2 * H : 2 * a.s_I_loc;
+  const int kbytes = MODE == 0 ? H / 2 : MODE == 1 ? I_loc / 2 : MODE == 2 ? 2 * H : MODE == 3 ? 2 * a.s_I_loc : 6 * H;
   const int nks_all = kbytes / 32;
   const int nkt = (nks_all + 3) / 4;
-  const int J = MODE == 0 ? I_loc / 64 : MODE == 2 ? a.s_I_loc / 64 : H / 128;  // weight tiles per row tile
+  const int J = MODE == 0 ? I_loc / 64 : MODE == 2 ? a.s_I_loc / 64 : MODE == 4 ? a.E / 128 : H / 128;  // weight tiles per row tile
 
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 4); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], kPfEpiWarps); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -242,7 +272,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           unsigned char* sfa = sm + kPfOffSfa + s * kSfStage;
           unsigned char* sfb = sm + kPfOffSfb + s * kSfStage;
           mbar_arrive_expect_tx(&full[s], 2 * kTile + (kF4 ? 2 * nks * 512 : 0));
-          tma_load_2d(sa, &mapA, kt * 128, pp0, &full[s]);
+          tma_load_2d(sa, &mapA, MODE == 4 ? (kt * 128) % (2 * H) : kt * 128, pp0, &full[s]);
           if (MODE == 0) {
             tma_load_3d(sb, &mapB, kt * 128, row0 + 64 * j, e, &full[s]);
             tma_load_3d(sb + kTile / 2, &mapB, kt * 128, Iw + row0 + 64 * j, e, &full[s]);
@@ -257,8 +287,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           } else if (MODE == 2) {
             tma_load_2d(sb, &mapB, kt * 128, a.s_row0 + 64 * j, &full[s]);
             tma_load_2d(sb + kTile / 2, &mapB, kt * 128, a.s_Iw + a.s_row0 + 64 * j, &full[s]);
-          } else {
+          } else if (MODE == 3) {
             tma_load_2d(sb, &mapB, 2 * a.s_row0 + kt * 128, 128 * j, &full[s]);
+          } else {
+            tma_load_2d(sb, &mapB, kt * 128, 128 * j, &full[s]);
           }
         }
       }
@@ -309,8 +341,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_wait(drain, 0, a.status);
     }
   } else {
-    // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ...
-    const int q = warp & 3;
+    // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ...;
+    // the two warps of a lane quarter split the columns in halves
+    const int q = warp & 3, hf = (warp - 2) >> 2;
+    float* wglob = reinterpret_cast<float*>(sm + kPfOffGlob) + (warp - 2) * 128;
     int ui = 0;
     for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
       const int buf = ui & 1;
@@ -324,25 +358,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 128;
       if (MODE == 0) {
         const uint8_t* rec = a.bank + a.lay.bytes * e;
-        const float* gglob = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * j;
-        const float* uglob = gglob + Iw;
+        {
+          // this unit's 64 gate and 64 up row globals into the warp's slot
+          const float* src = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * j +
+                             (lane < 16 ? 0 : Iw - 64);
+          reinterpret_cast<float4*>(wglob)[lane] = __ldg(reinterpret_cast<const float4*>(src) + lane);
+          __syncwarp();
+        }
         const int pp = pp0 + 32 * q + lane;
         uint32_t sfw = 0;
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 2 * hf; b < 2 * hf + 2; ++b) {
           uint32_t g[16], v[16];
           tc_ld16(taddr + 16 * b, g);
           tc_ld16(taddr + 64 + 16 * b, v);
           tc_wait16x2(g, v);
           float h[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float gg = __ldg(gglob + 16 * b + i), ug = __ldg(uglob + 16 * b + i);
-            h[i] = silu(__uint_as_float(g[i]) * gg) * (__uint_as_float(v[i]) * ug);
+          for (int i = 0; i < 16; i += 4) {
+            const float4 gg = *reinterpret_cast<const float4*>(wglob + 16 * b + i);
+            const float4 ug = *reinterpret_cast<const float4*>(wglob + 64 + 16 * b + i);
+            h[i] = silu_fast(__uint_as_float(g[i]) * gg.x) * (__uint_as_float(v[i]) * ug.x);
+            h[i + 1] = silu_fast(__uint_as_float(g[i + 1]) * gg.y) * (__uint_as_float(v[i + 1]) * ug.y);
+            h[i + 2] = silu_fast(__uint_as_float(g[i + 2]) * gg.z) * (__uint_as_float(v[i + 2]) * ug.z);
+            h[i + 3] = silu_fast(__uint_as_float(g[i + 3]) * gg.w) * (__uint_as_float(v[i + 3]) * ug.w);
           }
           uint8_t codes[8];
-          const uint8_t sc = quantize_block16(h, 1.0f, codes);
-          sfw |= (uint32_t)sc << (8 * b);
+          const uint8_t sc = quantize_act16_fast(h, codes);
+          sfw |= (uint32_t)sc << (8 * (b - 2 * hf));
           if (valid) {
             uint2 pk;
             pk.x = codes[0] | (codes[1] << 8) | (codes[2] << 16) | ((uint32_t)codes[3] << 24);
@@ -350,26 +393,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             *reinterpret_cast<uint2*>(a.hq + (int64_t)pp * a.hq_pitch + 32 * j + 8 * b) = pk;
           }
         }
-        *reinterpret_cast<uint32_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4) =
-            valid ? sfw : 0u;
+        *reinterpret_cast<uint16_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4 +
+                                     2 * hf) = valid ? (uint16_t)sfw : (uint16_t)0;
       } else if (MODE == 1) {
         const uint8_t* rec = a.bank + a.lay.bytes * e;
-        const float* gd = reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j;
+        reinterpret_cast<float4*>(wglob)[lane] =
+            __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j) +
+                  lane);
+        __syncwarp();
         const int64_t pos = s_off[e] + local;
         float* yrow = a.Y + pos * H + 128 * j;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
           uint32_t v[16];
           tc_ld16(taddr + 16 * c, v);
           tc_wait16(v);
           if (valid) {
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
+              const float4 gd = *reinterpret_cast<const float4*>(wglob + 16 * c + i);
               float4 o;
-              o.x = __uint_as_float(v[i]) * __ldg(gd + 16 * c + i);
-              o.y = __uint_as_float(v[i + 1]) * __ldg(gd + 16 * c + i + 1);
-              o.z = __uint_as_float(v[i + 2]) * __ldg(gd + 16 * c + i + 2);
-              o.w = __uint_as_float(v[i + 3]) * __ldg(gd + 16 * c + i + 3);
+              o.x = __uint_as_float(v[i]) * gd.x;
+              o.y = __uint_as_float(v[i + 1]) * gd.y;
+              o.z = __uint_as_float(v[i + 2]) * gd.z;
+              o.w = __uint_as_float(v[i + 3]) * gd.w;
               *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
             }
           }
@@ -378,7 +425,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int t = local;
         uint16_t* hrow = a.hs + (int64_t)t * a.s_I_loc + 64 * j;
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 2 * hf; b < 2 * hf + 2; ++b) {
           uint32_t g[16], v[16];
           tc_ld16(taddr + 16 * b, g);
           tc_ld16(taddr + 64 + 16 * b, v);
@@ -387,14 +434,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(v[2 * i]);
-              const float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
+              const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(v[2 * i]);
+              const float h1 = silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
               const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
               pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
             }
             uint4* dst = reinterpret_cast<uint4*>(hrow + 16 * b);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else if (MODE == 4) {
+        // logits of token t for experts [128 j, 128 j + 128) and their bounds
+        const int t = local;
+        const float xn = valid ? a.xnorm[t] : 0.f;
+#pragma unroll 1
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+          uint32_t v[16];
+          tc_ld16(taddr + 16 * c, v);
+          tc_wait16(v);
+          if (valid) {
+            const int e0 = 128 * j + 16 * c;
+            float* lrow = a.logits + (int64_t)t * a.E + e0;
+            float* erow = a.err + (int64_t)t * a.E + e0;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 wn = __ldg(reinterpret_cast<const float4*>(a.wnorm + e0 + i));
+              float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (a.router_bias) b = __ldg(reinterpret_cast<const float4*>(a.router_bias + e0 + i));
+              float4 l, er;
+              l.x = __uint_as_float(v[i]) + b.x;
+              l.y = __uint_as_float(v[i + 1]) + b.y;
+              l.z = __uint_as_float(v[i + 2]) + b.z;
+              l.w = __uint_as_float(v[i + 3]) + b.w;
+              er.x = a.kappa * xn * wn.x + 2.4e-7f * fabsf(l.x) + 1e-30f;
+              er.y = a.kappa * xn * wn.y + 2.4e-7f * fabsf(l.y) + 1e-30f;
+              er.z = a.kappa * xn * wn.z + 2.4e-7f * fabsf(l.z) + 1e-30f;
+              er.w = a.kappa * xn * wn.w + 2.4e-7f * fabsf(l.w) + 1e-30f;
+              *reinterpret_cast<float4*>(lrow + i) = l;
+              *reinterpret_cast<float4*>(erow + i) = er;
+            }
           }
         }
       } else {
@@ -406,7 +485,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float sig = valid ? a.sigma[t] : 0.f;
         const int64_t obase = (int64_t)t * H + 128 * j;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
           uint32_t v[16];
           tc_ld16(taddr + 16 * c, v);
           tc_wait16(v);
@@ -515,13 +594,18 @@ bool prefill_shared_supported(int H, int s_I_loc, int s_Iw, int s_row0, int top_
 
 cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m) {
   cudaError_t e;
+  if (a.x) {
+    const uint64_t dims[2] = {(uint64_t)2 * a.H, (uint64_t)a.T}, st[1] = {(uint64_t)2 * a.H};
+    const uint32_t box[2] = {128, 128};
+    if ((e = encode(&m->x, a.x, 2, dims, st, box)) != cudaSuccess) return e;
+  }
+  if (a.wcat) {
+    const uint64_t dims[2] = {(uint64_t)6 * a.H, (uint64_t)a.E}, st[1] = {(uint64_t)6 * a.H};
+    const uint32_t box[2] = {128, 128};
+    if ((e = encode(&m->wr, a.wcat, 2, dims, st, box)) != cudaSuccess) return e;
+  }
   if (a.sh_gu) {
     const int H = a.H;
-    {
-      const uint64_t dims[2] = {(uint64_t)2 * H, (uint64_t)a.T}, st[1] = {(uint64_t)2 * H};
-      const uint32_t box[2] = {128, 128};
-      if ((e = encode(&m->x, a.x, 2, dims, st, box)) != cudaSuccess) return e;
-    }
     {
       const uint64_t dims[2] = {(uint64_t)2 * H, (uint64_t)2 * a.s_Iw}, st[1] = {(uint64_t)2 * H};
       const uint32_t box[2] = {128, 64};
@@ -573,7 +657,9 @@ cudaError_t prefill_set_smem_limits() {
     return e;
   if ((e = cudaFuncSetAttribute(k_pf_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(k_pf_mma<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if ((e = cudaFuncSetAttribute(k_pf_mma<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_pf_mma<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw, int E, cudaStream_t s) {
@@ -599,6 +685,51 @@ cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms,
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   FTMOE_PROF_BEGIN("k_pf_down", s);
   k_pf_mma<1><<<num_sms, kPfThreads, smem, s>>>(a, m.hq, m.dn);
+  FTMOE_PROF_END(s);
+  return cudaGetLastError();
+}
+
+bool prefill_router_supported(int H, int E) { return E % 128 == 0 && E <= kPfMaxE && H % 64 == 0; }
+
+// Exact split of each fp32 router row into three bf16 parts (w - W1 and
+// (w - W1) - W2 are exact in fp32, and the last remainder has at most 8
+// significant bits, so W1 + W2 + W3 == w), and an upper bound of its norm.
+__global__ void __launch_bounds__(256) k_router_split(const float* __restrict__ w, int H, uint16_t* __restrict__ wcat,
+                                                      float* __restrict__ wnorm) {
+  const int e = blockIdx.x;
+  __shared__ float red[8];
+  float q = 0.f;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    const float v = w[(int64_t)e * H + h];
+    const __nv_bfloat16 b1 = __float2bfloat16_rn(v);
+    const float r1 = __fsub_rn(v, __bfloat162float(b1));
+    const __nv_bfloat16 b2 = __float2bfloat16_rn(r1);
+    const float r2 = __fsub_rn(r1, __bfloat162float(b2));
+    const __nv_bfloat16 b3 = __float2bfloat16_rn(r2);
+    uint16_t* row = wcat + (int64_t)e * 3 * H;
+    row[h] = *reinterpret_cast<const uint16_t*>(&b1);
+    row[H + h] = *reinterpret_cast<const uint16_t*>(&b2);
+    row[2 * H + h] = *reinterpret_cast<const uint16_t*>(&b3);
+    q = fmaf(v, v, q);
+  }
+  q = warp_sum(q);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = q;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int i = 0; i < 8; ++i) t += red[i];
+    wnorm[e] = sqrtf(t) * (1.0f + 1e-5f);
+  }
+}
+
+cudaError_t launch_router_split(const float* w, int E, int H, uint16_t* wcat, float* wnorm, cudaStream_t s) {
+  k_router_split<<<E, 256, 0, s>>>(w, H, wcat, wnorm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_router(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
+  FTMOE_PROF_BEGIN("k_pf_router", s);
+  k_pf_mma<4><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.x, m.wr);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }

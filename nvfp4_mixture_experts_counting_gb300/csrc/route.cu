@@ -108,6 +108,24 @@ __global__ void k_xquant_sigma(RouteArgs a) {
   } else if (lane == 0) {
     a.sigma[t] = 0.f;
   }
+  if (a.xnorm) {
+    // sum of squares of the bf16 values (exact products, fp32 sums), with a
+    // relative margin far above the sum's rounding error
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + (int64_t)t * a.H);
+    float q = 0.f;
+    for (int i = lane; i < a.H / 8; i += 32) {
+      const uint4 v = xr[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+        q = fmaf(lo, lo, q);
+        q = fmaf(hi, hi, q);
+      }
+    }
+    q = warp_sum(q);
+    if (lane == 0) a.xnorm[t] = sqrtf(q) * (1.0f + 1e-5f);
+  }
 }
 
 // ------------------------------------------------------------------ router logits
@@ -438,16 +456,16 @@ cudaError_t launch_quantize_act_bf16(const uint16_t* a, int64_t rows, int K, uin
   return cudaGetLastError();
 }
 
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int parts) {
   cudaError_t err;
-  {
+  if (parts & kRouteXq) {
     const int wpb = 8;
     FTMOE_PROF_BEGIN("k_xquant_sigma", s);
     k_xquant_sigma<<<(a.T + wpb - 1) / wpb, wpb * 32, 0, s>>>(a);
     FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  {
+  if (parts & kRouteLogits) {
     dim3 grid((a.E + kRouterWarps - 1) / kRouterWarps, (a.T + kRouterTT - 1) / kRouterTT);
     size_t smem = (size_t)kRouterTT * a.H * 2;
     FTMOE_PROF_BEGIN("k_router_logits", s);
@@ -455,14 +473,14 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  {
+  if (parts & kRouteTopk) {
     size_t smem = (size_t)kTopkWarps * a.E * (4 + 4 + 8);
     FTMOE_PROF_BEGIN("k_topk", s);
     k_topk<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, smem, s>>>(a);
     FTMOE_PROF_END(s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  {
+  if (parts & kRouteSort) {
     size_t smem = (size_t)kSortWarps * a.E * 4;
     FTMOE_PROF_BEGIN("k_sort", s);
     k_sort<<<1, kSortThreads, smem, s>>>(a);

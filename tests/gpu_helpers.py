@@ -103,7 +103,10 @@ def check_routing(aux: AuxBufs, ref: moe.LayerResult):
     assert np.array_equal(got["offsets"], ref.offsets), "offsets differ"
     assert np.array_equal(got["perm"], ref.perm), "perm differs"
     assert np.array_equal(got["inv"], ref.inv), "inv differs"
-    assert np.allclose(got["topk_w"], ref.topk_w, rtol=1e-5, atol=1e-6), "routing weights differ"
+    # the weights are fp32 softmaxes of fp32 logits; the tensor-core router's
+    # logits carry up to ~2^-19 * ||x|| * ||w|| (~1e-4) of error, which moves a
+    # renormalised weight by at most twice that, relatively
+    assert np.allclose(got["topk_w"], ref.topk_w, rtol=5e-4, atol=1e-6), "routing weights differ"
 
 
 def check_output(out: torch.Tensor, ref_out: np.ndarray, rows=None):

@@ -140,3 +140,36 @@ def test_prefill_halves_sum_to_full(prefill):
     layer.forward(0, x, half, out_flags=ftmoe.OUT_FP32, i0=320, I_loc=320)
     torch.cuda.synchronize()
     check_output(half, ref.out64, rows=rows)
+
+
+# ------------------------------------------------------------------ tensor-core router
+
+
+def test_prefill_router_logit_error_within_bound(prefill):
+    """The tensor-core router's logits (x times the three exact bf16 parts of
+    each fp32 router row, fp32 accumulation) stay within the bound the top-k
+    certificate assumes, kappa * ||x|| * ||w|| with kappa = 2^-15, by a
+    margin of at least 16 on every seed tried: the bound is empirical for the
+    tensor-core accumulation, and this test is its measurement."""
+    from oracle import moe
+    wl, bank, layer = prefill
+    T = 4096
+    rw = bank.router_w.cpu().numpy().astype(np.float64)
+    rb = bank.router_bias.cpu().numpy().astype(np.float64)
+    wn = np.linalg.norm(rw, axis=1)
+    worst = 0.0
+    for step in range(3):
+        x = W.hidden(wl, T, step=10 + step, device=DEV)
+        logits = torch.empty((T, wl.E), dtype=torch.float32, device=DEV)
+        aux = AuxBufs(T, wl.top_k, wl.E)
+        aux.c.logits = logits.data_ptr()
+        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=DEV)
+        layer.forward(0, x, out, aux=aux.c)
+        torch.cuda.synchronize()
+        x64 = x.float().cpu().numpy().astype(np.float64)
+        exact = moe.router_logits(x64, rw, rb)
+        rel = np.abs(logits.cpu().numpy() - exact) / (np.linalg.norm(x64, axis=1)[:, None] * wn[None, :])
+        worst = max(worst, float(rel.max()))
+        idx, _ = moe.select_topk(exact, wl.top_k)
+        assert np.array_equal(aux.topk_idx.cpu().numpy(), idx)
+    assert worst <= 2.0 ** -15 / 16, f"largest relative logit error {worst:.3e}"
