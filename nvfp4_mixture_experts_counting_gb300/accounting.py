@@ -55,6 +55,12 @@ def kernel_unit_bytes(kernel: str, H: int, I_loc: int, sI_loc: int, E: int = 0):
         # routed down rows of every touched expert, plus the shared expert's
         # bf16 down columns (one launch streams both)
         return down_window_bytes(H, I_loc), "touched expert (down window), + shared down", H * sI_loc * 2
+    if kernel == "k_dtc_gate_up":
+        # routed gate_up rows of every touched expert, plus the shared expert's
+        # bf16 gate_up rows (one launch streams both)
+        return gate_up_window_bytes(H, I_loc), "touched expert (gate_up window), + shared gate_up", 2 * sI_loc * H * 2
+    if kernel == "k_dtc_down":
+        return down_window_bytes(H, I_loc), "touched expert (down window), + shared down", H * sI_loc * 2
     if kernel == "k_dec_route":
         # fp32 router and the shared expert's bf16 gate_up rows
         return 0, "launch (router + shared gate_up)", E * H * 4 + 2 * sI_loc * H * 2

@@ -27,6 +27,7 @@ constexpr int kDecMaxT = 32;
 constexpr int kDecSmemMax = 220 * 1024;
 
 __global__ void k_dec_route(DecodeArgs a);
+__global__ void k_dec_topk(DecodeArgs a);
 __global__ void k_dec_gate_up(DecodeArgs a);
 __global__ void k_dec_down(DecodeArgs a);
 
@@ -93,22 +94,28 @@ __device__ __forceinline__ void swiglu_quant16(float g, float u, int l, bool wri
 // ------------------------------------------------------------------ layouts
 
 // k_dec_route: the router CTAs' quarter partial sums, or, in the last router
-// CTA, every logit and bound plus the top-k and sort working sets.
+// CTA, every logit and bound plus the top-k and sort working sets: per-warp
+// token rows, a shared list of (token, candidate expert, compensated logit)
+// for the tokens whose top-k needs re-ranking (capacity 4E), and per-token
+// bookkeeping.
 struct RtSmem {
-  int logits_off, err_off, ch_off, cand_off, l64_off, idx_off, hist_off, scan_off, total;
+  int logits_off, err_off, ch_off, le_off, lt_off, lv_off, idx_off, hist_off, scan_off, tok_off, total, cap;
 };
 
 __host__ __device__ inline RtSmem rt_smem_layout(int T, int E, int top_k) {
   RtSmem L;
   int o = 0;
+  L.cap = 4 * E;
   L.logits_off = o; o += align16(8 * E * 4);      // one token's logits, per warp
   L.err_off = o;    o += align16(8 * E * 4);      // and their bounds
   L.ch_off = o;     o += align16(8 * E);          // chosen flags, per warp
-  L.cand_off = o;   o += align16(8 * E * 4);      // candidates, per warp
-  L.l64_off = o;    o += 8 * E * 8;               // compensated logits of candidates, per warp
+  L.le_off = o;     o += align16(L.cap * 4);      // re-rank list: expert
+  L.lt_off = o;     o += align16(L.cap * 4);      //               token
+  L.lv_off = o;     o += L.cap * 8;               //               compensated logit
   L.idx_off = o;    o += align16(T * top_k * 4);  // chosen experts of every pair
   L.hist_off = o;   o += align16(8 * E * 4);      // sort histograms
   L.scan_off = o;   o += 32 * 4;
+  L.tok_off = o;    o += 32 * 16 + 16;            // per token: state, start, count, lower end
   const int router = 8 * T * 2 * 4;               // quarter partial sums of the router CTAs
   L.total = o > router ? o : router;
   return L;

@@ -1,9 +1,10 @@
-// k_dec_route: routing for the decode path.  Router CTAs compute the fp32
-// logits of 2 experts each (H split over 4 warps) with a rigorous error
-// bound; other CTAs run the shared expert's gate_up + SwiGLU and the x
-// quantisation with the shared gate; the last router CTA to finish stages
-// every logit and bound in shared memory, runs top-k (certified, with compensated
-// re-ranking of uncertain candidates) and the counting sort.
+// k_dec_route: routing for the decode path.  Router CTAs quantise a slice of
+// the activations and compute the fp32 logits of 2 experts each (H split
+// over 4 warps) with a rigorous error bound; optional CTAs run the shared
+// expert's gate_up + SwiGLU (the CUDA-core decode path); one CTA computes
+// the shared gate sigma; the last router CTA to finish stages every logit
+// and bound in shared memory, runs top-k (certified; the whole CTA re-ranks
+// uncertain tokens with compensated sums) and the counting sort.
 //
 // Pages: PR #385 "feat(qwen4_exp): tensor parallelism for Qwen3.8-Flash-Next
 // (offload backend)", "What this adds" (replicated router; shared expert and
@@ -19,11 +20,32 @@ __device__ __forceinline__ bool key_before(float la, int ea, float lb, int eb) {
 // Top-k of token t by one warp, from logits lg and bounds er in shared
 // memory.  The fp32 ranking is certified with the error bounds (every chosen
 // expert's interval lies above the next one's and above every unchosen
-// expert's); if it is not, every expert that could belong to the top-k is
-// re-ranked from compensated double-fp32 sums (about 2^-48 relative; FP64 is
-// far slower on this GPU).  Ties go to the lower index.
-__device__ void dec_topk_token(const DecodeArgs& a, int t, int lane, const float* lg, const float* er,
-                               uint8_t* ch, int* cand, df32* l64, int* s_idx) {
+// expert's).  A certified token's slots and weights are written here;
+// otherwise the lowest lower end of the chosen intervals is returned in
+// *lmin_out (every expert whose interval reaches it is a candidate) and the
+// token is re-ranked afterwards.  Ties go to the lower index.
+__device__ __forceinline__ void dec_write_slots(const DecodeArgs& a, int t, int lane, int my_idx, float my_l,
+                                                float lmax, const float* lg, int* s_idx) {
+  const int E = a.r.E, k = a.r.top_k;
+  // routing weights: softmax over the chosen (norm_topk_prob) or over all
+  const float ex = (lane < k) ? expf(my_l - lmax) : 0.f;
+  float den;
+  if (a.r.norm_topk_prob) {
+    den = warp_sum(ex);
+  } else {
+    float s = 0.f;
+    for (int e = lane; e < E; e += 32) s += expf(lg[e] - lmax);
+    den = warp_sum(s);
+  }
+  if (lane < k) {
+    a.r.topk_idx[(int64_t)t * k + lane] = my_idx;
+    a.r.topk_w[(int64_t)t * k + lane] = ex / den;
+    s_idx[t * k + lane] = my_idx;
+  }
+}
+
+__device__ bool dec_topk_fast(const DecodeArgs& a, int t, int lane, const float* lg, const float* er, uint8_t* ch,
+                              int* s_idx, float* lmin_out) {
   const int E = a.r.E, k = a.r.top_k;
   for (int e = lane; e < E; e += 32) ch[e] = 0;
   __syncwarp();
@@ -60,63 +82,104 @@ __device__ void dec_topk_token(const DecodeArgs& a, int t, int lane, const float
   for (int e = lane; e < E; e += 32)
     if (!ch[e] && lg[e] + er[e] >= lmin_lo) reach = true;
   if (__any_sync(0xffffffffu, reach)) certified = false;
-  if (!certified) {
-    if (lane == 0 && a.r.n_rerank) atomicAdd(a.r.n_rerank, 1ull);  // telemetry only
-    int nc = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      bool c = false;
-      if (e < E) c = ch[e] || (lg[e] + er[e] >= lmin_lo);
-      const unsigned m = __ballot_sync(0xffffffffu, c);
-      if (c) cand[nc + __popc(m & ((1u << lane) - 1))] = e;
-      nc += __popc(m);
+  *lmin_out = lmin_lo;
+  if (certified) dec_write_slots(a, t, lane, my_idx, my_l, lmax, lg, s_idx);
+  return certified;
+}
+
+// Re-rank of the uncertain tokens by the whole CTA, in rounds: each warp
+// lists the candidates of its pending tokens (every expert whose interval
+// reaches the token's lowest chosen lower end) while the shared list has
+// room; then every warp computes compensated logits of list entries in turn
+// (one warp per entry, about 2^-48 relative; FP64 is far slower on this
+// GPU); then each token's warp selects its k among its candidates.
+__device__ void dec_rerank(const DecodeArgs& a, const RtSmem& L, unsigned char* sm, int* s_idx) {
+  const int E = a.r.E, k = a.r.top_k, T = a.T, H = a.r.H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* le = reinterpret_cast<int*>(sm + L.le_off);
+  int* lt = reinterpret_cast<int*>(sm + L.lt_off);
+  df32* lv = reinterpret_cast<df32*>(sm + L.lv_off);
+  int* state = reinterpret_cast<int*>(sm + L.tok_off);  // 0 done, 1 pending, 2 listed
+  int* start = state + 32;
+  int* cnt = start + 32;
+  float* lmin = reinterpret_cast<float*>(cnt + 32);
+  int* s_cnt = reinterpret_cast<int*>(lmin + 32);
+  int* s_any = s_cnt + 1;
+  // every round lists at least one pending token (a token has at most E
+  // candidates and the list holds 4E), so T rounds always suffice
+  for (int round = 0; round <= T; ++round) {
+    if (tid == 0) { *s_cnt = 0; *s_any = 0; }
+    for (int i = tid; i < L.cap; i += kRtThreads) lt[i] = -1;
+    __syncthreads();
+    for (int t = warp; t < T; t += 8) {
+      if (state[t] != 1) continue;
+      if (lane == 0) *s_any = 1;
+      const float* lg = a.r.logits + (int64_t)t * E;
+      const float* er = a.r.err + (int64_t)t * E;
+      int nc = 0;
+      for (int e = lane; e < E; e += 32) nc += (__ldcg(lg + e) + __ldcg(er + e) >= lmin[t]) ? 1 : 0;
+      nc = __reduce_add_sync(0xffffffffu, nc);
+      int st = 0;
+      if (lane == 0) st = atomicAdd(s_cnt, nc);
+      st = __shfl_sync(0xffffffffu, st, 0);
+      if (st + nc > L.cap) break;  // no room left this round
+      int w = st;
+      for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        const bool c = e < E && (__ldcg(lg + e) + __ldcg(er + e) >= lmin[t]);
+        const unsigned m = __ballot_sync(0xffffffffu, c);
+        if (c) {
+          le[w + __popc(m & ((1u << lane) - 1))] = e;
+          lt[w + __popc(m & ((1u << lane) - 1))] = t;
+        }
+        w += __popc(m);
+      }
+      if (lane == 0) { start[t] = st; cnt[t] = nc; state[t] = 2; }
+      __syncwarp();
     }
-    __syncwarp();
-    const uint16_t* xrow = a.r.x + (int64_t)t * a.r.H;
-    for (int c = 0; c < nc; ++c) {
-      const int e = cand[c];
-      const df32 v = logit_df32(xrow, a.r.router_w + (int64_t)e * a.r.H, a.r.H,
+    __syncthreads();
+    if (!*s_any) break;
+    const int n = min(*s_cnt, L.cap);
+    for (int i = warp; i < n; i += 8) {
+      if (lt[i] < 0) continue;
+      const int e = le[i];
+      const df32 v = logit_df32(a.r.x + (int64_t)lt[i] * H, a.r.router_w + (int64_t)e * H, H,
                                 a.r.router_bias ? a.r.router_bias[e] : 0.f, lane);
-      if (lane == 0) l64[c] = v;
+      if (lane == 0) lv[i] = v;
     }
-    __syncwarp();
-    const df32 none = {-INFINITY, 0.f};
-    for (int j = 0; j < k; ++j) {
-      df32 bl = none;
-      int be = 0x7fffffff, bc = -1;
-      for (int c = lane; c < nc; c += 32) {
-        const df32 v = l64[c];
-        const int e = cand[c];
-        if (v.hi != -INFINITY && df_before(v, e, bl, be)) { bl = v; be = e; bc = c; }
-      }
+    __syncthreads();
+    for (int t = warp; t < T; t += 8) {
+      if (state[t] != 2) continue;
+      const int c0 = start[t], nc = cnt[t];
+      int my_idx = 0;
+      float my_l = 0.f, lmax = -INFINITY;
+      const df32 none = {-INFINITY, 0.f};
+      for (int j = 0; j < k; ++j) {
+        df32 bl = none;
+        int be = 0x7fffffff, bc = -1;
+        for (int c = lane; c < nc; c += 32) {
+          const df32 v = lv[c0 + c];
+          const int e = le[c0 + c];
+          if (v.hi != -INFINITY && df_before(v, e, bl, be)) { bl = v; be = e; bc = c; }
+        }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const df32 ol = {__shfl_xor_sync(0xffffffffu, bl.hi, o), __shfl_xor_sync(0xffffffffu, bl.lo, o)};
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-        if (df_before(ol, oe, bl, be)) { bl = ol; be = oe; bc = oc; }
+        for (int o = 16; o > 0; o >>= 1) {
+          const df32 ol = {__shfl_xor_sync(0xffffffffu, bl.hi, o), __shfl_xor_sync(0xffffffffu, bl.lo, o)};
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+          if (df_before(ol, oe, bl, be)) { bl = ol; be = oe; bc = oc; }
+        }
+        if (lane == j) { my_idx = be; my_l = bl.hi; }
+        if (j == 0) lmax = bl.hi;
+        __syncwarp();
+        if (lane == 0 && bc >= 0) lv[c0 + bc] = none;
+        __syncwarp();
       }
-      if (lane == j) { my_idx = be; my_l = bl.hi; }
-      if (j == 0) lmax = bl.hi;
-      __syncwarp();
-      if (lane == 0) l64[bc] = none;
+      dec_write_slots(a, t, lane, my_idx, my_l, lmax, a.r.logits + (int64_t)t * E, s_idx);
+      if (lane == 0) state[t] = 0;
       __syncwarp();
     }
-  }
-  // routing weights: softmax over the chosen (norm_topk_prob) or over all
-  const float ex = (lane < k) ? expf(my_l - lmax) : 0.f;
-  float den;
-  if (a.r.norm_topk_prob) {
-    den = warp_sum(ex);
-  } else {
-    float s = 0.f;
-    for (int e = lane; e < E; e += 32) s += expf(lg[e] - lmax);
-    den = warp_sum(s);
-  }
-  if (lane < k) {
-    a.r.topk_idx[(int64_t)t * k + lane] = my_idx;
-    a.r.topk_w[(int64_t)t * k + lane] = ex / den;
-    s_idx[t * k + lane] = my_idx;
+    __syncthreads();
   }
 }
 
@@ -253,6 +316,52 @@ __device__ void dec_split(const DecodeArgs& a, int* pre, int* scan) {
   }
 }
 
+// Top-k of every token (certified; uncertain tokens re-ranked by the whole
+// CTA), the counting sort and the gate_up work split, by one CTA.
+__device__ void dec_tail(const DecodeArgs& a, unsigned char* sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = a.T, E = a.r.E;
+  const RtSmem L = rt_smem_layout(T, E, a.top_k);
+  float* s_lg = reinterpret_cast<float*>(sm + L.logits_off) + warp * E;  // one token row per warp
+  float* s_er = reinterpret_cast<float*>(sm + L.err_off) + warp * E;
+  uint8_t* ch = sm + L.ch_off + warp * E;
+  int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
+  int* state = reinterpret_cast<int*>(sm + L.tok_off);
+  float* lmin = reinterpret_cast<float*>(state + 96);
+  for (int t = warp; t < T; t += 8) {
+    for (int e = lane; e < E; e += 32) {
+      s_lg[e] = __ldcg(a.r.logits + (int64_t)t * E + e);
+      s_er[e] = __ldcg(a.r.err + (int64_t)t * E + e);
+    }
+    __syncwarp();
+    float lo;
+    const bool cert = dec_topk_fast(a, t, lane, s_lg, s_er, ch, s_idx, &lo);
+    if (lane == 0) {
+      state[t] = cert ? 0 : 1;
+      lmin[t] = lo;
+      if (!cert && a.r.n_rerank) atomicAdd(a.r.n_rerank, 1ull);  // telemetry only
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  dec_rerank(a, L, sm, s_idx);
+  int* hist = reinterpret_cast<int*>(sm + L.hist_off);
+  int* scan = reinterpret_cast<int*>(sm + L.scan_off);
+  dec_sort(a, s_idx, hist, scan);
+  __syncthreads();
+  dec_split(a, hist, scan);
+}
+
+// The routing tail as its own one-CTA kernel (after the router kernel).
+__global__ void __launch_bounds__(kRtThreads) k_dec_topk(DecodeArgs a) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  // let the gate_up kernel launch now: its first phase (the shared expert)
+  // needs no routing, and this one-CTA grid is already resident
+  pdl_launch_dependents();
+  pdl_wait();
+  dec_tail(a, sm);
+}
+
 __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
   __shared__ int s_last;
@@ -261,6 +370,27 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
   const int H = a.r.H, T = a.T, E = a.r.E;
   const int b = blockIdx.x;
   if (b < a.n_router_ctas) {
+    // ---- this CTA's slice of the activation quantisation (global 1.0)
+    {
+      const int nb = T * (H / kBlock);
+      const int per = (nb + a.n_router_ctas - 1) / a.n_router_ctas;
+      const int q0 = b * per, q1 = min(nb, q0 + per);
+      for (int blk = q0 + tid; blk < q1; blk += kRtThreads) {
+        float v[16];
+        const uint4* p = reinterpret_cast<const uint4*>(a.r.x + (int64_t)blk * kBlock);
+        const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+        const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          v[2 * qq] = __uint_as_float(words[qq] << 16);
+          v[2 * qq + 1] = __uint_as_float(words[qq] & 0xffff0000u);
+        }
+        uint8_t c[8];
+        const uint8_t sc = quantize_block16(v, 1.0f, c);
+        *reinterpret_cast<uint2*>(a.r.xq_codes + (int64_t)blk * 8) = pack8(c);
+        a.r.xq_scales[blk] = sc;
+      }
+    }
     // ---- router: experts 2b (warps 0-3) and 2b+1 (warps 4-7), H in quarters
     float* part = reinterpret_cast<float*>(sm);  // [8 warps][T][2]
     const int e = 2 * b + (warp >> 2);
@@ -339,6 +469,7 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
         a.r.err[(int64_t)t * E + ee] = gamma * bb + 1.2e-7f * fabsf(l) + 1e-30f;
       }
     }
+    if (a.split_tail) return;  // top-k and the sort run in k_dec_topk
     // the last router CTA to arrive runs top-k and the sort
     __threadfence();
     __syncthreads();
@@ -346,28 +477,7 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    const RtSmem L = rt_smem_layout(T, E, a.top_k);
-    float* s_lg = reinterpret_cast<float*>(sm + L.logits_off) + warp * E;  // one token row per warp
-    float* s_er = reinterpret_cast<float*>(sm + L.err_off) + warp * E;
-    uint8_t* ch = sm + L.ch_off + warp * E;
-    int* cand = reinterpret_cast<int*>(sm + L.cand_off) + warp * E;
-    df32* l64 = reinterpret_cast<df32*>(sm + L.l64_off) + warp * E;
-    int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
-    for (int t = warp; t < T; t += 8) {
-      for (int e = lane; e < E; e += 32) {
-        s_lg[e] = __ldcg(a.r.logits + (int64_t)t * E + e);
-        s_er[e] = __ldcg(a.r.err + (int64_t)t * E + e);
-      }
-      __syncwarp();
-      dec_topk_token(a, t, lane, s_lg, s_er, ch, cand, l64, s_idx);
-      __syncwarp();
-    }
-    __syncthreads();
-    int* hist = reinterpret_cast<int*>(sm + L.hist_off);
-    int* scan = reinterpret_cast<int*>(sm + L.scan_off);
-    dec_sort(a, s_idx, hist, scan);
-    __syncthreads();
-    dec_split(a, hist, scan);
+    dec_tail(a, sm);
     if (tid == 0) *a.counter = 0;  // ready for the next launch
     return;
   }
@@ -447,35 +557,21 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
     }
     return;
   }
-  // ---- x quantisation (global 1.0) and sigma_t = sigmoid(g . x_t)
-  const int nb = H / kBlock;
+  // ---- sigma_t = sigmoid(g . x_t), one warp per token
   for (int t = warp; t < T; t += 8) {
     float z = 0.f;
-    for (int bb = lane; bb < nb; bb += 32) {
-      const int64_t blk = (int64_t)t * nb + bb;
-      float v[16];
-      const uint4* p = reinterpret_cast<const uint4*>(a.r.x + blk * kBlock);
-      const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
-      const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    if (a.r.sh_gate) {
+      const uint4* xr = reinterpret_cast<const uint4*>(a.r.x + (int64_t)t * H);
+      const uint4* gr = reinterpret_cast<const uint4*>(a.r.sh_gate);
+      for (int c = lane; c < H / 8; c += 32) {
+        const uint4 xv = __ldg(xr + c), gv = __ldg(gr + c);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-      for (int qq = 0; qq < 8; ++qq) {
-        v[2 * qq] = __uint_as_float(words[qq] << 16);
-        v[2 * qq + 1] = __uint_as_float(words[qq] & 0xffff0000u);
-      }
-      if (a.r.sh_gate) {
-        const uint4* gp = reinterpret_cast<const uint4*>(a.r.sh_gate + bb * kBlock);
-        const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
-        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq) {
-          z = fmaf(v[2 * qq], __uint_as_float(gw[qq] << 16), z);
-          z = fmaf(v[2 * qq + 1], __uint_as_float(gw[qq] & 0xffff0000u), z);
+        for (int qq = 0; qq < 4; ++qq) {
+          z = fmaf(__uint_as_float(xw[qq] << 16), __uint_as_float(gw[qq] << 16), z);
+          z = fmaf(__uint_as_float(xw[qq] & 0xffff0000u), __uint_as_float(gw[qq] & 0xffff0000u), z);
         }
       }
-      uint8_t c[8];
-      const uint8_t s = quantize_block16(v, 1.0f, c);
-      *reinterpret_cast<uint2*>(a.r.xq_codes + blk * 8) = pack8(c);
-      a.r.xq_scales[blk] = s;
     }
     z = warp_sum(z);
     if (lane == 0) a.r.sigma[t] = a.r.sh_gate ? 1.0f / (1.0f + expf(-z)) : 0.f;

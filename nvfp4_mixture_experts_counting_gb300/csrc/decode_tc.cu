@@ -1,0 +1,748 @@
+// Decode path on the tensor cores (1 <= T <= 32 tokens).
+//
+// At decode sizes the layer is a read of the touched experts' bytes (Issue
+// #62 "Offloaded MoE ignores tensor parallelism ...", "Why TP=2 loses
+// today"; PR #385 "feat(qwen4_exp): tensor parallelism for
+// Qwen3.8-Flash-Next (offload backend)", "Measurements").  Here the weights
+// are the 128-row A operand of a block-scaled NVFP4 MMA and the (at most 32)
+// tokens are N, so the SMs only issue TMA copies and MMAs while the weight
+// bytes stream; E2M1 values never pass through the CUDA cores.
+//
+//   k_dec_route      (decode_route.cu) routing and the activation codes
+//   k_dtc_gate_up    work units: (touched expert, 64 gate + 64 up window rows)
+//                    against every token's resident activation codes, and
+//                    (shared expert, 64 + 64 bf16 rows) against bf16 x; the
+//                    epilogue picks each pair's column, applies SwiGLU and
+//                    quantises the intermediate (NVFP4, global 1.0), or rounds
+//                    the shared intermediate to bf16
+//   k_dtc_down       CTA (128 output rows, expert group): the group's down
+//                    rows against each expert's intermediates, accumulated per
+//                    token in a fixed order; one more group holds the shared
+//                    expert (bf16) times sigmoid(gate).  The last CTA of an
+//                    output tile adds the groups' partials in group order, so
+//                    the result does not depend on timing (PR #385,
+//                    "Correctness": no value atomics).
+#include <cudaTypedefs.h>
+
+#include "decode_common.cuh"
+#include "tc_common.cuh"
+
+namespace ftmoe {
+
+namespace {
+
+constexpr int kDtThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kDtSmem = 220 * 1024;
+constexpr int kDtA = 16384;      // 128 weight rows x 128 bytes
+constexpr int kDtB = 4096;       // up to 32 token / pair rows x 128 bytes
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+  return p + ((1024 - (smem_u32(p) & 1023)) & 1023);
+}
+
+// ---- k_dtc_gate_up shared memory: stages (A tile, B tile for shared units,
+// A scale blocks), every token's activation codes (one [npad][128] box per
+// 256-element K tile), their scale blocks, the up values of the epilogue.
+// Routing metadata staged once per CTA: touched experts and their record
+// pointers, expert offsets, and per sorted position the token (and, for the
+// down kernel, the routing weight).
+struct Meta {
+  int touched_off, rec_off, off_off, tok_off, w_off, bytes;
+};
+
+__host__ __device__ inline Meta meta_layout(int E, int P, int base) {
+  Meta M;
+  int o = base;
+  M.rec_off = o;     o += E * 8;
+  M.touched_off = o; o += align16(E * 4);
+  M.off_off = o;     o += align16((E + 1) * 4);
+  M.tok_off = o;     o += align16(P * 4);
+  M.w_off = o;       o += align16(P * 4);
+  M.bytes = o - base;
+  return M;
+}
+
+struct DgLayout {
+  int npad, nkt, nks, stage, nst, xres_off, sfb_off, u_off, meta_off, bar_off, total;
+};
+
+__host__ __device__ inline DgLayout dg_layout(int H, int T, int E, int P) {
+  DgLayout L;
+  L.npad = T <= 16 ? 16 : 32;
+  L.nkt = H / 256;
+  L.nks = H / 64;
+  L.stage = kDtA + kDtB + 2048;  // 22 KB, a multiple of 1024
+  const int xres = L.nkt * L.npad * 128, sfb = L.nks * 512, u = 2 * 32 * 64 * 4;
+  const int meta = meta_layout(E, P, 0).bytes;
+  const int nst = (kDtSmem - 1024 - xres - sfb - u - meta - 256) / L.stage;
+  L.nst = nst > 8 ? 8 : nst;
+  int o = (L.nst > 0 ? L.nst : 0) * L.stage;
+  L.xres_off = o; o += xres;
+  L.sfb_off = o;  o += sfb;
+  L.u_off = o;    o += u;
+  L.meta_off = o; o += meta;
+  L.bar_off = o;  o += 256;
+  L.total = o + 1024;
+  return L;
+}
+
+// All threads: stage the routing metadata (after the routing kernels).
+__device__ __forceinline__ void stage_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M, int nt) {
+  const int E = a.r.E, P = a.T * a.top_k, k = a.top_k;
+  int* s_touched = reinterpret_cast<int*>(sm + M.touched_off);
+  const uint8_t** s_rec = reinterpret_cast<const uint8_t**>(sm + M.rec_off);
+  int* s_off = reinterpret_cast<int*>(sm + M.off_off);
+  int* s_tok = reinterpret_cast<int*>(sm + M.tok_off);
+  float* s_w = reinterpret_cast<float*>(sm + M.w_off);
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = a.r.offsets[i];
+  for (int i = threadIdx.x; i < nt; i += blockDim.x) {
+    const int e = a.r.touched[i];
+    s_touched[i] = e;
+    s_rec[i] = a.rec[e];
+  }
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    const int p = a.r.perm[i];
+    s_tok[i] = p / k;
+    s_w[i] = a.r.topk_w[p];
+  }
+}
+
+// ---- k_dtc_down shared memory: stages (A tile, B tile, A and B scale
+// blocks) and the per-token partial sums of the CTA's 128 output rows.
+struct DdLayout {
+  int npad, stage, nst, part_off, meta_off, bar_off, total;
+};
+
+__host__ __device__ inline DdLayout dd_layout(int T, int E, int P) {
+  DdLayout L;
+  L.npad = T <= 16 ? 16 : 32;
+  L.stage = kDtA + kDtB + 2048 + 2048;  // 24 KB
+  const int part = 32 * 128 * 4;
+  const int meta = meta_layout(E, P, 0).bytes;
+  const int nst = (kDtSmem - 1024 - part - meta - 256) / L.stage;
+  L.nst = nst > 8 ? 8 : nst;
+  int o = (L.nst > 0 ? L.nst : 0) * L.stage;
+  L.part_off = o; o += part;
+  L.meta_off = o; o += meta;
+  L.bar_off = o;  o += 256;
+  L.total = o + 1024;
+  return L;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ gate_up
+
+__global__ void __launch_bounds__(kDtThreads, 1)
+    k_dtc_gate_up(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_gu,
+                  const __grid_constant__ CUtensorMap map_xq, const __grid_constant__ CUtensorMap map_sgu,
+                  const __grid_constant__ CUtensorMap map_x) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* sm = align1024(sm_raw);
+  const int H = a.H, T = a.T, E = a.r.E;
+  const DgLayout L = dg_layout(H, T, E, T * a.top_k);
+  const Meta M = meta_layout(E, T * a.top_k, L.meta_off);
+  const int* s_touched = reinterpret_cast<const int*>(sm + M.touched_off);
+  const uint8_t* const* s_rec = reinterpret_cast<const uint8_t* const*>(sm + M.rec_off);
+  const int* s_off = reinterpret_cast<const int*>(sm + M.off_off);
+  const int* s_tok = reinterpret_cast<const int*>(sm + M.tok_off);
+  const int NST = L.nst, npad = L.npad;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bar_off);
+  uint64_t* empty = full + 8;
+  uint64_t* acc_full = empty + 8;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* xbar = acc_empty + 2;
+  uint64_t* drain = xbar + 1;
+  uint64_t* u_full = drain + 1;   // [2] up values written (the two up warps arrive)
+  uint64_t* u_free = u_full + 2;  // [2] up values consumed (the two gate warps arrive)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(u_free + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* U0 = reinterpret_cast<float*>(sm + L.u_off);  // [2][32 pairs][64]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // TMEM columns: accumulators [0, 2 npad), activation scales (4 per K
+  // step), then 16 per stage for the weight scales
+  const uint32_t kSfbCol = 64, kSfaCol = 64 + 4 * L.nks;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 4); }
+    mbar_init(xbar, 1);
+    mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) { mbar_init(&u_full[b], 2); mbar_init(&u_free[b], 2); }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_gu);
+    tma_prefetch_desc(&map_xq);
+    tma_prefetch_desc(&map_sgu);
+    tma_prefetch_desc(&map_x);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int J = a.win.I_loc / 64, Js = a.sh_gate_up ? a.s_I_loc / 64 : 0;
+  const int nkt_s = H / 64;  // bf16 K tiles of the shared gate_up (K = H)
+  const int row0 = a.win.row0, Iw = a.win.Iw;
+  const uint32_t id_f4 = idesc_nvf4(128, npad), id_bf = idesc_bf16(128, npad);
+  // Two phases.  0: the shared expert's units (they need only x, so they run
+  // while the routing kernels still work); 1: after the routing is known,
+  // this CTA's equal share of the routed units (touched expert, 64-row
+  // window tile), a contiguous range.  Ring positions carry over.
+  int kk = 0, ui = 0, nt = 0, r0 = 0;
+  const int q = warp & 3;
+  const bool up = q >= 2;
+  const int i = 32 * (q & 1) + lane;
+  for (int phase = 0; phase < 2; ++phase) {
+    int n_my;
+    if (phase == 0) {
+      n_my = (int)blockIdx.x < Js ? (Js - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    } else {
+      pdl_wait();  // routing and the activation codes
+      pdl_launch_dependents();
+      nt = a.r.n_touched[0];
+      stage_meta(a, sm, M, nt);
+      if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(xbar, L.nkt * npad * 128);
+        for (int kt = 0; kt < L.nkt; ++kt)
+          tma_load_2d(sm + L.xres_off + kt * npad * 128, &map_xq, kt * 128, 0, xbar);
+      }
+      if (warp == 1) {
+        // activation scale blocks into TMEM (once)
+        unsigned char* sfb = sm + L.sfb_off;
+        for (int ii = lane; ii < L.nks * 32; ii += 32) {
+          const int ks = ii >> 5, t = ii & 31;
+          uint32_t w = 0;
+          if (t < T) w = *reinterpret_cast<const uint32_t*>(a.r.xq_scales + (int64_t)t * (H / 16) + 4 * ks);
+          *reinterpret_cast<uint32_t*>(sfb + ks * 512 + t * 16) = w;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          for (int ks = 0; ks < L.nks; ++ks) tc_cp_sf(tmem + kSfbCol + 4 * ks, sdesc_sf(smem_u32(sfb) + 512 * ks));
+      }
+      __syncthreads();
+      const int R = nt * J;
+      r0 = (int)((int64_t)R * blockIdx.x / gridDim.x);
+      n_my = (int)((int64_t)R * (blockIdx.x + 1) / gridDim.x) - r0;
+    }
+    if (warp == 0) {
+      // ---------------- TMA producer
+      if (lane == 0) {
+        for (int it = 0; it < n_my && !*abort_flag; ++it) {
+          const bool shared = phase == 0;
+          const int rr = r0 + it;
+          const int j = shared ? (int)blockIdx.x + it * (int)gridDim.x : rr % J;
+          const int e = shared ? 0 : s_touched[rr / J];
+          const uint8_t* rec = shared ? nullptr : s_rec[rr / J];
+          const int nkt_u = shared ? nkt_s : L.nkt;
+          for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
+            const int s = kk % NST;
+            if (kk >= NST && !mbar_wait(&empty[s], ((kk / NST) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+            unsigned char* sa = sm + s * L.stage;
+            if (shared) {
+              mbar_arrive_expect_tx(&full[s], kDtA + npad * 128);
+              tma_load_2d(sa, &map_sgu, kt * 128, a.s_row0 + 64 * j, &full[s]);
+              tma_load_2d(sa + kDtA / 2, &map_sgu, kt * 128, a.s_Iw + a.s_row0 + 64 * j, &full[s]);
+              tma_load_2d(sa + kDtA, &map_x, kt * 128, 0, &full[s]);
+            } else {
+              mbar_arrive_expect_tx(&full[s], kDtA + 2048);
+              tma_load_3d(sa, &map_gu, kt * 128, row0 + 64 * j, e, &full[s]);
+              tma_load_3d(sa + kDtA / 2, &map_gu, kt * 128, Iw + row0 + 64 * j, e, &full[s]);
+              bulk_g2s(sa + kDtA + kDtB, rec + a.lay.gu_sf + ((int64_t)(row0 / 64 + j) * L.nks + 4 * kt) * 512,
+                       2048, &full[s]);
+            }
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------- MMA issuer
+      if (lane == 0) {
+        bool ok = phase == 0 || mbar_wait(xbar, 0, a.r.status);
+        if (!ok) *abort_flag = 1;
+        for (int it = 0; ok && it < n_my && !*abort_flag; ++it, ++ui) {
+          const bool shared = phase == 0;
+          const int nkt_u = shared ? nkt_s : L.nkt;
+          const int buf = ui & 1;
+          if (ui >= 2 && !mbar_wait(&acc_empty[buf], ((ui >> 1) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + buf * npad;
+          for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
+            const int s = kk % NST;
+            if (!mbar_wait(&full[s], (kk / NST) & 1, a.r.status)) { *abort_flag = 1; ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(sm + s * L.stage);
+            const uint64_t adesc = sdesc_k_sw128(sa);
+            if (shared) {
+              const uint64_t bdesc = sdesc_k_sw128(sa + kDtA);
+              for (int ks = 0; ks < 4; ++ks) tc_mma_bf16(d, adesc + 2 * ks, bdesc + 2 * ks, id_bf, (kt | ks) != 0);
+            } else {
+              const uint32_t sfa_col = tmem + kSfaCol + 16 * s;
+              for (int ks = 0; ks < 4; ++ks) tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
+              const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + L.xres_off + kt * npad * 128));
+              for (int ks = 0; ks < 4; ++ks)
+                tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, id_f4, sfa_col + 4 * ks,
+                            tmem + kSfbCol + 4 * (4 * kt + ks), (kt | ks) != 0);
+            }
+            tc_commit(&empty[s]);
+          }
+          if (!ok) break;
+          tc_commit(&acc_full[buf]);
+        }
+      }
+    } else {
+      // ---------------- epilogue: warp q = w % 4 holds TMEM lanes 32q..32q+31:
+      // gate rows (q = 0, 1) and up rows (q = 2, 3) of window index i.  The
+      // up warps hand their values to the gate warps through a double
+      // buffer guarded by mbarriers (bounded waits, so a timeout anywhere
+      // cannot strand a warp).
+      for (int it = 0; it < n_my && !*abort_flag; ++it, ++ui) {
+        const int buf = ui & 1;
+        const bool sh = phase == 0;
+        const int rr = r0 + it;
+        const int ti = sh ? 0 : rr / J, j = sh ? (int)blockIdx.x + it * (int)gridDim.x : rr % J;
+        const int e = sh ? 0 : s_touched[ti];
+        const int s0 = sh ? 0 : s_off[e];
+        const int m = sh ? T : s_off[e + 1] - s0;  // columns this unit uses
+        // the row global is loaded before the accumulator wait
+        const float gl =
+            sh ? 1.f : reinterpret_cast<const float*>(s_rec[ti] + a.lay.gu_global)[(up ? Iw : 0) + row0 + 64 * j + i];
+        if (!mbar_wait(&acc_full[buf], (ui >> 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * npad;
+        float* U = U0 + buf * 32 * 64;
+        bool ok = true;
+        if (up) {
+          if (ui >= 2 && !mbar_wait(&u_free[buf], ((ui >> 1) - 1) & 1, a.r.status)) ok = false;
+          if (ok)
+            for (int r = 0; r < m; ++r) U[r * 64 + i] = tc_ld1_wait(taddr + (sh ? r : s_tok[s0 + r])) * gl;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&u_full[buf]);
+        } else {
+          if (!mbar_wait(&u_full[buf], (ui >> 1) & 1, a.r.status)) ok = false;
+          if (ok && sh) {
+            // shared expert: hs[t][64 j + i] = bf16(silu(gate) * up)
+            for (int t = 0; t < T; ++t) {
+              const __nv_bfloat16 hb = __float2bfloat16_rn(silu(tc_ld1_wait(taddr + t)) * U[t * 64 + i]);
+              a.hs[(int64_t)t * a.s_I_loc + 64 * j + i] = *reinterpret_cast<const uint16_t*>(&hb);
+            }
+          } else if (ok) {
+            for (int r = 0; r < m; ++r) {
+              const int pos = s0 + r;
+              const float g = tc_ld1_wait(taddr + s_tok[pos]) * gl;
+              const float h = silu(g) * U[r * 64 + i];
+              // NVFP4 quantisation of the 16-element block held by this half-warp
+              float amax = fabsf(h);
+#pragma unroll
+              for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 16));
+              const uint8_t sc = e4m3_encode(__fdiv_rn(amax, kE2M1Max));
+              const float dsc = e4m3_decode(sc);
+              uint32_t code = 0;
+              if (sc != 0 && dsc != 0.f) code = e2m1x2_encode(__fdiv_rn(h, dsc), 0.0f) & 0xF;
+              // gather the half-warp's 16 nibbles into 8 bytes held by its first lane
+              const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+              const uint32_t byte = (code | (hi << 4)) & 0xFF;  // valid on even lanes
+              uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                w0 |= (__shfl_sync(0xffffffffu, byte, (lane & 16) + 2 * b) & 0xFF) << (8 * b);
+                w1 |= (__shfl_sync(0xffffffffu, byte, (lane & 16) + 8 + 2 * b) & 0xFF) << (8 * b);
+              }
+              if ((lane & 15) == 0) {
+                const int half = lane >> 4;
+                *reinterpret_cast<uint2*>(a.hq_codes + (int64_t)pos * a.hq_cpitch + 32 * j + 16 * (q & 1) +
+                                          8 * half) = make_uint2(w0, w1);
+                a.hsf[((int64_t)ti * J + j) * 512 + r * 16 + 2 * (q & 1) + half] = sc;
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&u_free[buf]);
+        }
+        if (!ok) *abort_flag = 1;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      }
+    }
+  }
+  // drain: nothing may be landing in shared memory, and every MMA and scale
+  // copy must be complete, before TMEM is released and the CTA exits
+  if (warp == 0 && lane == 0) {
+    for (int qq = kk - NST > 0 ? kk - NST : 0; qq < kk; ++qq) mbar_wait(&full[qq % NST], (qq / NST) & 1, a.r.status);
+    mbar_wait(xbar, 0, a.r.status);
+  }
+  if (warp == 1 && lane == 0) {
+    tc_commit(drain);
+    mbar_wait(drain, 0, a.r.status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ down
+
+__global__ void __launch_bounds__(kDtThreads, 1)
+    k_dtc_down(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_dn,
+               const __grid_constant__ CUtensorMap map_hq, const __grid_constant__ CUtensorMap map_sdn,
+               const __grid_constant__ CUtensorMap map_hs) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* sm = align1024(sm_raw);
+  __shared__ int s_last;
+  const int H = a.H, T = a.T, E = a.r.E;
+  const DdLayout L = dd_layout(T, E, T * a.top_k);
+  const Meta M = meta_layout(E, T * a.top_k, L.meta_off);
+  const int* s_touched = reinterpret_cast<const int*>(sm + M.touched_off);
+  const uint8_t* const* s_rec = reinterpret_cast<const uint8_t* const*>(sm + M.rec_off);
+  const int* s_off = reinterpret_cast<const int*>(sm + M.off_off);
+  const int* s_tok = reinterpret_cast<const int*>(sm + M.tok_off);
+  const float* s_w = reinterpret_cast<const float*>(sm + M.w_off);
+  const int NST = L.nst, npad = L.npad;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bar_off);
+  uint64_t* empty = full + 8;
+  uint64_t* acc_full = empty + 8;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* part = reinterpret_cast<float*>(sm + L.part_off);  // [32 tokens][128 rows]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ht = blockIdx.x, g = blockIdx.y;
+  const bool has_shared = a.sh_down != nullptr;
+  const int G = gridDim.y - (has_shared ? 1 : 0);  // routed expert groups
+  const bool shared = has_shared && g == G;
+  const int I_loc = a.win.I_loc, row0 = a.win.row0, Iw = a.win.Iw;
+  const int nks_r = I_loc / 64, nkt_r = (nks_r + 3) / 4;
+  const int nkt_s = a.s_I_loc / 64;  // bf16 K tiles of the shared down (K = s_I_loc)
+  const uint32_t kSfCol = 64;         // after the accumulators; 32 per stage
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 4); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_dn);
+    tma_prefetch_desc(&map_hq);
+    tma_prefetch_desc(&map_sdn);
+    tma_prefetch_desc(&map_hs);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  for (int i2 = tid; i2 < 32 * 128; i2 += kDtThreads) part[i2] = 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the intermediates of the gate_up kernel
+  const int nt = a.r.n_touched[0];
+  stage_meta(a, sm, M, nt);
+  __syncthreads();
+  const int ti0 = shared ? 0 : (int)((int64_t)g * nt / G), ti1 = shared ? 1 : (int)((int64_t)(g + 1) * nt / G);
+  const int n_items = ti1 - ti0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int kk = 0;
+      for (int it = 0; it < n_items && !*abort_flag; ++it) {
+        const int ti = ti0 + it;
+        const int e = shared ? 0 : s_touched[ti];
+        const int s0 = shared ? 0 : s_off[e];
+        const uint8_t* rec = shared ? nullptr : s_rec[ti];
+        const int nkt_u = shared ? nkt_s : nkt_r;
+        for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
+          const int s = kk % NST;
+          if (kk >= NST && !mbar_wait(&empty[s], ((kk / NST) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+          unsigned char* sa = sm + s * L.stage;
+          if (shared) {
+            mbar_arrive_expect_tx(&full[s], kDtA + npad * 128);
+            tma_load_2d(sa, &map_sdn, 2 * a.s_row0 + kt * 128, 128 * ht, &full[s]);
+            tma_load_2d(sa + kDtA, &map_hs, kt * 128, 0, &full[s]);
+          } else {
+            const int nks = min(4, nks_r - 4 * kt);
+            mbar_arrive_expect_tx(&full[s], kDtA + npad * 128 + 2 * nks * 512);
+            tma_load_3d(sa, &map_dn, row0 / 2 + kt * 128, 128 * ht, e, &full[s]);
+            tma_load_2d(sa + kDtA, &map_hq, kt * 128, s0, &full[s]);
+            bulk_g2s(sa + kDtA + kDtB, rec + a.lay.dn_sf + ((int64_t)ht * (Iw / 64) + row0 / 64 + 4 * kt) * 512,
+                     nks * 512, &full[s]);
+            bulk_g2s(sa + kDtA + kDtB + 2048, a.hsf + ((int64_t)ti * nks_r + 4 * kt) * 512, nks * 512, &full[s]);
+          }
+        }
+      }
+      for (int q = kk - NST > 0 ? kk - NST : 0; q < kk; ++q) mbar_wait(&full[q % NST], (q / NST) & 1, a.r.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_f4 = idesc_nvf4(128, npad), id_bf = idesc_bf16(128, npad);
+      int kk = 0;
+      bool ok = true;
+      for (int it = 0; it < n_items && !*abort_flag; ++it) {
+        const int buf = it & 1;
+        if (it >= 2 && !mbar_wait(&acc_empty[buf], ((it >> 1) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * npad;
+        const int nkt_u = shared ? nkt_s : nkt_r;
+        for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
+          const int s = kk % NST;
+          if (!mbar_wait(&full[s], (kk / NST) & 1, a.r.status)) { *abort_flag = 1; ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sm + s * L.stage);
+          const uint64_t adesc = sdesc_k_sw128(sa), bdesc = sdesc_k_sw128(sa + kDtA);
+          if (shared) {
+            for (int ks = 0; ks < 4; ++ks) tc_mma_bf16(d, adesc + 2 * ks, bdesc + 2 * ks, id_bf, (kt | ks) != 0);
+          } else {
+            const int nks = min(4, nks_r - 4 * kt);
+            const uint32_t sfa_col = tmem + kSfCol + 32 * s, sfb_col = sfa_col + 16;
+            for (int ks = 0; ks < nks; ++ks) {
+              tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
+              tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 2048 + 512 * ks));
+            }
+            for (int ks = 0; ks < nks; ++ks)
+              tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, id_f4, sfa_col + 4 * ks, sfb_col + 4 * ks,
+                          (kt | ks) != 0);
+          }
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.r.status);
+    }
+  } else {
+    // ---------------- epilogue: thread = output row h of the tile, TMEM lane h
+    const int q = warp & 3, h = 32 * q + lane;
+    const int hg = 128 * ht + h;
+    const float sig = (shared && lane < T) ? a.r.sigma[lane] : 0.f;
+    for (int it = 0; it < n_items && !*abort_flag; ++it) {
+      const int buf = it & 1;
+      const int e = shared ? 0 : s_touched[ti0 + it];
+      const int s0 = shared ? 0 : s_off[e], m = shared ? 0 : s_off[e + 1] - s0;
+      // the row global is loaded before the accumulator wait
+      const float gd = shared ? 0.f : reinterpret_cast<const float*>(s_rec[ti0 + it] + a.lay.dn_global)[hg];
+      if (!mbar_wait(&acc_full[buf], (it >> 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * npad;
+      if (shared) {
+        for (int t = 0; t < T; ++t) part[t * 128 + h] = __shfl_sync(0xffffffffu, sig, t) * tc_ld1_wait(taddr + t);
+      } else {
+        for (int r = 0; r < m; ++r) {
+          const int t = s_tok[s0 + r];
+          part[t * 128 + h] = fmaf(s_w[s0 + r], gd * tc_ld1_wait(taddr + r), part[t * 128 + h]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+    // this group's partials, then the last CTA of the tile adds all groups
+    // in group order
+    if (!*abort_flag) {
+      for (int t = 0; t < T; ++t) a.gpart[((int64_t)g * T + t) * H + hg] = part[t * 128 + h];
+      __threadfence();
+    }
+    named_barrier(1, 128);
+    if (tid == 64) s_last = *abort_flag ? 0 : (atomicAdd(&a.dn_counter[ht], 1) == (int)gridDim.y - 1);
+    named_barrier(1, 128);
+    if (s_last) {
+      __threadfence();
+      for (int t = 0; t < T; ++t) {
+        float o = 0.f;
+        for (int gg = 0; gg < (int)gridDim.y; ++gg) o += __ldcg(a.gpart + ((int64_t)gg * T + t) * H + hg);
+        const int64_t idx = (int64_t)t * H + hg;
+        if ((a.out_flags & 0xff) == 0) {
+          reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(o);
+        } else if (a.out_flags & 0x100) {
+          reinterpret_cast<float*>(a.out)[idx] += o;
+        } else {
+          reinterpret_cast<float*>(a.out)[idx] = o;
+        }
+      }
+      if (tid == 64) a.dn_counter[ht] = 0;  // ready for the next launch
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+int decode_tc_groups(int H, int num_sms) {
+  const int tiles = H / 128;
+  int g = num_sms / tiles - 1;  // routed groups; one more CTA row for the shared expert
+  return g < 1 ? 1 : g;
+}
+
+bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, int s_Iw, int s_row0, int T,
+                         int top_k, bool has_sf) {
+  if (!has_sf || T < 1 || T > 32 || E > 1024 || top_k > 32) return false;
+  if (H % 256 || I_loc % 64 || row0 % 64 || Iw % 64 || I_loc < 256 || Iw < 256) return false;
+  if (s_I_loc % 64 || s_row0 % 64 || s_Iw % 64) return false;
+  const DgLayout g = dg_layout(H, T, E, T * top_k);
+  if (g.nst < 3 || g.total > kDtSmem) return false;
+  // TMEM columns of the gate_up kernel: accumulators, activation scales,
+  // weight scales per stage
+  if (64 + 4 * g.nks + 16 * g.nst > 512) return false;
+  const DdLayout d = dd_layout(T, E, T * top_k);
+  return d.nst >= 3 && d.total <= kDtSmem;
+}
+
+cudaError_t decode_tc_set_smem_limits() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_dec_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemMax)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_dtc_gate_up, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtSmem)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_dtc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtSmem);
+}
+
+static cudaError_t encode_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                             const uint32_t* box) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return cudaErrorNotSupported;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides[i];
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d, st, b, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static cudaError_t launch_tc(void (*kern)(DecodeArgs, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap), dim3 grid,
+                             int smem, cudaStream_t s, bool pdl, const DecodeArgs& a, const CUtensorMap& m0,
+                             const CUtensorMap& m1, const CUtensorMap& m2, const CUtensorMap& m3) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kDtThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, m0, m1, m2, m3);
+}
+
+cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s) {
+  cudaError_t err;
+  const int H = a.H, T = a.T, P = T * a.top_k, E = a.r.E;
+  const int Iw = a.win.Iw, I_loc = a.win.I_loc;
+  const int npad = T <= 16 ? 16 : 32;
+  CUtensorMap m_gu, m_xq, m_sgu, m_x, m_dn, m_hq, m_sdn, m_hs;
+  const uint8_t* bank = a.bank;
+  {
+    const uint64_t dims[3] = {(uint64_t)H / 2, (uint64_t)2 * Iw, (uint64_t)E}, st[2] = {(uint64_t)H / 2, (uint64_t)a.lay.bytes};
+    const uint32_t box[3] = {128, 64, 1};
+    if ((err = encode_u8(&m_gu, bank + a.lay.gu_codes, 3, dims, st, box)) != cudaSuccess) return err;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)H / 2, (uint64_t)T}, st[1] = {(uint64_t)H / 2};
+    const uint32_t box[2] = {128, (uint32_t)npad};
+    if ((err = encode_u8(&m_xq, a.r.xq_codes, 2, dims, st, box)) != cudaSuccess) return err;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)Iw / 2, (uint64_t)H, (uint64_t)E}, st[2] = {(uint64_t)Iw / 2, (uint64_t)a.lay.bytes};
+    const uint32_t box[3] = {128, 128, 1};
+    if ((err = encode_u8(&m_dn, bank + a.lay.dn_codes, 3, dims, st, box)) != cudaSuccess) return err;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)I_loc / 2, (uint64_t)P}, st[1] = {(uint64_t)a.hq_cpitch};
+    const uint32_t box[2] = {128, (uint32_t)npad};
+    if ((err = encode_u8(&m_hq, a.hq_codes, 2, dims, st, box)) != cudaSuccess) return err;
+  }
+  m_sgu = m_gu;
+  m_x = m_xq;
+  m_sdn = m_dn;
+  m_hs = m_hq;
+  if (a.sh_gate_up) {
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * H, (uint64_t)2 * a.s_Iw}, st[1] = {(uint64_t)2 * H};
+      const uint32_t box[2] = {128, 64};
+      if ((err = encode_u8(&m_sgu, a.sh_gate_up, 2, dims, st, box)) != cudaSuccess) return err;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * H, (uint64_t)T}, st[1] = {(uint64_t)2 * H};
+      const uint32_t box[2] = {128, (uint32_t)npad};
+      if ((err = encode_u8(&m_x, a.r.x, 2, dims, st, box)) != cudaSuccess) return err;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * a.s_Iw, (uint64_t)H}, st[1] = {(uint64_t)2 * a.s_Iw};
+      const uint32_t box[2] = {128, 128};
+      if ((err = encode_u8(&m_sdn, a.sh_down, 2, dims, st, box)) != cudaSuccess) return err;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)2 * a.s_I_loc, (uint64_t)T}, st[1] = {(uint64_t)2 * a.s_I_loc};
+      const uint32_t box[2] = {128, (uint32_t)npad};
+      if ((err = encode_u8(&m_hs, a.hs, 2, dims, st, box)) != cudaSuccess) return err;
+    }
+  }
+  // routing (no shared gate_up CTAs: the shared expert runs on the tensor
+  // cores), then top-k and the sort in one CTA
+  a.n_router_ctas = (E + 1) / 2;
+  a.n_shared_ctas = 0;
+  a.split_tail = 1;
+  {
+    const RtSmem L = rt_smem_layout(T, E, a.top_k);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_router_ctas + 1);
+    cfg.blockDim = dim3(kRtThreads);
+    cfg.dynamicSmemBytes = 8 * T * 2 * 4;
+    cfg.stream = s;
+    FTMOE_PROF_BEGIN("k_dec_route", s);
+    err = cudaLaunchKernelEx(&cfg, k_dec_route, a);
+    FTMOE_PROF_END(s);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(1);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    FTMOE_PROF_BEGIN("k_dec_topk", s);
+    err = cudaLaunchKernelEx(&cfg, k_dec_topk, a);
+    FTMOE_PROF_END(s);
+    if (err != cudaSuccess) return err;
+  }
+  {
+    const DgLayout L = dg_layout(H, T, E, P);
+    FTMOE_PROF_BEGIN("k_dtc_gate_up", s);
+    err = launch_tc(k_dtc_gate_up, dim3(a.num_sms), L.total, s, a.pdl, a, m_gu, m_xq, m_sgu, m_x);
+    FTMOE_PROF_END(s);
+    if (err != cudaSuccess) return err;
+  }
+  {
+    const DdLayout L = dd_layout(T, E, P);
+    const int rows = a.n_groups + (a.sh_down ? 1 : 0);
+    FTMOE_PROF_BEGIN("k_dtc_down", s);
+    err = launch_tc(k_dtc_down, dim3(H / 128, rows), L.total, s, a.pdl, a, m_dn, m_hq, m_sdn, m_hs);
+    FTMOE_PROF_END(s);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace ftmoe

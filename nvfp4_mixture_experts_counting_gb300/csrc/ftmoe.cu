@@ -145,6 +145,12 @@ struct ftmoe_handle {
   uint8_t* pf_hq = nullptr;
   uint8_t* pf_hq_sf = nullptr;
   bool pf_enabled = false;
+  // tensor-core decode buffers
+  bool dtc_enabled = false;
+  uint8_t* dtc_hsf = nullptr;
+  float* dtc_gpart = nullptr;
+  int* dtc_counter = nullptr;
+  int dtc_groups = 0;
   uint32_t last_status = 0;
   EventProfiler* prof = nullptr;  // non-null while per-kernel timing is enabled
 };
@@ -282,8 +288,17 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
       {(void**)&h->counter, 16},             {(void**)&h->r.n_rerank, 16},
       {(void**)&h->gu_split, (int64_t)(prop.multiProcessorCount + 1) * 4},
   };
-  // tensor-core prefill buffers (padded pair order), for shapes it accepts
+  // tensor-core decode buffers
   const char* no_tc = getenv("FTMOE_NO_TC");
+  if (c.H % 256 == 0 && c.I % 64 == 0 && c.E <= 1024 && !(no_tc && no_tc[0] == '1')) {
+    h->dtc_enabled = true;
+    h->dtc_groups = decode_tc_groups(c.H, prop.multiProcessorCount);
+    const int64_t Td = T < 32 ? T : 32;
+    parts.push_back({(void**)&h->dtc_hsf, (int64_t)c.E * (c.I / 64) * 512});
+    parts.push_back({(void**)&h->dtc_gpart, (int64_t)(h->dtc_groups + 1) * Td * c.H * 4});
+    parts.push_back({(void**)&h->dtc_counter, (int64_t)(c.H / 128 + 1) * 4});
+  }
+  // tensor-core prefill buffers (padded pair order), for shapes it accepts
   if (c.max_tokens > 32 && c.H % 256 == 0 && c.I % 64 == 0 && c.E <= 1024 && !(no_tc && no_tc[0] == '1')) {
     h->pf_enabled = true;
     h->pf_pad_max = pf_pad_max(P, c.E);
@@ -312,6 +327,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
   if (e == cudaSuccess) e = experts_set_smem_limits(c.H, c.I > c.I_shared ? c.I : c.I_shared);
   if (e == cudaSuccess) e = decode_set_smem_limits();
   if (e == cudaSuccess) e = prefill_set_smem_limits();
+  if (e == cudaSuccess) e = decode_tc_set_smem_limits();
   if (e != cudaSuccess) {
     cuda_fail(e, "create");
     cudaFree(h->ws);
@@ -483,7 +499,19 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     d.gu_split = h->gu_split;
     d.num_sms = h->num_sms;
     d.pdl = 1;
-    CK(launch_decode(d, s));
+    if (h->dtc_enabled && decode_tc_supported(c.H, c.E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T,
+                                              c.top_k, L.lay.gu_sf_bytes != 0)) {
+      // weights through the tensor cores: intermediates as packed codes
+      d.bank = L.bank;
+      d.hsf = h->dtc_hsf;
+      d.gpart = h->dtc_gpart;
+      d.dn_counter = h->dtc_counter;
+      d.n_groups = h->dtc_groups;
+      d.hq_cpitch = (int)align_up(I_loc / 2, 16);
+      CK(launch_decode_tc(d, s));
+    } else {
+      CK(launch_decode(d, s));
+    }
   } else if (h->pf_enabled && T > 32 && L.lay.gu_sf_bytes &&
              prefill_supported(c.H, c.E, I_loc, L.lIw, a.win.row0)) {
     // prefill sizes: router logits, the routed GEMMs and the shared expert

@@ -131,6 +131,13 @@ struct DecodeArgs {
   int n_router_ctas, n_shared_ctas;
   int num_sms;
   int pdl;             // chain the kernels with programmatic dependent launch
+  // tensor-core decode kernels (decode_tc.cu)
+  const uint8_t* bank; // expert records, lay.bytes apart (rec[e] == bank + e * lay.bytes)
+  uint8_t* hsf;        // [E][I_loc/64][512] intermediate scale blocks per touched expert
+  float* gpart;        // [groups][T][H] partial outputs of the down kernel
+  int* dn_counter;     // [H/128] arrival counters (zero between launches)
+  int n_groups;        // down kernel: expert groups per 128-row output tile (+1 for the shared expert)
+  int split_tail;      // 1: top-k and the sort run in k_dec_topk instead of the last router CTA
 };
 
 int decode_hq_cpitch(int I_loc);
@@ -139,6 +146,11 @@ bool decode_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, in
                       int top_k);
 cudaError_t decode_set_smem_limits();
 cudaError_t launch_decode(DecodeArgs a, cudaStream_t s);
+bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, int s_Iw, int s_row0, int T,
+                         int top_k, bool has_sf);
+int decode_tc_groups(int H, int num_sms);
+cudaError_t decode_tc_set_smem_limits();
+cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s);
 
 // Prefill path: grouped block-scaled NVFP4 GEMMs on tcgen05 (prefill.cu).
 // Pairs are regrouped in a padded order where expert e owns rows

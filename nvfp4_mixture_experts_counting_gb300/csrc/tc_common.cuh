@@ -121,6 +121,20 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
+// One 32-bit TMEM column of 32 lanes (thread i gets lane quarter_base + i).
+__device__ __forceinline__ float tc_ld1_wait(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r) : : "memory");
+  return __uint_as_float(r);
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (TMA, tcgen05.cp, MMA operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Wait for this thread's TMEM loads; the registers are tied to the wait so
 // no use of them can be scheduled before it.
 __device__ __forceinline__ void tc_wait16(uint32_t (&r)[16]) {

@@ -59,6 +59,18 @@ def test_mid_layer_matches_oracle(mid, T):
     check_output(out, ref.out)
 
 
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 32])
+def test_mid_decode_sizes_match_oracle(mid, T):
+    """T <= 32 takes the decode kernels (tensor-core gate_up and down with
+    the tokens as the MMA's N dimension, padded to 16 or 32)."""
+    wl, bank, layer = mid
+    x = W.hidden(wl, T, step=7, device=DEV)
+    out, aux = _run(wl, layer, x)
+    ref = bank.oracle_layer(x)
+    check_routing(aux, ref)
+    check_output(out, ref.out)
+
+
 def test_mid_one_hot_expert(mid):
     """Every token routed to the same k experts: one populated group per
     expert, several full 128-row tiles plus a ragged one, the rest empty."""
