@@ -539,10 +539,150 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_stack(args):
+    """The layer stack (every layer's own seeded weights, RMS renorm between
+    layers), one CUDA graph per step replayed K times."""
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    from nvfp4_mixture_experts_counting_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if ws > 1:
+        dist.barrier()
+    from nvfp4_mixture_experts_counting_gb300 import accounting as A
+    from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
+
+    wl = W.WORKLOADS[args.workload]
+    T, K, Wm, NL = args.T, args.steps, max(args.warmup, 3), wl.layers
+    dev = "cuda"
+    layer = build_layers(wl, NL, T, dev)
+    x = W.hidden(wl, T, step=100 * rank, device=dev)
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        for _ in range(Wm):
+            layer.forward_stack(x, out, stream=cs)
+    cs.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        layer.forward_stack(x, out, stream=cs)
+    for _ in range(Wm):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    st0 = layer.stats(0)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    _barrier_and_sync(ws)
+    t_wall0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(K):
+        graph.replay()
+    ev1.record()
+    _barrier_and_sync(ws)
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    st1 = layer.stats(0)
+    ms_max = _max_over_ranks(ws, ev0.elapsed_time(ev1))
+    value = ws * T * K / (ms_max / 1e3)
+    touched_per_layer = (st1.touched_total - st0.touched_total) / (K * NL)
+    reranked = (st1.reranked_tokens - st0.reranked_tokens) / K
+    bytes_step = NL * A.layer_touched_bytes(wl.H, wl.E, wl.I, wl.I_s, T, touched_per_layer)
+    peak, peak_kind = load_peaks()
+
+    # per-kernel durations: separate steps without the graph, events around kernels
+    KP = min(K, 20)
+    ftmoe.ftmoe_profile_enable(layer.handle, True)
+    ftmoe.ftmoe_profile_read(layer.handle)
+    for _ in range(KP):
+        layer.forward_stack(x, out)
+    torch.cuda.synchronize()
+    ktimes = ftmoe.ftmoe_profile_read(layer.handle)
+    ftmoe.ftmoe_profile_enable(layer.handle, False)
+    total_k = sum(v[1] for v in ktimes.values()) or 1.0
+    dom = max(ktimes.items(), key=lambda kv: kv[1][1])[0] if ktimes else None
+    roof = None
+    if dom:
+        launches, kms = ktimes[dom]
+        avg_s = kms / launches / 1e3
+        unit_bytes, unit, fixed = A.kernel_unit_bytes(dom, wl.H, wl.I, wl.I_s, wl.E)
+        if unit_bytes is not None:
+            units = touched_per_layer if unit.startswith("touched") else 1.0
+            alg = unit_bytes * units + fixed
+            achieved = alg / avg_s / 1e9
+            roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom, f"{args.workload}_T{T}"),
+                    "algorithmic_bytes_per_launch": int(alg), "unit_bytes": unit_bytes,
+                    "units_per_launch": round(units, 2), "units": unit, "avg_launch_us": round(avg_s * 1e6, 2),
+                    "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+    shares = {k: {"launches": v[0], "ms": round(v[1], 3), "share": round(v[1] / total_k, 4)}
+              for k, v in ktimes.items()}
+
+    # end to end: the input in from pinned host memory and the output back,
+    # around every graph replay
+    xh = x.cpu().pin_memory()
+    oh = torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        x.copy_(xh, non_blocking=True)
+        graph.replay()
+        oh.copy_(out, non_blocking=True)
+    e1.record()
+    _barrier_and_sync(ws)
+    e2e_ms = _max_over_ranks(ws, e0.elapsed_time(e1))
+    launches_total = int(round(sum(v[0] for v in ktimes.values()) * K / KP))
+
+    if rank == 0:
+        line = {
+            "metric": "MoE-layer tokens/s at 1 GB300 (decode: % of HBM peak over touched bytes)",
+            "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+            "ms_per_step": round(ms_max / K, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate); bf16 shared expert",
+            "data": "synthetic, seeded",
+            "config": {"workload": f"{NL}-layer stack of the decode layer (H={wl.H} I={wl.I} I_s={wl.I_s} "
+                                   f"E={wl.E} top_k={wl.top_k}), independent seeded weights per layer, RMS "
+                                   f"renorm between layers, T={T}, one CUDA graph per step",
+                       "global_batch": T * ws,
+                       "l2": f"inputs larger than L2: {NL} layers x "
+                             f"{A.expert_window_bytes(wl.H, wl.I) * wl.E / 1e6:.0f} MB of banks per step",
+                       "parallelism": f"replicas x{ws} (token-parallel, no collective)"},
+            "moe_ms_per_step": round(ms_max / K, 4),
+            "touched_experts_per_layer": round(touched_per_layer, 2),
+            "touched_bytes_per_step": int(bytes_step),
+            "reranked_tokens_per_step": round(reranked, 4),
+            "stack_hbm_frac": round(bytes_step / (ms_max / K / 1e3) / 1e9 / peak, 4),
+            "stack_hbm_gbs": round(bytes_step / (ms_max / K / 1e3) / 1e9, 1),
+            "roofline": roof,
+            "kernel_shares": shares,
+            "kernel_shares_note": f"CUDA events around each kernel over {KP} steps run without the graph",
+            "gpu_launches": launches_total,
+            "e2e": {"value": round(ws * T * K / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * wl.H * 2, "d2h_bytes_per_step": T * wl.H * 2},
+            "clocks": clocks.summary(t_wall0, t_wall1),
+            "cpu_baseline": None,
+        }
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "stack48":
+        run_stack(args)
     else:
         run_gpu(args)
 

@@ -132,6 +132,7 @@ typedef struct {
   double residency;         /* offload mode: resident slots / E; resident mode: 1.0 */
   int32_t device_status;    /* last device status word read by ftmoe_check_status */
   int64_t reranked_tokens;  /* cumulative tokens (all layers) whose top-k needed re-ranking */
+  int64_t touched_total;    /* cumulative touched experts over every forward (all layers) */
 } ftmoe_stats;
 
 /* Create a handle on CUDA device `device` for layers of the given shape.
@@ -179,6 +180,15 @@ int ftmoe_forward(ftmoe_handle* h, int layer, const void* x, int T, void* out, i
  * Uses the whole loaded window of every layer.  Asynchronous; capturable in a
  * CUDA graph in resident mode. */
 int ftmoe_forward_stack(ftmoe_handle* h, const void* x, int T, void* out, ftmoe_stream_t stream);
+
+/* The renorm between the layers of ftmoe_forward_stack, on its own (the same
+ * kernel): x[t] = bf16(y[t] / sqrt(mean_h(y[t][h]^2) + 1e-6)) for t < T,
+ * sum of squares in fp32 (stack workload: "renormalised by RMS between
+ * layers, with no attention").
+ *   y: device fp32 [T, H];  x: device bf16 [T, H] (must not alias y)
+ * Asynchronous on `stream`.  Returns FTMOE_ERR_INVALID_ARG for null pointers
+ * or H, T < 0. */
+int ftmoe_rms_renorm(const float* y, void* x, int T, int H, ftmoe_stream_t stream);
 
 /* Release everything the handle owns.  Safe on NULL. */
 int ftmoe_destroy(ftmoe_handle* h);

@@ -234,6 +234,7 @@ __device__ void dec_sort(const DecodeArgs& a, const int* s_idx, int* hist /*[8][
   if (tid == kRtThreads - 1) {
     a.r.offsets[E] = P;
     a.r.n_touched[0] = toff;
+    if (a.r.touched_total) atomicAdd(a.r.touched_total, (unsigned long long)toff);
   }
   __syncthreads();
   for (int p0 = c0; p0 < c1; p0 += 32) {

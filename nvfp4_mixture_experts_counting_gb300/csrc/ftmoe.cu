@@ -286,6 +286,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
       {(void**)&h->stack_y, T * c.H * 4},    {(void**)&h->stack_x[0], T * c.H * 2},
       {(void**)&h->stack_x[1], T * c.H * 2}, {(void**)&h->status, 16},
       {(void**)&h->counter, 16},             {(void**)&h->r.n_rerank, 16},
+      {(void**)&h->r.touched_total, 16},
       {(void**)&h->gu_split, (int64_t)(prop.multiProcessorCount + 1) * 4},
   };
   // tensor-core decode buffers
@@ -649,6 +650,13 @@ int ftmoe_forward_stack(ftmoe_handle* h, const void* x, int T, void* out, ftmoe_
   return FTMOE_OK;
 }
 
+int ftmoe_rms_renorm(const float* y, void* x, int T, int H, ftmoe_stream_t stream) {
+  if (!y || !x || T < 0 || H <= 0 || (const void*)y == x) return FTMOE_ERR_INVALID_ARG;
+  if (T == 0) return FTMOE_OK;
+  CK(launch_rms_renorm(y, (uint16_t*)x, T, H, (cudaStream_t)stream));
+  return FTMOE_OK;
+}
+
 int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out) {
   if (!h || !out || layer < 0 || layer >= h->cfg.num_layers) return FTMOE_ERR_INVALID_ARG;
   CK(cudaSetDevice(h->device));
@@ -667,6 +675,9 @@ int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out) {
   unsigned long long nr = 0;
   CK(cudaMemcpy(&nr, h->r.n_rerank, 8, cudaMemcpyDeviceToHost));
   out->reranked_tokens = (int64_t)nr;
+  unsigned long long tt = 0;
+  CK(cudaMemcpy(&tt, h->r.touched_total, 8, cudaMemcpyDeviceToHost));
+  out->touched_total = (int64_t)tt;
   return FTMOE_OK;
 }
 

@@ -66,7 +66,8 @@ struct RouteArgs {
   int32_t* inv;      // [P]
   int32_t* touched;  // [E] touched experts, increasing
   int32_t* n_touched;  // [1]
-  unsigned long long* n_rerank;  // [1] cumulative count of fp64 re-ranked tokens (may be null)
+  unsigned long long* n_rerank;  // [1] cumulative count of re-ranked tokens (may be null)
+  unsigned long long* touched_total;  // [1] cumulative touched experts over forwards (may be null)
   uint32_t* status;
 };
 

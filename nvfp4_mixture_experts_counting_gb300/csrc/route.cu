@@ -412,7 +412,10 @@ __global__ void __launch_bounds__(kSortThreads) k_sort(RouteArgs a) {
     __threadfence_block();
     __syncthreads();
   }
-  if (threadIdx.x == 0) a.offsets[E] = P;
+  if (threadIdx.x == 0) {
+    a.offsets[E] = P;
+    if (a.touched_total) atomicAdd(a.touched_total, (unsigned long long)a.n_touched[0]);
+  }
   __syncthreads();
   for (int p0 = c0; p0 < c1; p0 += 32) {
     const int p = p0 + lane;

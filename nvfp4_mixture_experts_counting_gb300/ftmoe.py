@@ -57,7 +57,7 @@ class Stats(C.Structure):
     _fields_ = [("touched_experts", C.c_int32), ("resident_slots", C.c_int32),
                 ("touched_bytes", C.c_int64), ("hits", C.c_int64), ("misses", C.c_int64),
                 ("h2d_bytes", C.c_int64), ("residency", C.c_double), ("device_status", C.c_int32),
-                ("reranked_tokens", C.c_int64)]
+                ("reranked_tokens", C.c_int64), ("touched_total", C.c_int64)]
 
 
 class KernelTime(C.Structure):
@@ -73,6 +73,7 @@ SIGNATURES = {
     "ftmoe_forward": ([C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_int,
                        C.POINTER(Aux), C.c_void_p], C.c_int),
     "ftmoe_forward_stack": ([C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p], C.c_int),
+    "ftmoe_rms_renorm": ([C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p], C.c_int),
     "ftmoe_destroy": ([C.c_void_p], C.c_int),
     "ftmoe_error_string": ([C.c_int], C.c_char_p),
     "ftmoe_last_cuda_error": ([], C.c_char_p),
@@ -151,6 +152,10 @@ def ftmoe_forward(h: int, layer: int, x, T: int, out, out_flags: int, i0: int, I
 
 def ftmoe_forward_stack(h: int, x, T: int, out, stream=None):
     _check(lib().ftmoe_forward_stack(h, _ptr(x), T, _ptr(out), _stream(stream)), "ftmoe_forward_stack")
+
+
+def ftmoe_rms_renorm(y, x, T: int, H: int, stream=None):
+    _check(lib().ftmoe_rms_renorm(_ptr(y), _ptr(x), T, H, _stream(stream)), "ftmoe_rms_renorm")
 
 
 def ftmoe_destroy(h: int):
