@@ -90,8 +90,14 @@ typedef struct {
   int32_t max_tokens;      /* largest T a forward accepts; sizes the workspace once */
   int32_t norm_topk_prob;  /* 1: renormalise over the k chosen; 0: full-softmax probabilities */
   int32_t has_router_bias; /* 1: banks carry a per-expert router bias [E] */
-  int64_t hbm_slot_bytes;  /* 0: all banks resident in HBM; > 0: offload mode, this many bytes
-                              of HBM expert slots per handle, the banks kept in pinned host memory */
+  int64_t hbm_slot_bytes;  /* 0: all banks resident in HBM; > 0: offload mode.  The banks stay in
+                              pinned host memory and the handle keeps
+                              floor(hbm_slot_bytes / expert window bytes) expert slots in HBM,
+                              shared by all layers, filled least-recently-used first (PR #385
+                              "What this adds": a fraction of the experts resident, the rest
+                              streamed every step).  Expert window bytes = 2*Iw*(H/2 + H/16 + 4)
+                              + H*(Iw/2 + Iw/16 + 4) for the loaded window Iw; a slot physically
+                              also holds the tensor-core copy of the scales (about 1/8 more). */
 } ftmoe_config;
 
 /* One layer's weights, as given to ftmoe_load_bank.  Every array is the full
@@ -136,9 +142,11 @@ typedef struct {
 } ftmoe_stats;
 
 /* Create a handle on CUDA device `device` for layers of the given shape.
- * Allocates the workspace for config->max_tokens and, in offload mode, the
- * HBM slot pool.  Validates the config (INVALID_ARG, ALIGNMENT) and the device
- * (DEVICE).  On success *out owns everything until ftmoe_destroy. */
+ * Allocates the workspace for config->max_tokens (offload mode: also the
+ * copy stream; the HBM slot pool follows at the first ftmoe_load_bank, once
+ * the record size is known).  Validates the config (INVALID_ARG, ALIGNMENT)
+ * and the device (DEVICE).  On success *out owns everything until
+ * ftmoe_destroy. */
 int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out);
 
 /* Load layer `layer`'s weights, keeping the intermediate window
@@ -167,8 +175,11 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* desc, int
  * Routing always uses the full replicated router.  Asynchronous on `stream`;
  * resident mode does no host synchronisation and may be captured in a CUDA
  * graph.  Offload mode reads the step's routing back to the host once per
- * call (one synchronisation) to plan its slot copies.  T == 0 returns OK and
- * does nothing. */
+ * call (one synchronisation) to plan its slot copies; a forward touching more
+ * experts than there are slots runs its experts in batches of at most the
+ * slot count; offload needs the tensor-core shapes (H a multiple of 256,
+ * windows multiples of 64 and at least 256 wide; INVALID_ARG otherwise) and
+ * is not capturable.  T == 0 returns OK and does nothing. */
 int ftmoe_forward(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags,
                   int i0, int I_loc, const ftmoe_aux* aux, ftmoe_stream_t stream);
 

@@ -47,7 +47,7 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
 // pointers, expert offsets, and per sorted position the token (and, for the
 // down kernel, the routing weight).
 struct Meta {
-  int touched_off, rec_off, off_off, tok_off, w_off, bytes;
+  int touched_off, z_off, rec_off, off_off, tok_off, w_off, bytes;
 };
 
 __host__ __device__ inline Meta meta_layout(int E, int P, int base) {
@@ -55,6 +55,7 @@ __host__ __device__ inline Meta meta_layout(int E, int P, int base) {
   int o = base;
   M.rec_off = o;     o += E * 8;
   M.touched_off = o; o += align16(E * 4);
+  M.z_off = o;       o += align16(E * 4);
   M.off_off = o;     o += align16((E + 1) * 4);
   M.tok_off = o;     o += align16(P * 4);
   M.w_off = o;       o += align16(P * 4);
@@ -90,6 +91,7 @@ __host__ __device__ inline DgLayout dg_layout(int H, int T, int E, int P) {
 __device__ __forceinline__ void stage_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M, int nt) {
   const int E = a.r.E, P = a.T * a.top_k, k = a.top_k;
   int* s_touched = reinterpret_cast<int*>(sm + M.touched_off);
+  int* s_z = reinterpret_cast<int*>(sm + M.z_off);
   const uint8_t** s_rec = reinterpret_cast<const uint8_t**>(sm + M.rec_off);
   int* s_off = reinterpret_cast<int*>(sm + M.off_off);
   int* s_tok = reinterpret_cast<int*>(sm + M.tok_off);
@@ -98,6 +100,7 @@ __device__ __forceinline__ void stage_meta(const DecodeArgs& a, unsigned char* s
   for (int i = threadIdx.x; i < nt; i += blockDim.x) {
     const int e = a.r.touched[i];
     s_touched[i] = e;
+    s_z[i] = a.rec_z ? a.rec_z[e] : e;
     s_rec[i] = a.rec[e];
   }
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   const DgLayout L = dg_layout(H, T, E, T * a.top_k);
   const Meta M = meta_layout(E, T * a.top_k, L.meta_off);
   const int* s_touched = reinterpret_cast<const int*>(sm + M.touched_off);
+  const int* s_z = reinterpret_cast<const int*>(sm + M.z_off);
   const uint8_t* const* s_rec = reinterpret_cast<const uint8_t* const*>(sm + M.rec_off);
   const int* s_off = reinterpret_cast<const int*>(sm + M.off_off);
   const int* s_tok = reinterpret_cast<const int*>(sm + M.tok_off);
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int J = a.win.I_loc / 64, Js = a.sh_gate_up ? a.s_I_loc / 64 : 0;
+  const int J = a.win.I_loc / 64, Js = (a.sh_gate_up && !a.skip_shared) ? a.s_I_loc / 64 : 0;
   const int nkt_s = H / 64;  // bf16 K tiles of the shared gate_up (K = H)
   const int row0 = a.win.row0, Iw = a.win.Iw;
   const uint32_t id_f4 = idesc_nvf4(128, npad), id_bf = idesc_bf16(128, npad);
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
           const bool shared = phase == 0;
           const int rr = r0 + it;
           const int j = shared ? (int)blockIdx.x + it * (int)gridDim.x : rr % J;
-          const int e = shared ? 0 : s_touched[rr / J];
+          const int z = shared ? 0 : s_z[rr / J];  // record index in the bank / slot pool
           const uint8_t* rec = shared ? nullptr : s_rec[rr / J];
           const int nkt_u = shared ? nkt_s : L.nkt;
           for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
@@ -249,8 +253,8 @@ __global__ void __launch_bounds__(kDtThreads, 1)
               tma_load_2d(sa + kDtA, &map_x, kt * 128, 0, &full[s]);
             } else {
               mbar_arrive_expect_tx(&full[s], kDtA + 2048);
-              tma_load_3d(sa, &map_gu, kt * 128, row0 + 64 * j, e, &full[s]);
-              tma_load_3d(sa + kDtA / 2, &map_gu, kt * 128, Iw + row0 + 64 * j, e, &full[s]);
+              tma_load_3d(sa, &map_gu, kt * 128, row0 + 64 * j, z, &full[s]);
+              tma_load_3d(sa + kDtA / 2, &map_gu, kt * 128, Iw + row0 + 64 * j, z, &full[s]);
               bulk_g2s(sa + kDtA + kDtB, rec + a.lay.gu_sf + ((int64_t)(row0 / 64 + j) * L.nks + 4 * kt) * 512,
                        2048, &full[s]);
             }
@@ -399,6 +403,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   const DdLayout L = dd_layout(T, E, T * a.top_k);
   const Meta M = meta_layout(E, T * a.top_k, L.meta_off);
   const int* s_touched = reinterpret_cast<const int*>(sm + M.touched_off);
+  const int* s_z = reinterpret_cast<const int*>(sm + M.z_off);
   const uint8_t* const* s_rec = reinterpret_cast<const uint8_t* const*>(sm + M.rec_off);
   const int* s_off = reinterpret_cast<const int*>(sm + M.off_off);
   const int* s_tok = reinterpret_cast<const int*>(sm + M.tok_off);
@@ -414,7 +419,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   float* part = reinterpret_cast<float*>(sm + L.part_off);  // [32 tokens][128 rows]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ht = blockIdx.x, g = blockIdx.y;
-  const bool has_shared = a.sh_down != nullptr;
+  const bool has_shared = a.sh_down != nullptr && !a.skip_shared;
   const int G = gridDim.y - (has_shared ? 1 : 0);  // routed expert groups
   const bool shared = has_shared && g == G;
   const int I_loc = a.win.I_loc, row0 = a.win.row0, Iw = a.win.Iw;
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
           } else {
             const int nks = min(4, nks_r - 4 * kt);
             mbar_arrive_expect_tx(&full[s], kDtA + npad * 128 + 2 * nks * 512);
-            tma_load_3d(sa, &map_dn, row0 / 2 + kt * 128, 128 * ht, e, &full[s]);
+            tma_load_3d(sa, &map_dn, row0 / 2 + kt * 128, 128 * ht, s_z[ti], &full[s]);
             tma_load_2d(sa + kDtA, &map_hq, kt * 128, s0, &full[s]);
             bulk_g2s(sa + kDtA + kDtB, rec + a.lay.dn_sf + ((int64_t)ht * (Iw / 64) + row0 / 64 + 4 * kt) * 512,
                      nks * 512, &full[s]);
@@ -646,7 +651,7 @@ static cudaError_t launch_tc(void (*kern)(DecodeArgs, CUtensorMap, CUtensorMap, 
   return cudaLaunchKernelEx(&cfg, kern, a, m0, m1, m2, m3);
 }
 
-cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s) {
+cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
   cudaError_t err;
   const int H = a.H, T = a.T, P = T * a.top_k, E = a.r.E;
   const int Iw = a.win.Iw, I_loc = a.win.I_loc;
@@ -654,7 +659,8 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s) {
   CUtensorMap m_gu, m_xq, m_sgu, m_x, m_dn, m_hq, m_sdn, m_hs;
   const uint8_t* bank = a.bank;
   {
-    const uint64_t dims[3] = {(uint64_t)H / 2, (uint64_t)2 * Iw, (uint64_t)E}, st[2] = {(uint64_t)H / 2, (uint64_t)a.lay.bytes};
+    const uint64_t dims[3] = {(uint64_t)H / 2, (uint64_t)2 * Iw, (uint64_t)a.n_records},
+                   st[2] = {(uint64_t)H / 2, (uint64_t)a.lay.bytes};
     const uint32_t box[3] = {128, 64, 1};
     if ((err = encode_u8(&m_gu, bank + a.lay.gu_codes, 3, dims, st, box)) != cudaSuccess) return err;
   }
@@ -664,7 +670,8 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s) {
     if ((err = encode_u8(&m_xq, a.r.xq_codes, 2, dims, st, box)) != cudaSuccess) return err;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)Iw / 2, (uint64_t)H, (uint64_t)E}, st[2] = {(uint64_t)Iw / 2, (uint64_t)a.lay.bytes};
+    const uint64_t dims[3] = {(uint64_t)Iw / 2, (uint64_t)H, (uint64_t)a.n_records},
+                   st[2] = {(uint64_t)Iw / 2, (uint64_t)a.lay.bytes};
     const uint32_t box[3] = {128, 128, 1};
     if ((err = encode_u8(&m_dn, bank + a.lay.dn_codes, 3, dims, st, box)) != cudaSuccess) return err;
   }
@@ -704,7 +711,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s) {
   a.n_router_ctas = (E + 1) / 2;
   a.n_shared_ctas = 0;
   a.split_tail = 1;
-  {
+  if (parts & 1) {
     const RtSmem L = rt_smem_layout(T, E, a.top_k);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.n_router_ctas + 1);
@@ -727,6 +734,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s) {
     FTMOE_PROF_END(s);
     if (err != cudaSuccess) return err;
   }
+  if (!(parts & 2)) return cudaSuccess;
   {
     const DgLayout L = dg_layout(H, T, E, P);
     FTMOE_PROF_BEGIN("k_dtc_gate_up", s);
@@ -736,7 +744,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s) {
   }
   {
     const DdLayout L = dd_layout(T, E, P);
-    const int rows = a.n_groups + (a.sh_down ? 1 : 0);
+    const int rows = a.n_groups + ((a.sh_down && !a.skip_shared) ? 1 : 0);
     FTMOE_PROF_BEGIN("k_dtc_down", s);
     err = launch_tc(k_dtc_down, dim3(H / 128, rows), L.total, s, a.pdl, a, m_dn, m_hq, m_sdn, m_hs);
     FTMOE_PROF_END(s);

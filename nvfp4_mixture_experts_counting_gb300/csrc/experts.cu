@@ -425,6 +425,29 @@ cudaError_t launch_experts(const ExpertArgs& a, cudaStream_t s, int parts) {
   return cudaSuccess;
 }
 
+__global__ void k_store_out(const float* __restrict__ y, void* out, int out_flags, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = y[i];
+    if ((out_flags & 0xff) == 0) {
+      reinterpret_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+    } else if (out_flags & 0x100) {
+      reinterpret_cast<float*>(out)[i] += v;
+    } else {
+      reinterpret_cast<float*>(out)[i] = v;
+    }
+  }
+}
+
+cudaError_t launch_store_out(const float* y, void* out, int out_flags, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  FTMOE_PROF_BEGIN("k_store_out", s);
+  k_store_out<<<(int)blocks, 256, 0, s>>>(y, out, out_flags, n);
+  FTMOE_PROF_END(s);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rms_renorm(const float* y, uint16_t* x, int T, int H, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   FTMOE_PROF_BEGIN("k_rms_renorm", s);

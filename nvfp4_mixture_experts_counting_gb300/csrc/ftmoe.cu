@@ -2,6 +2,7 @@
 // slicing), workspace, forward orchestration, stats and status.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -10,6 +11,7 @@
 
 #include "../../include/ftmoe.h"
 #include "kernels.h"
+#include "slot_cache.h"
 
 namespace ftmoe {
 cudaError_t route_set_smem_limits(int H, int E);
@@ -112,6 +114,10 @@ struct Layer {
   uint16_t* sh_gate = nullptr;
   uint16_t* router_wcat = nullptr;  // [E][3H] bf16 parts of the router rows (tensor-core router)
   float* router_wnorm = nullptr;    // [E]
+  // offload mode
+  uint8_t* host_bank = nullptr;     // pinned host: E records
+  int32_t* rec_z_dev = nullptr;     // [E] slot of each expert in the current batch
+  uint8_t* active_dev = nullptr;    // [E] experts of the current batch
   int last_T = 0;
   int last_I_loc = 0;
 };
@@ -145,6 +151,19 @@ struct ftmoe_handle {
   uint8_t* pf_hq = nullptr;
   uint8_t* pf_hq_sf = nullptr;
   bool pf_enabled = false;
+  // offload mode: HBM slot pool, LRU placement, copy stream, pinned staging
+  bool offload = false;
+  SlotCache cache;
+  uint8_t* slot_pool = nullptr;
+  int64_t slot_rec_bytes = 0;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_compute = nullptr, ev_copied = nullptr;
+  int32_t* h_touched = nullptr;   // pinned [E + 1]: touched experts, then their count
+  unsigned char* h_stage = nullptr;  // pinned per-batch tables
+  size_t stage_bytes = 0;
+  int max_batches = 0;
+  float* off_y = nullptr;         // [T][H] fp32 sum of a batched decode forward
+  std::vector<int64_t> h2d_bytes;
   // tensor-core decode buffers
   bool dtc_enabled = false;
   uint8_t* dtc_hsf = nullptr;
@@ -194,6 +213,9 @@ void free_layer(Layer& L) {
   cudaFree(L.sh_gate);
   cudaFree(L.router_wcat);
   cudaFree(L.router_wnorm);
+  if (L.host_bank) cudaFreeHost(L.host_bank);
+  cudaFree(L.rec_z_dev);
+  cudaFree(L.active_dev);
   L = Layer{};
 }
 
@@ -207,7 +229,6 @@ int validate_config(const ftmoe_config* c) {
       c->top_k > c->E || c->max_tokens > (1 << 20))
     return FTMOE_ERR_INVALID_ARG;
   if (c->hbm_slot_bytes < 0) return FTMOE_ERR_INVALID_ARG;
-  if (c->hbm_slot_bytes > 0) return FTMOE_ERR_INVALID_ARG;  // offload mode: not in this build yet
   return FTMOE_OK;
 }
 
@@ -287,6 +308,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
       {(void**)&h->stack_x[1], T * c.H * 2}, {(void**)&h->status, 16},
       {(void**)&h->counter, 16},             {(void**)&h->r.n_rerank, 16},
       {(void**)&h->r.touched_total, 16},
+      {(void**)&h->off_y, c.hbm_slot_bytes > 0 ? T * c.H * 4 : 16},
       {(void**)&h->gu_split, (int64_t)(prop.multiProcessorCount + 1) * 4},
   };
   // tensor-core decode buffers
@@ -329,6 +351,14 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
   if (e == cudaSuccess) e = decode_set_smem_limits();
   if (e == cudaSuccess) e = prefill_set_smem_limits();
   if (e == cudaSuccess) e = decode_tc_set_smem_limits();
+  if (e == cudaSuccess && c.hbm_slot_bytes > 0) {
+    h->offload = true;
+    h->h2d_bytes.assign(c.num_layers, 0);
+    e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_compute, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_copied, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaHostAlloc((void**)&h->h_touched, (size_t)(c.E + 1) * 4, cudaHostAllocDefault);
+  }
   if (e != cudaSuccess) {
     cuda_fail(e, "create");
     cudaFree(h->ws);
@@ -344,6 +374,12 @@ int ftmoe_destroy(ftmoe_handle* h) {
   if (!h) return FTMOE_OK;
   cudaSetDevice(h->device);
   for (auto& L : h->layers) free_layer(L);
+  if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+  if (h->ev_compute) cudaEventDestroy(h->ev_compute);
+  if (h->ev_copied) cudaEventDestroy(h->ev_copied);
+  if (h->h_touched) cudaFreeHost(h->h_touched);
+  if (h->h_stage) cudaFreeHost(h->h_stage);
+  cudaFree(h->slot_pool);
   delete h->prof;
   cudaFree(h->ws);
   delete h;
@@ -370,9 +406,38 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0
   free_layer(L);
   const int H = c.H, E = c.E, I = c.I, Iw = I_loc;
   L.lay = make_rec_layout(H, Iw);
-  const int64_t bank_bytes = L.lay.bytes * E;
+  // resident: every record in HBM; offload: records built one at a time in
+  // HBM and kept in pinned host memory, HBM slots shared by all layers
+  const bool off = h->offload;
+  if (off) {
+    if (h->slot_pool && h->slot_rec_bytes != L.lay.bytes) return FTMOE_ERR_INVALID_ARG;  // one layout per handle
+    if (!h->slot_pool) {
+      const int64_t per = (int64_t)2 * Iw * (H / 2 + H / 16 + 4) + (int64_t)H * (Iw / 2 + Iw / 16 + 4);
+      int64_t n = c.hbm_slot_bytes / per;
+      n = std::min<int64_t>(n, (int64_t)E * c.num_layers);
+      if (n < 1) return FTMOE_ERR_INVALID_ARG;
+      if (cudaMalloc(&h->slot_pool, n * L.lay.bytes) != cudaSuccess) { cudaGetLastError(); return FTMOE_ERR_OOM; }
+      h->slot_rec_bytes = L.lay.bytes;
+      h->max_batches = (int)((E + n - 1) / n);
+      h->stage_bytes = (size_t)align_up((int64_t)E * 8 + (int64_t)E * 4 + (int64_t)(E + 4) * 4 + E, 256);
+      if (cudaHostAlloc((void**)&h->h_stage, h->stage_bytes * h->max_batches, cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        return FTMOE_ERR_OOM;
+      }
+      h->cache.reset((int)n, c.num_layers, E);
+    }
+    h->cache.reset(h->cache.slots(), c.num_layers, E);  // a reload empties every slot
+  }
+  const int64_t bank_bytes = off ? L.lay.bytes : L.lay.bytes * E;
   if (cudaMalloc(&L.bank, bank_bytes) != cudaSuccess || cudaMalloc(&L.rec_dev, E * sizeof(void*)) != cudaSuccess ||
       cudaMalloc(&L.router_w, (size_t)E * H * 4) != cudaSuccess) {
+    cudaGetLastError();
+    free_layer(L);
+    return FTMOE_ERR_OOM;
+  }
+  if (off && (cudaHostAlloc((void**)&L.host_bank, (size_t)L.lay.bytes * E, cudaHostAllocDefault) != cudaSuccess ||
+              cudaMalloc(&L.rec_z_dev, (size_t)E * 4) != cudaSuccess ||
+              cudaMalloc(&L.active_dev, (size_t)E) != cudaSuccess)) {
     cudaGetLastError();
     free_layer(L);
     return FTMOE_ERR_OOM;
@@ -385,7 +450,7 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0
   }
   const int64_t gcb = H / 2, gsb = H / 16;  // gate_up row bytes (codes, scales)
   for (int e = 0; e < E; ++e) {
-    uint8_t* rec = L.bank + L.lay.bytes * e;
+    uint8_t* rec = off ? L.bank : L.bank + L.lay.bytes * e;
     const int64_t r_gate = (int64_t)e * 2 * I + i0, r_up = (int64_t)e * 2 * I + I + i0;
     CK(cudaMemcpyAsync(rec + L.lay.gu_codes, d->gu_codes + r_gate * gcb, Iw * gcb, K, s));
     CK(cudaMemcpyAsync(rec + L.lay.gu_codes + Iw * gcb, d->gu_codes + r_up * gcb, Iw * gcb, K, s));
@@ -398,8 +463,18 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0
     CK(cudaMemcpy2DAsync(rec + L.lay.dn_scales, Iw / 16, d->dn_scales + (int64_t)e * H * (I / 16) + i0 / 16,
                          I / 16, Iw / 16, H, K, s));
     CK(cudaMemcpyAsync(rec + L.lay.dn_global, d->dn_global + (int64_t)e * H, H * 4, K, s));
+    if (off) {
+      CK(launch_repack_sf(L.bank, L.lay, H, Iw, 1, s));
+      CK(cudaMemcpyAsync(L.host_bank + (int64_t)e * L.lay.bytes, L.bank, L.lay.bytes, cudaMemcpyDeviceToHost, s));
+      CK(cudaStreamSynchronize(s));  // the one staging record is reused
+    }
   }
-  CK(launch_repack_sf(L.bank, L.lay, H, Iw, E, s));
+  if (off) {
+    cudaFree(L.bank);
+    L.bank = nullptr;
+  } else {
+    CK(launch_repack_sf(L.bank, L.lay, H, Iw, E, s));
+  }
   if (h->pf_enabled && prefill_router_supported(H, E)) {
     if (cudaMalloc(&L.router_wcat, (size_t)E * 3 * H * 2) != cudaSuccess ||
         cudaMalloc(&L.router_wnorm, (size_t)E * 4) != cudaSuccess) {
@@ -410,7 +485,7 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0
     CK(launch_router_split(L.router_w, E, H, L.router_wcat, L.router_wnorm, s));
   }
   std::vector<uint8_t*> ptrs(E);
-  for (int e = 0; e < E; ++e) ptrs[e] = L.bank + L.lay.bytes * e;
+  for (int e = 0; e < E; ++e) ptrs[e] = off ? h->slot_pool : L.bank + L.lay.bytes * e;
   CK(cudaMemcpyAsync(L.rec_dev, ptrs.data(), E * sizeof(void*), cudaMemcpyHostToDevice, s));
   if (c.I_shared > 0) {
     if (cudaMalloc(&L.sh_gu, (size_t)2 * sI * H * 2) != cudaSuccess ||
@@ -434,10 +509,10 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0
   return FTMOE_OK;
 }
 
-static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags, int i0,
-                        int I_loc, const ftmoe_aux* aux, cudaStream_t s) {
+// ---- argument builders shared by the resident and offloaded forwards
+
+static RouteArgs route_args(ftmoe_handle* h, Layer& L, const void* x, int T) {
   const ftmoe_config& c = h->cfg;
-  Layer& L = h->layers[layer];
   RouteArgs r = h->r;
   r.x = (const uint16_t*)x;
   r.router_w = L.router_w;
@@ -448,7 +523,14 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
   r.E = c.E;
   r.top_k = c.top_k;
   r.norm_topk_prob = c.norm_topk_prob;
+  return r;
+}
+
+static ExpertArgs expert_args(ftmoe_handle* h, Layer& L, const RouteArgs& r, int T, void* out, int out_flags,
+                              int i0, int I_loc) {
+  const ftmoe_config& c = h->cfg;
   ExpertArgs a{};
+  a.r = r;
   a.rec = L.rec_dev;
   a.lay = L.lay;
   a.win.row0 = i0 - L.li0;
@@ -474,96 +556,152 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
   a.out = out;
   a.out_flags = out_flags;
   a.num_sms = h->num_sms;
+  return a;
+}
+
+static DecodeArgs decode_args(ftmoe_handle* h, const ExpertArgs& a) {
+  DecodeArgs d{};
+  d.r = a.r;
+  d.rec = a.rec;
+  d.lay = a.lay;
+  d.win = a.win;
+  d.H = a.H;
+  d.T = a.T;
+  d.top_k = a.top_k;
+  d.sh_gate_up = a.sh_gate_up;
+  d.sh_down = a.sh_down;
+  d.s_row0 = a.s_row0;
+  d.s_I_loc = a.s_I_loc;
+  d.s_Iw = a.s_Iw;
+  d.hs = h->hs;
+  d.hq_codes = h->hq_codes;
+  d.hq_scales = h->hq_scales;
+  d.hq_cpitch = decode_hq_cpitch(a.win.I_loc);
+  d.hq_spitch = decode_hq_spitch(a.win.I_loc);
+  d.out = a.out;
+  d.out_flags = a.out_flags;
+  d.counter = h->counter;
+  d.gu_split = h->gu_split;
+  d.num_sms = h->num_sms;
+  d.pdl = 1;
+  return d;
+}
+
+// The tensor-core decode kernels' extra arguments.
+static void decode_tc_args(ftmoe_handle* h, Layer& L, DecodeArgs& d) {
+  d.bank = h->offload ? h->slot_pool : L.bank;
+  d.rec_z = h->offload ? L.rec_z_dev : nullptr;
+  d.n_records = h->offload ? h->cache.slots() : h->cfg.E;
+  d.hsf = h->dtc_hsf;
+  d.gpart = h->dtc_gpart;
+  d.dn_counter = h->dtc_counter;
+  d.n_groups = h->dtc_groups;
+  d.hq_cpitch = (int)align_up(d.win.I_loc / 2, 16);
+}
+
+static PfArgs prefill_args(ftmoe_handle* h, Layer& L, const ExpertArgs& a, const void* x, void* out, int out_flags,
+                           bool tc_shared, bool tc_router) {
+  const ftmoe_config& c = h->cfg;
+  const RouteArgs& r = a.r;
+  PfArgs p{};
+  p.offsets = r.offsets;
+  p.perm = r.perm;
+  p.xq_codes = r.xq_codes;
+  p.xq_scales = r.xq_scales;
+  p.bank = h->offload ? h->slot_pool : L.bank;
+  p.rec_z = h->offload ? L.rec_z_dev : nullptr;
+  p.n_records = h->offload ? h->cache.slots() : c.E;
+  p.lay = L.lay;
+  p.win = a.win;
+  p.H = c.H;
+  p.T = a.T;
+  p.E = c.E;
+  p.top_k = c.top_k;
+  p.P_pad_max = (int)h->pf_pad_max;
+  p.pad_off = h->pf_pad_off;
+  p.xg = h->pf_xg;
+  p.xg_sf = h->pf_xg_sf;
+  p.hq = h->pf_hq;
+  p.hq_sf = h->pf_hq_sf;
+  p.hq_pitch = (int)align_up(a.win.I_loc / 2, 16);
+  p.Y = h->Y;
+  p.status = h->status;
+  if (tc_shared || tc_router) p.x = (const uint16_t*)x;
+  if (tc_shared) {
+    p.sh_gu = a.sh_gate_up;
+    p.sh_dn = a.sh_down;
+    p.s_row0 = a.s_row0;
+    p.s_I_loc = a.s_I_loc;
+    p.s_Iw = a.s_Iw;
+    p.hs = h->hs;
+    p.inv = r.inv;
+    p.topk_w = r.topk_w;
+    p.sigma = r.sigma;
+    p.out = out;
+    p.out_flags = out_flags;
+  }
+  if (tc_router) {
+    p.wcat = L.router_wcat;
+    p.wnorm = L.router_wnorm;
+    p.xnorm = r.xnorm;
+    p.router_bias = L.router_bias;
+    p.logits = r.logits;
+    p.err = r.err;
+    p.kappa = kRouterKappa;
+  }
+  return p;
+}
+
+static int copy_aux(ftmoe_handle* h, const RouteArgs& r, int T, const ftmoe_aux* aux, cudaStream_t s) {
+  if (!aux) return FTMOE_OK;
+  const ftmoe_config& c = h->cfg;
+  const int64_t P = (int64_t)T * c.top_k;
+  if (aux->topk_idx) CK(cudaMemcpyAsync(aux->topk_idx, r.topk_idx, P * 4, cudaMemcpyDeviceToDevice, s));
+  if (aux->topk_w) CK(cudaMemcpyAsync(aux->topk_w, r.topk_w, P * 4, cudaMemcpyDeviceToDevice, s));
+  if (aux->offsets) CK(cudaMemcpyAsync(aux->offsets, r.offsets, (c.E + 1) * 4, cudaMemcpyDeviceToDevice, s));
+  if (aux->perm) CK(cudaMemcpyAsync(aux->perm, r.perm, P * 4, cudaMemcpyDeviceToDevice, s));
+  if (aux->inv) CK(cudaMemcpyAsync(aux->inv, r.inv, P * 4, cudaMemcpyDeviceToDevice, s));
+  if (aux->logits) CK(cudaMemcpyAsync(aux->logits, r.logits, (int64_t)T * c.E * 4, cudaMemcpyDeviceToDevice, s));
+  return FTMOE_OK;
+}
+
+static bool prefill_path(ftmoe_handle* h, Layer& L, int T, int I_loc, int row0) {
+  return h->pf_enabled && T > 32 && L.lay.gu_sf_bytes && prefill_supported(h->cfg.H, h->cfg.E, I_loc, L.lIw, row0);
+}
+
+static bool decode_tc_path(ftmoe_handle* h, Layer& L, const ExpertArgs& a, int T) {
+  const ftmoe_config& c = h->cfg;
+  return h->dtc_enabled && decode_tc_supported(c.H, c.E, a.win.I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw,
+                                               a.s_row0, T, c.top_k, L.lay.gu_sf_bytes != 0);
+}
+
+static int forward_offload(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags, int i0,
+                           int I_loc, const ftmoe_aux* aux, cudaStream_t s);
+
+static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags, int i0,
+                        int I_loc, const ftmoe_aux* aux, cudaStream_t s) {
+  if (h->offload) return forward_offload(h, layer, x, T, out, out_flags, i0, I_loc, aux, s);
+  const ftmoe_config& c = h->cfg;
+  Layer& L = h->layers[layer];
+  RouteArgs r = route_args(h, L, x, T);
+  ExpertArgs a = expert_args(h, L, r, T, out, out_flags, i0, I_loc);
   if (decode_supported(c.H, c.E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T, c.top_k)) {
     // decode sizes: routing, streamed gate_up, fused down + combine
-    DecodeArgs d{};
-    d.r = r;
-    d.rec = a.rec;
-    d.lay = a.lay;
-    d.win = a.win;
-    d.H = c.H;
-    d.T = T;
-    d.top_k = c.top_k;
-    d.sh_gate_up = a.sh_gate_up;
-    d.sh_down = a.sh_down;
-    d.s_row0 = a.s_row0;
-    d.s_I_loc = a.s_I_loc;
-    d.s_Iw = a.s_Iw;
-    d.hs = h->hs;
-    d.hq_codes = h->hq_codes;
-    d.hq_scales = h->hq_scales;
-    d.hq_cpitch = decode_hq_cpitch(I_loc);
-    d.hq_spitch = decode_hq_spitch(I_loc);
-    d.out = out;
-    d.out_flags = out_flags;
-    d.counter = h->counter;
-    d.gu_split = h->gu_split;
-    d.num_sms = h->num_sms;
-    d.pdl = 1;
-    if (h->dtc_enabled && decode_tc_supported(c.H, c.E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T,
-                                              c.top_k, L.lay.gu_sf_bytes != 0)) {
+    DecodeArgs d = decode_args(h, a);
+    if (decode_tc_path(h, L, a, T)) {
       // weights through the tensor cores: intermediates as packed codes
-      d.bank = L.bank;
-      d.hsf = h->dtc_hsf;
-      d.gpart = h->dtc_gpart;
-      d.dn_counter = h->dtc_counter;
-      d.n_groups = h->dtc_groups;
-      d.hq_cpitch = (int)align_up(I_loc / 2, 16);
+      decode_tc_args(h, L, d);
       CK(launch_decode_tc(d, s));
     } else {
       CK(launch_decode(d, s));
     }
-  } else if (h->pf_enabled && T > 32 && L.lay.gu_sf_bytes &&
-             prefill_supported(c.H, c.E, I_loc, L.lIw, a.win.row0)) {
+  } else if (prefill_path(h, L, T, I_loc, a.win.row0)) {
     // prefill sizes: router logits, the routed GEMMs and the shared expert
     // (its down product fused with the combine) on the tensor cores where
     // the shapes fit them
     const bool tc_shared = a.sh_gate_up && prefill_shared_supported(c.H, a.s_I_loc, a.s_Iw, a.s_row0, c.top_k);
     const bool tc_router = L.router_wcat != nullptr;
-    PfArgs p{};
-    p.offsets = r.offsets;
-    p.perm = r.perm;
-    p.xq_codes = r.xq_codes;
-    p.xq_scales = r.xq_scales;
-    p.bank = L.bank;
-    p.lay = L.lay;
-    p.win = a.win;
-    p.H = c.H;
-    p.T = T;
-    p.E = c.E;
-    p.top_k = c.top_k;
-    p.P_pad_max = (int)h->pf_pad_max;
-    p.pad_off = h->pf_pad_off;
-    p.xg = h->pf_xg;
-    p.xg_sf = h->pf_xg_sf;
-    p.hq = h->pf_hq;
-    p.hq_sf = h->pf_hq_sf;
-    p.hq_pitch = (int)align_up(I_loc / 2, 16);
-    p.Y = h->Y;
-    p.status = h->status;
-    if (tc_shared || tc_router) p.x = (const uint16_t*)x;
-    if (tc_shared) {
-      p.sh_gu = a.sh_gate_up;
-      p.sh_dn = a.sh_down;
-      p.s_row0 = a.s_row0;
-      p.s_I_loc = a.s_I_loc;
-      p.s_Iw = a.s_Iw;
-      p.hs = h->hs;
-      p.inv = r.inv;
-      p.topk_w = r.topk_w;
-      p.sigma = r.sigma;
-      p.out = out;
-      p.out_flags = out_flags;
-    }
-    if (tc_router) {
-      p.wcat = L.router_wcat;
-      p.wnorm = L.router_wnorm;
-      p.xnorm = r.xnorm;
-      p.router_bias = L.router_bias;
-      p.logits = r.logits;
-      p.err = r.err;
-      p.kappa = kRouterKappa;
-    }
+    PfArgs p = prefill_args(h, L, a, x, out, out_flags, tc_shared, tc_router);
     PfMaps maps;
     CK(prefill_make_maps(p, &maps));
     if (tc_router) {
@@ -573,7 +711,6 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     } else {
       CK(launch_route(r, s));
     }
-    a.r = r;
     if (tc_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
     else CK(launch_experts(a, s, kPartSharedGateUp));
     CK(launch_prefill_routed(p, maps, h->num_sms, s));
@@ -581,19 +718,119 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     else CK(launch_experts(a, s, kPartTail));
   } else {
     CK(launch_route(r, s));
-    a.r = r;
     CK(launch_experts(a, s));
   }
-  if (aux) {
-    const int64_t P = (int64_t)T * c.top_k;
-    if (aux->topk_idx) CK(cudaMemcpyAsync(aux->topk_idx, r.topk_idx, P * 4, cudaMemcpyDeviceToDevice, s));
-    if (aux->topk_w) CK(cudaMemcpyAsync(aux->topk_w, r.topk_w, P * 4, cudaMemcpyDeviceToDevice, s));
-    if (aux->offsets) CK(cudaMemcpyAsync(aux->offsets, r.offsets, (c.E + 1) * 4, cudaMemcpyDeviceToDevice, s));
-    if (aux->perm) CK(cudaMemcpyAsync(aux->perm, r.perm, P * 4, cudaMemcpyDeviceToDevice, s));
-    if (aux->inv) CK(cudaMemcpyAsync(aux->inv, r.inv, P * 4, cudaMemcpyDeviceToDevice, s));
-    if (aux->logits)
-      CK(cudaMemcpyAsync(aux->logits, r.logits, (int64_t)T * c.E * 4, cudaMemcpyDeviceToDevice, s));
+  int rc = copy_aux(h, r, T, aux, s);
+  if (rc) return rc;
+  L.last_T = T;
+  L.last_I_loc = I_loc;
+  return FTMOE_OK;
+}
+
+// Offload mode: route, read the touched experts back (one host
+// synchronisation), then for each batch of at most slots() touched experts
+// place them in HBM slots (copying the missed records from pinned host
+// memory on the copy stream), point the layer's record tables at the slots
+// and run the expert kernels on that batch.  With several batches the routed
+// outputs add up in an fp32 buffer, converted to the caller's output at the
+// end (prefill keeps every pair's Y and combines once).
+static int forward_offload(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags, int i0,
+                           int I_loc, const ftmoe_aux* aux, cudaStream_t s) {
+  const ftmoe_config& c = h->cfg;
+  Layer& L = h->layers[layer];
+  const int E = c.E;
+  RouteArgs r = route_args(h, L, x, T);
+  ExpertArgs a = expert_args(h, L, r, T, out, out_flags, i0, I_loc);
+  const bool dec = T <= 32;
+  if (dec ? !decode_tc_path(h, L, a, T) : !prefill_path(h, L, T, I_loc, a.win.row0)) return FTMOE_ERR_INVALID_ARG;
+  DecodeArgs d{};
+  PfArgs p{};
+  PfMaps maps;
+  bool tc_shared = false, tc_router = false;
+  // ---- routing
+  if (dec) {
+    d = decode_args(h, a);
+    decode_tc_args(h, L, d);
+    CK(launch_decode_tc(d, s, 1));
+  } else {
+    tc_shared = a.sh_gate_up && prefill_shared_supported(c.H, a.s_I_loc, a.s_Iw, a.s_row0, c.top_k);
+    tc_router = L.router_wcat != nullptr;
+    p = prefill_args(h, L, a, x, out, out_flags, tc_shared, tc_router);
+    CK(prefill_make_maps(p, &maps));
+    if (tc_router) {
+      CK(launch_route(r, s, kRouteXq));
+      CK(launch_prefill_router(p, maps, h->num_sms, s));
+      CK(launch_route(r, s, kRouteTopk | kRouteSort));
+    } else {
+      CK(launch_route(r, s));
+    }
   }
+  CK(cudaMemcpyAsync(h->h_touched, r.touched, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(h->h_touched + E, r.n_touched, 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  const int nt = h->h_touched[E];
+  if (nt < 0 || nt > E) return FTMOE_ERR_DEVICE_CHECK;
+  const int S = h->cache.slots();
+  const int nb = (nt + S - 1) / S;
+  if (nb > h->max_batches) return FTMOE_ERR_INVALID_ARG;
+  if (!dec && tc_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
+  if (!dec && !tc_shared) CK(launch_experts(a, s, kPartSharedGateUp));
+  for (int b = 0; b < nb; ++b) {
+    const int* batch = h->h_touched + (int64_t)b * S;
+    const int n = std::min(S, nt - b * S);
+    const std::vector<SlotCache::Placement> pl = h->cache.place(layer, batch, n);
+    // kernels already queued may still read the slots about to be filled
+    CK(cudaEventRecord(h->ev_compute, s));
+    CK(cudaStreamWaitEvent(h->copy_stream, h->ev_compute, 0));
+    for (int i = 0; i < n; ++i) {
+      if (!pl[i].miss) continue;
+      CK(cudaMemcpyAsync(h->slot_pool + (int64_t)pl[i].slot * L.lay.bytes,
+                         L.host_bank + (int64_t)batch[i] * L.lay.bytes, L.lay.bytes, cudaMemcpyHostToDevice,
+                         h->copy_stream));
+      h->h2d_bytes[layer] += L.lay.bytes;
+    }
+    CK(cudaEventRecord(h->ev_copied, h->copy_stream));
+    CK(cudaStreamWaitEvent(s, h->ev_copied, 0));
+    // this batch's tables, staged in pinned memory of their own
+    unsigned char* st = h->h_stage + (size_t)b * h->stage_bytes;
+    const uint8_t** rec = reinterpret_cast<const uint8_t**>(st);
+    int32_t* z = reinterpret_cast<int32_t*>(st + (size_t)E * 8);
+    int32_t* list = z + E;
+    uint8_t* active = reinterpret_cast<uint8_t*>(list + E + 4);
+    for (int e = 0; e < E; ++e) { rec[e] = h->slot_pool; z[e] = 0; active[e] = 0; }
+    for (int i = 0; i < n; ++i) {
+      rec[batch[i]] = h->slot_pool + (int64_t)pl[i].slot * L.lay.bytes;
+      z[batch[i]] = pl[i].slot;
+      active[batch[i]] = 1;
+      list[i] = batch[i];
+    }
+    list[E] = n;
+    CK(cudaMemcpyAsync(L.rec_dev, rec, (size_t)E * 8, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(L.rec_z_dev, z, (size_t)E * 4, cudaMemcpyHostToDevice, s));
+    if (dec) {
+      CK(cudaMemcpyAsync(r.touched, list, (size_t)n * 4, cudaMemcpyHostToDevice, s));
+      CK(cudaMemcpyAsync(r.n_touched, list + E, 4, cudaMemcpyHostToDevice, s));
+      d.skip_shared = b > 0;
+      d.out = nb == 1 ? out : (void*)h->off_y;
+      d.out_flags = nb == 1 ? out_flags : (b == 0 ? FTMOE_OUT_FP32 : (FTMOE_OUT_FP32 | FTMOE_OUT_ACCUMULATE));
+      CK(launch_decode_tc(d, s, 2));
+    } else {
+      CK(cudaMemcpyAsync(L.active_dev, active, (size_t)E, cudaMemcpyHostToDevice, s));
+      p.active = L.active_dev;
+      CK(launch_prefill_routed(p, maps, h->num_sms, s));
+    }
+  }
+  if (dec && nb > 1) CK(launch_store_out(h->off_y, out, out_flags, (int64_t)T * c.H, s));
+  if (dec && nb == 0) {
+    // nothing routed (cannot happen with T >= 1): still the shared expert
+    return FTMOE_ERR_DEVICE_CHECK;
+  }
+  if (!dec) {
+    if (tc_shared) CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
+    else CK(launch_experts(a, s, kPartTail));
+  }
+  int rc = copy_aux(h, r, T, aux, s);
+  if (rc) return rc;
   L.last_T = T;
   L.last_I_loc = I_loc;
   return FTMOE_OK;
@@ -669,8 +906,13 @@ int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out) {
   const int H = h->cfg.H, W = L.last_I_loc;
   const int64_t per_expert = (int64_t)2 * W * (H / 2 + H / 16 + 4) + (int64_t)H * (W / 2 + W / 16) + (int64_t)H * 4;
   out->touched_bytes = out->touched_experts * per_expert;
-  out->resident_slots = h->cfg.E;
-  out->residency = 1.0;
+  out->resident_slots = h->offload ? h->cache.slots() : h->cfg.E;
+  out->residency = h->offload ? (double)h->cache.slots() / ((double)h->cfg.E * h->cfg.num_layers) : 1.0;
+  if (h->offload && h->cache.slots() > 0) {
+    out->hits = h->cache.hits(layer);
+    out->misses = h->cache.misses(layer);
+    out->h2d_bytes = h->h2d_bytes[layer];
+  }
   out->device_status = (int32_t)h->last_status;
   unsigned long long nr = 0;
   CK(cudaMemcpy(&nr, h->r.n_rerank, 8, cudaMemcpyDeviceToHost));

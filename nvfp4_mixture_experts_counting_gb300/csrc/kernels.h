@@ -133,12 +133,15 @@ struct DecodeArgs {
   int num_sms;
   int pdl;             // chain the kernels with programmatic dependent launch
   // tensor-core decode kernels (decode_tc.cu)
-  const uint8_t* bank; // expert records, lay.bytes apart (rec[e] == bank + e * lay.bytes)
+  const uint8_t* bank; // expert records, lay.bytes apart (rec[e] == bank + rec_z[e] * lay.bytes)
+  const int32_t* rec_z;  // [E] record index of each expert in `bank` (null: the expert index)
+  int n_records;         // records in `bank` (E when resident, the slot count when offloaded)
   uint8_t* hsf;        // [E][I_loc/64][512] intermediate scale blocks per touched expert
   float* gpart;        // [groups][T][H] partial outputs of the down kernel
   int* dn_counter;     // [H/128] arrival counters (zero between launches)
   int n_groups;        // down kernel: expert groups per 128-row output tile (+1 for the shared expert)
   int split_tail;      // 1: top-k and the sort run in k_dec_topk instead of the last router CTA
+  int skip_shared;     // 1: leave the shared expert out (a later expert batch of an offloaded forward)
 };
 
 int decode_hq_cpitch(int I_loc);
@@ -151,7 +154,10 @@ bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc,
                          int top_k, bool has_sf);
 int decode_tc_groups(int H, int num_sms);
 cudaError_t decode_tc_set_smem_limits();
-cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s);
+// parts: 1 = routing (router, top-k, sort), 2 = the expert kernels
+cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts = 3);
+// out (bf16, fp32 or fp32 += per out_flags) <- fp32 y [T][H]
+cudaError_t launch_store_out(const float* y, void* out, int out_flags, int64_t n, cudaStream_t s);
 
 // Prefill path: grouped block-scaled NVFP4 GEMMs on tcgen05 (prefill.cu).
 // Pairs are regrouped in a padded order where expert e owns rows
@@ -162,6 +168,9 @@ struct PfArgs {
   const uint8_t* xq_codes;    // [T][H/2]
   const uint8_t* xq_scales;   // [T][H/16]
   const uint8_t* bank;        // expert records, lay.bytes apart
+  const int32_t* rec_z;       // [E] record index of each expert in `bank` (null: the expert index)
+  const uint8_t* active;      // [E] experts this call computes (null: all); others keep Y as is
+  int n_records;              // records in `bank` (E when resident, the slot count when offloaded)
   RecLayout lay;
   Window win;
   int H, T, E, top_k;

@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
   const int E = a.E, H = a.H;
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = a.offsets[e];
   __syncthreads();
-  if (threadIdx.x < 32) warp_excl_scan(E, [&](int e) { return (s_off[e + 1] - s_off[e] + 127) & ~127; }, s_pad);
+  if (threadIdx.x < 32)
+    warp_excl_scan(
+        E, [&](int e) { return (!a.active || a.active[e]) ? (s_off[e + 1] - s_off[e] + 127) & ~127 : 0; }, s_pad);
   __syncthreads();
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e <= E; e += blockDim.x) a.pad_off[e] = s_pad[e];
@@ -259,7 +261,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int e = find_le(s_up, E, u), r = u - s_up[e];
         const int nt = r / J, j = r % J;
         const int pp0 = s_pad[e] + nt * 128;
-        const uint8_t* rec = kF4 ? a.bank + a.lay.bytes * e : nullptr;
+        const int z = kF4 && a.rec_z ? a.rec_z[e] : e;  // record index in the bank / slot pool
+        const uint8_t* rec = kF4 ? a.bank + a.lay.bytes * z : nullptr;
         for (int kt = 0; kt < nkt; ++kt, ++k) {
           const int s = k % kPfStages;
           if (k >= kPfStages && !mbar_wait(&empty[s], ((k / kPfStages) - 1) & 1, a.status)) {
@@ -274,13 +277,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           mbar_arrive_expect_tx(&full[s], 2 * kTile + (kF4 ? 2 * nks * 512 : 0));
           tma_load_2d(sa, &mapA, MODE == 4 ? (kt * 128) % (2 * H) : kt * 128, pp0, &full[s]);
           if (MODE == 0) {
-            tma_load_3d(sb, &mapB, kt * 128, row0 + 64 * j, e, &full[s]);
-            tma_load_3d(sb + kTile / 2, &mapB, kt * 128, Iw + row0 + 64 * j, e, &full[s]);
+            tma_load_3d(sb, &mapB, kt * 128, row0 + 64 * j, z, &full[s]);
+            tma_load_3d(sb + kTile / 2, &mapB, kt * 128, Iw + row0 + 64 * j, z, &full[s]);
             bulk_g2s(sfa, a.xg_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
             bulk_g2s(sfb, rec + a.lay.gu_sf + ((int64_t)(row0 / 64 + j) * nks_all + 4 * kt) * 512, nks * 512,
                      &full[s]);
           } else if (MODE == 1) {
-            tma_load_3d(sb, &mapB, row0 / 2 + kt * 128, 128 * j, e, &full[s]);
+            tma_load_3d(sb, &mapB, row0 / 2 + kt * 128, 128 * j, z, &full[s]);
             bulk_g2s(sfa, a.hq_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
             bulk_g2s(sfb, rec + a.lay.dn_sf + ((int64_t)j * (Iw / 64) + row0 / 64 + 4 * kt) * 512, nks * 512,
                      &full[s]);
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool valid = local < s_off[e + 1] - s_off[e];
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 128;
       if (MODE == 0) {
-        const uint8_t* rec = a.bank + a.lay.bytes * e;
+        const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
         {
           // this unit's 64 gate and 64 up row globals into the warp's slot
           const float* src = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * j +
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         *reinterpret_cast<uint16_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4 +
                                      2 * hf) = valid ? (uint16_t)sfw : (uint16_t)0;
       } else if (MODE == 1) {
-        const uint8_t* rec = a.bank + a.lay.bytes * e;
+        const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
         reinterpret_cast<float4*>(wglob)[lane] =
             __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j) +
                   lane);
@@ -629,7 +632,7 @@ cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m) {
     if ((e = encode(&m->xg, a.xg, 2, dims, st, box)) != cudaSuccess) return e;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)H / 2, (uint64_t)2 * Iw, (uint64_t)a.E};
+    const uint64_t dims[3] = {(uint64_t)H / 2, (uint64_t)2 * Iw, (uint64_t)a.n_records};
     const uint64_t st[2] = {(uint64_t)H / 2, (uint64_t)a.lay.bytes};
     const uint32_t box[3] = {128, 64, 1};
     if ((e = encode(&m->gu, a.bank + a.lay.gu_codes, 3, dims, st, box)) != cudaSuccess) return e;
@@ -640,7 +643,7 @@ cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m) {
     if ((e = encode(&m->hq, a.hq, 2, dims, st, box)) != cudaSuccess) return e;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)Iw / 2, (uint64_t)H, (uint64_t)a.E};
+    const uint64_t dims[3] = {(uint64_t)Iw / 2, (uint64_t)H, (uint64_t)a.n_records};
     const uint64_t st[2] = {(uint64_t)Iw / 2, (uint64_t)a.lay.bytes};
     const uint32_t box[3] = {128, 128, 1};
     if ((e = encode(&m->dn, a.bank + a.lay.dn_codes, 3, dims, st, box)) != cudaSuccess) return e;
