@@ -63,6 +63,9 @@ def parse_args():
     p.add_argument("--layers", type=int, default=0,
                    help="independently seeded layers rotated per step (default: 8 for decode, 2 for prefill)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--slots-frac", type=float, default=0.37,
+                   help="offload workload: HBM slots as a fraction of the experts (byte budget of full windows)")
+    p.add_argument("--iloc", type=int, default=0, help="load and run the window [0, iloc) (0: all of I)")
     return p.parse_args()
 
 
@@ -256,12 +259,13 @@ def cpu_threads() -> int:
 
 # ------------------------------------------------------------------ GPU arm
 
-def build_layers(wl, n_layers, max_tokens, dev):
+def build_layers(wl, n_layers, max_tokens, dev, hbm_slot_bytes=0, I_loc=0):
     import torch
     from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
     cfg = ftmoe.make_config(H=wl.H, I=wl.I, E=wl.E, top_k=wl.top_k, I_shared=wl.I_s,
                             num_layers=n_layers, max_tokens=max_tokens,
-                            norm_topk_prob=wl.norm_topk_prob, has_router_bias=wl.router_bias)
+                            norm_topk_prob=wl.norm_topk_prob, has_router_bias=wl.router_bias,
+                            hbm_slot_bytes=hbm_slot_bytes)
     layer = ftmoe.Layer(cfg, torch.cuda.current_device())
     E, I, H = wl.E, wl.I, wl.H
     for l in range(n_layers):
@@ -287,7 +291,7 @@ def build_layers(wl, n_layers, max_tokens, dev):
         sgu, sdn, sg = W.shared_weights(wl, l, device=dev)
         desc = ftmoe.bank_desc(rw, rb, q["gu_codes"], q["gu_scales"], q["gu_global"], q["dn_codes"],
                                q["dn_scales"], q["dn_global"], sgu, sdn, sg, on_device=True)
-        layer.load_bank(l, desc)
+        layer.load_bank(l, desc, 0, I_loc or None)
         del q
         torch.cuda.synchronize()
     return layer
@@ -328,17 +332,24 @@ def run_gpu(args):
 
     wl = W.WORKLOADS[args.workload]
     T, K, Wm = args.T, args.steps, max(args.warmup, 3)
-    L = args.layers or (8 if T <= 32 else 2)
+    offload = args.workload == "offload"
+    L = args.layers or (1 if offload else (8 if T <= 32 else 2))
     dev = "cuda"
-    layer = build_layers(wl, L, T, dev)
-    I_loc, sI_loc = wl.I, wl.I_s
-    NX = 8
-    xs = [W.hidden(wl, T, step=s + 100 * rank, device=dev) for s in range(NX)]
+    I_loc = args.iloc or wl.I
+    sI_loc = I_loc * wl.I_s // wl.I
+    # offload: the slot budget is a fraction of the experts at full-window
+    # bytes; a narrower window keeps the byte budget (more, smaller slots)
+    slot_bytes = int(round(args.slots_frac * wl.E)) * A.expert_window_bytes(wl.H, wl.I) if offload else 0
+    layer = build_layers(wl, L, T, dev, hbm_slot_bytes=slot_bytes, I_loc=I_loc)
+    # offload: a fresh input every step (the slot cache must not see repeats);
+    # otherwise 8 inputs in turn
+    NX = (K + Wm) if offload else 8
+    xs = [W.hidden(wl, T, step=s + 100000 * rank, device=dev) for s in range(NX)]
     out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(i, o=out, x=None):
-        layer.forward(i % L, xs[i % NX] if x is None else x, o, stream=stream)
+        layer.forward(i % L, xs[i % NX] if x is None else x, o, I_loc=I_loc, stream=stream)
 
     for i in range(Wm):
         step(i)
@@ -346,7 +357,8 @@ def run_gpu(args):
 
     # ---- timed region: the steps alone (per-kernel events would sit between
     # the kernels and stop programmatic dependent launch from overlapping them)
-    rerank0 = layer.stats(0).reranked_tokens
+    st_before = layer.stats(0)
+    rerank0 = st_before.reranked_tokens
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -355,14 +367,15 @@ def run_gpu(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for i in range(K):
-        step(i)
+        step(Wm + i)
     ev1.record(stream)
     _barrier_and_sync(ws)
     t_wall1 = time.time()
     time.sleep(0.25)
     clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    reranked = layer.stats(0).reranked_tokens - rerank0
+    st_after = layer.stats(0)
+    reranked = st_after.reranked_tokens - rerank0
     ms_max = _max_over_ranks(ws, ms)
     value = ws * T * K / (ms_max / 1e3)
 
@@ -383,10 +396,10 @@ def run_gpu(args):
     touched = {}
     for li in range(L):
         for xi in range(NX):
-            layer.forward(li, xs[xi], out, aux=aux, stream=stream)
+            layer.forward(li, xs[xi], out, I_loc=I_loc, aux=aux, stream=stream)
             o = offs.cpu()
             touched[(li, xi)] = int(((o[1:] - o[:-1]) > 0).sum())
-    per_step_touched = [touched[(i % L, i % NX)] for i in range(K)]
+    per_step_touched = [touched[((Wm + i) % L, (Wm + i) % NX)] for i in range(K)]
     mean_touched = sum(per_step_touched) / K
     bytes_step = sum(A.layer_touched_bytes(wl.H, wl.E, I_loc, sI_loc, T, tt) for tt in per_step_touched) / K
     routed_bytes_step = mean_touched * A.expert_window_bytes(wl.H, I_loc)
@@ -476,13 +489,23 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate); bf16 shared expert",
             "data": "synthetic, seeded",
             "config": {"workload": f"{args.workload} layer: H={wl.H} I={wl.I} I_s={wl.I_s} E={wl.E} "
-                                   f"top_k={wl.top_k}, T={T}, full I window"
-                                   + (", Zipf(1.1) router bias" if wl.router_bias else ""),
+                                   f"top_k={wl.top_k}, T={T}, "
+                                   + (f"window [0, {I_loc})" if I_loc != wl.I else "full I window")
+                                   + (", Zipf(1.1) router bias" if wl.router_bias else "")
+                                   + (f", offloaded banks, HBM slots for {args.slots_frac:.0%} of the experts"
+                                      if offload else ""),
                        "global_batch": T * ws, "layers_rotated": L,
                        "l2": f"inputs larger than L2: {L} independently seeded layers rotated per step "
                              f"({L} x {A.expert_window_bytes(wl.H, I_loc) * wl.E / 1e6:.0f} MB of banks)",
                        "parallelism": f"replicas x{ws} (token-parallel, no collective)"},
             "touched_experts_per_step": round(mean_touched, 2),
+            **({"offload": {"slots": st_after.resident_slots, "residency": round(st_after.residency, 4),
+                            "hit_rate": round((st_after.hits - st_before.hits) /
+                                              max(1, st_after.hits - st_before.hits + st_after.misses
+                                                  - st_before.misses), 4),
+                            "h2d_gbs": round((st_after.h2d_bytes - st_before.h2d_bytes) / (ms_max / 1e3) / 1e9, 1),
+                            "h2d_bytes_per_step": int((st_after.h2d_bytes - st_before.h2d_bytes) / K)}}
+               if offload else {}),
             "reranked_tokens_per_step": round(reranked / K, 4),
             "touched_bytes_per_step": int(bytes_step),
             "layer_hbm_frac": round(bytes_step / (ms_max / K / 1e3) / 1e9 / peak, 4),
