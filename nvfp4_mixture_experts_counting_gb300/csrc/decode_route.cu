@@ -105,6 +105,10 @@ __device__ void dec_rerank(const DecodeArgs& a, const RtSmem& L, unsigned char* 
   float* lmin = reinterpret_cast<float*>(cnt + 32);
   int* s_cnt = reinterpret_cast<int*>(lmin + 32);
   int* s_any = s_cnt + 1;
+  // nothing to do in the common case: every token certified
+  bool any = false;
+  for (int t = 0; t < T; ++t) any |= state[t] != 0;
+  if (!any) return;
   // every round lists at least one pending token (a token has at most E
   // candidates and the list holds 4E), so T rounds always suffice
   for (int round = 0; round <= T; ++round) {
@@ -317,6 +321,9 @@ __device__ void dec_split(const DecodeArgs& a, int* pre, int* scan) {
   }
 }
 
+// Largest number of K-chunk partials of the tensor-core router.
+constexpr int kMaxRparts = 16;
+
 // Top-k of every token (certified; uncertain tokens re-ranked by the whole
 // CTA), the counting sort and the gate_up work split, by one CTA.
 __device__ void dec_tail(const DecodeArgs& a, unsigned char* sm) {
@@ -329,6 +336,39 @@ __device__ void dec_tail(const DecodeArgs& a, unsigned char* sm) {
   int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
   int* state = reinterpret_cast<int*>(sm + L.tok_off);
   float* lmin = reinterpret_cast<float*>(state + 96);
+  if (a.n_rparts > 0) {
+    // tensor-core router: add the K-chunk partials of every (token, expert)
+    // in order, spread over the whole CTA; the bound is the accumulation
+    // bound kappa ||x|| ||w|| plus the rounding of these fp32 additions and
+    // of the bias
+    const float gam = (float)(a.n_rparts + 2) * 5.9604645e-8f;
+    const int C = a.n_rparts;  // at most kMaxRparts
+    for (int g = tid; g < T * E / 4; g += kRtThreads) {
+      const int i = 4 * g, t = i / E, e = i - t * E;
+      const float4* pp = reinterpret_cast<const float4*>(a.rpart + (int64_t)t * E + e);
+      float4 v[kMaxRparts];
+#pragma unroll
+      for (int c = 0; c < kMaxRparts; ++c)  // every load in flight before the sums
+        if (c < C) v[c] = __ldcg(pp + (int64_t)c * T * E / 4);
+      float s[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kMaxRparts; ++c) {
+        if (c < C) {
+          s[0] += v[c].x; s[1] += v[c].y; s[2] += v[c].z; s[3] += v[c].w;
+          sa[0] += fabsf(v[c].x); sa[1] += fabsf(v[c].y); sa[2] += fabsf(v[c].z); sa[3] += fabsf(v[c].w);
+        }
+      }
+      const float xn = __ldcg(a.r.xnorm + t);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float bias = a.r.router_bias ? a.r.router_bias[e + q] : 0.f;
+        const float l = s[q] + bias;
+        a.r.logits[i + q] = l;
+        a.r.err[i + q] = a.kappa * xn * a.wnorm[e + q] + gam * (sa[q] + fabsf(bias)) + 1.2e-7f * fabsf(l) + 1e-30f;
+      }
+    }
+    __syncthreads();
+  }
   for (int t = warp; t < T; t += 8) {
     for (int e = lane; e < E; e += 32) {
       s_lg[e] = __ldcg(a.r.logits + (int64_t)t * E + e);
@@ -349,8 +389,10 @@ __device__ void dec_tail(const DecodeArgs& a, unsigned char* sm) {
   int* hist = reinterpret_cast<int*>(sm + L.hist_off);
   int* scan = reinterpret_cast<int*>(sm + L.scan_off);
   dec_sort(a, s_idx, hist, scan);
-  __syncthreads();
-  dec_split(a, hist, scan);
+  if (!a.split_tail) {  // the CUDA-core gate_up kernel's work split
+    __syncthreads();
+    dec_split(a, hist, scan);
+  }
 }
 
 // The routing tail as its own one-CTA kernel (after the router kernel).

@@ -33,6 +33,10 @@ namespace {
 
 constexpr int kDtThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kDtSmem = 220 * 1024;
+// the down kernel runs two CTAs per SM (each issues its own MMAs), so it
+// keeps to half of the shared memory and of TMEM
+constexpr int kDdSmem = 112 * 1024;
+constexpr uint32_t kDdTmemCols = 256;
 constexpr int kDtA = 16384;      // 128 weight rows x 128 bytes
 constexpr int kDtB = 4096;       // up to 32 token / pair rows x 128 bytes
 
@@ -122,7 +126,7 @@ __host__ __device__ inline DdLayout dd_layout(int T, int E, int P) {
   L.stage = kDtA + kDtB + 2048 + 2048;  // 24 KB
   const int part = 32 * 128 * 4;
   const int meta = meta_layout(E, P, 0).bytes;
-  const int nst = (kDtSmem - 1024 - part - meta - 256) / L.stage;
+  const int nst = (kDdSmem - 1024 - part - meta - 256) / L.stage;
   L.nst = nst > 8 ? 8 : nst;
   int o = (L.nst > 0 ? L.nst : 0) * L.stage;
   L.part_off = o; o += part;
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
 
 // ------------------------------------------------------------------ down
 
-__global__ void __launch_bounds__(kDtThreads, 1)
+__global__ void __launch_bounds__(kDtThreads, 2)
     k_dtc_down(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_dn,
                const __grid_constant__ CUtensorMap map_hq, const __grid_constant__ CUtensorMap map_sdn,
                const __grid_constant__ CUtensorMap map_hs) {
@@ -440,7 +444,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
     tma_prefetch_desc(&map_sdn);
     tma_prefetch_desc(&map_hs);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tmem_alloc(tmem_slot, kDdTmemCols);
   for (int i2 = tid; i2 < 32 * 128; i2 += kDtThreads) part[i2] = 0.f;
   tc_fence_before();
   __syncthreads();
@@ -577,7 +581,150 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kDdTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ router
+
+// Router logits on the tensor cores, split over K: CTA (128-expert tile m,
+// K chunk c) forms rpart[c][t][128 m + r] = sum over the chunk of
+// x[t] . [W1 | W2 | W3][128 m + r] (x repeated along K; the three bf16 parts
+// add up to the fp32 router row exactly).  Further CTAs quantise the
+// activations (global 1.0) and one computes sigma = sigmoid(g . x) and an
+// upper bound of ||x|| per token.
+constexpr int kRtKc = 8;  // K tiles per router CTA (all in flight at once)
+
+__device__ __forceinline__ int rt_units(int H, int E) {
+  const int nkt = 6 * H / 128;
+  return (E / 128) * ((nkt + kRtKc - 1) / kRtKc);
+}
+__host__ __device__ inline int rt_xq_ctas(int T, int H) {
+  const int nb = T * (H / kBlock);
+  const int n = (nb + kDtThreads - 1) / kDtThreads;
+  return n < 1 ? 1 : (n > 64 ? 64 : n);
+}
+
+__global__ void __launch_bounds__(kDtThreads)
+    k_dtc_router(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_wr,
+                 const __grid_constant__ CUtensorMap map_x) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* sm = align1024(sm_raw);
+  const int H = a.H, T = a.T, E = a.r.E;
+  const int npad = T <= 16 ? 16 : 32;
+  const int nkt = 6 * H / 128, C = (nkt + kRtKc - 1) / kRtKc;
+  const int n_units = (E / 128) * C;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x;
+  // the next kernels may launch once every CTA here holds its TMEM (a CTA of
+  // theirs that allocated TMEM first could otherwise wait on this grid)
+  if (b >= n_units) pdl_launch_dependents();
+  if (b < n_units) {
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kRtKc * (kDtA + kDtB));
+    uint64_t* accb = full + kRtKc;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+    const int m = b / C, c = b % C;
+    const int kt0 = c * kRtKc, nk = min(kRtKc, nkt - kt0);
+    if (tid == 0) {
+      for (int i = 0; i < kRtKc; ++i) mbar_init(&full[i], 1);
+      mbar_init(accb, 1);
+      fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 32);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+      // every tile of the chunk at once (x is an input of the forward)
+      for (int i = 0; i < nk; ++i) {
+        const int kt = kt0 + i;
+        unsigned char* sa = sm + i * (kDtA + kDtB);
+        mbar_arrive_expect_tx(&full[i], kDtA + npad * 128);
+        tma_load_2d(sa, &map_wr, kt * 128, 128 * m, &full[i]);
+        tma_load_2d(sa + kDtA, &map_x, (kt * 128) % (2 * H), 0, &full[i]);
+      }
+    } else if (warp == 1 && lane == 0) {
+      const uint32_t id = idesc_bf16(128, npad);
+      for (int i = 0; i < nk; ++i) {
+        if (!mbar_wait(&full[i], 0, a.r.status)) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(sm + i * (kDtA + kDtB));
+        const uint64_t adesc = sdesc_k_sw128(sa), bdesc = sdesc_k_sw128(sa + kDtA);
+        for (int ks = 0; ks < 4; ++ks) tc_mma_bf16(tmem, adesc + 2 * ks, bdesc + 2 * ks, id, (i | ks) != 0);
+      }
+      tc_commit(accb);  // every MMA this thread issued
+    } else if (warp >= 2) {
+      const int q = warp & 3, row = 32 * q + lane;
+      const bool ok = mbar_wait(accb, 0, a.r.status);
+      tc_fence_after();
+      if (ok) {
+        float* dst = a.rpart + (int64_t)c * T * E + 128 * m + row;
+        for (int t = 0; t < T; ++t) dst[(int64_t)t * E] = tc_ld1_wait(tmem + ((uint32_t)(32 * q) << 16) + t);
+      }
+    }
+    if (warp == 0 && lane == 0)  // nothing may still be landing when the CTA exits
+      for (int i = 0; i < nk; ++i) mbar_wait(&full[i], 0, a.r.status);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 32);
+    }
+    return;
+  }
+  const int nxq = rt_xq_ctas(T, H);
+  if (b < n_units + nxq) {
+    // a slice of the activation quantisation
+    const int nb = T * (H / kBlock);
+    const int per = (nb + nxq - 1) / nxq;
+    const int q0 = (b - n_units) * per, q1 = min(nb, q0 + per);
+    for (int blk = q0 + tid; blk < q1; blk += kDtThreads) {
+      float v[16];
+      const uint4* p = reinterpret_cast<const uint4*>(a.r.x + (int64_t)blk * kBlock);
+      const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+      const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) {
+        v[2 * qq] = __uint_as_float(words[qq] << 16);
+        v[2 * qq + 1] = __uint_as_float(words[qq] & 0xffff0000u);
+      }
+      uint8_t cq[8];
+      const uint8_t sc = quantize_block16(v, 1.0f, cq);
+      *reinterpret_cast<uint2*>(a.r.xq_codes + (int64_t)blk * 8) = pack8(cq);
+      a.r.xq_scales[blk] = sc;
+    }
+    return;
+  }
+  // sigma_t = sigmoid(g . x_t) and an upper bound of ||x_t||, one warp per token
+  for (int t = warp; t < T; t += kDtThreads / 32) {
+    const uint4* xr = reinterpret_cast<const uint4*>(a.r.x + (int64_t)t * H);
+    const uint4* gr = reinterpret_cast<const uint4*>(a.r.sh_gate);
+    float z = 0.f, q = 0.f;
+    for (int i = lane; i < H / 8; i += 32) {
+      const uint4 xv = __ldg(xr + i);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      uint32_t gw[4] = {0, 0, 0, 0};
+      if (gr) {
+        const uint4 gv = __ldg(gr + i);
+        gw[0] = gv.x; gw[1] = gv.y; gw[2] = gv.z; gw[3] = gv.w;
+      }
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        const float lo = __uint_as_float(xw[k2] << 16), hi = __uint_as_float(xw[k2] & 0xffff0000u);
+        z = fmaf(lo, __uint_as_float(gw[k2] << 16), z);
+        z = fmaf(hi, __uint_as_float(gw[k2] & 0xffff0000u), z);
+        q = fmaf(lo, lo, q);
+        q = fmaf(hi, hi, q);
+      }
+    }
+    z = warp_sum(z);
+    q = warp_sum(q);
+    if (lane == 0) {
+      a.r.sigma[t] = gr ? 1.0f / (1.0f + expf(-z)) : 0.f;
+      a.r.xnorm[t] = sqrtf(q) * (1.0f + 1e-5f);
+    }
   }
 }
 
@@ -585,13 +732,16 @@ __global__ void __launch_bounds__(kDtThreads, 1)
 
 int decode_tc_groups(int H, int num_sms) {
   const int tiles = H / 128;
-  int g = num_sms / tiles - 1;  // routed groups; one more CTA row for the shared expert
+  int g = 2 * num_sms / tiles - 1;  // routed groups (two CTAs per SM); one more CTA row for the shared expert
   return g < 1 ? 1 : g;
 }
 
 bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, int s_Iw, int s_row0, int T,
                          int top_k, bool has_sf) {
   if (!has_sf || T < 1 || T > 32 || E > 1024 || top_k > 32) return false;
+  // the tensor-core router's K chunks (8 tiles of 128 bytes of 3H bf16 each)
+  // are summed by the top-k kernel, which takes at most 16 of them
+  if (E % 128 == 0 && (6 * H / 128 + 7) / 8 > 16) return false;
   if (H % 256 || I_loc % 64 || row0 % 64 || Iw % 64 || I_loc < 256 || Iw < 256) return false;
   if (s_I_loc % 64 || s_row0 % 64 || s_Iw % 64) return false;
   const DgLayout g = dg_layout(H, T, E, T * top_k);
@@ -600,17 +750,20 @@ bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc,
   // weight scales per stage
   if (64 + 4 * g.nks + 16 * g.nst > 512) return false;
   const DdLayout d = dd_layout(T, E, T * top_k);
-  return d.nst >= 3 && d.total <= kDtSmem;
+  return d.nst >= 3 && d.total <= kDdSmem && 64 + 32 * d.nst <= (int)kDdTmemCols;
 }
 
 cudaError_t decode_tc_set_smem_limits() {
   cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_dtc_router, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                1024 + kRtKc * (kDtA + kDtB) + 256)) != cudaSuccess)
+    return e;
   if ((e = cudaFuncSetAttribute(k_dec_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemMax)) !=
       cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_dtc_gate_up, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtSmem)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(k_dtc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtSmem);
+  return cudaFuncSetAttribute(k_dtc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kDdSmem);
 }
 
 static cudaError_t encode_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
@@ -714,18 +867,43 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
   if (parts & 1) {
     const RtSmem L = rt_smem_layout(T, E, a.top_k);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.n_router_ctas + 1);
-    cfg.blockDim = dim3(kRtThreads);
-    cfg.dynamicSmemBytes = 8 * T * 2 * 4;
     cfg.stream = s;
-    FTMOE_PROF_BEGIN("k_dec_route", s);
-    err = cudaLaunchKernelEx(&cfg, k_dec_route, a);
-    FTMOE_PROF_END(s);
+    if (a.wcat) {
+      // router logits on the tensor cores (split K), activation codes, sigma
+      CUtensorMap m_wr, m_xr;
+      {
+        const uint64_t dims[2] = {(uint64_t)6 * H, (uint64_t)E}, st[1] = {(uint64_t)6 * H};
+        const uint32_t box[2] = {128, 128};
+        if ((err = encode_u8(&m_wr, a.wcat, 2, dims, st, box)) != cudaSuccess) return err;
+      }
+      {
+        const uint64_t dims[2] = {(uint64_t)2 * H, (uint64_t)T}, st[1] = {(uint64_t)2 * H};
+        const uint32_t box[2] = {128, (uint32_t)npad};
+        if ((err = encode_u8(&m_xr, a.r.x, 2, dims, st, box)) != cudaSuccess) return err;
+      }
+      const int nkt = 6 * H / 128;
+      a.n_rparts = (nkt + kRtKc - 1) / kRtKc;
+      const int units = (E / 128) * a.n_rparts;
+      cfg.gridDim = dim3(units + rt_xq_ctas(T, H) + 1);
+      cfg.blockDim = dim3(kDtThreads);
+      cfg.dynamicSmemBytes = 1024 + kRtKc * (kDtA + kDtB) + 256;
+      FTMOE_PROF_BEGIN("k_dtc_router", s);
+      err = cudaLaunchKernelEx(&cfg, k_dtc_router, a, m_wr, m_xr);
+      FTMOE_PROF_END(s);
+    } else {
+      cfg.gridDim = dim3(a.n_router_ctas + 1);
+      cfg.blockDim = dim3(kRtThreads);
+      cfg.dynamicSmemBytes = 8 * T * 2 * 4;
+      FTMOE_PROF_BEGIN("k_dec_route", s);
+      err = cudaLaunchKernelEx(&cfg, k_dec_route, a);
+      FTMOE_PROF_END(s);
+    }
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kRtThreads);
     cfg.dynamicSmemBytes = L.total;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
@@ -735,6 +913,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
     if (err != cudaSuccess) return err;
   }
   if (!(parts & 2)) return cudaSuccess;
+  if (a.wcat) a.n_rparts = (6 * H / 128 + kRtKc - 1) / kRtKc;
   {
     const DgLayout L = dg_layout(H, T, E, P);
     FTMOE_PROF_BEGIN("k_dtc_gate_up", s);

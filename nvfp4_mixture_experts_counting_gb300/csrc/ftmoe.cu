@@ -169,6 +169,7 @@ struct ftmoe_handle {
   uint8_t* dtc_hsf = nullptr;
   float* dtc_gpart = nullptr;
   int* dtc_counter = nullptr;
+  float* dtc_rpart = nullptr;  // router K-chunk partial logits [chunks][T][E]
   int dtc_groups = 0;
   uint32_t last_status = 0;
   EventProfiler* prof = nullptr;  // non-null while per-kernel timing is enabled
@@ -181,6 +182,12 @@ namespace ftmoe {
 // logits on the prefill layer (T = 4096 and 16384, four seeds) was 2^-19.5;
 // 2^-15 leaves a margin above 16.
 constexpr float kRouterKappa = 1.0f / 32768.0f;
+// The same bound for the decode router, whose tensor-core sums run over
+// chunks of 256 products and are then added in fp32 (that addition has its
+// own rigorous term in the top-k kernel).  Empirical: the largest error of
+// the whole logit measured against fp64 on the decode layer (T = 32, 40
+// seeds) was 2^-24.6 ||x|| ||w||; 2^-20 leaves a margin above 16.
+constexpr float kRouterKappaSplit = 1.0f / 1048576.0f;
 
 RecLayout make_rec_layout(int H, int Iw) {
   RecLayout L{};
@@ -320,6 +327,8 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
     parts.push_back({(void**)&h->dtc_hsf, (int64_t)c.E * (c.I / 64) * 512});
     parts.push_back({(void**)&h->dtc_gpart, (int64_t)(h->dtc_groups + 1) * Td * c.H * 4});
     parts.push_back({(void**)&h->dtc_counter, (int64_t)(c.H / 128 + 1) * 4});
+    if (c.E % 128 == 0)  // chunks of 8 K tiles of 128 bytes over [W1 | W2 | W3] (K = 3H bf16)
+      parts.push_back({(void**)&h->dtc_rpart, (int64_t)((6 * c.H / 128 + 7) / 8) * Td * c.E * 4});
   }
   // tensor-core prefill buffers (padded pair order), for shapes it accepts
   if (c.max_tokens > 32 && c.H % 256 == 0 && c.I % 64 == 0 && c.E <= 1024 && !(no_tc && no_tc[0] == '1')) {
@@ -475,7 +484,7 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* d, int i0
   } else {
     CK(launch_repack_sf(L.bank, L.lay, H, Iw, E, s));
   }
-  if (h->pf_enabled && prefill_router_supported(H, E)) {
+  if ((h->pf_enabled || h->dtc_enabled) && prefill_router_supported(H, E)) {
     if (cudaMalloc(&L.router_wcat, (size_t)E * 3 * H * 2) != cudaSuccess ||
         cudaMalloc(&L.router_wnorm, (size_t)E * 4) != cudaSuccess) {
       cudaGetLastError();
@@ -597,6 +606,12 @@ static void decode_tc_args(ftmoe_handle* h, Layer& L, DecodeArgs& d) {
   d.dn_counter = h->dtc_counter;
   d.n_groups = h->dtc_groups;
   d.hq_cpitch = (int)align_up(d.win.I_loc / 2, 16);
+  if (L.router_wcat && h->dtc_rpart) {
+    d.wcat = L.router_wcat;
+    d.wnorm = L.router_wnorm;
+    d.rpart = h->dtc_rpart;
+    d.kappa = kRouterKappaSplit;
+  }
 }
 
 static PfArgs prefill_args(ftmoe_handle* h, Layer& L, const ExpertArgs& a, const void* x, void* out, int out_flags,

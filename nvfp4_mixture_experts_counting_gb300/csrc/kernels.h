@@ -142,6 +142,13 @@ struct DecodeArgs {
   int n_groups;        // down kernel: expert groups per 128-row output tile (+1 for the shared expert)
   int split_tail;      // 1: top-k and the sort run in k_dec_topk instead of the last router CTA
   int skip_shared;     // 1: leave the shared expert out (a later expert batch of an offloaded forward)
+  // router logits on the tensor cores (split K): partial sums rpart[c][t][e]
+  // of x . (W1 + W2 + W3) over K chunk c; the top-k kernel adds them in order
+  const uint16_t* wcat;  // [E][3H] bf16 parts of the router rows, or null (CUDA-core router)
+  const float* wnorm;    // [E] upper bound of ||w_e||
+  float* rpart;          // [n_rparts][T][E]
+  int n_rparts;
+  float kappa;           // bound of the tensor-core accumulation: kappa * ||x|| * ||w||
 };
 
 int decode_hq_cpitch(int I_loc);

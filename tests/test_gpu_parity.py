@@ -235,6 +235,34 @@ def test_decode_layer_matches_oracle(decode, T):
     check_output(out, ref.out)
 
 
+def test_decode_router_logit_error_within_bound(decode):
+    """The decode router's logits (tensor cores over the exact three-way bf16
+    split of the fp32 router, 256-product chunks added in fp32) stay within
+    the bound its top-k certificate assumes, 2^-20 * ||x|| * ||w|| (plus the
+    rigorous term of the chunk additions), by a margin of 16: the bound is
+    empirical, and this test is its measurement."""
+    wl, bank, layer = decode
+    rw = bank.router_w.cpu().numpy().astype(np.float64)
+    wn = np.linalg.norm(rw, axis=1)
+    worst = 0.0
+    for step in range(3):
+        T = 32
+        x = W.hidden(wl, T, step=300 + step, device=DEV)
+        logits = torch.empty((T, wl.E), dtype=torch.float32, device=DEV)
+        aux = AuxBufs(T, wl.top_k, wl.E)
+        aux.c.logits = logits.data_ptr()
+        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=DEV)
+        layer.forward(0, x, out, aux=aux.c)
+        torch.cuda.synchronize()
+        x64 = x.float().cpu().numpy().astype(np.float64)
+        exact = moe.router_logits(x64, rw, None)
+        rel = np.abs(logits.cpu().numpy() - exact) / (np.linalg.norm(x64, axis=1)[:, None] * wn[None, :])
+        worst = max(worst, float(rel.max()))
+        idx, _ = moe.select_topk(exact, wl.top_k)
+        assert np.array_equal(aux.topk_idx.cpu().numpy(), idx)
+    assert worst <= 2.0 ** -20 / 16, f"largest relative logit error {worst:.3e}"
+
+
 def test_decode_bank_bytes_sampled(decode):
     wl, bank, _ = decode
     for e in (0, 77, 255):
