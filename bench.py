@@ -302,17 +302,30 @@ def _barrier_and_sync(ws):
     import torch.distributed as dist
     if ws > 1:
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def _max_over_ranks(ws, v: float) -> float:
+    """The largest of the ranks' values (the job's time is its slowest rank's)."""
     if ws == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_step_seed(rank: int, step: int) -> int:
+    """Input step index of a replica: every rank draws its own tokens."""
+    return step + 100000 * rank
+
+
+def whole_job_tokens_per_s(ws: int, T: int, steps: int, ms_max: float) -> float:
+    """Tokens all ranks processed / the slowest rank's time."""
+    return ws * T * steps / (ms_max / 1e3)
 
 
 def run_gpu(args):
@@ -344,7 +357,7 @@ def run_gpu(args):
     # offload: a fresh input every step (the slot cache must not see repeats);
     # otherwise 8 inputs in turn
     NX = (K + Wm) if offload else 8
-    xs = [W.hidden(wl, T, step=s + 100000 * rank, device=dev) for s in range(NX)]
+    xs = [W.hidden(wl, T, step=replica_step_seed(rank, s), device=dev) for s in range(NX)]
     out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -377,7 +390,7 @@ def run_gpu(args):
     st_after = layer.stats(0)
     reranked = st_after.reranked_tokens - rerank0
     ms_max = _max_over_ranks(ws, ms)
-    value = ws * T * K / (ms_max / 1e3)
+    value = whole_job_tokens_per_s(ws, T, K, ms_max)
 
     # ---- per-kernel durations: a second pass of the same steps with CUDA
     # events around every kernel on the launch stream
@@ -461,7 +474,7 @@ def run_gpu(args):
     e1.record(stream)
     _barrier_and_sync(ws)
     e2e_ms = _max_over_ranks(ws, e0.elapsed_time(e1))
-    e2e_value = ws * T * K / (e2e_ms / 1e3)
+    e2e_value = whole_job_tokens_per_s(ws, T, K, e2e_ms)
 
     # ---- GPU launch count inside the timed region (the profiled pass counts
     # the launches of KP steps)
@@ -583,7 +596,7 @@ def run_stack(args):
     T, K, Wm, NL = args.T, args.steps, max(args.warmup, 3), wl.layers
     dev = "cuda"
     layer = build_layers(wl, NL, T, dev)
-    x = W.hidden(wl, T, step=100 * rank, device=dev)
+    x = W.hidden(wl, T, step=replica_step_seed(rank, 0), device=dev)
     out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
     cs = torch.cuda.Stream()
     cs.wait_stream(torch.cuda.current_stream())
@@ -615,7 +628,7 @@ def run_stack(args):
     clocks.stop()
     st1 = layer.stats(0)
     ms_max = _max_over_ranks(ws, ev0.elapsed_time(ev1))
-    value = ws * T * K / (ms_max / 1e3)
+    value = whole_job_tokens_per_s(ws, T, K, ms_max)
     touched_per_layer = (st1.touched_total - st0.touched_total) / (K * NL)
     reranked = (st1.reranked_tokens - st0.reranked_tokens) / K
     bytes_step = NL * A.layer_touched_bytes(wl.H, wl.E, wl.I, wl.I_s, T, touched_per_layer)
@@ -688,7 +701,7 @@ def run_stack(args):
             "kernel_shares": shares,
             "kernel_shares_note": f"CUDA events around each kernel over {KP} steps run without the graph",
             "gpu_launches": launches_total,
-            "e2e": {"value": round(ws * T * K / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+            "e2e": {"value": round(whole_job_tokens_per_s(ws, T, K, e2e_ms), 2), "unit": "tokens/s",
                     "h2d_bytes_per_step": T * wl.H * 2, "d2h_bytes_per_step": T * wl.H * 2},
             "clocks": clocks.summary(t_wall0, t_wall1),
             "cpu_baseline": None,

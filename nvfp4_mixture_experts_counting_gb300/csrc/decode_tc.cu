@@ -736,12 +736,16 @@ int decode_tc_groups(int H, int num_sms) {
   return g < 1 ? 1 : g;
 }
 
+bool decode_tc_router_supported(int H, int E) {
+  // the tensor-core router's K chunks (8 tiles of 128 bytes of 3H bf16 each)
+  // are summed by the top-k kernel, which takes at most 16 of them; larger H
+  // routes on the CUDA cores (k_dec_route) ahead of the same expert kernels
+  return E % 128 == 0 && E <= 1024 && (6 * H / 128 + 7) / 8 <= 16;
+}
+
 bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, int s_Iw, int s_row0, int T,
                          int top_k, bool has_sf) {
   if (!has_sf || T < 1 || T > 32 || E > 1024 || top_k > 32) return false;
-  // the tensor-core router's K chunks (8 tiles of 128 bytes of 3H bf16 each)
-  // are summed by the top-k kernel, which takes at most 16 of them
-  if (E % 128 == 0 && (6 * H / 128 + 7) / 8 > 16) return false;
   if (H % 256 || I_loc % 64 || row0 % 64 || Iw % 64 || I_loc < 256 || Iw < 256) return false;
   if (s_I_loc % 64 || s_row0 % 64 || s_Iw % 64) return false;
   const DgLayout g = dg_layout(H, T, E, T * top_k);

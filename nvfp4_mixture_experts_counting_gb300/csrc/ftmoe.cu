@@ -327,7 +327,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
     parts.push_back({(void**)&h->dtc_hsf, (int64_t)c.E * (c.I / 64) * 512});
     parts.push_back({(void**)&h->dtc_gpart, (int64_t)(h->dtc_groups + 1) * Td * c.H * 4});
     parts.push_back({(void**)&h->dtc_counter, (int64_t)(c.H / 128 + 1) * 4});
-    if (c.E % 128 == 0)  // chunks of 8 K tiles of 128 bytes over [W1 | W2 | W3] (K = 3H bf16)
+    if (decode_tc_router_supported(c.H, c.E))  // chunks of 8 K tiles of 128 bytes over [W1 | W2 | W3]
       parts.push_back({(void**)&h->dtc_rpart, (int64_t)((6 * c.H / 128 + 7) / 8) * Td * c.E * 4});
   }
   // tensor-core prefill buffers (padded pair order), for shapes it accepts
@@ -606,7 +606,7 @@ static void decode_tc_args(ftmoe_handle* h, Layer& L, DecodeArgs& d) {
   d.dn_counter = h->dtc_counter;
   d.n_groups = h->dtc_groups;
   d.hq_cpitch = (int)align_up(d.win.I_loc / 2, 16);
-  if (L.router_wcat && h->dtc_rpart) {
+  if (L.router_wcat && h->dtc_rpart && decode_tc_router_supported(h->cfg.H, h->cfg.E)) {
     d.wcat = L.router_wcat;
     d.wnorm = L.router_wnorm;
     d.rpart = h->dtc_rpart;

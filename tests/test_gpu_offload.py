@@ -111,3 +111,42 @@ def test_offload_bf16_output_matches_oracle():
         ref = bank.oracle_layer(x)
         check_routing(aux, ref)
         check_output(out, ref.out)
+
+
+def test_offload_full_size_decode_matches_resident_and_lru():
+    """The offload workload's own sizes (H=4096, I=2048, E=256, 95 slots =
+    37% of the experts): a run of single-token and small decode steps, each
+    with fresh tokens, must give the resident handle's output and exactly
+    the hits and misses of the replacement rule (a touched list read back
+    stale would show up as too many hits)."""
+    wl = W.WORKLOADS["offload"]
+    bank = GpuBank(wl)
+    res = make_layer(wl, max_tokens=32)
+    res.load_bank(0, bank.desc())
+    n_slots = int(round(0.37 * wl.E))
+    cfg = ftmoe.make_config(H=wl.H, I=wl.I, E=wl.E, top_k=wl.top_k, I_shared=wl.I_s, max_tokens=32,
+                            hbm_slot_bytes=n_slots * A.expert_window_bytes(wl.H, wl.I))
+    off = ftmoe.Layer(cfg)
+    off.load_bank(0, bank.desc())
+    assert off.stats(0).resident_slots == n_slots
+    steps = []
+    for i, T in enumerate([1, 1, 1, 1, 16, 1, 1, 32, 1, 1, 8, 1]):
+        x = W.hidden(wl, T, step=300 + i, device=DEV)
+        ya = torch.empty((T, wl.H), dtype=torch.float32, device=DEV)
+        yb = torch.empty_like(ya)
+        aux = AuxBufs(T, wl.top_k, wl.E)
+        res.forward(0, x, ya, out_flags=ftmoe.OUT_FP32)
+        off.forward(0, x, yb, out_flags=ftmoe.OUT_FP32, aux=aux.c)
+        torch.cuda.synchronize()
+        assert off.check_status() == 0
+        offs = aux.offsets.cpu().numpy()
+        touched = [e for e in range(wl.E) if offs[e + 1] > offs[e]]
+        steps.append(touched)
+        if len(touched) <= n_slots:
+            assert torch.equal(ya.view(torch.int32), yb.view(torch.int32)), f"step {i} T={T}"
+        else:
+            assert rel_l2(yb.cpu().numpy(), ya.cpu().numpy()) <= 1e-6, f"step {i} T={T}"
+    st = off.stats(0)
+    hits, misses = simulate_lru(n_slots, steps)
+    assert (st.hits, st.misses) == (hits, misses)
+    assert st.h2d_bytes == misses * (st.h2d_bytes // max(misses, 1))
