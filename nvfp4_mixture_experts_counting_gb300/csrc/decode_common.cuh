@@ -121,6 +121,28 @@ __host__ __device__ inline RtSmem rt_smem_layout(int T, int E, int top_k) {
   return L;
 }
 
+// k_dec_topk: one CTA per token (its logits and bounds, the chosen slots by
+// rank, the re-rank candidates), and in the last CTA the counting sort over
+// every token (chosen experts of every pair, histograms, scan).
+struct TkSmem {
+  int lg_off, er_off, sl_off, le_off, lv_off, idx_off, hist_off, scan_off, total;
+};
+
+__host__ __device__ inline TkSmem tk_smem_layout(int T, int E, int top_k) {
+  TkSmem L;
+  int o = 0;
+  L.lg_off = o;   o += align16(E * 4);            // logits of the CTA's token
+  L.er_off = o;   o += align16(E * 4);            // their bounds
+  L.sl_off = o;   o += 3 * 32 * 4;                // chosen by rank: logit, bound, expert
+  L.le_off = o;   o += align16(E * 4);            // re-rank candidates: expert
+  L.lv_off = o;   o += E * 8;                     //                     compensated logit
+  L.idx_off = o;  o += align16(T * top_k * 4);    // chosen experts of every pair (sort)
+  L.hist_off = o; o += align16(8 * E * 4);        // sort histograms
+  L.scan_off = o; o += 32 * 4 + 64;               // scan, flags
+  L.total = o;
+  return L;
+}
+
 // k_dec_gate_up.  A stage holds one item: 16 gate and 16 up rows (codes,
 // scales, globals).  Beside it: every token's raw activations (bulk-copied
 // once), the current pass's activations as half2 code values and fp32 scales,

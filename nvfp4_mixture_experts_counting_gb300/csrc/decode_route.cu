@@ -395,14 +395,204 @@ __device__ void dec_tail(const DecodeArgs& a, unsigned char* sm) {
   }
 }
 
-// The routing tail as its own one-CTA kernel (after the router kernel).
+// ---- the routing tail as its own kernel: one CTA per token, then the sort
+// in the last CTA to finish.
+
+// Ranking key of a logit: NaN orders as -infinity, so the order (logit
+// descending, then index ascending) stays total.
+__device__ __forceinline__ float tk_key(float v) { return v != v ? -INFINITY : v; }
+
+// Logits and bounds of token t into shared memory: from the tensor-core
+// router's K-chunk partials, added in chunk order (the bound is the
+// accumulation bound kappa ||x|| ||w|| plus the rounding of these fp32
+// additions and of the bias), else as the CUDA-core router wrote them.
+// lg is padded with -infinity to a multiple of 4 entries.
+__device__ void tk_logits(const DecodeArgs& a, int t, float* lg, float* er) {
+  const int tid = threadIdx.x, T = a.T, E = a.r.E;
+  if (a.n_rparts > 0) {
+    const float gam = (float)(a.n_rparts + 2) * 5.9604645e-8f;
+    const int C = a.n_rparts;  // at most kMaxRparts
+    const float xn = __ldcg(a.r.xnorm + t);
+    for (int g = tid; g < E / 4; g += kRtThreads) {
+      const int e = 4 * g;
+      const float4* pp = reinterpret_cast<const float4*>(a.rpart + (int64_t)t * E + e);
+      float4 v[kMaxRparts];
+#pragma unroll
+      for (int c = 0; c < kMaxRparts; ++c)  // every load in flight before the sums
+        if (c < C) v[c] = __ldcg(pp + (int64_t)c * T * E / 4);
+      float s[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kMaxRparts; ++c) {
+        if (c < C) {
+          s[0] += v[c].x; s[1] += v[c].y; s[2] += v[c].z; s[3] += v[c].w;
+          sa[0] += fabsf(v[c].x); sa[1] += fabsf(v[c].y); sa[2] += fabsf(v[c].z); sa[3] += fabsf(v[c].w);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float bias = a.r.router_bias ? a.r.router_bias[e + q] : 0.f;
+        const float l = s[q] + bias;
+        const float b = a.kappa * xn * a.wnorm[e + q] + gam * (sa[q] + fabsf(bias)) + 1.2e-7f * fabsf(l) + 1e-30f;
+        a.r.logits[(int64_t)t * E + e + q] = l;
+        a.r.err[(int64_t)t * E + e + q] = b;
+        lg[e + q] = tk_key(l);
+        er[e + q] = b;
+      }
+    }
+  } else {
+    for (int e = tid; e < E; e += kRtThreads) {
+      lg[e] = tk_key(__ldcg(a.r.logits + (int64_t)t * E + e));
+      er[e] = __ldcg(a.r.err + (int64_t)t * E + e);
+    }
+  }
+  for (int e = E + tid; e < ((E + 3) & ~3); e += kRtThreads) lg[e] = -INFINITY;
+  __syncthreads();
+}
+
+// Top-k of the CTA's token with the certificate of the fp32 ranking, and the
+// compensated re-rank when the bounds cannot certify it.  Every thread ranks
+// its experts against all E (ranks < k are the chosen slots, in order); the
+// ranking is certified when each chosen interval lies above the next one and
+// no unchosen interval reaches the lowest chosen lower end.  Otherwise every
+// expert whose interval reaches it is a candidate: its logit is recomputed
+// with compensated sums (one warp per candidate) and the k best candidates
+// are taken in (logit, index) order.
+__device__ void tk_select(const DecodeArgs& a, const TkSmem& L, unsigned char* sm, int t) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.r.E, k = a.r.top_k, H = a.r.H;
+  float* lg = reinterpret_cast<float*>(sm + L.lg_off);
+  float* er = reinterpret_cast<float*>(sm + L.er_off);
+  float* sl_l = reinterpret_cast<float*>(sm + L.sl_off);
+  float* sl_r = sl_l + 32;
+  int* sl_e = reinterpret_cast<int*>(sl_r + 32);
+  int* le = reinterpret_cast<int*>(sm + L.le_off);
+  df32* lv = reinterpret_cast<df32*>(sm + L.lv_off);
+  int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
+  int* flags = reinterpret_cast<int*>(sm + L.scan_off) + 32;  // [0] chain ok, [1] lowest chosen lower end, [2] nc
+  // ---- ranks (at most 4 experts per thread: E <= 1024)
+  int rk[4];
+  const float4* k4 = reinterpret_cast<const float4*>(lg);
+  const int E4 = (E + 3) >> 2;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int e = tid + m * kRtThreads;
+    rk[m] = k;
+    if (e < E) {
+      const float v = lg[e];
+      int r = 0;
+#pragma unroll 4
+      for (int f4 = 0; f4 < E4; ++f4) {
+        const float4 u = k4[f4];
+        const int f = 4 * f4;
+        r += (u.x > v) | ((u.x == v) & (f < e));
+        r += (u.y > v) | ((u.y == v) & (f + 1 < e));
+        r += (u.z > v) | ((u.z == v) & (f + 2 < e));
+        r += (u.w > v) | ((u.w == v) & (f + 3 < e));
+      }
+      rk[m] = r;
+      if (r < k) { sl_l[r] = v; sl_r[r] = er[e]; sl_e[r] = e; }
+    }
+  }
+  __syncthreads();
+  // ---- certificate
+  if (warp == 0) {
+    float lo = INFINITY, hi = -INFINITY;
+    if (lane < k) { lo = sl_l[lane] - sl_r[lane]; hi = sl_l[lane] + sl_r[lane]; }
+    const float prev_lo = __shfl_up_sync(0xffffffffu, lo, 1);
+    const bool ok = __all_sync(0xffffffffu, lane >= k || hi < (lane == 0 ? INFINITY : prev_lo));
+    float lmin = lo;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+    if (lane == 0) { flags[0] = ok; reinterpret_cast<float*>(flags)[1] = lmin; }
+  }
+  __syncthreads();
+  const float lmin = reinterpret_cast<const float*>(flags)[1];
+  bool reach = false;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int e = tid + m * kRtThreads;
+    if (e < E && rk[m] >= k && lg[e] + er[e] >= lmin) reach = true;
+  }
+  const bool cert = __syncthreads_or(reach) == 0 && flags[0] != 0;
+  if (cert) {
+    if (warp == 0)
+      dec_write_slots(a, t, lane, lane < k ? sl_e[lane] : 0, lane < k ? sl_l[lane] : 0.f, sl_l[0], lg, s_idx);
+    return;
+  }
+  // ---- re-rank: candidates in index order
+  if (tid == 0 && a.r.n_rerank) atomicAdd(a.r.n_rerank, 1ull);  // telemetry only
+  if (warp == 0) {
+    int w = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const bool c = e < E && lg[e] + er[e] >= lmin;
+      const unsigned msk = __ballot_sync(0xffffffffu, c);
+      if (c) le[w + __popc(msk & ((1u << lane) - 1))] = e;
+      w += __popc(msk);
+    }
+    if (lane == 0) flags[2] = w;
+  }
+  __syncthreads();
+  const int nc = flags[2];
+  for (int i = warp; i < nc; i += kRtThreads / 32) {
+    const int e = le[i];
+    const df32 v = logit_df32(a.r.x + (int64_t)t * H, a.r.router_w + (int64_t)e * H, H,
+                              a.r.router_bias ? a.r.router_bias[e] : 0.f, lane);
+    if (lane == 0) lv[i] = v;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int my_idx = 0;
+    float my_l = 0.f, lmax = -INFINITY;
+    const df32 none = {-INFINITY, 0.f};
+    for (int j = 0; j < k; ++j) {
+      df32 bl = none;
+      int be = 0x7fffffff, bc = -1;
+      for (int c = lane; c < nc; c += 32) {
+        const df32 v = lv[c];
+        const int e = le[c];
+        if (v.hi != -INFINITY && df_before(v, e, bl, be)) { bl = v; be = e; bc = c; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const df32 ol = {__shfl_xor_sync(0xffffffffu, bl.hi, o), __shfl_xor_sync(0xffffffffu, bl.lo, o)};
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        if (df_before(ol, oe, bl, be)) { bl = ol; be = oe; bc = oc; }
+      }
+      if (lane == j) { my_idx = be; my_l = bl.hi; }
+      if (j == 0) lmax = bl.hi;
+      __syncwarp();
+      if (lane == 0 && bc >= 0) lv[bc] = none;
+      __syncwarp();
+    }
+    dec_write_slots(a, t, lane, my_idx, my_l, lmax, lg, s_idx);
+  }
+}
+
+// After the router kernel: CTA t selects token t's experts; the last CTA to
+// finish (arrival counter) runs the counting sort over every token.
 __global__ void __launch_bounds__(kRtThreads) k_dec_topk(DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
+  __shared__ int s_last;
   // let the gate_up kernel launch now: its first phase (the shared expert)
-  // needs no routing, and this one-CTA grid is already resident
+  // needs no routing
   pdl_launch_dependents();
   pdl_wait();
-  dec_tail(a, sm);
+  const int tid = threadIdx.x, t = blockIdx.x;
+  const TkSmem L = tk_smem_layout(a.T, a.r.E, a.top_k);
+  tk_logits(a, t, reinterpret_cast<float*>(sm + L.lg_off), reinterpret_cast<float*>(sm + L.er_off));
+  tk_select(a, L, sm, t);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(a.counter, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
+  for (int i = tid; i < a.T * a.top_k; i += kRtThreads) s_idx[i] = __ldcg(a.r.topk_idx + i);
+  dec_sort(a, s_idx, reinterpret_cast<int*>(sm + L.hist_off), reinterpret_cast<int*>(sm + L.scan_off));
+  if (tid == 0) *a.counter = 0;  // ready for the next launch
 }
 
 __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {

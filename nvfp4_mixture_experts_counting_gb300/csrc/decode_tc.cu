@@ -140,6 +140,25 @@ __host__ __device__ inline DdLayout dd_layout(int T, int E, int P) {
 
 // ------------------------------------------------------------------ gate_up
 
+// First routed unit of CTA b (of G) when the CTAs' whole loads are balanced
+// in K tiles: the R routed units cost nkt tiles each, and the Js shared
+// units (nkt_s tiles each) went round-robin to the CTAs first, so CTAs
+// before b ran cum(b) = (Js / G) * b + min(b, Js % G) of them.  With the
+// cumulative target b * total / G, the routed units before CTA b are
+// (b * total / G - nkt_s * cum(b)) / nkt, clamped to [0, R]; that is
+// non-decreasing in b (where it falls, it is below zero) and reaches R at
+// b = G.
+__device__ __forceinline__ int dtc_split(int b, int G, int R, int nkt, int Js, int nkt_s) {
+  if (b >= G) return R;
+  const int64_t total = (int64_t)R * nkt + (int64_t)Js * nkt_s;
+  const int rem = Js % G;
+  const int64_t cum = (int64_t)(Js / G) * b + (b < rem ? b : rem);
+  const int64_t num = (int64_t)b * total - (int64_t)G * nkt_s * cum;
+  if (num <= 0) return 0;
+  const int64_t r = num / ((int64_t)G * nkt);
+  return r < R ? (int)r : R;
+}
+
 __global__ void __launch_bounds__(kDtThreads, 1)
     k_dtc_gate_up(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_gu,
                   const __grid_constant__ CUtensorMap map_xq, const __grid_constant__ CUtensorMap map_sgu,
@@ -200,6 +219,8 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   // this CTA's equal share of the routed units (touched expert, 64-row
   // window tile), a contiguous range.  Ring positions carry over.
   int kk = 0, ui = 0, nt = 0, r0 = 0;
+  int rs = 0;         // ring stage of kk (kk mod NST) and its phase parity, kept
+  uint32_t rph = 0;   // incrementally: NST is a run-time value and divisions cost
   const int q = warp & 3;
   const bool up = q >= 2;
   const int i = 32 * (q & 1) + lane;
@@ -233,8 +254,8 @@ __global__ void __launch_bounds__(kDtThreads, 1)
       }
       __syncthreads();
       const int R = nt * J;
-      r0 = (int)((int64_t)R * blockIdx.x / gridDim.x);
-      n_my = (int)((int64_t)R * (blockIdx.x + 1) / gridDim.x) - r0;
+      r0 = dtc_split(blockIdx.x, gridDim.x, R, L.nkt, Js, nkt_s);
+      n_my = dtc_split(blockIdx.x + 1, gridDim.x, R, L.nkt, Js, nkt_s) - r0;
     }
     if (warp == 0) {
       // ---------------- TMA producer
@@ -247,8 +268,10 @@ __global__ void __launch_bounds__(kDtThreads, 1)
           const uint8_t* rec = shared ? nullptr : s_rec[rr / J];
           const int nkt_u = shared ? nkt_s : L.nkt;
           for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
-            const int s = kk % NST;
-            if (kk >= NST && !mbar_wait(&empty[s], ((kk / NST) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+            const int s = rs;
+            const uint32_t ph = rph;
+            if (++rs == NST) { rs = 0; rph ^= 1; }
+            if (kk >= NST && !mbar_wait(&empty[s], ph ^ 1, a.r.status)) { *abort_flag = 1; break; }
             unsigned char* sa = sm + s * L.stage;
             if (shared) {
               mbar_arrive_expect_tx(&full[s], kDtA + npad * 128);
@@ -278,8 +301,10 @@ __global__ void __launch_bounds__(kDtThreads, 1)
           tc_fence_after();
           const uint32_t d = tmem + buf * npad;
           for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
-            const int s = kk % NST;
-            if (!mbar_wait(&full[s], (kk / NST) & 1, a.r.status)) { *abort_flag = 1; ok = false; break; }
+            const int s = rs;
+            const uint32_t ph = rph;
+            if (++rs == NST) { rs = 0; rph ^= 1; }
+            if (!mbar_wait(&full[s], ph, a.r.status)) { *abort_flag = 1; ok = false; break; }
             tc_fence_after();
             const uint32_t sa = smem_u32(sm + s * L.stage);
             const uint64_t adesc = sdesc_k_sw128(sa);
@@ -459,7 +484,8 @@ __global__ void __launch_bounds__(kDtThreads, 2)
 
   if (warp == 0) {
     if (lane == 0) {
-      int kk = 0;
+      int kk = 0, rs = 0;  // ring position, its stage and phase parity
+      uint32_t rph = 0;
       for (int it = 0; it < n_items && !*abort_flag; ++it) {
         const int ti = ti0 + it;
         const int e = shared ? 0 : s_touched[ti];
@@ -467,8 +493,10 @@ __global__ void __launch_bounds__(kDtThreads, 2)
         const uint8_t* rec = shared ? nullptr : s_rec[ti];
         const int nkt_u = shared ? nkt_s : nkt_r;
         for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
-          const int s = kk % NST;
-          if (kk >= NST && !mbar_wait(&empty[s], ((kk / NST) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+          const int s = rs;
+          const uint32_t ph = rph;
+          if (++rs == NST) { rs = 0; rph ^= 1; }
+          if (kk >= NST && !mbar_wait(&empty[s], ph ^ 1, a.r.status)) { *abort_flag = 1; break; }
           unsigned char* sa = sm + s * L.stage;
           if (shared) {
             mbar_arrive_expect_tx(&full[s], kDtA + npad * 128);
@@ -490,7 +518,8 @@ __global__ void __launch_bounds__(kDtThreads, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_f4 = idesc_nvf4(128, npad), id_bf = idesc_bf16(128, npad);
-      int kk = 0;
+      int kk = 0, rs = 0;
+      uint32_t rph = 0;
       bool ok = true;
       for (int it = 0; it < n_items && !*abort_flag; ++it) {
         const int buf = it & 1;
@@ -499,8 +528,10 @@ __global__ void __launch_bounds__(kDtThreads, 2)
         const uint32_t d = tmem + buf * npad;
         const int nkt_u = shared ? nkt_s : nkt_r;
         for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
-          const int s = kk % NST;
-          if (!mbar_wait(&full[s], (kk / NST) & 1, a.r.status)) { *abort_flag = 1; ok = false; break; }
+          const int s = rs;
+          const uint32_t ph = rph;
+          if (++rs == NST) { rs = 0; rph ^= 1; }
+          if (!mbar_wait(&full[s], ph, a.r.status)) { *abort_flag = 1; ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(sm + s * L.stage);
           const uint64_t adesc = sdesc_k_sw128(sa), bdesc = sdesc_k_sw128(sa + kDtA);
@@ -869,7 +900,6 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
   a.n_shared_ctas = 0;
   a.split_tail = 1;
   if (parts & 1) {
-    const RtSmem L = rt_smem_layout(T, E, a.top_k);
     cudaLaunchConfig_t cfg = {};
     cfg.stream = s;
     if (a.wcat) {
@@ -906,9 +936,9 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(1);
+    cfg.gridDim = dim3(T);  // one CTA per token; the last one sorts
     cfg.blockDim = dim3(kRtThreads);
-    cfg.dynamicSmemBytes = L.total;
+    cfg.dynamicSmemBytes = tk_smem_layout(T, E, a.top_k).total;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
     FTMOE_PROF_BEGIN("k_dec_topk", s);

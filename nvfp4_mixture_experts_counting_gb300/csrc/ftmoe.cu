@@ -700,10 +700,11 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
   Layer& L = h->layers[layer];
   RouteArgs r = route_args(h, L, x, T);
   ExpertArgs a = expert_args(h, L, r, T, out, out_flags, i0, I_loc);
-  if (decode_supported(c.H, c.E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T, c.top_k)) {
+  const bool dtc = decode_tc_path(h, L, a, T);
+  if (dtc || decode_supported(c.H, c.E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T, c.top_k)) {
     // decode sizes: routing, streamed gate_up, fused down + combine
     DecodeArgs d = decode_args(h, a);
-    if (decode_tc_path(h, L, a, T)) {
+    if (dtc) {
       // weights through the tensor cores: intermediates as packed codes
       decode_tc_args(h, L, d);
       CK(launch_decode_tc(d, s));
