@@ -32,6 +32,7 @@ namespace ftmoe {
 namespace {
 
 constexpr int kDtThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kDgThreads = 224;  // gate_up and down: the same, and warp 6 copies scale factors into TMEM
 constexpr int kDtSmem = 220 * 1024;
 // the down kernel runs two CTAs per SM (each issues its own MMAs), so it
 // keeps to half of the shared memory and of TMEM
@@ -83,14 +84,14 @@ __host__ __device__ inline DgLayout dg_layout(int H, int T, int E, int P) {
   L.stage = kDtA + kDtB + 2048;  // 22 KB, a multiple of 1024
   const int xres = L.nkt * L.npad * 128, sfb = L.nks * 512, u = 2 * 32 * 64 * 4;
   const int meta = meta_layout(E, P, 0).bytes;
-  const int nst = (kDtSmem - 1024 - xres - sfb - u - meta - 256) / L.stage;
+  const int nst = (kDtSmem - 1024 - xres - sfb - u - meta - 512) / L.stage;
   L.nst = nst > 8 ? 8 : nst;
   int o = (L.nst > 0 ? L.nst : 0) * L.stage;
   L.xres_off = o; o += xres;
   L.sfb_off = o;  o += sfb;
   L.u_off = o;    o += u;
   L.meta_off = o; o += meta;
-  L.bar_off = o;  o += 256;
+  L.bar_off = o;  o += 512;
   L.total = o + 1024;
   return L;
 }
@@ -130,12 +131,12 @@ __host__ __device__ inline DdLayout dd_layout(int T, int E, int P) {
   L.stage = kDtA + kDtB + 2048 + 2048;  // 24 KB
   const int part = 32 * 128 * 4;
   const int meta = meta_layout(E, P, 0).bytes;
-  const int nst = (kDdSmem - 1024 - part - meta - 256) / L.stage;
+  const int nst = (kDdSmem - 1024 - part - meta - 512) / L.stage;
   L.nst = nst > 8 ? 8 : nst;
   int o = (L.nst > 0 ? L.nst : 0) * L.stage;
   L.part_off = o; o += part;
   L.meta_off = o; o += meta;
-  L.bar_off = o;  o += 256;
+  L.bar_off = o;  o += 512;
   L.total = o + 1024;
   return L;
 }
@@ -163,7 +164,7 @@ __device__ __forceinline__ int dtc_split(int b, int G, int R, int nkt, int Js, i
   return r < R ? (int)r : R;
 }
 
-__global__ void __launch_bounds__(kDtThreads, 1)
+__global__ void __launch_bounds__(kDgThreads, 1)
     k_dtc_gate_up(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_gu,
                   const __grid_constant__ CUtensorMap map_xq, const __grid_constant__ CUtensorMap map_sgu,
                   const __grid_constant__ CUtensorMap map_x) {
@@ -186,7 +187,9 @@ __global__ void __launch_bounds__(kDtThreads, 1)
   uint64_t* drain = xbar + 1;
   uint64_t* u_full = drain + 1;   // [2] up values written (the two up warps arrive)
   uint64_t* u_free = u_full + 2;  // [2] up values consumed (the two gate warps arrive)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(u_free + 2);
+  uint64_t* sf_ready = u_free + 2;  // [8] stage landed and its weight scales are in TMEM
+  uint64_t* sf_drain = sf_ready + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* U0 = reinterpret_cast<float*>(sm + L.u_off);  // [2][32 pairs][64]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -200,6 +203,8 @@ __global__ void __launch_bounds__(kDtThreads, 1)
     mbar_init(xbar, 1);
     mbar_init(drain, 1);
     for (int b = 0; b < 2; ++b) { mbar_init(&u_full[b], 2); mbar_init(&u_free[b], 2); }
+    for (int s = 0; s < NST; ++s) mbar_init(&sf_ready[s], 1);
+    mbar_init(sf_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -244,19 +249,33 @@ __global__ void __launch_bounds__(kDtThreads, 1)
         for (int kt = 0; kt < L.nkt; ++kt)
           tma_load_2d(sm + L.xres_off + kt * npad * 128, &map_xq, kt * 128, 0, xbar);
       }
-      if (warp == 1) {
-        // activation scale blocks into TMEM (once)
+      if (warp == 6) {
+        // activation scale blocks into TMEM (once): lane t stages token t's
+        // scales (H/16 bytes, 16-byte loads all in flight) as word t of
+        // each K step's block
         unsigned char* sfb = sm + L.sfb_off;
-        for (int ii = lane; ii < L.nks * 32; ii += 32) {
-          const int ks = ii >> 5, t = ii & 31;
-          uint32_t w = 0;
-          if (t < T) w = *reinterpret_cast<const uint32_t*>(a.r.xq_scales + (int64_t)t * (H / 16) + 4 * ks);
-          *reinterpret_cast<uint32_t*>(sfb + ks * 512 + t * 16) = w;
+        const uint4* src = reinterpret_cast<const uint4*>(a.r.xq_scales + (int64_t)lane * (H / 16));
+        for (int c0 = 0; c0 < L.nks / 4; c0 += 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) v[c] = (lane < T && c0 + c < L.nks / 4) ? __ldg(src + c0 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c0 + c < L.nks / 4) {
+              const int ks = 4 * (c0 + c);
+              *reinterpret_cast<uint32_t*>(sfb + (ks + 0) * 512 + lane * 16) = v[c].x;
+              *reinterpret_cast<uint32_t*>(sfb + (ks + 1) * 512 + lane * 16) = v[c].y;
+              *reinterpret_cast<uint32_t*>(sfb + (ks + 2) * 512 + lane * 16) = v[c].z;
+              *reinterpret_cast<uint32_t*>(sfb + (ks + 3) * 512 + lane * 16) = v[c].w;
+            }
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
+        // the first scale-factor commit of phase 1 covers these copies too
         if (lane == 0)
           for (int ks = 0; ks < L.nks; ++ks) tc_cp_sf(tmem + kSfbCol + 4 * ks, sdesc_sf(smem_u32(sfb) + 512 * ks));
+        __syncwarp();
       }
       __syncthreads();
       const int R = nt * J;
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
             const int s = rs;
             const uint32_t ph = rph;
             if (++rs == NST) { rs = 0; rph ^= 1; }
-            if (!mbar_wait(&full[s], ph, a.r.status)) { *abort_flag = 1; ok = false; break; }
+            if (!mbar_wait(&sf_ready[s], ph, a.r.status)) { *abort_flag = 1; ok = false; break; }
             tc_fence_after();
             const uint32_t sa = smem_u32(sm + s * L.stage);
             const uint64_t adesc = sdesc_k_sw128(sa);
@@ -321,7 +340,6 @@ __global__ void __launch_bounds__(kDtThreads, 1)
               for (int ks = 0; ks < 4; ++ks) tc_mma_bf16(d, adesc + 2 * ks, bdesc + 2 * ks, id_bf, (kt | ks) != 0);
             } else {
               const uint32_t sfa_col = tmem + kSfaCol + 16 * s;
-              for (int ks = 0; ks < 4; ++ks) tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
               const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + L.xres_off + kt * npad * 128));
               for (int ks = 0; ks < 4; ++ks)
                 tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, id_f4, sfa_col + 4 * ks,
@@ -333,6 +351,33 @@ __global__ void __launch_bounds__(kDtThreads, 1)
           tc_commit(&acc_full[buf]);
         }
       }
+    } else if (warp == 6) {
+      // ---------------- scale factors: once a stage has landed, its weight
+      // scale blocks go into that stage's TMEM columns and sf_ready[s]
+      // completes when they are there (for a shared unit's stage, as soon
+      // as it has landed), so the MMA thread only issues MMAs
+      if (lane == 0) {
+        for (int it = 0; it < n_my && !*abort_flag; ++it) {
+          const bool shared = phase == 0;
+          const int nkt_u = shared ? nkt_q : L.nkt;
+          for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
+            const int s = rs;
+            const uint32_t ph = rph;
+            if (++rs == NST) { rs = 0; rph ^= 1; }
+            if (!mbar_wait(&full[s], ph, a.r.status)) { *abort_flag = 1; break; }
+            if (shared) {
+              mbar_arrive(&sf_ready[s]);
+              continue;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(sm + s * L.stage);
+            const uint32_t sfa_col = tmem + kSfaCol + 16 * s;
+            for (int ks = 0; ks < 4; ++ks) tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
+            tc_commit(&sf_ready[s]);
+          }
+        }
+      }
+      __syncwarp();
     } else {
       // ---------------- epilogue: warp q = w % 4 holds TMEM lanes 32q..32q+31:
       // gate rows (q = 0, 1) and up rows (q = 2, 3) of window index i.
@@ -450,6 +495,10 @@ __global__ void __launch_bounds__(kDtThreads, 1)
     tc_commit(drain);
     mbar_wait(drain, 0, a.r.status);
   }
+  if (warp == 6 && lane == 0) {
+    tc_commit(sf_drain);
+    mbar_wait(sf_drain, 0, a.r.status);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -460,7 +509,7 @@ __global__ void __launch_bounds__(kDtThreads, 1)
 
 // ------------------------------------------------------------------ down
 
-__global__ void __launch_bounds__(kDtThreads, 2)
+__global__ void __launch_bounds__(kDgThreads, 2)
     k_dtc_down(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_dn,
                const __grid_constant__ CUtensorMap map_hq, const __grid_constant__ CUtensorMap map_sdn,
                const __grid_constant__ CUtensorMap map_hs) {
@@ -482,7 +531,9 @@ __global__ void __launch_bounds__(kDtThreads, 2)
   uint64_t* acc_full = empty + 8;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_ready = drain + 1;  // [8] stage landed and its scale blocks are in TMEM
+  uint64_t* sf_drain = sf_ready + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* part = reinterpret_cast<float*>(sm + L.part_off);  // [32 tokens][128 rows]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -499,6 +550,8 @@ __global__ void __launch_bounds__(kDtThreads, 2)
     for (int s = 0; s < NST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 4); }
     mbar_init(drain, 1);
+    for (int s = 0; s < NST; ++s) mbar_init(&sf_ready[s], 1);
+    mbar_init(sf_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -509,7 +562,7 @@ __global__ void __launch_bounds__(kDtThreads, 2)
     tma_prefetch_desc(&map_hs);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kDdTmemCols);
-  for (int i2 = tid; i2 < 32 * 128; i2 += kDtThreads) part[i2] = 0.f;
+  for (int i2 = tid; i2 < 32 * 128; i2 += blockDim.x) part[i2] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -570,7 +623,7 @@ __global__ void __launch_bounds__(kDtThreads, 2)
           const int s = rs;
           const uint32_t ph = rph;
           if (++rs == NST) { rs = 0; rph ^= 1; }
-          if (!mbar_wait(&full[s], ph, a.r.status)) { *abort_flag = 1; ok = false; break; }
+          if (!mbar_wait(&sf_ready[s], ph, a.r.status)) { *abort_flag = 1; ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(sm + s * L.stage);
           const uint64_t adesc = sdesc_k_sw128(sa), bdesc = sdesc_k_sw128(sa + kDtA);
@@ -579,10 +632,6 @@ __global__ void __launch_bounds__(kDtThreads, 2)
           } else {
             const int nks = min(4, nks_r - 4 * kt);
             const uint32_t sfa_col = tmem + kSfCol + 32 * s, sfb_col = sfa_col + 16;
-            for (int ks = 0; ks < nks; ++ks) {
-              tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
-              tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 2048 + 512 * ks));
-            }
             for (int ks = 0; ks < nks; ++ks)
               tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, id_f4, sfa_col + 4 * ks, sfb_col + 4 * ks,
                           (kt | ks) != 0);
@@ -595,6 +644,40 @@ __global__ void __launch_bounds__(kDtThreads, 2)
       tc_commit(drain);
       mbar_wait(drain, 0, a.r.status);
     }
+  } else if (warp == 6) {
+    // ---------------- scale factors: once a stage has landed, its weight
+    // and intermediate scale blocks go into that stage's TMEM columns and
+    // sf_ready[s] completes when they are there (for the shared group's
+    // stages, as soon as they have landed)
+    if (lane == 0) {
+      int kk = 0, rs = 0;
+      uint32_t rph = 0;
+      for (int it = 0; it < n_items && !*abort_flag; ++it) {
+        const int nkt_u = shared ? nkt_s : nkt_r;
+        for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
+          const int s = rs;
+          const uint32_t ph = rph;
+          if (++rs == NST) { rs = 0; rph ^= 1; }
+          if (!mbar_wait(&full[s], ph, a.r.status)) { *abort_flag = 1; break; }
+          if (shared) {
+            mbar_arrive(&sf_ready[s]);
+            continue;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sm + s * L.stage);
+          const int nks = min(4, nks_r - 4 * kt);
+          const uint32_t sfa_col = tmem + kSfCol + 32 * s, sfb_col = sfa_col + 16;
+          for (int ks = 0; ks < nks; ++ks) {
+            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
+            tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 2048 + 512 * ks));
+          }
+          tc_commit(&sf_ready[s]);
+        }
+      }
+      tc_commit(sf_drain);
+      mbar_wait(sf_drain, 0, a.r.status);
+    }
+    __syncwarp();
   } else {
     // ---------------- epilogue: thread = output row h of the tile, TMEM lane h
     const int q = warp & 3, h = 32 * q + lane;
@@ -863,11 +946,12 @@ static cudaError_t encode_u8(CUtensorMap* m, const void* base, int rank, const u
 }
 
 static cudaError_t launch_tc(void (*kern)(DecodeArgs, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap), dim3 grid,
-                             int smem, cudaStream_t s, bool pdl, const DecodeArgs& a, const CUtensorMap& m0,
-                             const CUtensorMap& m1, const CUtensorMap& m2, const CUtensorMap& m3) {
+                             int threads, int smem, cudaStream_t s, bool pdl, const DecodeArgs& a,
+                             const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorMap& m2,
+                             const CUtensorMap& m3) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kDtThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -990,7 +1074,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
   {
     const DgLayout L = dg_layout(H, T, E, P);
     FTMOE_PROF_BEGIN("k_dtc_gate_up", s);
-    err = launch_tc(k_dtc_gate_up, dim3(a.num_sms), L.total, s, a.pdl, a, m_gu, m_xq, m_sgu, m_x);
+    err = launch_tc(k_dtc_gate_up, dim3(a.num_sms), kDgThreads, L.total, s, a.pdl, a, m_gu, m_xq, m_sgu, m_x);
     FTMOE_PROF_END(s);
     if (err != cudaSuccess) return err;
   }
@@ -998,7 +1082,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
     const DdLayout L = dd_layout(T, E, P);
     const int rows = a.n_groups + ((a.sh_down && !a.skip_shared) ? 1 : 0);
     FTMOE_PROF_BEGIN("k_dtc_down", s);
-    err = launch_tc(k_dtc_down, dim3(H / 128, rows), L.total, s, a.pdl, a, m_dn, m_hq, m_sdn, m_hs);
+    err = launch_tc(k_dtc_down, dim3(H / 128, rows), kDgThreads, L.total, s, a.pdl, a, m_dn, m_hq, m_sdn, m_hs);
     FTMOE_PROF_END(s);
     if (err != cudaSuccess) return err;
   }
