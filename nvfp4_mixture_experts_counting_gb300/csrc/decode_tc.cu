@@ -704,37 +704,61 @@ __global__ void __launch_bounds__(kDgThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    // this group's partials, then the last CTA of the tile adds all groups
-    // in group order
+    // this group's partials gpart[g][tile][t][128], then the last CTA of
+    // the tile adds all groups in group order
     if (!*abort_flag) {
-      for (int t = 0; t < T; ++t) a.gpart[((int64_t)g * T + t) * H + hg] = part[t * 128 + h];
+      float* gp = a.gpart + ((int64_t)g * gridDim.x + ht) * T * 128;
+      for (int t = 0; t < T; ++t) gp[t * 128 + h] = part[t * 128 + h];
       __threadfence();
     }
     named_barrier(1, 128);
     if (tid == 64) s_last = *abort_flag ? 0 : (atomicAdd(&a.dn_counter[ht], 1) == (int)gridDim.y - 1);
     named_barrier(1, 128);
-    if (s_last) {
-      __threadfence();
-      for (int t = 0; t < T; ++t) {
-        float o = 0.f;
-        for (int gg = 0; gg < (int)gridDim.y; ++gg) o += __ldcg(a.gpart + ((int64_t)gg * T + t) * H + hg);
-        const int64_t idx = (int64_t)t * H + hg;
-        if ((a.out_flags & 0xff) == 0) {
-          reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(o);
-        } else if (a.out_flags & 0x100) {
-          reinterpret_cast<float*>(a.out)[idx] += o;
-        } else {
-          reinterpret_cast<float*>(a.out)[idx] = o;
-        }
-      }
-      if (tid == 64) a.dn_counter[ht] = 0;  // ready for the next launch
-    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kDdTmemCols);
+  }
+  if (s_last) {
+    // every thread of the last CTA: items (token, 4 output rows), each the
+    // sum over the groups in group order, with the groups' loads in flight
+    // together
+    __threadfence();
+    const int ng = gridDim.y;
+    const float4* g4 = reinterpret_cast<const float4*>(a.gpart);
+    const int64_t gstride = (int64_t)gridDim.x * T * 32;  // float4s per group
+    for (int item = tid; item < T * 32; item += blockDim.x) {
+      const int t = item >> 5, c4 = item & 31;
+      const float4* src = g4 + ((int64_t)ht * T + t) * 32 + c4;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int g0 = 0; g0 < ng; g0 += 16) {
+        float4 v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (g0 + k < ng) v[k] = __ldcg(src + (g0 + k) * gstride);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (g0 + k < ng) { o.x += v[k].x; o.y += v[k].y; o.z += v[k].z; o.w += v[k].w; }
+      }
+      const int64_t idx = (int64_t)t * H + 128 * ht + 4 * c4;
+      if ((a.out_flags & 0xff) == 0) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + idx) = pk;
+      } else if (a.out_flags & 0x100) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + idx);
+        float4 c = *dst;
+        c.x += o.x; c.y += o.y; c.z += o.z; c.w += o.w;
+        *dst = c;
+      } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + idx) = o;
+      }
+    }
+    if (tid == 64) a.dn_counter[ht] = 0;  // ready for the next launch
   }
 }
 
