@@ -97,6 +97,8 @@ __host__ __device__ inline DgLayout dg_layout(int H, int T, int E, int P) {
 }
 
 // All threads: stage the routing metadata (after the routing kernels).
+// Loads go to L2 (the producing grid ran on other SMs), first-level ones
+// together, so a thread waits for two round trips.
 __device__ __forceinline__ void stage_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M, int nt) {
   const int E = a.r.E, P = a.T * a.top_k, k = a.top_k;
   int* s_touched = reinterpret_cast<int*>(sm + M.touched_off);
@@ -105,17 +107,19 @@ __device__ __forceinline__ void stage_meta(const DecodeArgs& a, unsigned char* s
   int* s_off = reinterpret_cast<int*>(sm + M.off_off);
   int* s_tok = reinterpret_cast<int*>(sm + M.tok_off);
   float* s_w = reinterpret_cast<float*>(sm + M.w_off);
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = a.r.offsets[i];
-  for (int i = threadIdx.x; i < nt; i += blockDim.x) {
-    const int e = a.r.touched[i];
-    s_touched[i] = e;
-    s_z[i] = a.rec_z ? a.rec_z[e] : e;
-    s_rec[i] = a.rec[e];
-  }
-  for (int i = threadIdx.x; i < P; i += blockDim.x) {
-    const int p = a.r.perm[i];
-    s_tok[i] = p / k;
-    s_w[i] = a.r.topk_w[p];
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = __ldcg(a.r.offsets + i);
+  for (int i = threadIdx.x; i < nt || i < P; i += blockDim.x) {
+    const int e = i < nt ? __ldcg(a.r.touched + i) : 0;
+    const int p = i < P ? __ldcg(a.r.perm + i) : 0;
+    if (i < nt) {
+      s_touched[i] = e;
+      s_z[i] = a.rec_z ? __ldcg(a.rec_z + e) : e;
+      s_rec[i] = reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(a.rec) + e));
+    }
+    if (i < P) {
+      s_tok[i] = p / k;
+      s_w[i] = __ldcg(a.r.topk_w + p);
+    }
   }
 }
 
@@ -567,8 +571,10 @@ __global__ void __launch_bounds__(kDgThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the intermediates of the gate_up kernel
-  const int nt = a.r.n_touched[0];
+  // The routing metadata is read before this grid's dependency wait: the
+  // routing kernels completed (and their writes were made visible) before
+  // the gate_up kernel that launched this grid passed its own wait.
+  const int nt = __ldcg(a.r.n_touched);
   stage_meta(a, sm, M, nt);
   __syncthreads();
   const int ti0 = shared ? 0 : (int)((int64_t)g * nt / G), ti1 = shared ? 1 : (int)((int64_t)(g + 1) * nt / G);
@@ -576,33 +582,47 @@ __global__ void __launch_bounds__(kDgThreads, 2)
 
   if (warp == 0) {
     if (lane == 0) {
-      int kk = 0, rs = 0;  // ring position, its stage and phase parity
-      uint32_t rph = 0;
-      for (int it = 0; it < n_items && !*abort_flag; ++it) {
+      // Stage s of K tile kt of item it: the weight part (down rows and their
+      // scales; the shared expert's bf16 columns) and the activation part
+      // (the item's intermediates and their scales; the bf16 hs).
+      auto issue = [&](int s, int it, int kt, bool expect, bool weights, bool acts) {
         const int ti = ti0 + it;
-        const int e = shared ? 0 : s_touched[ti];
-        const int s0 = shared ? 0 : s_off[e];
-        const uint8_t* rec = shared ? nullptr : s_rec[ti];
-        const int nkt_u = shared ? nkt_s : nkt_r;
-        for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
+        unsigned char* sa = sm + s * L.stage;
+        if (shared) {
+          if (expect) mbar_arrive_expect_tx(&full[s], kDtA + npad * 128);
+          if (weights) tma_load_2d(sa, &map_sdn, 2 * a.s_row0 + kt * 128, 128 * ht, &full[s]);
+          if (acts) tma_load_2d(sa + kDtA, &map_hs, kt * 128, 0, &full[s]);
+        } else {
+          const int nks = min(4, nks_r - 4 * kt);
+          if (expect) mbar_arrive_expect_tx(&full[s], kDtA + npad * 128 + 2 * nks * 512);
+          if (weights) {
+            tma_load_3d(sa, &map_dn, row0 / 2 + kt * 128, 128 * ht, s_z[ti], &full[s]);
+            bulk_g2s(sa + kDtA + kDtB, s_rec[ti] + a.lay.dn_sf + ((int64_t)ht * (Iw / 64) + row0 / 64 + 4 * kt) * 512,
+                     nks * 512, &full[s]);
+          }
+          if (acts) {
+            tma_load_2d(sa + kDtA, &map_hq, kt * 128, s_off[s_touched[ti]], &full[s]);
+            bulk_g2s(sa + kDtA + kDtB + 2048, a.hsf + ((int64_t)ti * nks_r + 4 * kt) * 512, nks * 512, &full[s]);
+          }
+        }
+      };
+      const int nkt_u = shared ? nkt_s : nkt_r;
+      // the weights of the first NST K tiles stream before the dependency
+      // wait (they do not depend on the gate_up kernel) ...
+      const int pre = min(NST, n_items * nkt_u);
+      for (int k2 = 0; k2 < pre; ++k2) issue(k2, k2 / nkt_u, k2 % nkt_u, true, true, false);
+      pdl_wait();  // the intermediates of the gate_up kernel
+      // ... their activations after it, then the ring as usual
+      for (int k2 = 0; k2 < pre; ++k2) issue(k2, k2 / nkt_u, k2 % nkt_u, false, false, true);
+      int kk = pre, rs = pre == NST ? 0 : pre;  // ring position, its stage and phase parity
+      uint32_t rph = pre == NST ? 1 : 0;
+      for (int it = kk / nkt_u; it < n_items && !*abort_flag; ++it) {
+        for (int kt = (it == pre / nkt_u) ? pre % nkt_u : 0; kt < nkt_u; ++kt, ++kk) {
           const int s = rs;
           const uint32_t ph = rph;
           if (++rs == NST) { rs = 0; rph ^= 1; }
           if (kk >= NST && !mbar_wait(&empty[s], ph ^ 1, a.r.status)) { *abort_flag = 1; break; }
-          unsigned char* sa = sm + s * L.stage;
-          if (shared) {
-            mbar_arrive_expect_tx(&full[s], kDtA + npad * 128);
-            tma_load_2d(sa, &map_sdn, 2 * a.s_row0 + kt * 128, 128 * ht, &full[s]);
-            tma_load_2d(sa + kDtA, &map_hs, kt * 128, 0, &full[s]);
-          } else {
-            const int nks = min(4, nks_r - 4 * kt);
-            mbar_arrive_expect_tx(&full[s], kDtA + npad * 128 + 2 * nks * 512);
-            tma_load_3d(sa, &map_dn, row0 / 2 + kt * 128, 128 * ht, s_z[ti], &full[s]);
-            tma_load_2d(sa + kDtA, &map_hq, kt * 128, s0, &full[s]);
-            bulk_g2s(sa + kDtA + kDtB, rec + a.lay.dn_sf + ((int64_t)ht * (Iw / 64) + row0 / 64 + 4 * kt) * 512,
-                     nks * 512, &full[s]);
-            bulk_g2s(sa + kDtA + kDtB + 2048, a.hsf + ((int64_t)ti * nks_r + 4 * kt) * 512, nks * 512, &full[s]);
-          }
+          issue(s, it, kt, true, true, true);
         }
       }
       for (int q = kk - NST > 0 ? kk - NST : 0; q < kk; ++q) mbar_wait(&full[q % NST], (q / NST) & 1, a.r.status);
