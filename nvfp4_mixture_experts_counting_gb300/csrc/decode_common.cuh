@@ -133,7 +133,7 @@ __host__ __device__ inline TkSmem tk_smem_layout(int T, int E, int top_k) {
   int o = 0;
   L.lg_off = o;   o += align16(E * 4);            // logits of the CTA's token
   L.er_off = o;   o += align16(E * 4);            // their bounds
-  L.sl_off = o;   o += 3 * 32 * 4;                // chosen by rank: logit, bound, expert
+  L.sl_off = o;   o += 4 * 32 * 4;                // chosen by rank: logit, bound, expert, count
   L.le_off = o;   o += align16(E * 4);            // re-rank candidates: expert
   L.lv_off = o;   o += E * 8;                     //                     compensated logit
   L.idx_off = o;  o += align16(T * top_k * 4);    // chosen experts of every pair (sort)

@@ -469,7 +469,13 @@ __device__ void tk_select(const DecodeArgs& a, const TkSmem& L, unsigned char* s
   df32* lv = reinterpret_cast<df32*>(sm + L.lv_off);
   int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
   int* flags = reinterpret_cast<int*>(sm + L.scan_off) + 32;  // [0] chain ok, [1] lowest chosen lower end, [2] nc
-  // ---- ranks (at most 4 experts per thread: E <= 1024)
+  // ---- ranks (at most 4 experts per thread: E <= 1024).  Fast pass: the
+  // number of keys strictly above each key (four independent counts); it is
+  // the rank unless keys tie, which shows as a chosen rank held by other
+  // than exactly one expert, and then the exact pass ranks ties by index.
+  int* sl_cnt = sl_e + 32;
+  if (tid < 32) sl_cnt[tid] = 0;
+  __syncthreads();
   int rk[4];
   const float4* k4 = reinterpret_cast<const float4*>(lg);
   const int E4 = (E + 3) >> 2;
@@ -479,21 +485,47 @@ __device__ void tk_select(const DecodeArgs& a, const TkSmem& L, unsigned char* s
     rk[m] = k;
     if (e < E) {
       const float v = lg[e];
-      int r = 0;
-#pragma unroll 4
+      int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+#pragma unroll 8
       for (int f4 = 0; f4 < E4; ++f4) {
         const float4 u = k4[f4];
-        const int f = 4 * f4;
-        r += (u.x > v) | ((u.x == v) & (f < e));
-        r += (u.y > v) | ((u.y == v) & (f + 1 < e));
-        r += (u.z > v) | ((u.z == v) & (f + 2 < e));
-        r += (u.w > v) | ((u.w == v) & (f + 3 < e));
+        c0 += u.x > v;
+        c1 += u.y > v;
+        c2 += u.z > v;
+        c3 += u.w > v;
       }
+      const int r = c0 + c1 + c2 + c3;
       rk[m] = r;
-      if (r < k) { sl_l[r] = v; sl_r[r] = er[e]; sl_e[r] = e; }
+      if (r < k) {
+        atomicAdd(&sl_cnt[r], 1);
+        sl_l[r] = v; sl_r[r] = er[e]; sl_e[r] = e;
+      }
     }
   }
   __syncthreads();
+  if (__syncthreads_or(tid < k && sl_cnt[tid] != 1)) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = tid + m * kRtThreads;
+      rk[m] = k;
+      if (e < E) {
+        const float v = lg[e];
+        int r = 0;
+#pragma unroll 4
+        for (int f4 = 0; f4 < E4; ++f4) {
+          const float4 u = k4[f4];
+          const int f = 4 * f4;
+          r += (u.x > v) | ((u.x == v) & (f < e));
+          r += (u.y > v) | ((u.y == v) & (f + 1 < e));
+          r += (u.z > v) | ((u.z == v) & (f + 2 < e));
+          r += (u.w > v) | ((u.w == v) & (f + 3 < e));
+        }
+        rk[m] = r;
+        if (r < k) { sl_l[r] = v; sl_r[r] = er[e]; sl_e[r] = e; }
+      }
+    }
+    __syncthreads();
+  }
   // ---- certificate
   if (warp == 0) {
     float lo = INFINITY, hi = -INFINITY;

@@ -571,6 +571,10 @@ __global__ void __launch_bounds__(kDgThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the next grid (the next forward's router) may launch once every CTA here
+  // holds its TMEM; it waits for this grid before it touches anything this
+  // grid reads or writes
+  pdl_launch_dependents();
   // The routing metadata is read before this grid's dependency wait: the
   // routing kernels completed (and their writes were made visible) before
   // the gate_up kernel that launched this grid passed its own wait.
@@ -834,14 +838,15 @@ __global__ void __launch_bounds__(kDtThreads)
     const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
     if (warp == 0 && lane == 0) {
-      // every tile of the chunk at once (x is an input of the forward)
+      // every tile of the chunk at once: the router tiles before this grid's
+      // dependency wait (they are weights), x after it
       for (int i = 0; i < nk; ++i) {
-        const int kt = kt0 + i;
-        unsigned char* sa = sm + i * (kDtA + kDtB);
         mbar_arrive_expect_tx(&full[i], kDtA + npad * 128);
-        tma_load_2d(sa, &map_wr, kt * 128, 128 * m, &full[i]);
-        tma_load_2d(sa + kDtA, &map_x, (kt * 128) % (2 * H), 0, &full[i]);
+        tma_load_2d(sm + i * (kDtA + kDtB), &map_wr, (kt0 + i) * 128, 128 * m, &full[i]);
       }
+      pdl_wait();
+      for (int i = 0; i < nk; ++i)
+        tma_load_2d(sm + i * (kDtA + kDtB) + kDtA, &map_x, ((kt0 + i) * 128) % (2 * H), 0, &full[i]);
     } else if (warp == 1 && lane == 0) {
       const uint32_t id = idesc_bf16(128, npad);
       for (int i = 0; i < nk; ++i) {
@@ -854,6 +859,7 @@ __global__ void __launch_bounds__(kDtThreads)
       tc_commit(accb);  // every MMA this thread issued
     } else if (warp >= 2) {
       const int q = warp & 3, row = 32 * q + lane;
+      pdl_wait();  // rpart may still be read by the grid before this one
       const bool ok = mbar_wait(accb, 0, a.r.status);
       tc_fence_after();
       if (ok) {
@@ -871,6 +877,7 @@ __global__ void __launch_bounds__(kDtThreads)
     }
     return;
   }
+  pdl_wait();  // x, and the buffers below, belong to the grid before this one until it ends
   const int nxq = rt_xq_ctas(T, H);
   if (b < n_units + nxq) {
     // a slice of the activation quantisation
@@ -1088,6 +1095,13 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
       cfg.gridDim = dim3(units + rt_xq_ctas(T, H) + 1);
       cfg.blockDim = dim3(kDtThreads);
       cfg.dynamicSmemBytes = 1024 + kRtKc * (kDtA + kDtB) + 256;
+      // programmatic launch: the router tiles stream while the grid before
+      // this one (the previous forward's down kernel) finishes
+      cudaLaunchAttribute rattr[1];
+      rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      rattr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = rattr;
+      cfg.numAttrs = a.pdl ? 1 : 0;
       FTMOE_PROF_BEGIN("k_dtc_router", s);
       err = cudaLaunchKernelEx(&cfg, k_dtc_router, a, m_wr, m_xr);
       FTMOE_PROF_END(s);

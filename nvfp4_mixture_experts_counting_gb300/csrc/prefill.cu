@@ -34,7 +34,7 @@ namespace ftmoe {
 namespace {
 
 constexpr int kPfStages = 5;
-constexpr int kPfThreads = 320;    // producer, MMA, 8 epilogue warps
+constexpr int kPfThreads = 352;    // producer, MMA, 8 epilogue warps, scale-factor copier
 constexpr int kPfEpiWarps = 8;
 constexpr int kTile = 16384;        // one 128 x 128-byte operand tile
 constexpr int kSfStage = 2048;      // four 512-byte scale blocks
@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* acc_full = empty + kPfStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_ready = drain + 1;  // [kPfStages] stage landed and its scale blocks are in TMEM
+  uint64_t* sf_drain = sf_ready + kPfStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int E = kF4 ? a.E : 1, H = a.H;
   int* s_off = reinterpret_cast<int*>(sm + kPfOffTab);
@@ -226,6 +228,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int s = 0; s < kPfStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], kPfEpiWarps); }
     mbar_init(drain, 1);
+    for (int s = 0; s < kPfStages; ++s) mbar_init(&sf_ready[s], 1);
+    mbar_init(sf_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -314,19 +318,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         bool ok = true;
         for (int kt = 0; kt < nkt; ++kt, ++k) {
           const int s = k % kPfStages;
-          if (!mbar_wait(&full[s], (k / kPfStages) & 1, a.status)) { *abort_flag = 1; ok = false; break; }
+          // NVFP4: the scale-factor warp completes sf_ready[s] once the stage
+          // has landed and its scale blocks are in TMEM
+          if (!mbar_wait(kF4 ? &sf_ready[s] : &full[s], (k / kPfStages) & 1, a.status)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const int nks = min(4, nks_all - 4 * kt);
           const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + kPfOffA + s * kTile));
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + kPfOffB + s * kTile));
           if (kF4) {
             const uint32_t sfa_col = tmem + kSfCol0 + s * 32, sfb_col = sfa_col + 16;
-            const uint32_t sfa_smem = smem_u32(sm + kPfOffSfa + s * kSfStage);
-            const uint32_t sfb_smem = smem_u32(sm + kPfOffSfb + s * kSfStage);
-            for (int ks = 0; ks < nks; ++ks) {
-              tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
-              tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sfb_smem + 512 * ks));
-            }
             for (int ks = 0; ks < nks; ++ks)
               tc_mma_nvf4(d, adesc + 2 * ks, bdesc + 2 * ks, idesc, sfa_col + 4 * ks, sfb_col + 4 * ks,
                           (kt | ks) != 0);
@@ -338,11 +342,35 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!ok) break;
         tc_commit(&acc_full[buf]);
       }
-      // every MMA and scale copy this thread issued has completed before
-      // TMEM is released
+      // every MMA this thread issued has completed before TMEM is released
       tc_commit(drain);
       mbar_wait(drain, 0, a.status);
     }
+  } else if (warp == 2 + kPfEpiWarps) {
+    // ---------------- scale factors (NVFP4 modes): once a stage has landed,
+    // its scale blocks go into that stage's TMEM columns
+    if (kF4 && lane == 0) {
+      int k = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kPfStages;
+          if (!mbar_wait(&full[s], (k / kPfStages) & 1, a.status)) { *abort_flag = 1; break; }
+          tc_fence_after();
+          const int nks = min(4, nks_all - 4 * kt);
+          const uint32_t sfa_col = tmem + kSfCol0 + s * 32, sfb_col = sfa_col + 16;
+          const uint32_t sfa_smem = smem_u32(sm + kPfOffSfa + s * kSfStage);
+          const uint32_t sfb_smem = smem_u32(sm + kPfOffSfb + s * kSfStage);
+          for (int ks = 0; ks < nks; ++ks) {
+            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
+            tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sfb_smem + 512 * ks));
+          }
+          tc_commit(&sf_ready[s]);
+        }
+      }
+      tc_commit(sf_drain);
+      mbar_wait(sf_drain, 0, a.status);
+    }
+    __syncwarp();
   } else {
     // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ...;
     // the two warps of a lane quarter split the columns in halves
