@@ -187,31 +187,33 @@ __device__ void dec_rerank(const DecodeArgs& a, const RtSmem& L, unsigned char* 
   }
 }
 
-// Counting sort of P <= 1024 pairs by the 256 threads of one CTA: per-warp
-// chunk histograms, a scan over experts, then each warp scatters its chunk in
-// order, so every expert's pairs come out in increasing pair id.
+// Counting sort of the P = T * k <= 1024 pairs (T <= 32) by one CTA of
+// kRtThreads threads.  A token picks an expert at most once, so expert e's
+// pairs are fixed by the mask of tokens that picked it: its count is the
+// mask's population, and pair (t, j) of expert e goes to offsets[e] + the
+// number of earlier tokens in the mask -- every expert's pairs in
+// increasing pair id.  hist holds [E] masks and [E] offsets.
 __device__ void dec_sort(const DecodeArgs& a, const int* s_idx, int* hist /*[8][E]*/, int* scan /*[32]*/) {
-  const int E = a.r.E, P = a.T * a.top_k;
+  const int E = a.r.E, k = a.top_k, P = a.T * k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < 8 * E; i += kRtThreads) hist[i] = 0;
+  uint32_t* mask = reinterpret_cast<uint32_t*>(hist);
+  int* off = hist + E;
+  for (int e = tid; e < E; e += kRtThreads) mask[e] = 0u;
   __syncthreads();
-  const int CH = (P + 7) / 8;
-  const int c0 = min(P, warp * CH), c1 = min(P, c0 + CH);
-  for (int p = c0 + lane; p < c1; p += 32) {
+  for (int p = tid; p < P; p += kRtThreads) {
     int e = s_idx[p];
     if ((unsigned)e >= (unsigned)E) { set_status(a.r.status, kStatusRange); e = 0; }
-    atomicAdd(&hist[warp * E + e], 1);
+    atomicOr(&mask[e], 1u << (p / k));
   }
   __syncthreads();
-  // each thread owns experts [e0, e1): totals, then a block scan of them
+  // each thread owns experts [e0, e1): pair and touched counts, block scan
   const int per = (E + kRtThreads - 1) / kRtThreads;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
   int cnt = 0, tcnt = 0;
   for (int e = e0; e < e1; ++e) {
-    int c = 0;
-    for (int w = 0; w < 8; ++w) c += hist[w * E + e];
-    cnt += c;
-    tcnt += c > 0;
+    const uint32_t m = mask[e];
+    cnt += __popc(m);
+    tcnt += m != 0u;
   }
   int inc = cnt, tinc = tcnt;
 #pragma unroll
@@ -223,17 +225,13 @@ __device__ void dec_sort(const DecodeArgs& a, const int* s_idx, int* hist /*[8][
   __syncthreads();
   int wbase = 0, twbase = 0;
   for (int w = 0; w < warp; ++w) { wbase += scan[w]; twbase += scan[16 + w]; }
-  int off = wbase + inc - cnt, toff = twbase + tinc - tcnt;
+  int run = wbase + inc - cnt, toff = twbase + tinc - tcnt;
   for (int e = e0; e < e1; ++e) {
-    int c = 0;
-    for (int w = 0; w < 8; ++w) {
-      const int h = hist[w * E + e];
-      hist[w * E + e] = off + c;
-      c += h;
-    }
-    a.r.offsets[e] = off;
-    if (c > 0) a.r.touched[toff++] = e;
-    off += c;
+    const uint32_t m = mask[e];
+    off[e] = run;
+    a.r.offsets[e] = run;
+    if (m) a.r.touched[toff++] = e;
+    run += __popc(m);
   }
   if (tid == kRtThreads - 1) {
     a.r.offsets[E] = P;
@@ -241,22 +239,13 @@ __device__ void dec_sort(const DecodeArgs& a, const int* s_idx, int* hist /*[8][
     if (a.r.touched_total) atomicAdd(a.r.touched_total, (unsigned long long)toff);
   }
   __syncthreads();
-  for (int p0 = c0; p0 < c1; p0 += 32) {
-    const int p = p0 + lane;
-    const bool valid = p < c1;
-    int e = valid ? s_idx[p] : -1 - lane;
-    if (valid && (unsigned)e >= (unsigned)E) e = 0;
-    const unsigned mask = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(mask & ((1u << lane) - 1));
-    int pos = 0;
-    if (valid) pos = hist[warp * E + e] + rank;
-    __syncwarp();
-    if (valid) {
-      a.r.perm[pos] = p;
-      a.r.inv[p] = pos;
-      if (rank == 0) hist[warp * E + e] += __popc(mask);
-    }
-    __syncwarp();
+  for (int p = tid; p < P; p += kRtThreads) {
+    int e = s_idx[p];
+    if ((unsigned)e >= (unsigned)E) e = 0;
+    const int t = p / k;
+    const int pos = off[e] + __popc(mask[e] & ((1u << t) - 1u));
+    a.r.perm[pos] = p;
+    a.r.inv[p] = pos;
   }
 }
 

@@ -508,13 +508,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       } else {
-        // combine for token t over output rows [128 j, 128 j + 128)
+        // combine for token t over output rows [128 j, 128 j + 128): the
+        // slots' rows of Y in slot order, then sigma * the shared expert.
+        // Up to 8 slots keep their positions and weights in registers and
+        // have their Y loads in flight four slots at a time.
         const int t = local;
         const int k = a.top_k;
         const int32_t* pos = a.inv + (int64_t)t * k;
         const float* w = a.topk_w + (int64_t)t * k;
         const float sig = valid ? a.sigma[t] : 0.f;
         const int64_t obase = (int64_t)t * H + 128 * j;
+        int pj[8];
+        float wj[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          pj[jj] = (valid && jj < k) ? __ldg(pos + jj) : 0;
+          wj[jj] = (valid && jj < k) ? __ldg(w + jj) : 0.f;
+        }
 #pragma unroll 1
         for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
           uint32_t v[16];
@@ -524,16 +534,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             float o[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = 0.f;
-            for (int jj = 0; jj < k; ++jj) {
-              const float wj = __ldg(w + jj);
-              const float4* yp = reinterpret_cast<const float4*>(a.Y + (int64_t)__ldg(pos + jj) * H + 128 * j + 16 * c);
+            if (k <= 8) {
 #pragma unroll
-              for (int i4 = 0; i4 < 4; ++i4) {
-                const float4 y = yp[i4];
-                o[4 * i4] = fmaf(wj, y.x, o[4 * i4]);
-                o[4 * i4 + 1] = fmaf(wj, y.y, o[4 * i4 + 1]);
-                o[4 * i4 + 2] = fmaf(wj, y.z, o[4 * i4 + 2]);
-                o[4 * i4 + 3] = fmaf(wj, y.w, o[4 * i4 + 3]);
+              for (int j0 = 0; j0 < 8; j0 += 4) {
+                if (j0 < k) {
+                  float4 y[4][4];
+#pragma unroll
+                  for (int q2 = 0; q2 < 4; ++q2) {
+                    const float4* yp = reinterpret_cast<const float4*>(a.Y + (int64_t)pj[j0 + q2] * H + 128 * j + 16 * c);
+#pragma unroll
+                    for (int i4 = 0; i4 < 4; ++i4)
+                      y[q2][i4] = (j0 + q2 < k) ? __ldg(yp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  }
+#pragma unroll
+                  for (int q2 = 0; q2 < 4; ++q2) {
+                    if (j0 + q2 < k) {
+#pragma unroll
+                      for (int i4 = 0; i4 < 4; ++i4) {
+                        o[4 * i4] = fmaf(wj[j0 + q2], y[q2][i4].x, o[4 * i4]);
+                        o[4 * i4 + 1] = fmaf(wj[j0 + q2], y[q2][i4].y, o[4 * i4 + 1]);
+                        o[4 * i4 + 2] = fmaf(wj[j0 + q2], y[q2][i4].z, o[4 * i4 + 2]);
+                        o[4 * i4 + 3] = fmaf(wj[j0 + q2], y[q2][i4].w, o[4 * i4 + 3]);
+                      }
+                    }
+                  }
+                }
+              }
+            } else {
+              for (int jj = 0; jj < k; ++jj) {
+                const float wv = __ldg(w + jj);
+                const float4* yp = reinterpret_cast<const float4*>(a.Y + (int64_t)__ldg(pos + jj) * H + 128 * j + 16 * c);
+#pragma unroll
+                for (int i4 = 0; i4 < 4; ++i4) {
+                  const float4 y = yp[i4];
+                  o[4 * i4] = fmaf(wv, y.x, o[4 * i4]);
+                  o[4 * i4 + 1] = fmaf(wv, y.y, o[4 * i4 + 1]);
+                  o[4 * i4 + 2] = fmaf(wv, y.z, o[4 * i4 + 2]);
+                  o[4 * i4 + 3] = fmaf(wv, y.w, o[4 * i4 + 3]);
+                }
               }
             }
 #pragma unroll
