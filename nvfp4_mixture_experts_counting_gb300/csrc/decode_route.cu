@@ -604,6 +604,12 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_topk(DecodeArgs a) {
   const TkSmem L = tk_smem_layout(a.T, a.r.E, a.top_k);
   tk_logits(a, t, reinterpret_cast<float*>(sm + L.lg_off), reinterpret_cast<float*>(sm + L.er_off));
   tk_select(a, L, sm, t);
+  if (a.meta_masks) {
+    // token t's bit in each chosen expert's mask (lane j of warp 0 wrote
+    // slot j); the expert kernels build the sorted tables from the masks
+    if (tid < a.top_k) atomicOr(a.r.emask + reinterpret_cast<const int*>(sm + L.idx_off)[t * a.top_k + tid], 1u << t);
+    return;
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(a.counter, 1) == (int)gridDim.x - 1);
@@ -811,6 +817,9 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
     }
     return;
   }
+  // ---- the token masks of the top-k kernel start empty
+  if (a.r.emask)
+    for (int e = tid; e < E; e += kRtThreads) a.r.emask[e] = 0u;
   // ---- sigma_t = sigmoid(g . x_t), one warp per token
   for (int t = warp; t < T; t += 8) {
     float z = 0.f;

@@ -56,7 +56,7 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
 // pointers, expert offsets, and per sorted position the token (and, for the
 // down kernel, the routing weight).
 struct Meta {
-  int touched_off, z_off, rec_off, off_off, tok_off, w_off, bytes;
+  int touched_off, z_off, rec_off, off_off, tok_off, w_off, mask_off, scan_off, bytes;
 };
 
 __host__ __device__ inline Meta meta_layout(int E, int P, int base) {
@@ -68,6 +68,8 @@ __host__ __device__ inline Meta meta_layout(int E, int P, int base) {
   M.off_off = o;     o += align16((E + 1) * 4);
   M.tok_off = o;     o += align16(P * 4);
   M.w_off = o;       o += align16(P * 4);
+  M.mask_off = o;    o += align16(E * 4);
+  M.scan_off = o;    o += 80 * 4;
   M.bytes = o - base;
   return M;
 }
@@ -121,6 +123,98 @@ __device__ __forceinline__ void stage_meta(const DecodeArgs& a, unsigned char* s
       s_w[i] = __ldcg(a.r.topk_w + p);
     }
   }
+}
+
+// All threads: the routing tables from the token masks of the top-k kernel
+// and the chosen experts.  A token picks an expert at most once, so expert
+// e's pairs are its mask's tokens in increasing order: the count is the
+// mask's population and pair (t, j) goes to offsets[e] + the mask's tokens
+// before t -- the same stable order as a counting sort.  With `globals`
+// (one CTA) the offsets, touched list, pair order and telemetry also go to
+// HBM.  Returns the number of touched experts.
+__device__ int build_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M, bool globals) {
+  const int E = a.r.E, k = a.top_k, P = a.T * k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  int* s_touched = reinterpret_cast<int*>(sm + M.touched_off);
+  int* s_z = reinterpret_cast<int*>(sm + M.z_off);
+  const uint8_t** s_rec = reinterpret_cast<const uint8_t**>(sm + M.rec_off);
+  int* s_off = reinterpret_cast<int*>(sm + M.off_off);
+  int* s_tok = reinterpret_cast<int*>(sm + M.tok_off);
+  float* s_w = reinterpret_cast<float*>(sm + M.w_off);
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(sm + M.mask_off);
+  int* s_scan = reinterpret_cast<int*>(sm + M.scan_off);  // [32] pairs, [32] touched, [1] total touched
+  // first-level loads together: the masks and this thread's pairs
+  constexpr int kPairs = 8;  // P <= 1024 pairs over at least 128 threads
+  int pe[kPairs];
+  float pw[kPairs];
+#pragma unroll
+  for (int m = 0; m < kPairs; ++m) {
+    const int p = tid + m * nthr;
+    pe[m] = p < P ? __ldcg(a.r.topk_idx + p) : 0;
+    pw[m] = p < P ? __ldcg(a.r.topk_w + p) : 0.f;
+  }
+  for (int e = tid; e < E; e += nthr) s_mask[e] = __ldcg(a.r.emask + e);
+  __syncthreads();
+  // each thread owns experts [e0, e1): pair and touched counts, block scan
+  const int per = (E + nthr - 1) / nthr;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int cnt = 0, tcnt = 0;
+  for (int e = e0; e < e1; ++e) {
+    const uint32_t msk = s_mask[e];
+    cnt += __popc(msk);
+    tcnt += msk != 0u;
+  }
+  int inc = cnt, tinc = tcnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o), tn = __shfl_up_sync(0xffffffffu, tinc, o);
+    if (lane >= o) { inc += n; tinc += tn; }
+  }
+  if (lane == 31) { s_scan[warp] = inc; s_scan[32 + warp] = tinc; }
+  __syncthreads();
+  int run = inc - cnt, toff = tinc - tcnt;
+  for (int w = 0; w < warp; ++w) { run += s_scan[w]; toff += s_scan[32 + w]; }
+  for (int e = e0; e < e1; ++e) {
+    const uint32_t msk = s_mask[e];
+    s_off[e] = run;
+    if (globals) a.r.offsets[e] = run;
+    if (msk) {
+      s_touched[toff] = e;
+      s_z[toff] = a.rec_z ? __ldcg(a.rec_z + e) : e;
+      s_rec[toff] = reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(a.rec) + e));
+      if (globals) a.r.touched[toff] = e;
+      ++toff;
+    }
+    run += __popc(msk);
+  }
+  if (tid == nthr - 1) {
+    s_off[E] = run;
+    s_scan[64] = toff;
+    if (globals) {
+      a.r.offsets[E] = run;
+      a.r.n_touched[0] = toff;
+      if (a.r.touched_total) atomicAdd(a.r.touched_total, (unsigned long long)toff);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < kPairs; ++m) {
+    const int p = tid + m * nthr;
+    if (p < P) {
+      int e = pe[m];
+      if ((unsigned)e >= (unsigned)E) { set_status(a.r.status, kStatusRange); e = 0; }
+      const int t = p / k;
+      const int pos = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
+      s_tok[pos] = t;
+      s_w[pos] = pw[m];
+      if (globals) {
+        a.r.perm[pos] = p;
+        a.r.inv[p] = pos;
+      }
+    }
+  }
+  __syncthreads();
+  return s_scan[64];
 }
 
 // ---- k_dtc_down shared memory: stages (A tile, B tile, A and B scale
@@ -246,8 +340,12 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     } else {
       pdl_wait();  // routing and the activation codes
       pdl_launch_dependents();
-      nt = a.r.n_touched[0];
-      stage_meta(a, sm, M, nt);
+      if (a.meta_masks) {
+        nt = build_meta(a, sm, M, blockIdx.x == 0);
+      } else {
+        nt = __ldcg(a.r.n_touched);
+        stage_meta(a, sm, M, nt);
+      }
       if (warp == 0 && lane == 0) {
         mbar_arrive_expect_tx(xbar, L.nkt * npad * 128);
         for (int kt = 0; kt < L.nkt; ++kt)
@@ -578,9 +676,14 @@ __global__ void __launch_bounds__(kDgThreads, 2)
   // The routing metadata is read before this grid's dependency wait: the
   // routing kernels completed (and their writes were made visible) before
   // the gate_up kernel that launched this grid passed its own wait.
-  const int nt = __ldcg(a.r.n_touched);
-  stage_meta(a, sm, M, nt);
-  __syncthreads();
+  int nt;
+  if (a.meta_masks) {
+    nt = build_meta(a, sm, M, false);
+  } else {
+    nt = __ldcg(a.r.n_touched);
+    stage_meta(a, sm, M, nt);
+    __syncthreads();
+  }
   const int ti0 = shared ? 0 : (int)((int64_t)g * nt / G), ti1 = shared ? 1 : (int)((int64_t)(g + 1) * nt / G);
   const int n_items = ti1 - ti0;
 
@@ -901,6 +1004,9 @@ __global__ void __launch_bounds__(kDtThreads)
     }
     return;
   }
+  // the token masks of the top-k kernel start empty
+  if (a.r.emask)
+    for (int e = tid; e < E; e += kDtThreads) a.r.emask[e] = 0u;
   // sigma_t = sigmoid(g . x_t) and an upper bound of ||x_t||, one warp per token
   for (int t = warp; t < T; t += kDtThreads / 32) {
     const uint4* xr = reinterpret_cast<const uint4*>(a.r.x + (int64_t)t * H);
@@ -1073,6 +1179,9 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
   a.n_router_ctas = (E + 1) / 2;
   a.n_shared_ctas = 0;
   a.split_tail = 1;
+  // a whole forward: the expert kernels sort from the token masks; routing
+  // alone (offload): the top-k kernel sorts, for the host to read
+  a.meta_masks = parts == 3;
   if (parts & 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.stream = s;

@@ -309,6 +309,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
       {(void**)&h->r.xnorm, T * 4},
       {(void**)&h->r.perm, P * 4},           {(void**)&h->r.inv, P * 4},
       {(void**)&h->r.touched, (int64_t)c.E * 4}, {(void**)&h->r.n_touched, 16},
+      {(void**)&h->r.emask, (int64_t)c.E * 4},
       {(void**)&h->hs, T * (c.I_shared > 0 ? c.I_shared : 16) * 2},
       // intermediate rows padded to 16 bytes (the decode path copies them in bulk)
       {(void**)&h->hq_codes, P * align_up(c.I * 2, 16)}, {(void**)&h->hq_scales, P * align_up(c.I / 16 * 4, 16)},

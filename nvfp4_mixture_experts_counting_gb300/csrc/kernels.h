@@ -66,6 +66,7 @@ struct RouteArgs {
   int32_t* inv;      // [P]
   int32_t* touched;  // [E] touched experts, increasing
   int32_t* n_touched;  // [1]
+  uint32_t* emask;   // [E] decode: bit t set when token t picked expert e (zeroed by the router kernels)
   unsigned long long* n_rerank;  // [1] cumulative count of re-ranked tokens (may be null)
   unsigned long long* touched_total;  // [1] cumulative touched experts over forwards (may be null)
   uint32_t* status;
@@ -142,6 +143,7 @@ struct DecodeArgs {
   int n_groups;        // down kernel: expert groups per 128-row output tile (+1 for the shared expert)
   int split_tail;      // 1: top-k and the sort run in k_dec_topk instead of the last router CTA
   int skip_shared;     // 1: leave the shared expert out (a later expert batch of an offloaded forward)
+  int meta_masks;      // 1: the top-k kernel only sets emask; the expert kernels build the sorted tables
   float* spart;        // [I_shared / 64 * 4][32][128] shared gate_up partial sums per K quarter
   int* scnt;           // [I_shared / 64][2] arrival counters of the shared gate_up half tiles (zero between launches)
   // router logits on the tensor cores (split K): partial sums rpart[c][t][e]
@@ -192,6 +194,7 @@ struct PfArgs {
   uint8_t* hq_sf;             // [P_pad_max/128][I_loc/64][512]
   int hq_pitch;
   float* Y;                   // [P][H] fp32, rows in sorted order
+  int stage_y;                // down: Y goes out through shared memory (set by the launcher)
   uint32_t* status;
   // shared expert on the tensor cores, fused with the combine
   const uint16_t* x;          // [T][H] bf16

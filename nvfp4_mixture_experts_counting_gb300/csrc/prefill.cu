@@ -51,6 +51,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;   // scale-factor columns start after the two accumulators
 
 __host__ __device__ inline int pf_smem_bytes(int E) { return 1024 + kPfOffTab + 3 * 4 * (E + 1); }
+// Down mode: each epilogue warp turns its 32 rows x 32 columns of Y through
+// shared memory (rows 36 floats apart), so that every store instruction
+// writes four whole 128-byte row segments.  It sits after the tables.
+constexpr int kPfStgRow = 36;
+constexpr int kPfStgBytes = kPfEpiWarps * 32 * kPfStgRow * 4;
+__host__ __device__ inline int pf_stg_off(int E) { return (kPfOffTab + 3 * 4 * (E + 1) + 15) & ~15; }
+__host__ __device__ inline int pf_smem_bytes_staged(int E) { return 1024 + pf_stg_off(E) + kPfStgBytes; }
 
 // Exclusive scan over n values val(i) by one warp: out[i] = sum_{j<i} val(j),
 // out[n] = the total.
@@ -432,23 +439,61 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j) +
                   lane);
         __syncwarp();
-        const int64_t pos = s_off[e] + local;
-        float* yrow = a.Y + pos * H + 128 * j;
+        if (a.stage_y) {
+          // rows [row_w, row_w + 32) of the unit are this warp's lanes; the
+          // first nvalid of them exist (the rest pad the expert's last tile)
+          const int row_w = nt * 128 + 32 * q;
+          const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
+          float* stg = reinterpret_cast<float*>(sm + pf_stg_off(E)) + (warp - 2) * 32 * kPfStgRow;
+          float* Yw = a.Y + (s_off[e] + (int64_t)row_w) * H + 128 * j;
 #pragma unroll 1
-        for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
-          uint32_t v[16];
-          tc_ld16(taddr + 16 * c, v);
-          tc_wait16(v);
-          if (valid) {
+          for (int cc = 0; cc < 2; ++cc) {
+            const int cb = 64 * hf + 32 * cc;  // first of the chunk's 32 columns
+            uint32_t v0[16], v1[16];
+            tc_ld16(taddr + cb, v0);
+            tc_ld16(taddr + cb + 16, v1);
+            tc_wait16x2(v0, v1);
+            float* srow = stg + lane * kPfStgRow;
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
-              const float4 gd = *reinterpret_cast<const float4*>(wglob + 16 * c + i);
-              float4 o;
-              o.x = __uint_as_float(v[i]) * gd.x;
-              o.y = __uint_as_float(v[i + 1]) * gd.y;
-              o.z = __uint_as_float(v[i + 2]) * gd.z;
-              o.w = __uint_as_float(v[i + 3]) * gd.w;
-              *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
+              const float4 g0 = *reinterpret_cast<const float4*>(wglob + cb + i);
+              const float4 g1 = *reinterpret_cast<const float4*>(wglob + cb + 16 + i);
+              *reinterpret_cast<float4*>(srow + i) =
+                  make_float4(__uint_as_float(v0[i]) * g0.x, __uint_as_float(v0[i + 1]) * g0.y,
+                              __uint_as_float(v0[i + 2]) * g0.z, __uint_as_float(v0[i + 3]) * g0.w);
+              *reinterpret_cast<float4*>(srow + 16 + i) =
+                  make_float4(__uint_as_float(v1[i]) * g1.x, __uint_as_float(v1[i + 1]) * g1.y,
+                              __uint_as_float(v1[i + 2]) * g1.z, __uint_as_float(v1[i + 3]) * g1.w);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + (lane >> 3), c4 = 4 * (lane & 7);
+              if (r < nvalid)
+                *reinterpret_cast<float4*>(Yw + (int64_t)r * H + cb + c4) =
+                    *reinterpret_cast<const float4*>(stg + r * kPfStgRow + c4);
+            }
+            __syncwarp();
+          }
+        } else {
+          const int64_t pos = s_off[e] + local;
+          float* yrow = a.Y + pos * H + 128 * j;
+#pragma unroll 1
+          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+            uint32_t v[16];
+            tc_ld16(taddr + 16 * c, v);
+            tc_wait16(v);
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                const float4 gd = *reinterpret_cast<const float4*>(wglob + 16 * c + i);
+                float4 o;
+                o.x = __uint_as_float(v[i]) * gd.x;
+                o.y = __uint_as_float(v[i + 1]) * gd.y;
+                o.z = __uint_as_float(v[i + 2]) * gd.z;
+                o.w = __uint_as_float(v[i + 3]) * gd.w;
+                *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
+              }
             }
           }
         }
@@ -722,7 +767,8 @@ cudaError_t prefill_set_smem_limits() {
   const int bytes = pf_smem_bytes(kPfMaxE);
   if ((e = cudaFuncSetAttribute(k_pf_mma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) !=
+      cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_pf_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
@@ -752,8 +798,11 @@ cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms,
   k_pf_mma<0><<<num_sms, kPfThreads, smem, s>>>(a, m.xg, m.gu);
   FTMOE_PROF_END(s);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  // the down epilogue stages Y through shared memory where it fits
+  PfArgs ad = a;
+  ad.stage_y = pf_smem_bytes_staged(a.E) <= 227 * 1024;
   FTMOE_PROF_BEGIN("k_pf_down", s);
-  k_pf_mma<1><<<num_sms, kPfThreads, smem, s>>>(a, m.hq, m.dn);
+  k_pf_mma<1><<<num_sms, kPfThreads, ad.stage_y ? pf_smem_bytes_staged(a.E) : smem, s>>>(ad, m.hq, m.dn);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
