@@ -321,8 +321,9 @@ __global__ void k_combine(ExpertArgs a) {
     const int t = (int)(i / H), h = (int)(i % H);
     float acc = 0.f;
     for (int j = 0; j < k; ++j) {
-      const int pos = r.inv[(int64_t)t * k + j];
-      acc = fmaf(r.topk_w[(int64_t)t * k + j], a.Y[(int64_t)pos * H + h], acc);
+      const float y = a.y_tiles ? a.Y[(((int64_t)t * (H / 128) + h / 128) * k + j) * 128 + (h & 127)]
+                                : a.Y[(int64_t)r.inv[(int64_t)t * k + j] * H + h];
+      acc = fmaf(r.topk_w[(int64_t)t * k + j], y, acc);
     }
     if (a.sh_gate_up) acc = fmaf(r.sigma[t], a.S[i], acc);
     if ((a.out_flags & 0xff) == 0) {

@@ -739,8 +739,12 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     if (tc_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
     else CK(launch_experts(a, s, kPartSharedGateUp));
     CK(launch_prefill_routed(p, maps, h->num_sms, s));
-    if (tc_shared) CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
-    else CK(launch_experts(a, s, kPartTail));
+    if (tc_shared) {
+      CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
+    } else {
+      a.y_tiles = 1;  // the tensor-core down kernel's layout of Y
+      CK(launch_experts(a, s, kPartTail));
+    }
   } else {
     CK(launch_route(r, s));
     CK(launch_experts(a, s));
@@ -851,8 +855,12 @@ static int forward_offload(ftmoe_handle* h, int layer, const void* x, int T, voi
     return FTMOE_ERR_DEVICE_CHECK;
   }
   if (!dec) {
-    if (tc_shared) CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
-    else CK(launch_experts(a, s, kPartTail));
+    if (tc_shared) {
+      CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
+    } else {
+      a.y_tiles = 1;  // the tensor-core down kernel's layout of Y
+      CK(launch_experts(a, s, kPartTail));
+    }
   }
   int rc = copy_aux(h, r, T, aux, s);
   if (rc) return rc;

@@ -96,7 +96,8 @@ struct ExpertArgs {
   uint16_t* hs;        // [T][s_I_loc] bf16 shared intermediate
   uint8_t* hq_codes;   // [P][I_loc/2]
   uint8_t* hq_scales;  // [P][I_loc/16]
-  float* Y;            // [P][H] fp32, rows in sorted order
+  float* Y;            // [P][H] fp32, rows in sorted order (y_tiles: [T][H/128][k][128], pair (t, slot))
+  int y_tiles;         // 1: Y was written by the tensor-core prefill down kernel, in its layout
   float* S;            // [T][H] fp32
   void* out;
   int out_flags;
@@ -193,7 +194,7 @@ struct PfArgs {
   uint8_t* hq;                // [P_pad_max][hq_pitch] intermediate codes (I_loc/2 used)
   uint8_t* hq_sf;             // [P_pad_max/128][I_loc/64][512]
   int hq_pitch;
-  float* Y;                   // [P][H] fp32, rows in sorted order
+  float* Y;                   // [T][H/128][k][128] fp32: pair (t, slot)'s output, per column tile
   int stage_y;                // down: Y goes out through shared memory (set by the launcher)
   uint32_t* status;
   // shared expert on the tensor cores, fused with the combine

@@ -445,7 +445,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int row_w = nt * 128 + 32 * q;
           const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
           float* stg = reinterpret_cast<float*>(sm + pf_stg_off(E)) + (warp - 2) * 32 * kPfStgRow;
-          float* Yw = a.Y + (s_off[e] + (int64_t)row_w) * H + 128 * j;
+          // Y is [token][H / 128 column tiles][slot][128]: the lane's row is
+          // pair p = t * k + slot, its tile-j segment at (t * H/128 + j) * k + slot
+          int yseg = 0;
+          if (lane < nvalid) {
+            const int pr = __ldg(a.perm + s_off[e] + row_w + lane);
+            yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
+          }
 #pragma unroll 1
           for (int cc = 0; cc < 2; ++cc) {
             const int cb = 64 * hf + 32 * cc;  // first of the chunk's 32 columns
@@ -469,15 +475,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int r = 4 * i + (lane >> 3), c4 = 4 * (lane & 7);
+              const int seg = __shfl_sync(0xffffffffu, yseg, r);
               if (r < nvalid)
-                *reinterpret_cast<float4*>(Yw + (int64_t)r * H + cb + c4) =
+                *reinterpret_cast<float4*>(a.Y + (int64_t)seg * 128 + cb + c4) =
                     *reinterpret_cast<const float4*>(stg + r * kPfStgRow + c4);
             }
             __syncwarp();
           }
         } else {
-          const int64_t pos = s_off[e] + local;
-          float* yrow = a.Y + pos * H + 128 * j;
+          int yseg = 0;
+          if (valid) {
+            const int pr = __ldg(a.perm + s_off[e] + local);
+            yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
+          }
+          float* yrow = a.Y + (int64_t)yseg * 128;
 #pragma unroll 1
           for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
             uint32_t v[16];
@@ -559,17 +570,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // have their Y loads in flight four slots at a time.
         const int t = local;
         const int k = a.top_k;
-        const int32_t* pos = a.inv + (int64_t)t * k;
         const float* w = a.topk_w + (int64_t)t * k;
         const float sig = valid ? a.sigma[t] : 0.f;
         const int64_t obase = (int64_t)t * H + 128 * j;
-        int pj[8];
+        // the token's k slot segments of column tile j, contiguous
+        const float* yt = a.Y + ((int64_t)t * (H / 128) + j) * k * 128;
         float wj[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          pj[jj] = (valid && jj < k) ? __ldg(pos + jj) : 0;
-          wj[jj] = (valid && jj < k) ? __ldg(w + jj) : 0.f;
-        }
+        for (int jj = 0; jj < 8; ++jj) wj[jj] = (valid && jj < k) ? __ldg(w + jj) : 0.f;
 #pragma unroll 1
         for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
           uint32_t v[16];
@@ -586,7 +594,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                   float4 y[4][4];
 #pragma unroll
                   for (int q2 = 0; q2 < 4; ++q2) {
-                    const float4* yp = reinterpret_cast<const float4*>(a.Y + (int64_t)pj[j0 + q2] * H + 128 * j + 16 * c);
+                    const float4* yp = reinterpret_cast<const float4*>(yt + (j0 + q2) * 128 + 16 * c);
 #pragma unroll
                     for (int i4 = 0; i4 < 4; ++i4)
                       y[q2][i4] = (j0 + q2 < k) ? __ldg(yp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -608,7 +616,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             } else {
               for (int jj = 0; jj < k; ++jj) {
                 const float wv = __ldg(w + jj);
-                const float4* yp = reinterpret_cast<const float4*>(a.Y + (int64_t)__ldg(pos + jj) * H + 128 * j + 16 * c);
+                const float4* yp = reinterpret_cast<const float4*>(yt + jj * 128 + 16 * c);
 #pragma unroll
                 for (int i4 = 0; i4 < 4; ++i4) {
                   const float4 y = yp[i4];

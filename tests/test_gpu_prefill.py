@@ -13,6 +13,7 @@ import pytest
 import torch
 
 from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
+from oracle import moe
 
 from gpu_helpers import AuxBufs, GpuBank, check_output, check_routing, make_layer, rel_l2
 
@@ -185,3 +186,28 @@ def test_prefill_router_logit_error_within_bound(prefill):
         idx, _ = moe.select_topk(exact, wl.top_k)
         assert np.array_equal(aux.topk_idx.cpu().numpy(), idx)
     assert worst <= 2.0 ** -15 / 16, f"largest relative logit error {worst:.3e}"
+
+
+@pytest.mark.parametrize("T", [8, 100, 300])
+def test_mid_without_shared_expert_matches_oracle(mid, T):
+    """No shared expert (I_shared = 0): the routed sum alone, through the
+    decode kernels (T <= 32) and through the tensor-core prefill GEMMs whose
+    combine then runs on its own.  The oracle's shared expert with all-zero
+    weights contributes exactly zero."""
+    wl, bank, _ = mid
+    cfg = ftmoe.make_config(H=wl.H, I=wl.I, E=wl.E, top_k=wl.top_k, I_shared=0, max_tokens=512,
+                            norm_topk_prob=wl.norm_topk_prob, has_router_bias=wl.router_bias)
+    layer = ftmoe.Layer(cfg)
+    layer.load_bank(0, ftmoe.bank_desc(bank.router_w, bank.router_bias, bank.gu_codes, bank.gu_scales,
+                                       bank.gu_global, bank.dn_codes, bank.dn_scales, bank.dn_global,
+                                       None, None, None, on_device=True))
+    x = W.hidden(wl, T, step=900, device=DEV)
+    out, aux = _run(wl, layer, x)
+    z = np.zeros
+    ref = moe.moe_layer(x.float().cpu().numpy(), bank.router_w.cpu().numpy(),
+                        None if bank.router_bias is None else bank.router_bias.cpu().numpy(),
+                        bank.oracle_expert, z((2 * wl.I, wl.H)), z((wl.H, wl.I)), z(wl.H),
+                        I=wl.I, I_s=wl.I, top_k=wl.top_k, norm_topk_prob=wl.norm_topk_prob)
+    check_routing(aux, ref)
+    check_output(out, ref.out)
+    layer.close()
