@@ -141,20 +141,34 @@ __device__ __forceinline__ df32 logit_df32(const uint16_t* x, const float* w, in
   float s = 0.f, c = 0.f;
   const uint2* x4 = reinterpret_cast<const uint2*>(x);
   const float4* w4 = reinterpret_cast<const float4*>(w);
-#pragma unroll 4
-  for (int i = lane; i < H / 4; i += 32) {
-    const uint2 xv = __ldg(x4 + i);
-    const float4 wv = __ldg(w4 + i);
-    const float xs[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xffff0000u),
-                         __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xffff0000u)};
-    const float ws[4] = {wv.x, wv.y, wv.z, wv.w};
+  const int n4 = H / 4;
+  // eight chunks' loads in flight before their (in-order) accumulation
+  for (int i0 = lane; i0 < n4; i0 += 32 * 8) {
+    uint2 xv[8];
+    float4 wv[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float p = __fmul_rn(xs[k], ws[k]);
-      const float pe = __fmaf_rn(xs[k], ws[k], -p);
-      const df32 t = df_two_sum(s, p);
-      s = t.hi;
-      c = __fadd_rn(c, __fadd_rn(t.lo, pe));
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 32 * u;
+      if (i < n4) {
+        xv[u] = __ldg(x4 + i);
+        wv[u] = __ldg(w4 + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (i0 + 32 * u < n4) {
+        const float xs[4] = {__uint_as_float(xv[u].x << 16), __uint_as_float(xv[u].x & 0xffff0000u),
+                             __uint_as_float(xv[u].y << 16), __uint_as_float(xv[u].y & 0xffff0000u)};
+        const float ws[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p = __fmul_rn(xs[k], ws[k]);
+          const float pe = __fmaf_rn(xs[k], ws[k], -p);
+          const df32 t = df_two_sum(s, p);
+          s = t.hi;
+          c = __fadd_rn(c, __fadd_rn(t.lo, pe));
+        }
+      }
     }
   }
   df32 v = df_two_sum(s, c);

@@ -169,19 +169,44 @@ __global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
     for (int e = threadIdx.x; e <= E; e += blockDim.x) a.pad_off[e] = s_pad[e];
   const int total = s_pad[E], hc = H / 2, nks = H / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  // codes: one warp per padded row (rows past an expert's pairs stay as
+  // they are: their MMA rows are never read)
   for (int pp = blockIdx.x * nw + warp; pp < total; pp += gridDim.x * nw) {
     const int e = find_le(s_pad, E, pp);
     const int local = pp - s_pad[e], m = s_off[e + 1] - s_off[e];
-    uint8_t* sfrow = a.xg_sf + (int64_t)(pp >> 7) * nks * 512 + sf_slot(pp);
     if (local < m) {
       const int t = a.perm[s_off[e] + local] / a.top_k;
       const uint4* src = reinterpret_cast<const uint4*>(a.xq_codes + (int64_t)t * hc);
       uint4* dst = reinterpret_cast<uint4*>(a.xg + (int64_t)pp * hc);
       for (int i = lane; i < hc / 16; i += 32) dst[i] = src[i];
-      const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.xq_scales + (int64_t)t * (H / 16));
-      for (int ks = lane; ks < nks; ks += 32) *reinterpret_cast<uint32_t*>(sfrow + (int64_t)ks * 512) = ssrc[ks];
-    } else {
-      for (int ks = lane; ks < nks; ks += 32) *reinterpret_cast<uint32_t*>(sfrow + (int64_t)ks * 512) = 0u;
+    }
+  }
+  // scales: a 128-row tile per 128 threads, a thread per row: its token's
+  // scales (16-byte loads in flight together), one 4-byte word into each
+  // K step's 512-byte block, so every block is written whole; padding rows
+  // get zero scales
+  const int ntile = total >> 7;
+  for (int tile = blockIdx.x * 2 + (threadIdx.x >> 7); tile < ntile; tile += gridDim.x * 2) {
+    const int pp = tile * 128 + (threadIdx.x & 127);
+    const int e = find_le(s_pad, E, pp);
+    const int local = pp - s_pad[e], m = s_off[e + 1] - s_off[e];
+    const uint4* src = nullptr;
+    if (local < m) src = reinterpret_cast<const uint4*>(a.xq_scales + (int64_t)(a.perm[s_off[e] + local] / a.top_k) * (H / 16));
+    uint8_t* dst = a.xg_sf + (int64_t)tile * nks * 512 + sf_slot(pp);
+    for (int c0 = 0; c0 < nks / 4; c0 += 8) {  // nks / 4 16-byte groups of 4 K steps
+      uint4 v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) v[c] = (src && c0 + c < nks / 4) ? __ldg(src + c0 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        if (c0 + c < nks / 4) {
+          uint8_t* d = dst + (int64_t)4 * (c0 + c) * 512;
+          *reinterpret_cast<uint32_t*>(d) = v[c].x;
+          *reinterpret_cast<uint32_t*>(d + 512) = v[c].y;
+          *reinterpret_cast<uint32_t*>(d + 1024) = v[c].z;
+          *reinterpret_cast<uint32_t*>(d + 1536) = v[c].w;
+        }
+      }
     }
   }
 }

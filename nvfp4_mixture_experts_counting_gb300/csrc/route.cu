@@ -204,17 +204,20 @@ __device__ __forceinline__ bool before(float la, int ea, float lb, int eb) {
 // its order with the error bounds; if not certified, recompute compensated
 // double-fp32 logits (about 2^-48 relative; FP64 is far slower on this GPU)
 // for every expert that could belong to the top-k and select among those.
+// The recomputations of all the CTA's uncertain tokens are spread over its
+// warps.
 __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
+  __shared__ int s_nc[kTopkWarps];
   const int E = a.E, k = a.top_k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* lw = reinterpret_cast<float*>(sm) + warp * E;                // working logits
   int* cand = reinterpret_cast<int*>(sm) + kTopkWarps * E + warp * E;  // candidate list
   df32* l64 = reinterpret_cast<df32*>(sm + (size_t)kTopkWarps * E * 8) + warp * E;
   const int t = blockIdx.x * kTopkWarps + warp;
-  if (t >= a.T) return;
-  const float* lg = a.logits + (int64_t)t * E;
-  const float* er = a.err + (int64_t)t * E;
+  const bool have = t < a.T;
+  const float* lg = a.logits + (int64_t)(have ? t : 0) * E;
+  const float* er = a.err + (int64_t)(have ? t : 0) * E;
   for (int e = lane; e < E; e += 32) lw[e] = lg[e];
   __syncwarp();
 
@@ -253,10 +256,11 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
   if (__any_sync(0xffffffffu, reach)) certified = false;
 
   float w64[32];
+  if (!have) certified = true;
+  // candidates: the chosen plus every unchosen expert that may outrank one
+  int nc = 0;
   if (!certified) {
     if (lane == 0 && a.n_rerank) atomicAdd(a.n_rerank, 1ull);  // telemetry only
-    // candidates: the chosen plus every unchosen expert that may outrank one
-    int nc = 0;
     for (int base = 0; base < E; base += 32) {
       int e = base + lane;
       bool c = false;
@@ -265,15 +269,26 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
       if (c) cand[nc + __popc(m & ((1u << lane) - 1))] = e;
       nc += __popc(m);
     }
-    __syncwarp();
-    const uint16_t* xrow = a.x + (int64_t)t * a.H;
-    for (int c = 0; c < nc; ++c) {
-      const int e = cand[c];
-      const df32 v = logit_df32(xrow, a.router_w + (int64_t)e * a.H, a.H,
+  }
+  if (lane == 0) s_nc[warp] = nc;
+  __syncthreads();
+  {
+    // every warp computes compensated logits of the CTA's candidates in turn
+    int total = 0;
+    for (int w = 0; w < kTopkWarps; ++w) total += s_nc[w];
+    for (int item = warp; item < total; item += kTopkWarps) {
+      int w = 0, c = item;
+      while (c >= s_nc[w]) { c -= s_nc[w]; ++w; }
+      const int tw = blockIdx.x * kTopkWarps + w;
+      const int e = reinterpret_cast<const int*>(sm)[kTopkWarps * E + w * E + c];
+      const df32 v = logit_df32(a.x + (int64_t)tw * a.H, a.router_w + (int64_t)e * a.H, a.H,
                                 a.router_bias ? a.router_bias[e] : 0.f, lane);
-      if (lane == 0) l64[c] = v;
+      if (lane == 0) reinterpret_cast<df32*>(sm + (size_t)kTopkWarps * E * 8)[w * E + c] = v;
     }
-    __syncwarp();
+  }
+  __syncthreads();
+  if (!have) return;
+  if (!certified) {
     // select k among the candidates by (compensated logit desc, index asc)
     const df32 none = {-INFINITY, 0.f};
     for (int j = 0; j < k; ++j) {
@@ -376,10 +391,22 @@ __global__ void __launch_bounds__(kSortThreads) k_sort(RouteArgs a) {
   __syncthreads();
   const int CH = (P + kSortWarps - 1) / kSortWarps;
   const int c0 = min(P, warp * CH), c1 = min(P, c0 + CH);
-  for (int p = c0 + lane; p < c1; p += 32) {
-    int e = a.topk_idx[p];
-    if ((unsigned)e >= (unsigned)E) { set_status(a.status, kStatusRange); e = 0; }
-    atomicAdd(&hist[warp * E + e], 1);
+  // eight of the lane's loads in flight at a time
+  for (int p0 = c0; p0 < c1; p0 += 32 * 8) {
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = p0 + 32 * u + lane;
+      ev[u] = p < c1 ? __ldg(a.topk_idx + p) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (p0 + 32 * u + lane < c1) {
+        int e = ev[u];
+        if ((unsigned)e >= (unsigned)E) { set_status(a.status, kStatusRange); e = 0; }
+        atomicAdd(&hist[warp * E + e], 1);
+      }
+    }
   }
   __syncthreads();
   for (int base = 0; base < E; base += kSortThreads) {
@@ -417,22 +444,33 @@ __global__ void __launch_bounds__(kSortThreads) k_sort(RouteArgs a) {
     if (a.touched_total) atomicAdd(a.touched_total, (unsigned long long)a.n_touched[0]);
   }
   __syncthreads();
-  for (int p0 = c0; p0 < c1; p0 += 32) {
-    const int p = p0 + lane;
-    const bool valid = p < c1;
-    int e = valid ? a.topk_idx[p] : -1 - lane;
-    if (valid && (unsigned)e >= (unsigned)E) e = 0;
-    const unsigned mask = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(mask & ((1u << lane) - 1));
-    int pos = 0;
-    if (valid) pos = hist[warp * E + e] + rank;
-    __syncwarp();
-    if (valid) {
-      a.perm[pos] = p;
-      a.inv[p] = pos;
-      if (rank == 0) hist[warp * E + e] += __popc(mask);
+  for (int p8 = c0; p8 < c1; p8 += 32 * 8) {
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = p8 + 32 * u + lane;
+      ev[u] = p < c1 ? __ldg(a.topk_idx + p) : -1;
     }
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p0 = p8 + 32 * u;
+      if (p0 >= c1) break;  // uniform across the warp
+      const int p = p0 + lane;
+      const bool valid = p < c1;
+      int e = valid ? ev[u] : -1 - lane;
+      if (valid && (unsigned)e >= (unsigned)E) e = 0;
+      const unsigned mask = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(mask & ((1u << lane) - 1));
+      int pos = 0;
+      if (valid) pos = hist[warp * E + e] + rank;
+      __syncwarp();
+      if (valid) {
+        a.perm[pos] = p;
+        a.inv[p] = pos;
+        if (rank == 0) hist[warp * E + e] += __popc(mask);
+      }
+      __syncwarp();
+    }
   }
 }
 
