@@ -456,21 +456,45 @@ def run_gpu(args):
     shares = {k: {"launches": v[0], "ms": round(v[1], 3), "share": round(v[1] / total_k, 4)}
               for k, v in ktimes.items()}
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: every step copies
+    # its tokens in from pinned host memory and its output back, on a copy
+    # stream with two buffers each way, so step i+1's input lands while step
+    # i computes and step i's output leaves while step i+1 computes
     xh = [x.cpu().pin_memory() for x in xs]
-    oh = torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(xs[0])
-    for i in range(Wm):
-        xd.copy_(xh[i % NX], non_blocking=True)
-        step(i, out, xd)
-        oh.copy_(out, non_blocking=True)
+    oh = [torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(xs[0]) for _ in range(2)]
+    od = [torch.empty_like(out) for _ in range(2)]
+    cs = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+
+    def copy_in(i):
+        b = i % 2
+        with torch.cuda.stream(cs):
+            if i >= 2:
+                cs.wait_event(done[b])  # step i-2 has finished with xd[b]
+            xd[b].copy_(xh[i % NX], non_blocking=True)
+            ready[b].record(cs)
+
+    def run_e2e(n):
+        copy_in(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                copy_in(i + 1)
+            stream.wait_event(ready[b])
+            step(i, od[b], xd[b])
+            done[b].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[b])
+                oh[b].copy_(od[b], non_blocking=True)
+        stream.wait_stream(cs)
+
+    run_e2e(Wm)
     _barrier_and_sync(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(K):
-        xd.copy_(xh[i % NX], non_blocking=True)
-        step(i, out, xd)
-        oh.copy_(out, non_blocking=True)
+    run_e2e(K)
     e1.record(stream)
     _barrier_and_sync(ws)
     e2e_ms = _max_over_ranks(ws, e0.elapsed_time(e1))

@@ -9,6 +9,7 @@
 // sigmoid(gate) * shared before one reduce) and "Correctness" (no value
 // atomics: every sum here runs in a fixed order).
 #include "common.cuh"
+#include "tma.cuh"
 #include "kernels.h"
 
 namespace ftmoe {
@@ -340,6 +341,10 @@ __global__ void k_combine(ExpertArgs a) {
 // ------------------------------------------------------------------ RMS renorm
 
 __global__ void k_rms_renorm(const float* __restrict__ y, uint16_t* __restrict__ x, int H) {
+  // launched programmatically: the next layer's router may start streaming
+  // its tiles now, and this grid waits for the one that wrote y
+  pdl_launch_dependents();
+  pdl_wait();
   const int t = blockIdx.x;
   const float* yr = y + (int64_t)t * H;
   __shared__ float red[32];
@@ -451,9 +456,19 @@ cudaError_t launch_store_out(const float* y, void* out, int out_flags, int64_t n
 
 cudaError_t launch_rms_renorm(const float* y, uint16_t* x, int T, int H, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   FTMOE_PROF_BEGIN("k_rms_renorm", s);
-  k_rms_renorm<<<T, 256, 0, s>>>(y, x, H);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_rms_renorm, y, x, H);
   FTMOE_PROF_END(s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -802,10 +802,23 @@ static int forward_offload(ftmoe_handle* h, int layer, const void* x, int T, voi
   const int S = h->cache.slots();
   const int nb = (nt + S - 1) / S;
   if (nb > h->max_batches) return FTMOE_ERR_INVALID_ARG;
+  // experts already resident go first (in expert order), then the rest: when
+  // the touched experts need several batches, the resident ones are all hits
+  // of the first batch instead of being evicted by earlier misses
+  std::vector<int> order;
+  order.reserve(nt);
+  for (int i = 0; i < nt; ++i)
+    if (h->cache.slot_of(layer, h->h_touched[i]) >= 0) order.push_back(h->h_touched[i]);
+  for (int i = 0; i < nt; ++i)
+    if (h->cache.slot_of(layer, h->h_touched[i]) < 0) order.push_back(h->h_touched[i]);
+  // within a batch the kernels take the experts in expert order, as a
+  // resident forward does (the same sums in the same order)
+  for (int b = 0; b < nb; ++b)
+    std::sort(order.begin() + (int64_t)b * S, order.begin() + std::min<int64_t>((int64_t)(b + 1) * S, nt));
   if (!dec && tc_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
   if (!dec && !tc_shared) CK(launch_experts(a, s, kPartSharedGateUp));
   for (int b = 0; b < nb; ++b) {
-    const int* batch = h->h_touched + (int64_t)b * S;
+    const int* batch = order.data() + (int64_t)b * S;
     const int n = std::min(S, nt - b * S);
     const std::vector<SlotCache::Placement> pl = h->cache.place(layer, batch, n);
     // kernels already queued may still read the slots about to be filled

@@ -4,10 +4,10 @@
 // PR #385 "feat(qwen4_exp): tensor parallelism for Qwen3.8-Flash-Next
 // (offload backend)", "What this adds": a fraction of the NVFP4 experts stays
 // resident in GPU memory and the rest are streamed from host memory every
-// step.  Here a forward's touched experts are placed in slots in batches of
-// at most the slot count; within a batch, hits are refreshed first, then
-// every miss takes an empty slot or else the least recently used slot that
-// the batch does not use.
+// step.  Here a forward's touched experts -- those already resident first --
+// are placed in slots in batches of at most the slot count; within a batch,
+// hits are refreshed first, then every miss takes an empty slot or else the
+// least recently used slot that the batch does not use.
 #pragma once
 
 #include <stdint.h>

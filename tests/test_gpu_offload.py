@@ -27,14 +27,17 @@ def _built():
 
 
 def simulate_lru(n_slots, steps):
-    """Hits and misses of the replacement rule, per forward batch: refresh the
-    hits, then give each miss the lowest empty slot, else the least recently
-    used slot the batch does not use."""
+    """Hits and misses of the replacement rule: a forward's touched experts,
+    those already resident first (each group in expert order), go in
+    batches of n_slots; per batch, refresh the hits, then give each miss the
+    lowest empty slot, else the least recently used slot the batch does not
+    use."""
     slot_of, owner, stamp = {}, [None] * n_slots, [0] * n_slots
     clock = hits = misses = 0
     for touched in steps:
+        touched = [e for e in touched if e in slot_of] + [e for e in touched if e not in slot_of]
         for b0 in range(0, len(touched), n_slots):
-            batch = touched[b0:b0 + n_slots]
+            batch = sorted(touched[b0:b0 + n_slots])  # the kernels' order within a batch
             start = clock + 1
             for e in batch:
                 if e in slot_of:
