@@ -154,10 +154,22 @@ __device__ int build_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M,
     pw[m] = p < P ? __ldcg(a.r.topk_w + p) : 0.f;
   }
   for (int e = tid; e < E; e += nthr) s_mask[e] = __ldcg(a.r.emask + e);
-  __syncthreads();
-  // each thread owns experts [e0, e1): pair and touched counts, block scan
+  // each thread owns experts [e0, e1) (at most 5: E <= 1024 over >= 224
+  // threads); their records' pointers and indices load with the masks
   const int per = (E + nthr - 1) / nthr;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  constexpr int kPer = 5;
+  const uint8_t* rp[kPer];
+  int rz[kPer];
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) {
+    const int e = e0 + m;
+    rp[m] = e < e1 ? reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(a.rec) + e))
+                   : nullptr;
+    rz[m] = e < e1 ? (a.rec_z ? __ldcg(a.rec_z + e) : e) : 0;
+  }
+  __syncthreads();
+  // pair and touched counts, block scan
   int cnt = 0, tcnt = 0;
   for (int e = e0; e < e1; ++e) {
     const uint32_t msk = s_mask[e];
@@ -174,14 +186,17 @@ __device__ int build_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M,
   __syncthreads();
   int run = inc - cnt, toff = tinc - tcnt;
   for (int w = 0; w < warp; ++w) { run += s_scan[w]; toff += s_scan[32 + w]; }
-  for (int e = e0; e < e1; ++e) {
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) {
+    const int e = e0 + m;
+    if (e >= e1) break;
     const uint32_t msk = s_mask[e];
     s_off[e] = run;
     if (globals) a.r.offsets[e] = run;
     if (msk) {
       s_touched[toff] = e;
-      s_z[toff] = a.rec_z ? __ldcg(a.rec_z + e) : e;
-      s_rec[toff] = reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(a.rec) + e));
+      s_z[toff] = rz[m];
+      s_rec[toff] = rp[m];
       if (globals) a.r.touched[toff] = e;
       ++toff;
     }
