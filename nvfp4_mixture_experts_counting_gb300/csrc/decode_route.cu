@@ -817,9 +817,11 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_route(DecodeArgs a) {
     }
     return;
   }
-  // ---- the token masks of the top-k kernel start empty
+  // ---- the token masks of the top-k kernel start empty, and so does the
+  // gate_up kernel's unit counter
   if (a.r.emask)
     for (int e = tid; e < E; e += kRtThreads) a.r.emask[e] = 0u;
+  if (a.meta_masks && tid == 0) *a.counter = 0;
   // ---- sigma_t = sigmoid(g . x_t), one warp per token
   for (int t = warp; t < T; t += 8) {
     float z = 0.f;

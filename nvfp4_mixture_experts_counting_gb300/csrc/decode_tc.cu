@@ -302,7 +302,9 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   uint64_t* u_free = u_full + 2;  // [2] up values consumed (the two gate warps arrive)
   uint64_t* sf_ready = u_free + 2;  // [8] stage landed and its weight scales are in TMEM
   uint64_t* sf_drain = sf_ready + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  uint64_t* uq_full = sf_drain + 1;  // [8] phase-1 unit queue: entry written
+  volatile int* uq = reinterpret_cast<volatile int*>(uq_full + 8);  // [8] routed unit, -1 = none left
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uq_full + 12);  // after the 8 queue entries
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* U0 = reinterpret_cast<float*>(sm + L.u_off);  // [2][32 pairs][64]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -318,6 +320,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     for (int b = 0; b < 2; ++b) { mbar_init(&u_full[b], 2); mbar_init(&u_free[b], 2); }
     for (int s = 0; s < NST; ++s) mbar_init(&sf_ready[s], 1);
     mbar_init(sf_drain, 1);
+    for (int q = 0; q < 8; ++q) mbar_init(&uq_full[q], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -342,7 +345,31 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   // after the routing is known, a contiguous range of the routed units
   // (touched expert, 64-row window tile) that balances the CTAs' whole
   // loads.  Ring positions carry over.
-  int kk = 0, ui = 0, uu = 0, nt = 0, r0 = 0;
+  int kk = 0, ui = 0, uu = 0, nt = 0, r0 = 0, R = 0;
+  int qn = 0;  // phase-1 unit queue entries this thread has produced or consumed
+  // With more than 16 tokens a whole forward takes its phase-1 units from a
+  // global counter (CTAs that start late or ran a shared unit simply take
+  // fewer); the producer draws them and passes them to the other roles
+  // through a queue of 8 entries (at most about 3 units are in flight in a
+  // CTA: the ring holds less than a unit and the accumulators two).  With
+  // fewer tokens, and for offload batches, the static balanced split: its
+  // CTAs end staggered, so the down kernel's CTAs take the freed SMs and
+  // set up early, which measured faster there (T=1: 26.2k vs 24.8k tokens/s,
+  // T=16: 174k vs 171k; T=32: 245k vs 251k the other way).
+  const bool dyn_units = a.meta_masks != 0 && T > 16;
+  // the next unit of this role: the static range, or the queue
+  auto next_unit = [&](int it, int phase, int* rr) -> bool {
+    if (phase == 0 || !dyn_units) {
+      if (it >= 0x7fffffff) return false;
+      *rr = r0 + it;
+      return true;
+    }
+    const int q = qn & 7;
+    if (!mbar_wait(&uq_full[q], (qn >> 3) & 1, a.r.status)) { *abort_flag = 1; return false; }
+    ++qn;
+    *rr = uq[q];
+    return *rr >= 0;
+  };
   int rs = 0;         // ring stage of kk (kk mod NST) and its phase parity, kept
   uint32_t rph = 0;   // incrementally: NST is a run-time value and divisions cost
   const int q = warp & 3;
@@ -395,16 +422,25 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         __syncwarp();
       }
       __syncthreads();
-      const int R = nt * J;
+      R = nt * J;
       r0 = dtc_split(blockIdx.x, gridDim.x, R, L.nkt, Us, nkt_q);
-      n_my = dtc_split(blockIdx.x + 1, gridDim.x, R, L.nkt, Us, nkt_q) - r0;
+      n_my = dyn_units ? 0x7fffffff : dtc_split(blockIdx.x + 1, gridDim.x, R, L.nkt, Us, nkt_q) - r0;
     }
     if (warp == 0) {
       // ---------------- TMA producer
       if (lane == 0) {
         for (int it = 0; it < n_my && !*abort_flag; ++it) {
           const bool shared = phase == 0;
-          const int rr = r0 + it;
+          int rr = r0 + it;
+          if (!shared && dyn_units) {
+            // draw the next unit and publish it to the other roles
+            rr = atomicAdd(a.counter, 1);
+            if (rr >= R) rr = -1;
+            uq[qn & 7] = rr;
+            mbar_arrive(&uq_full[qn & 7]);
+            ++qn;
+            if (rr < 0) break;
+          }
           const int us = (int)blockIdx.x + it * (int)gridDim.x;  // shared unit
           const int j = shared ? us / kShKq : rr % J;
           const int kt0 = shared ? (us % kShKq) * nkt_q : 0;     // first K tile of the unit
@@ -439,6 +475,8 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         if (!ok) *abort_flag = 1;
         for (int it = 0; ok && it < n_my && !*abort_flag; ++it, ++ui) {
           const bool shared = phase == 0;
+          int rr_unused;
+          if (!shared && !next_unit(it, phase, &rr_unused)) break;
           const int nkt_u = shared ? nkt_q : L.nkt;
           const int buf = ui & 1;
           if (ui >= 2 && !mbar_wait(&acc_empty[buf], ((ui >> 1) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
@@ -476,6 +514,8 @@ __global__ void __launch_bounds__(kDgThreads, 1)
       if (lane == 0) {
         for (int it = 0; it < n_my && !*abort_flag; ++it) {
           const bool shared = phase == 0;
+          int rr_unused;
+          if (!shared && !next_unit(it, phase, &rr_unused)) break;
           const int nkt_u = shared ? nkt_q : L.nkt;
           for (int kt = 0; kt < nkt_u; ++kt, ++kk) {
             const int s = rs;
@@ -508,7 +548,8 @@ __global__ void __launch_bounds__(kDgThreads, 1)
       for (int it = 0; it < n_my && !*abort_flag; ++it, ++ui) {
         const int buf = ui & 1;
         const bool sh = phase == 0;
-        const int rr = r0 + it;
+        int rr = r0 + it;
+        if (!sh && !next_unit(it, phase, &rr)) break;
         const int us = (int)blockIdx.x + it * (int)gridDim.x;
         const int ti = sh ? 0 : rr / J, j = sh ? us / kShKq : rr % J;
         const int e = sh ? 0 : s_touched[ti];
@@ -1019,9 +1060,11 @@ __global__ void __launch_bounds__(kDtThreads)
     }
     return;
   }
-  // the token masks of the top-k kernel start empty
+  // the token masks of the top-k kernel start empty, and so does the
+  // gate_up kernel's unit counter
   if (a.r.emask)
     for (int e = tid; e < E; e += kDtThreads) a.r.emask[e] = 0u;
+  if (a.meta_masks && tid == 0) *a.counter = 0;
   // sigma_t = sigmoid(g . x_t) and an upper bound of ||x_t||, one warp per token
   for (int t = warp; t < T; t += kDtThreads / 32) {
     const uint4* xr = reinterpret_cast<const uint4*>(a.r.x + (int64_t)t * H);
