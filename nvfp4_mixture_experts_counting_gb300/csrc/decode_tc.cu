@@ -347,16 +347,15 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   // loads.  Ring positions carry over.
   int kk = 0, ui = 0, uu = 0, nt = 0, r0 = 0, R = 0;
   int qn = 0;  // phase-1 unit queue entries this thread has produced or consumed
-  // With more than 16 tokens a whole forward takes its phase-1 units from a
-  // global counter (CTAs that start late or ran a shared unit simply take
-  // fewer); the producer draws them and passes them to the other roles
-  // through a queue of 8 entries (at most about 3 units are in flight in a
-  // CTA: the ring holds less than a unit and the accumulators two).  With
-  // fewer tokens, and for offload batches, the static balanced split: its
-  // CTAs end staggered, so the down kernel's CTAs take the freed SMs and
-  // set up early, which measured faster there (T=1: 26.2k vs 24.8k tokens/s,
-  // T=16: 174k vs 171k; T=32: 245k vs 251k the other way).
-  const bool dyn_units = a.meta_masks != 0 && T > 16;
+  // When a whole forward has more routed units than CTAs it hands them out
+  // dynamically: each CTA's first unit is fixed (CTAs without a shared unit
+  // first), the rest come from a global counter, so CTAs that start late or
+  // ran a shared unit simply take fewer.  The producer draws them and passes
+  // them to the other roles through a queue of 8 entries (at most about 3
+  // units are in flight in a CTA: the ring holds less than a unit and the
+  // accumulators two).  With fewer units than CTAs (one token), and for
+  // offload batches, the static balanced split.
+  bool dyn_units = false;
   // the next unit of this role: the static range, or the queue
   auto next_unit = [&](int it, int phase, int* rr) -> bool {
     if (phase == 0 || !dyn_units) {
@@ -423,6 +422,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
       }
       __syncthreads();
       R = nt * J;
+      dyn_units = a.meta_masks != 0 && R > (int)gridDim.x;
       r0 = dtc_split(blockIdx.x, gridDim.x, R, L.nkt, Us, nkt_q);
       n_my = dyn_units ? 0x7fffffff : dtc_split(blockIdx.x + 1, gridDim.x, R, L.nkt, Us, nkt_q) - r0;
     }
@@ -433,8 +433,11 @@ __global__ void __launch_bounds__(kDgThreads, 1)
           const bool shared = phase == 0;
           int rr = r0 + it;
           if (!shared && dyn_units) {
-            // draw the next unit and publish it to the other roles
-            rr = atomicAdd(a.counter, 1);
+            // this CTA's fixed first unit, then draws from the counter; the
+            // unit goes to the other roles through the queue
+            const int G = gridDim.x, b = blockIdx.x, Un = min(Us, G);
+            if (it == 0) rr = b >= Un ? b - Un : (G - Un) + b;
+            else rr = G + atomicAdd(a.counter, 1);
             if (rr >= R) rr = -1;
             uq[qn & 7] = rr;
             mbar_arrive(&uq_full[qn & 7]);
