@@ -114,9 +114,10 @@ __device__ __forceinline__ void stage_meta(const DecodeArgs& a, unsigned char* s
     const int e = i < nt ? __ldcg(a.r.touched + i) : 0;
     const int p = i < P ? __ldcg(a.r.perm + i) : 0;
     if (i < nt) {
+      const int z = a.rec_z ? __ldcg(a.rec_z + e) : e;
       s_touched[i] = e;
-      s_z[i] = a.rec_z ? __ldcg(a.rec_z + e) : e;
-      s_rec[i] = reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(a.rec) + e));
+      s_z[i] = z;
+      s_rec[i] = a.bank + (int64_t)z * a.lay.bytes;
     }
     if (i < P) {
       s_tok[i] = p / k;
@@ -155,17 +156,16 @@ __device__ int build_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M,
   }
   for (int e = tid; e < E; e += nthr) s_mask[e] = __ldcg(a.r.emask + e);
   // each thread owns experts [e0, e1) (at most 5: E <= 1024 over >= 224
-  // threads); their records' pointers and indices load with the masks
+  // threads); their record indices load with the masks (an offloaded
+  // forward's slots; resident, the index is the expert), and a record
+  // starts at bank + index * record size
   const int per = (E + nthr - 1) / nthr;
   const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
   constexpr int kPer = 5;
-  const uint8_t* rp[kPer];
   int rz[kPer];
 #pragma unroll
   for (int m = 0; m < kPer; ++m) {
     const int e = e0 + m;
-    rp[m] = e < e1 ? reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(a.rec) + e))
-                   : nullptr;
     rz[m] = e < e1 ? (a.rec_z ? __ldcg(a.rec_z + e) : e) : 0;
   }
   __syncthreads();
@@ -196,7 +196,7 @@ __device__ int build_meta(const DecodeArgs& a, unsigned char* sm, const Meta& M,
     if (msk) {
       s_touched[toff] = e;
       s_z[toff] = rz[m];
-      s_rec[toff] = rp[m];
+      s_rec[toff] = a.bank + (int64_t)rz[m] * a.lay.bytes;
       if (globals) a.r.touched[toff] = e;
       ++toff;
     }
@@ -381,16 +381,18 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     } else {
       pdl_wait();  // routing and the activation codes
       pdl_launch_dependents();
+      if (warp == 0 && lane == 0) {
+        // every token's activation codes (they do not depend on the tables)
+        mbar_arrive_expect_tx(xbar, L.nkt * npad * 128);
+        for (int kt = 0; kt < L.nkt; ++kt)
+          tma_load_2d(sm + L.xres_off + kt * npad * 128, &map_xq, kt * 128, 0, xbar);
+      }
       if (a.meta_masks) {
         nt = build_meta(a, sm, M, blockIdx.x == 0);
       } else {
         nt = __ldcg(a.r.n_touched);
         stage_meta(a, sm, M, nt);
-      }
-      if (warp == 0 && lane == 0) {
-        mbar_arrive_expect_tx(xbar, L.nkt * npad * 128);
-        for (int kt = 0; kt < L.nkt; ++kt)
-          tma_load_2d(sm + L.xres_off + kt * npad * 128, &map_xq, kt * 128, 0, xbar);
+        __syncthreads();
       }
       if (warp == 6) {
         // activation scale blocks into TMEM (once): lane t stages token t's
@@ -416,11 +418,12 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         // the first scale-factor commit of phase 1 covers these copies too
+        // (the MMA thread waits for it before its first MMA, so nothing
+        // else waits for this warp here)
         if (lane == 0)
           for (int ks = 0; ks < L.nks; ++ks) tc_cp_sf(tmem + kSfbCol + 4 * ks, sdesc_sf(smem_u32(sfb) + 512 * ks));
         __syncwarp();
       }
-      __syncthreads();
       R = nt * J;
       dyn_units = a.meta_masks != 0 && R > (int)gridDim.x;
       r0 = dtc_split(blockIdx.x, gridDim.x, R, L.nkt, Us, nkt_q);
@@ -429,15 +432,19 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     if (warp == 0) {
       // ---------------- TMA producer
       if (lane == 0) {
+        int drawn = 0;  // the counter's answer for the next unit, asked one unit ahead
         for (int it = 0; it < n_my && !*abort_flag; ++it) {
           const bool shared = phase == 0;
           int rr = r0 + it;
           if (!shared && dyn_units) {
-            // this CTA's fixed first unit, then draws from the counter; the
-            // unit goes to the other roles through the queue
+            // this CTA's fixed first unit, then draws from the counter (the
+            // draw for unit it + 1 goes out when unit it starts, so its round
+            // trip overlaps the unit's loads); the unit goes to the other
+            // roles through the queue
             const int G = gridDim.x, b = blockIdx.x, Un = min(Us, G);
             if (it == 0) rr = b >= Un ? b - Un : (G - Un) + b;
-            else rr = G + atomicAdd(a.counter, 1);
+            else rr = G + drawn;
+            if (rr < R) drawn = atomicAdd(a.counter, 1);
             if (rr >= R) rr = -1;
             uq[qn & 7] = rr;
             mbar_arrive(&uq_full[qn & 7]);
@@ -471,6 +478,9 @@ __global__ void __launch_bounds__(kDgThreads, 1)
           }
         }
       }
+      // the other lanes wait here for lane 0: a lane that went ahead to the
+      // next phase's dependency wait would hold the whole warp there
+      __syncwarp();
     } else if (warp == 1) {
       // ---------------- MMA issuer
       if (lane == 0) {
@@ -509,6 +519,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
           tc_commit(&acc_full[buf]);
         }
       }
+      __syncwarp();  // as for the producer warp
     } else if (warp == 6) {
       // ---------------- scale factors: once a stage has landed, its weight
       // scale blocks go into that stage's TMEM columns and sf_ready[s]
@@ -979,9 +990,12 @@ __global__ void __launch_bounds__(kDtThreads)
   const int n_units = (E / 128) * C;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
-  // the next kernels may launch once every CTA here holds its TMEM (a CTA of
-  // theirs that allocated TMEM first could otherwise wait on this grid)
-  if (b >= n_units) pdl_launch_dependents();
+  // Every CTA lets the next kernels launch only after its own dependency
+  // wait: the expert kernel launched after the top-k kernel reads x and
+  // writes its shared-expert buffers before its own wait, so the grid
+  // before this one (which may have written x, or still read those
+  // buffers) must have ended by then.  (Unit CTAs also hold their TMEM by
+  // then, so no CTA of a later grid can take it first.)
   if (b < n_units) {
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + kRtKc * (kDtA + kDtB));
     uint64_t* accb = full + kRtKc;
@@ -998,15 +1012,18 @@ __global__ void __launch_bounds__(kDtThreads)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_launch_dependents();
+    // every tile of the chunk at once: the router tiles before this grid's
+    // dependency wait (they are weights), x after it
     if (warp == 0 && lane == 0) {
-      // every tile of the chunk at once: the router tiles before this grid's
-      // dependency wait (they are weights), x after it
       for (int i = 0; i < nk; ++i) {
         mbar_arrive_expect_tx(&full[i], kDtA + npad * 128);
         tma_load_2d(sm + i * (kDtA + kDtB), &map_wr, (kt0 + i) * 128, 128 * m, &full[i]);
       }
-      pdl_wait();
+    }
+    __syncwarp();
+    pdl_wait();  // x, and rpart (the grid before this one may still read it)
+    pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
       for (int i = 0; i < nk; ++i)
         tma_load_2d(sm + i * (kDtA + kDtB) + kDtA, &map_x, ((kt0 + i) * 128) % (2 * H), 0, &full[i]);
     } else if (warp == 1 && lane == 0) {
@@ -1021,7 +1038,6 @@ __global__ void __launch_bounds__(kDtThreads)
       tc_commit(accb);  // every MMA this thread issued
     } else if (warp >= 2) {
       const int q = warp & 3, row = 32 * q + lane;
-      pdl_wait();  // rpart may still be read by the grid before this one
       const bool ok = mbar_wait(accb, 0, a.r.status);
       tc_fence_after();
       if (ok) {
@@ -1040,6 +1056,7 @@ __global__ void __launch_bounds__(kDtThreads)
     return;
   }
   pdl_wait();  // x, and the buffers below, belong to the grid before this one until it ends
+  pdl_launch_dependents();
   const int nxq = rt_xq_ctas(T, H);
   if (b < n_units + nxq) {
     // a slice of the activation quantisation
