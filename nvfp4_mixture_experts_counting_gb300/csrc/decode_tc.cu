@@ -40,10 +40,6 @@ constexpr int kDdSmem = 112 * 1024;
 constexpr uint32_t kDdTmemCols = 256;
 constexpr int kDtA = 16384;      // 128 weight rows x 128 bytes
 constexpr int kDtB = 4096;       // up to 32 token / pair rows x 128 bytes
-// A shared-expert gate_up unit (64 gate + 64 up rows) is split into K
-// quarters, each as long as a routed unit (H / 256 tiles); the quarters'
-// fp32 partial sums are added in quarter order by the last warp to finish.
-constexpr int kShKq = 4;
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
   return p + ((1024 - (smem_u32(p) & 1023)) & 1023);
@@ -336,8 +332,8 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int J = a.win.I_loc / 64, Js = (a.sh_gate_up && !a.skip_shared) ? a.s_I_loc / 64 : 0;
-  const int nkt_q = H / 64 / kShKq;  // bf16 K tiles of one K quarter of the shared gate_up
-  const int Us = Js * kShKq;          // shared units: (window tile, K quarter)
+  const int nkt_q = H / 64;  // bf16 K tiles of a shared unit (its whole K)
+  const int Us = Js;         // shared units: window tiles of 64 gate + 64 up rows
   const int row0 = a.win.row0, Iw = a.win.Iw;
   const uint32_t id_f4 = idesc_nvf4(128, npad), id_bf = idesc_bf16(128, npad);
   // Two phases.  0: the shared expert's units (they need only x, so they run
@@ -452,8 +448,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             if (rr < 0) break;
           }
           const int us = (int)blockIdx.x + it * (int)gridDim.x;  // shared unit
-          const int j = shared ? us / kShKq : rr % J;
-          const int kt0 = shared ? (us % kShKq) * nkt_q : 0;     // first K tile of the unit
+          const int j = shared ? us : rr % J;
           const int z = shared ? 0 : s_z[rr / J];  // record index in the bank / slot pool
           const uint8_t* rec = shared ? nullptr : s_rec[rr / J];
           const int nkt_u = shared ? nkt_q : L.nkt;
@@ -465,9 +460,9 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             unsigned char* sa = sm + s * L.stage;
             if (shared) {
               mbar_arrive_expect_tx(&full[s], kDtA + npad * 128);
-              tma_load_2d(sa, &map_sgu, (kt0 + kt) * 128, a.s_row0 + 64 * j, &full[s]);
-              tma_load_2d(sa + kDtA / 2, &map_sgu, (kt0 + kt) * 128, a.s_Iw + a.s_row0 + 64 * j, &full[s]);
-              tma_load_2d(sa + kDtA, &map_x, (kt0 + kt) * 128, 0, &full[s]);
+              tma_load_2d(sa, &map_sgu, kt * 128, a.s_row0 + 64 * j, &full[s]);
+              tma_load_2d(sa + kDtA / 2, &map_sgu, kt * 128, a.s_Iw + a.s_row0 + 64 * j, &full[s]);
+              tma_load_2d(sa + kDtA, &map_x, kt * 128, 0, &full[s]);
             } else {
               mbar_arrive_expect_tx(&full[s], kDtA + 2048);
               tma_load_3d(sa, &map_gu, kt * 128, row0 + 64 * j, z, &full[s]);
@@ -552,20 +547,18 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     } else {
       // ---------------- epilogue: warp q = w % 4 holds TMEM lanes 32q..32q+31:
       // gate rows (q = 0, 1) and up rows (q = 2, 3) of window index i.
-      // Routed units: the up warps hand their values to the gate warps
-      // through a double buffer guarded by mbarriers (bounded waits, so a
-      // timeout anywhere cannot strand a warp).  Shared units: every warp
-      // stores its rows' partial sums of the unit's K quarter; for each half
-      // of the window tile, the warp that completes its gate and up stores
-      // of all quarters adds the quarters in order and writes the bf16
-      // intermediate of those 32 window indices.
+      // The up warps hand their values to the gate warps through a double
+      // buffer guarded by mbarriers (bounded waits, so a timeout anywhere
+      // cannot strand a warp).  A shared unit's columns are the tokens and
+      // its SwiGLU output goes to hs in bf16; a routed unit's columns are its
+      // expert's pairs, and the output is quantised to NVFP4.
       for (int it = 0; it < n_my && !*abort_flag; ++it, ++ui) {
         const int buf = ui & 1;
         const bool sh = phase == 0;
         int rr = r0 + it;
         if (!sh && !next_unit(it, phase, &rr)) break;
         const int us = (int)blockIdx.x + it * (int)gridDim.x;
-        const int ti = sh ? 0 : rr / J, j = sh ? us / kShKq : rr % J;
+        const int ti = sh ? 0 : rr / J, j = sh ? us : rr % J;
         const int e = sh ? 0 : s_touched[ti];
         const int s0 = sh ? 0 : s_off[e];
         const int m = sh ? T : s_off[e + 1] - s0;  // columns this unit uses
@@ -576,80 +569,55 @@ __global__ void __launch_bounds__(kDgThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * npad;
         bool ok = true;
-        if (sh) {
-          // spart[us][t][row]: this K quarter's sums of the tile's 128 rows
-          float* sp = a.spart + (int64_t)us * 32 * 128;
-          for (int t = 0; t < T; ++t) sp[t * 128 + 32 * q + lane] = tc_ld1_wait(taddr + t);
-          __threadfence();
+        const int ub = uu & 1;
+        float* U = U0 + ub * 32 * 64;
+        if (up) {
+          if (uu >= 2 && !mbar_wait(&u_free[ub], ((uu >> 1) - 1) & 1, a.r.status)) ok = false;
+          if (ok)
+            for (int r = 0; r < m; ++r) U[r * 64 + i] = tc_ld1_wait(taddr + (sh ? r : s_tok[s0 + r])) * gl;
           __syncwarp();
-          // window indices 32 half .. 32 half + 31 need gate warp q = half
-          // and up warp q = 2 + half of all K quarters: 2 * kShKq stores
-          const int half = q & 1;
-          int last = 0;
-          if (lane == 0) last = atomicAdd(&a.scnt[2 * j + half], 1) == 2 * kShKq - 1;
-          if (__shfl_sync(0xffffffffu, last, 0)) {
-            __threadfence();
-            const int ii = 32 * half + lane;
-#pragma unroll 4
-            for (int t = 0; t < T; ++t) {
-              float g = 0.f, u = 0.f;
-#pragma unroll
-              for (int kq = 0; kq < kShKq; ++kq) {
-                const float* p = a.spart + ((int64_t)(j * kShKq + kq) * 32 + t) * 128;
-                g += __ldcg(p + ii);
-                u += __ldcg(p + 64 + ii);
-              }
-              const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * u);
-              a.hs[(int64_t)t * a.s_I_loc + 64 * j + ii] = *reinterpret_cast<const uint16_t*>(&hb);
-            }
-            if (lane == 0) a.scnt[2 * j + half] = 0;  // ready for the next launch
-          }
+          if (lane == 0) mbar_arrive(&u_full[ub]);
         } else {
-          const int ub = uu & 1;
-          float* U = U0 + ub * 32 * 64;
-          if (up) {
-            if (uu >= 2 && !mbar_wait(&u_free[ub], ((uu >> 1) - 1) & 1, a.r.status)) ok = false;
-            if (ok)
-              for (int r = 0; r < m; ++r) U[r * 64 + i] = tc_ld1_wait(taddr + s_tok[s0 + r]) * gl;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&u_full[ub]);
-          } else {
-            if (!mbar_wait(&u_full[ub], (uu >> 1) & 1, a.r.status)) ok = false;
-            if (ok) {
-              for (int r = 0; r < m; ++r) {
-                const int pos = s0 + r;
-                const float g = tc_ld1_wait(taddr + s_tok[pos]) * gl;
-                const float h = silu(g) * U[r * 64 + i];
-                // NVFP4 quantisation of the 16-element block held by this half-warp
-                float amax = fabsf(h);
+          if (!mbar_wait(&u_full[ub], (uu >> 1) & 1, a.r.status)) ok = false;
+          if (ok && sh) {
+            for (int t = 0; t < m; ++t) {
+              const __nv_bfloat16 hb = __float2bfloat16_rn(silu(tc_ld1_wait(taddr + t)) * U[t * 64 + i]);
+              a.hs[(int64_t)t * a.s_I_loc + 64 * j + i] = *reinterpret_cast<const uint16_t*>(&hb);
+            }
+          } else if (ok) {
+            for (int r = 0; r < m; ++r) {
+              const int pos = s0 + r;
+              const float g = tc_ld1_wait(taddr + s_tok[pos]) * gl;
+              const float h = silu(g) * U[r * 64 + i];
+              // NVFP4 quantisation of the 16-element block held by this half-warp
+              float amax = fabsf(h);
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 16));
-                const uint8_t sc = e4m3_encode(__fdiv_rn(amax, kE2M1Max));
-                const float dsc = e4m3_decode(sc);
-                uint32_t code = 0;
-                if (sc != 0 && dsc != 0.f) code = e2m1x2_encode(__fdiv_rn(h, dsc), 0.0f) & 0xF;
-                // gather the half-warp's 16 nibbles into 8 bytes held by its first lane
-                const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
-                const uint32_t byte = (code | (hi << 4)) & 0xFF;  // valid on even lanes
-                uint32_t w0 = 0, w1 = 0;
+              for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 16));
+              const uint8_t sc = e4m3_encode(__fdiv_rn(amax, kE2M1Max));
+              const float dsc = e4m3_decode(sc);
+              uint32_t code = 0;
+              if (sc != 0 && dsc != 0.f) code = e2m1x2_encode(__fdiv_rn(h, dsc), 0.0f) & 0xF;
+              // gather the half-warp's 16 nibbles into 8 bytes held by its first lane
+              const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+              const uint32_t byte = (code | (hi << 4)) & 0xFF;  // valid on even lanes
+              uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                  w0 |= (__shfl_sync(0xffffffffu, byte, (lane & 16) + 2 * b) & 0xFF) << (8 * b);
-                  w1 |= (__shfl_sync(0xffffffffu, byte, (lane & 16) + 8 + 2 * b) & 0xFF) << (8 * b);
-                }
-                if ((lane & 15) == 0) {
-                  const int half = lane >> 4;
-                  *reinterpret_cast<uint2*>(a.hq_codes + (int64_t)pos * a.hq_cpitch + 32 * j + 16 * (q & 1) +
-                                            8 * half) = make_uint2(w0, w1);
-                  a.hsf[((int64_t)ti * J + j) * 512 + r * 16 + 2 * (q & 1) + half] = sc;
-                }
+              for (int b = 0; b < 4; ++b) {
+                w0 |= (__shfl_sync(0xffffffffu, byte, (lane & 16) + 2 * b) & 0xFF) << (8 * b);
+                w1 |= (__shfl_sync(0xffffffffu, byte, (lane & 16) + 8 + 2 * b) & 0xFF) << (8 * b);
+              }
+              if ((lane & 15) == 0) {
+                const int half = lane >> 4;
+                *reinterpret_cast<uint2*>(a.hq_codes + (int64_t)pos * a.hq_cpitch + 32 * j + 16 * (q & 1) +
+                                          8 * half) = make_uint2(w0, w1);
+                a.hsf[((int64_t)ti * J + j) * 512 + r * 16 + 2 * (q & 1) + half] = sc;
               }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&u_free[ub]);
           }
-          ++uu;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&u_free[ub]);
         }
+        ++uu;
         if (!ok) *abort_flag = 1;
         tc_fence_before();
         __syncwarp();

@@ -170,8 +170,6 @@ struct ftmoe_handle {
   float* dtc_gpart = nullptr;
   int* dtc_counter = nullptr;
   float* dtc_rpart = nullptr;  // router K-chunk partial logits [chunks][T][E]
-  float* dtc_spart = nullptr;  // shared gate_up partial sums per K quarter
-  int* dtc_scnt = nullptr;     // their arrival counters
   int dtc_groups = 0;
   uint32_t last_status = 0;
   EventProfiler* prof = nullptr;  // non-null while per-kernel timing is enabled
@@ -330,10 +328,6 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
     parts.push_back({(void**)&h->dtc_hsf, (int64_t)c.E * (c.I / 64) * 512});
     parts.push_back({(void**)&h->dtc_gpart, (int64_t)(h->dtc_groups + 1) * Td * c.H * 4});
     parts.push_back({(void**)&h->dtc_counter, (int64_t)(c.H / 128 + 1) * 4});
-    if (c.I_shared > 0) {  // K quarters of the shared gate_up tiles: [tiles * 4][32 tokens][128 rows]
-      parts.push_back({(void**)&h->dtc_spart, (int64_t)(c.I_shared / 64) * 4 * 32 * 128 * 4});
-      parts.push_back({(void**)&h->dtc_scnt, (int64_t)(c.I_shared / 64 + 1) * 2 * 4});
-    }
     if (decode_tc_router_supported(c.H, c.E))  // chunks of 8 K tiles of 128 bytes over [W1 | W2 | W3]
       parts.push_back({(void**)&h->dtc_rpart, (int64_t)((6 * c.H / 128 + 7) / 8) * Td * c.E * 4});
   }
@@ -611,8 +605,6 @@ static void decode_tc_args(ftmoe_handle* h, Layer& L, DecodeArgs& d) {
   d.hsf = h->dtc_hsf;
   d.gpart = h->dtc_gpart;
   d.dn_counter = h->dtc_counter;
-  d.spart = h->dtc_spart;
-  d.scnt = h->dtc_scnt;
   d.n_groups = h->dtc_groups;
   d.hq_cpitch = (int)align_up(d.win.I_loc / 2, 16);
   if (L.router_wcat && h->dtc_rpart && decode_tc_router_supported(h->cfg.H, h->cfg.E)) {

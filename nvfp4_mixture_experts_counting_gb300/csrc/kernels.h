@@ -145,8 +145,6 @@ struct DecodeArgs {
   int split_tail;      // 1: top-k and the sort run in k_dec_topk instead of the last router CTA
   int skip_shared;     // 1: leave the shared expert out (a later expert batch of an offloaded forward)
   int meta_masks;      // 1: the top-k kernel only sets emask; the expert kernels build the sorted tables
-  float* spart;        // [I_shared / 64 * 4][32][128] shared gate_up partial sums per K quarter
-  int* scnt;           // [I_shared / 64][2] arrival counters of the shared gate_up half tiles (zero between launches)
   // router logits on the tensor cores (split K): partial sums rpart[c][t][e]
   // of x . (W1 + W2 + W3) over K chunk c; the top-k kernel adds them in order
   const uint16_t* wcat;  // [E][3H] bf16 parts of the router rows, or null (CUDA-core router)
