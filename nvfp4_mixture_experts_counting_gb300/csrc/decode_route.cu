@@ -310,8 +310,10 @@ __device__ void dec_split(const DecodeArgs& a, int* pre, int* scan) {
   }
 }
 
-// Largest number of K-chunk partials of the tensor-core router.
-constexpr int kMaxRparts = 16;
+// Largest number of K-chunk partials of the tensor-core router; the top-k
+// kernel adds them in four contiguous runs of at most kRpRun.
+constexpr int kMaxRparts = 32;
+constexpr int kRpRun = kMaxRparts / 4;
 
 // Top-k of every token (certified; uncertain tokens re-ranked by the whole
 // CTA), the counting sort and the gate_up work split, by one CTA.
@@ -325,39 +327,8 @@ __device__ void dec_tail(const DecodeArgs& a, unsigned char* sm) {
   int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
   int* state = reinterpret_cast<int*>(sm + L.tok_off);
   float* lmin = reinterpret_cast<float*>(state + 96);
-  if (a.n_rparts > 0) {
-    // tensor-core router: add the K-chunk partials of every (token, expert)
-    // in order, spread over the whole CTA; the bound is the accumulation
-    // bound kappa ||x|| ||w|| plus the rounding of these fp32 additions and
-    // of the bias
-    const float gam = (float)(a.n_rparts + 2) * 5.9604645e-8f;
-    const int C = a.n_rparts;  // at most kMaxRparts
-    for (int g = tid; g < T * E / 4; g += kRtThreads) {
-      const int i = 4 * g, t = i / E, e = i - t * E;
-      const float4* pp = reinterpret_cast<const float4*>(a.rpart + (int64_t)t * E + e);
-      float4 v[kMaxRparts];
-#pragma unroll
-      for (int c = 0; c < kMaxRparts; ++c)  // every load in flight before the sums
-        if (c < C) v[c] = __ldcg(pp + (int64_t)c * T * E / 4);
-      float s[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < kMaxRparts; ++c) {
-        if (c < C) {
-          s[0] += v[c].x; s[1] += v[c].y; s[2] += v[c].z; s[3] += v[c].w;
-          sa[0] += fabsf(v[c].x); sa[1] += fabsf(v[c].y); sa[2] += fabsf(v[c].z); sa[3] += fabsf(v[c].w);
-        }
-      }
-      const float xn = __ldcg(a.r.xnorm + t);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float bias = a.r.router_bias ? a.r.router_bias[e + q] : 0.f;
-        const float l = s[q] + bias;
-        a.r.logits[i + q] = l;
-        a.r.err[i + q] = a.kappa * xn * a.wnorm[e + q] + gam * (sa[q] + fabsf(bias)) + 1.2e-7f * fabsf(l) + 1e-30f;
-      }
-    }
-    __syncthreads();
-  }
+  // (the tensor-core router always runs the split tail, k_dec_topk, so the
+  // logits and their bounds are in a.r.logits / a.r.err here)
   for (int t = warp; t < T; t += 8) {
     for (int e = lane; e < E; e += 32) {
       s_lg[e] = __ldcg(a.r.logits + (int64_t)t * E + e);
@@ -396,32 +367,55 @@ __device__ __forceinline__ float tk_key(float v) { return v != v ? -INFINITY : v
 // accumulation bound kappa ||x|| ||w|| plus the rounding of these fp32
 // additions and of the bias), else as the CUDA-core router wrote them.
 // lg is padded with -infinity to a multiple of 4 entries.
-__device__ void tk_logits(const DecodeArgs& a, int t, float* lg, float* er) {
+__device__ void tk_logits(const DecodeArgs& a, int t, float* lg, float* er, float* scratch) {
   const int tid = threadIdx.x, T = a.T, E = a.r.E;
   if (a.n_rparts > 0) {
+    // the K-chunk partials of every expert in four contiguous runs (thread
+    // = (expert quad, run), the run's loads in flight together), then the
+    // runs added in order; the bound is the accumulation bound
+    // kappa ||x|| ||w|| plus the rounding of these fp32 additions (at most
+    // C + 2 of them along any path) and of the bias
     const float gam = (float)(a.n_rparts + 2) * 5.9604645e-8f;
     const int C = a.n_rparts;  // at most kMaxRparts
+    const int Q = E / 4;       // expert quads, at most kRtThreads
     const float xn = __ldcg(a.r.xnorm + t);
-    for (int g = tid; g < E / 4; g += kRtThreads) {
-      const int e = 4 * g;
-      const float4* pp = reinterpret_cast<const float4*>(a.rpart + (int64_t)t * E + e);
-      float4 v[kMaxRparts];
+    const float4 wn = tid < Q ? __ldg(reinterpret_cast<const float4*>(a.wnorm) + tid) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* ps = reinterpret_cast<float4*>(scratch);  // [4][Q] run sums, then [4][Q] run sums of |.|
+    for (int w = tid; w < 4 * Q; w += kRtThreads) {
+      const int g = w % Q, r = w / Q;
+      const int c0 = r * C / 4, c1 = (r + 1) * C / 4;
+      const float4* pp = reinterpret_cast<const float4*>(a.rpart + (int64_t)t * E) + g;
+      float4 v[kRpRun];
 #pragma unroll
-      for (int c = 0; c < kMaxRparts; ++c)  // every load in flight before the sums
-        if (c < C) v[c] = __ldcg(pp + (int64_t)c * T * E / 4);
-      float s[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = 0; c < kRpRun; ++c)
+        if (c0 + c < c1) v[c] = __ldcg(pp + (int64_t)(c0 + c) * T * Q);
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f), sa = s;
 #pragma unroll
-      for (int c = 0; c < kMaxRparts; ++c) {
-        if (c < C) {
-          s[0] += v[c].x; s[1] += v[c].y; s[2] += v[c].z; s[3] += v[c].w;
-          sa[0] += fabsf(v[c].x); sa[1] += fabsf(v[c].y); sa[2] += fabsf(v[c].z); sa[3] += fabsf(v[c].w);
+      for (int c = 0; c < kRpRun; ++c) {
+        if (c0 + c < c1) {
+          s.x += v[c].x; s.y += v[c].y; s.z += v[c].z; s.w += v[c].w;
+          sa.x += fabsf(v[c].x); sa.y += fabsf(v[c].y); sa.z += fabsf(v[c].z); sa.w += fabsf(v[c].w);
         }
       }
+      ps[r * Q + g] = s;
+      ps[(4 + r) * Q + g] = sa;
+    }
+    __syncthreads();
+    if (tid < Q) {
+      const int e = 4 * tid;
+      float s[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 u = ps[r * Q + tid], ua = ps[(4 + r) * Q + tid];
+        s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
+        sa[0] += ua.x; sa[1] += ua.y; sa[2] += ua.z; sa[3] += ua.w;
+      }
+      const float w4[4] = {wn.x, wn.y, wn.z, wn.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float bias = a.r.router_bias ? a.r.router_bias[e + q] : 0.f;
         const float l = s[q] + bias;
-        const float b = a.kappa * xn * a.wnorm[e + q] + gam * (sa[q] + fabsf(bias)) + 1.2e-7f * fabsf(l) + 1e-30f;
+        const float b = a.kappa * xn * w4[q] + gam * (sa[q] + fabsf(bias)) + 1.2e-7f * fabsf(l) + 1e-30f;
         a.r.logits[(int64_t)t * E + e + q] = l;
         a.r.err[(int64_t)t * E + e + q] = b;
         lg[e + q] = tk_key(l);
@@ -602,7 +596,8 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_topk(DecodeArgs a) {
   pdl_wait();
   const int tid = threadIdx.x, t = blockIdx.x;
   const TkSmem L = tk_smem_layout(a.T, a.r.E, a.top_k);
-  tk_logits(a, t, reinterpret_cast<float*>(sm + L.lg_off), reinterpret_cast<float*>(sm + L.er_off));
+  tk_logits(a, t, reinterpret_cast<float*>(sm + L.lg_off), reinterpret_cast<float*>(sm + L.er_off),
+            reinterpret_cast<float*>(sm + L.hist_off));
   tk_select(a, L, sm, t);
   if (a.meta_masks) {
     // token t's bit in each chosen expert's mask (lane j of warp 0 wrote

@@ -935,7 +935,7 @@ __global__ void __launch_bounds__(kDgThreads, 2)
 // add up to the fp32 router row exactly).  Further CTAs quantise the
 // activations (global 1.0) and one computes sigma = sigmoid(g . x) and an
 // upper bound of ||x|| per token.
-constexpr int kRtKc = 8;  // K tiles per router CTA (all in flight at once)
+constexpr int kRtKc = 4;  // K tiles per router CTA (all in flight at once)
 
 __device__ __forceinline__ int rt_units(int H, int E) {
   const int nkt = 6 * H / 128;
@@ -1092,11 +1092,14 @@ int decode_tc_groups(int H, int num_sms) {
   return g < 1 ? 1 : g;
 }
 
+int decode_tc_router_chunks(int H) { return (6 * H / 128 + kRtKc - 1) / kRtKc; }
+
 bool decode_tc_router_supported(int H, int E) {
-  // the tensor-core router's K chunks (8 tiles of 128 bytes of 3H bf16 each)
-  // are summed by the top-k kernel, which takes at most 16 of them; larger H
-  // routes on the CUDA cores (k_dec_route) ahead of the same expert kernels
-  return E % 128 == 0 && E <= 1024 && (6 * H / 128 + 7) / 8 <= 16;
+  // the tensor-core router's K chunks (kRtKc tiles of 128 bytes of 3H bf16
+  // each) are summed by the top-k kernel, which takes at most 32 of them;
+  // larger H routes on the CUDA cores (k_dec_route) ahead of the same expert
+  // kernels
+  return E % 128 == 0 && E <= 1024 && decode_tc_router_chunks(H) <= 32;
 }
 
 bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, int s_Iw, int s_row0, int T,

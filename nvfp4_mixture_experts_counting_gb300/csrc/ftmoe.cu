@@ -328,8 +328,8 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
     parts.push_back({(void**)&h->dtc_hsf, (int64_t)c.E * (c.I / 64) * 512});
     parts.push_back({(void**)&h->dtc_gpart, (int64_t)(h->dtc_groups + 1) * Td * c.H * 4});
     parts.push_back({(void**)&h->dtc_counter, (int64_t)(c.H / 128 + 1) * 4});
-    if (decode_tc_router_supported(c.H, c.E))  // chunks of 8 K tiles of 128 bytes over [W1 | W2 | W3]
-      parts.push_back({(void**)&h->dtc_rpart, (int64_t)((6 * c.H / 128 + 7) / 8) * Td * c.E * 4});
+    if (decode_tc_router_supported(c.H, c.E))  // partial logits per K chunk of [W1 | W2 | W3]
+      parts.push_back({(void**)&h->dtc_rpart, (int64_t)decode_tc_router_chunks(c.H) * Td * c.E * 4});
   }
   // tensor-core prefill buffers (padded pair order), for shapes it accepts
   if (c.max_tokens > 32 && c.H % 256 == 0 && c.I % 64 == 0 && c.E <= 1024 && !(no_tc && no_tc[0] == '1')) {

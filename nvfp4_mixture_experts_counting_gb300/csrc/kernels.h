@@ -161,6 +161,7 @@ bool decode_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, in
 cudaError_t decode_set_smem_limits();
 cudaError_t launch_decode(DecodeArgs a, cudaStream_t s);
 bool decode_tc_router_supported(int H, int E);
+int decode_tc_router_chunks(int H);  // K chunks (partial logits) of the tensor-core router
 bool decode_tc_supported(int H, int E, int I_loc, int Iw, int row0, int s_I_loc, int s_Iw, int s_row0, int T,
                          int top_k, bool has_sf);
 int decode_tc_groups(int H, int num_sms);
