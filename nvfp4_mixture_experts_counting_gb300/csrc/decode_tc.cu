@@ -79,7 +79,10 @@ __host__ __device__ inline DgLayout dg_layout(int H, int T, int E, int P) {
   L.npad = T <= 16 ? 16 : 32;
   L.nkt = H / 256;
   L.nks = H / 64;
-  L.stage = kDtA + kDtB + 2048;  // 22 KB, a multiple of 1024
+  // the A tile, then one region: a routed stage's A scale blocks (2 KB) or a
+  // shared stage's x tile (npad rows of 128 bytes); 18 or 20 KB, multiples
+  // of 1024
+  L.stage = kDtA + (L.npad * 128 > 2048 ? L.npad * 128 : 2048);
   const int xres = L.nkt * L.npad * 128, sfb = L.nks * 512, u = 2 * 32 * 64 * 4;
   const int meta = meta_layout(E, P, 0).bytes;
   const int nst = (kDtSmem - 1024 - xres - sfb - u - meta - 512) / L.stage;
@@ -237,8 +240,9 @@ struct DdLayout {
 __host__ __device__ inline DdLayout dd_layout(int T, int E, int P) {
   DdLayout L;
   L.npad = T <= 16 ? 16 : 32;
-  L.stage = kDtA + kDtB + 2048 + 2048;  // 24 KB
-  const int part = 32 * 128 * 4;
+  // A tile, B tile (npad rows of 128 bytes), A and B scale blocks: 22 or 24 KB
+  L.stage = kDtA + L.npad * 128 + 2048 + 2048;
+  const int part = L.npad * 128 * 4;
   const int meta = meta_layout(E, P, 0).bytes;
   const int nst = (kDdSmem - 1024 - part - meta - 512) / L.stage;
   L.nst = nst > 8 ? 8 : nst;
@@ -440,12 +444,14 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             const int G = gridDim.x, b = blockIdx.x, Un = min(Us, G);
             if (it == 0) rr = b >= Un ? b - Un : (G - Un) + b;
             else rr = G + drawn;
-            if (rr < R) drawn = atomicAdd(a.counter, 1);
             if (rr >= R) rr = -1;
             uq[qn & 7] = rr;
-            mbar_arrive(&uq_full[qn & 7]);
+            mbar_arrive(&uq_full[qn & 7]);  // release: the entry is visible
             ++qn;
             if (rr < 0) break;
+            // the next unit's draw; the stage barriers below arrive without
+            // release semantics, so nothing waits for it before the next unit
+            drawn = atomicAdd(a.counter, 1);
           }
           const int us = (int)blockIdx.x + it * (int)gridDim.x;  // shared unit
           const int j = shared ? us : rr % J;
@@ -464,10 +470,10 @@ __global__ void __launch_bounds__(kDgThreads, 1)
               tma_load_2d(sa + kDtA / 2, &map_sgu, kt * 128, a.s_Iw + a.s_row0 + 64 * j, &full[s]);
               tma_load_2d(sa + kDtA, &map_x, kt * 128, 0, &full[s]);
             } else {
-              mbar_arrive_expect_tx(&full[s], kDtA + 2048);
+              mbar_arrive_expect_tx_relaxed(&full[s], kDtA + 2048);
               tma_load_3d(sa, &map_gu, kt * 128, row0 + 64 * j, z, &full[s]);
               tma_load_3d(sa + kDtA / 2, &map_gu, kt * 128, Iw + row0 + 64 * j, z, &full[s]);
-              bulk_g2s(sa + kDtA + kDtB, rec + a.lay.gu_sf + ((int64_t)(row0 / 64 + j) * L.nks + 4 * kt) * 512,
+              bulk_g2s(sa + kDtA, rec + a.lay.gu_sf + ((int64_t)(row0 / 64 + j) * L.nks + 4 * kt) * 512,
                        2048, &full[s]);
             }
           }
@@ -538,7 +544,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             tc_fence_after();
             const uint32_t sa = smem_u32(sm + s * L.stage);
             const uint32_t sfa_col = tmem + kSfaCol + 16 * s;
-            for (int ks = 0; ks < 4; ++ks) tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
+            for (int ks = 0; ks < 4; ++ks) tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + 512 * ks));
             tc_commit(&sf_ready[s]);
           }
         }
@@ -702,7 +708,7 @@ __global__ void __launch_bounds__(kDgThreads, 2)
     tma_prefetch_desc(&map_hs);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kDdTmemCols);
-  for (int i2 = tid; i2 < 32 * 128; i2 += blockDim.x) part[i2] = 0.f;
+  for (int i2 = tid; i2 < npad * 128; i2 += blockDim.x) part[i2] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -742,12 +748,12 @@ __global__ void __launch_bounds__(kDgThreads, 2)
           if (expect) mbar_arrive_expect_tx(&full[s], kDtA + npad * 128 + 2 * nks * 512);
           if (weights) {
             tma_load_3d(sa, &map_dn, row0 / 2 + kt * 128, 128 * ht, s_z[ti], &full[s]);
-            bulk_g2s(sa + kDtA + kDtB, s_rec[ti] + a.lay.dn_sf + ((int64_t)ht * (Iw / 64) + row0 / 64 + 4 * kt) * 512,
+            bulk_g2s(sa + kDtA + npad * 128, s_rec[ti] + a.lay.dn_sf + ((int64_t)ht * (Iw / 64) + row0 / 64 + 4 * kt) * 512,
                      nks * 512, &full[s]);
           }
           if (acts) {
             tma_load_2d(sa + kDtA, &map_hq, kt * 128, s_off[s_touched[ti]], &full[s]);
-            bulk_g2s(sa + kDtA + kDtB + 2048, a.hsf + ((int64_t)ti * nks_r + 4 * kt) * 512, nks * 512, &full[s]);
+            bulk_g2s(sa + kDtA + npad * 128 + 2048, a.hsf + ((int64_t)ti * nks_r + 4 * kt) * 512, nks * 512, &full[s]);
           }
         }
       };
@@ -833,8 +839,8 @@ __global__ void __launch_bounds__(kDgThreads, 2)
           const int nks = min(4, nks_r - 4 * kt);
           const uint32_t sfa_col = tmem + kSfCol + 32 * s, sfb_col = sfa_col + 16;
           for (int ks = 0; ks < nks; ++ks) {
-            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 512 * ks));
-            tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sa + kDtA + kDtB + 2048 + 512 * ks));
+            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sa + kDtA + npad * 128 + 512 * ks));
+            tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sa + kDtA + npad * 128 + 2048 + 512 * ks));
           }
           tc_commit(&sf_ready[s]);
         }
