@@ -939,9 +939,10 @@ __global__ void __launch_bounds__(kDgThreads, 2)
 // K chunk c) forms rpart[c][t][128 m + r] = sum over the chunk of
 // x[t] . [W1 | W2 | W3][128 m + r] (x repeated along K; the three bf16 parts
 // add up to the fp32 router row exactly).  Further CTAs quantise the
-// activations (global 1.0) and one computes sigma = sigmoid(g . x) and an
-// upper bound of ||x|| per token.
+// activations (global 1.0), and the last ones compute, one warp per token,
+// sigma = sigmoid(g . x) and an upper bound of ||x||.
 constexpr int kRtKc = 4;  // K tiles per router CTA (all in flight at once)
+constexpr int kSgBatch = 12;  // 16-byte pieces of x and g per lane in flight (sigma CTAs; H <= 3072 in one go)
 
 __device__ __forceinline__ int rt_units(int H, int E) {
   const int nkt = 6 * H / 128;
@@ -1056,22 +1057,32 @@ __global__ void __launch_bounds__(kDtThreads)
   }
   // the token masks of the top-k kernel start empty, and so does the
   // gate_up kernel's unit counter
-  if (a.r.emask)
-    for (int e = tid; e < E; e += kDtThreads) a.r.emask[e] = 0u;
-  if (a.meta_masks && tid == 0) *a.counter = 0;
-  // sigma_t = sigmoid(g . x_t) and an upper bound of ||x_t||, one warp per token
-  for (int t = warp; t < T; t += kDtThreads / 32) {
-    const uint4* xr = reinterpret_cast<const uint4*>(a.r.x + (int64_t)t * H);
-    const uint4* gr = reinterpret_cast<const uint4*>(a.r.sh_gate);
-    float z = 0.f, q = 0.f;
-    for (int i = lane; i < H / 8; i += 32) {
-      const uint4 xv = __ldg(xr + i);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t gw[4] = {0, 0, 0, 0};
-      if (gr) {
-        const uint4 gv = __ldg(gr + i);
-        gw[0] = gv.x; gw[1] = gv.y; gw[2] = gv.z; gw[3] = gv.w;
-      }
+  const int b0 = b - n_units - nxq;  // sigma CTA index
+  if (b0 == 0) {
+    if (a.r.emask)
+      for (int e = tid; e < E; e += kDtThreads) a.r.emask[e] = 0u;
+    if (a.meta_masks && tid == 0) *a.counter = 0;
+  }
+  // sigma_t = sigmoid(g . x_t) and an upper bound of ||x_t||, one warp per
+  // token (kDtThreads / 32 tokens per CTA), kSgBatch 16-byte pieces of x
+  // and of g per lane in flight at a time
+  const int t = b0 * (kDtThreads / 32) + warp;
+  if (t >= T) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(a.r.x + (int64_t)t * H);
+  const uint4* gr = reinterpret_cast<const uint4*>(a.r.sh_gate);
+  float z = 0.f, q = 0.f;
+  for (int i0 = 0; i0 < H / 8; i0 += 32 * kSgBatch) {
+    uint4 xv[kSgBatch], gv[kSgBatch];
+#pragma unroll
+    for (int k = 0; k < kSgBatch; ++k) {
+      const int i = i0 + 32 * k + lane;
+      xv[k] = i < H / 8 ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+      gv[k] = (gr && i < H / 8) ? __ldg(gr + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kSgBatch; ++k) {
+      const uint32_t xw[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
+      const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
 #pragma unroll
       for (int k2 = 0; k2 < 4; ++k2) {
         const float lo = __uint_as_float(xw[k2] << 16), hi = __uint_as_float(xw[k2] & 0xffff0000u);
@@ -1081,12 +1092,12 @@ __global__ void __launch_bounds__(kDtThreads)
         q = fmaf(hi, hi, q);
       }
     }
-    z = warp_sum(z);
-    q = warp_sum(q);
-    if (lane == 0) {
-      a.r.sigma[t] = gr ? 1.0f / (1.0f + expf(-z)) : 0.f;
-      a.r.xnorm[t] = sqrtf(q) * (1.0f + 1e-5f);
-    }
+  }
+  z = warp_sum(z);
+  q = warp_sum(q);
+  if (lane == 0) {
+    a.r.sigma[t] = gr ? 1.0f / (1.0f + expf(-z)) : 0.f;
+    a.r.xnorm[t] = sqrtf(q) * (1.0f + 1e-5f);
   }
 }
 
@@ -1256,7 +1267,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
       const int nkt = 6 * H / 128;
       a.n_rparts = (nkt + kRtKc - 1) / kRtKc;
       const int units = (E / 128) * a.n_rparts;
-      cfg.gridDim = dim3(units + rt_xq_ctas(T, H) + 1);
+      cfg.gridDim = dim3(units + rt_xq_ctas(T, H) + (T + kDtThreads / 32 - 1) / (kDtThreads / 32));
       cfg.blockDim = dim3(kDtThreads);
       cfg.dynamicSmemBytes = 1024 + kRtKc * (kDtA + kDtB) + 256;
       // programmatic launch: the router tiles stream while the grid before
