@@ -32,7 +32,8 @@ namespace ftmoe {
 namespace {
 
 constexpr int kDtThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr int kDgThreads = 224;  // gate_up and down: the same, and warp 6 copies scale factors into TMEM
+constexpr int kDgThreads = 224;  // gate_up: warp 0 TMA, 1 MMA, 2-5 epilogue, 6 scale factors into TMEM
+constexpr int kDdThreads = 256;  // down: warp 7 joins only the group reduction
 constexpr int kDtSmem = 220 * 1024;
 // the down kernel runs two CTAs per SM (each issues its own MMAs), so it
 // keeps to half of the shared memory and of TMEM
@@ -655,7 +656,7 @@ __global__ void __launch_bounds__(kDgThreads, 1)
 
 // ------------------------------------------------------------------ down
 
-__global__ void __launch_bounds__(kDgThreads, 2)
+__global__ void __launch_bounds__(kDdThreads, 2)
     k_dtc_down(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_dn,
                const __grid_constant__ CUtensorMap map_hq, const __grid_constant__ CUtensorMap map_sdn,
                const __grid_constant__ CUtensorMap map_hs) {
@@ -849,6 +850,8 @@ __global__ void __launch_bounds__(kDgThreads, 2)
       mbar_wait(sf_drain, 0, a.r.status);
     }
     __syncwarp();
+  } else if (warp == 7) {
+    // only the group reduction below (its loads spread over one more warp)
   } else {
     // ---------------- epilogue: thread = output row h of the tile, TMEM lane h
     const int q = warp & 3, h = 32 * q + lane;
@@ -1315,7 +1318,7 @@ cudaError_t launch_decode_tc(DecodeArgs a, cudaStream_t s, int parts) {
     const DdLayout L = dd_layout(T, E, P);
     const int rows = a.n_groups + ((a.sh_down && !a.skip_shared) ? 1 : 0);
     FTMOE_PROF_BEGIN("k_dtc_down", s);
-    err = launch_tc(k_dtc_down, dim3(H / 128, rows), kDgThreads, L.total, s, a.pdl, a, m_dn, m_hq, m_sdn, m_hs);
+    err = launch_tc(k_dtc_down, dim3(H / 128, rows), kDdThreads, L.total, s, a.pdl, a, m_dn, m_hq, m_sdn, m_hs);
     FTMOE_PROF_END(s);
     if (err != cudaSuccess) return err;
   }
