@@ -427,10 +427,13 @@ def run_gpu(args):
     if dom:
         launches, kms = ktimes[dom]
         avg_s = kms / launches / 1e3
+        # a step's work over that kernel's launches in a step (an offloaded
+        # forward launches the expert kernels once per batch of slots)
+        per = KP / launches
         unit_bytes, unit, fixed = A.kernel_unit_bytes(dom, wl.H, I_loc, sI_loc, wl.E)
         unit_flops, funit, path = A.kernel_unit_flops(dom, wl.H, I_loc, sI_loc, wl.E)
         if unit_flops is not None:
-            units = pairs if funit == "pair" else T
+            units = (pairs if funit == "pair" else T) * per
             achieved = unit_flops * units / avg_s / 1e12
             if path.startswith("nvfp4"):
                 pk, pk_src, bound = fp4_peak, fp4_kind, "tensor"
@@ -440,11 +443,11 @@ def run_gpu(args):
                     "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
                     "traffic": ncu_traffic(dom, f"{args.workload}_T{T}"),
                     "algorithmic_flops_per_launch": int(unit_flops * units), "unit_flops": unit_flops,
-                    "units_per_launch": units, "units": funit, "datapath": path,
+                    "units_per_launch": round(units, 2), "units": funit, "datapath": path,
                     "avg_launch_us": round(avg_s * 1e6, 2), "peak_source": pk_src}
         elif unit_bytes is not None:
-            units = mean_touched if unit.startswith("touched") else 1.0
-            alg = unit_bytes * units + fixed
+            units = (mean_touched if unit.startswith("touched") else 1.0) * per
+            alg = unit_bytes * units + fixed * per
             achieved = alg / avg_s / 1e9
             roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4),
