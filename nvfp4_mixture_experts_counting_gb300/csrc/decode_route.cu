@@ -451,14 +451,12 @@ __device__ void tk_select(const DecodeArgs& a, const TkSmem& L, unsigned char* s
   int* le = reinterpret_cast<int*>(sm + L.le_off);
   df32* lv = reinterpret_cast<df32*>(sm + L.lv_off);
   int* s_idx = reinterpret_cast<int*>(sm + L.idx_off);
-  int* flags = reinterpret_cast<int*>(sm + L.scan_off) + 32;  // [0] chain ok, [1] lowest chosen lower end, [2] nc
+  int* flags = reinterpret_cast<int*>(sm + L.scan_off) + 32;  // [2] number of re-rank candidates
   // ---- ranks (at most 4 experts per thread: E <= 1024).  Fast pass: the
   // number of keys strictly above each key (four independent counts); it is
   // the rank unless keys tie, which shows as a chosen rank held by other
   // than exactly one expert, and then the exact pass ranks ties by index.
-  int* sl_cnt = sl_e + 32;
-  if (tid < 32) sl_cnt[tid] = 0;
-  __syncthreads();
+  int* sl_cnt = sl_e + 32;  // zeroed by the caller before the logits' barrier
   int rk[4];
   const float4* k4 = reinterpret_cast<const float4*>(lg);
   const int E4 = (E + 3) >> 2;
@@ -509,26 +507,27 @@ __device__ void tk_select(const DecodeArgs& a, const TkSmem& L, unsigned char* s
     }
     __syncthreads();
   }
-  // ---- certificate
-  if (warp == 0) {
+  // ---- certificate, every warp for itself (the chosen intervals are in
+  // shared memory since the last barrier): each chosen interval above the
+  // next one, and the lowest chosen lower end
+  float lmin;
+  bool chain_ok;
+  {
     float lo = INFINITY, hi = -INFINITY;
     if (lane < k) { lo = sl_l[lane] - sl_r[lane]; hi = sl_l[lane] + sl_r[lane]; }
     const float prev_lo = __shfl_up_sync(0xffffffffu, lo, 1);
-    const bool ok = __all_sync(0xffffffffu, lane >= k || hi < (lane == 0 ? INFINITY : prev_lo));
-    float lmin = lo;
+    chain_ok = __all_sync(0xffffffffu, lane >= k || hi < (lane == 0 ? INFINITY : prev_lo));
+    lmin = lo;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lmin = fminf(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
-    if (lane == 0) { flags[0] = ok; reinterpret_cast<float*>(flags)[1] = lmin; }
   }
-  __syncthreads();
-  const float lmin = reinterpret_cast<const float*>(flags)[1];
   bool reach = false;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int e = tid + m * kRtThreads;
     if (e < E && rk[m] >= k && lg[e] + er[e] >= lmin) reach = true;
   }
-  const bool cert = __syncthreads_or(reach) == 0 && flags[0] != 0;
+  const bool cert = __syncthreads_or(reach) == 0 && chain_ok;
   if (cert) {
     if (warp == 0)
       dec_write_slots(a, t, lane, lane < k ? sl_e[lane] : 0, lane < k ? sl_l[lane] : 0.f, sl_l[0], lg, s_idx);
@@ -596,6 +595,7 @@ __global__ void __launch_bounds__(kRtThreads) k_dec_topk(DecodeArgs a) {
   pdl_wait();
   const int tid = threadIdx.x, t = blockIdx.x;
   const TkSmem L = tk_smem_layout(a.T, a.r.E, a.top_k);
+  if (tid < 32) reinterpret_cast<int*>(sm + L.sl_off)[3 * 32 + tid] = 0;  // rank counts of tk_select
   tk_logits(a, t, reinterpret_cast<float*>(sm + L.lg_off), reinterpret_cast<float*>(sm + L.er_off),
             reinterpret_cast<float*>(sm + L.hist_off));
   tk_select(a, L, sm, t);
