@@ -222,7 +222,7 @@ def decode():
     return wl, bank, layer
 
 
-@pytest.mark.parametrize("T", [1, 8, 16, 32, 40])
+@pytest.mark.parametrize("T", [1, 8, 16, 24, 32, 40])
 def test_decode_layer_matches_oracle(decode, T):
     wl, bank, layer = decode
     x = W.hidden(wl, T, device=DEV)
