@@ -328,6 +328,43 @@ def whole_job_tokens_per_s(ws: int, T: int, steps: int, ms_max: float) -> float:
     return ws * T * steps / (ms_max / 1e3)
 
 
+def kernel_roofline(kernel: str, launches: int, kernel_ms: float, steps: int, unit_bytes_info, unit_flops_info,
+                    pairs: int, T: int, touched_per_step: float, hbm_peak, fp4_peak):
+    """The dominant kernel's achieved rate against its roofline: algorithmic
+    bytes (or flops) per launch over the mean launch time.  `steps` steps
+    made `launches` launches taking `kernel_ms` in all; a step's work is
+    spread over that kernel's launches in a step (an offloaded forward
+    launches the expert kernels once per batch of slots)."""
+    avg_s = kernel_ms / launches / 1e3
+    per = steps / launches
+    unit_bytes, unit, fixed = unit_bytes_info
+    unit_flops, funit, path = unit_flops_info
+    if unit_flops is not None:
+        units = (pairs if funit == "pair" else T) * per
+        achieved = unit_flops * units / avg_s / 1e12
+        if path.startswith("nvfp4"):
+            (pk, pk_src), bound = fp4_peak, "tensor"
+        else:
+            pk, pk_src, bound = FP32_ALU_TFLOPS, FP32_ALU_SOURCE, "alu"
+        return {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1), "peak": round(pk, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / pk, 4), "traffic": None,
+                "algorithmic_flops_per_launch": int(unit_flops * units), "unit_flops": unit_flops,
+                "units_per_launch": round(units, 2), "units": funit, "datapath": path,
+                "avg_launch_us": round(avg_s * 1e6, 2), "peak_source": pk_src}
+    if unit_bytes is None:
+        return None  # no algorithmic accounting for this kernel
+    peak, peak_kind = hbm_peak
+    units = (touched_per_step if unit.startswith("touched") else 1.0) * per
+    alg = unit_bytes * units + fixed * per
+    achieved = alg / avg_s / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+            "algorithmic_bytes_per_launch": int(alg), "unit_bytes": unit_bytes,
+            "units_per_launch": round(units, 2), "units": unit,
+            "avg_launch_us": round(avg_s * 1e6, 2),
+            "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -426,36 +463,11 @@ def run_gpu(args):
     roof = None
     if dom:
         launches, kms = ktimes[dom]
-        avg_s = kms / launches / 1e3
-        # a step's work over that kernel's launches in a step (an offloaded
-        # forward launches the expert kernels once per batch of slots)
-        per = KP / launches
-        unit_bytes, unit, fixed = A.kernel_unit_bytes(dom, wl.H, I_loc, sI_loc, wl.E)
-        unit_flops, funit, path = A.kernel_unit_flops(dom, wl.H, I_loc, sI_loc, wl.E)
-        if unit_flops is not None:
-            units = (pairs if funit == "pair" else T) * per
-            achieved = unit_flops * units / avg_s / 1e12
-            if path.startswith("nvfp4"):
-                pk, pk_src, bound = fp4_peak, fp4_kind, "tensor"
-            else:
-                pk, pk_src, bound = FP32_ALU_TFLOPS, FP32_ALU_SOURCE, "alu"
-            roof = {"bound": bound, "kernel": dom, "achieved": round(achieved, 1), "peak": round(pk, 1),
-                    "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
-                    "traffic": ncu_traffic(dom, f"{args.workload}_T{T}"),
-                    "algorithmic_flops_per_launch": int(unit_flops * units), "unit_flops": unit_flops,
-                    "units_per_launch": round(units, 2), "units": funit, "datapath": path,
-                    "avg_launch_us": round(avg_s * 1e6, 2), "peak_source": pk_src}
-        elif unit_bytes is not None:
-            units = (mean_touched if unit.startswith("touched") else 1.0) * per
-            alg = unit_bytes * units + fixed * per
-            achieved = alg / avg_s / 1e9
-            roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "GB/s", "frac": round(achieved / peak, 4),
-                    "traffic": ncu_traffic(dom, f"{args.workload}_T{T}"),
-                    "algorithmic_bytes_per_launch": int(alg), "unit_bytes": unit_bytes,
-                    "units_per_launch": round(units, 2), "units": unit,
-                    "avg_launch_us": round(avg_s * 1e6, 2),
-                    "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+        roof = kernel_roofline(dom, launches, kms, KP, A.kernel_unit_bytes(dom, wl.H, I_loc, sI_loc, wl.E),
+                               A.kernel_unit_flops(dom, wl.H, I_loc, sI_loc, wl.E), pairs, T, mean_touched,
+                               (peak, peak_kind), (fp4_peak, fp4_kind))
+        if roof:
+            roof["traffic"] = ncu_traffic(dom, f"{args.workload}_T{T}")
     shares = {k: {"launches": v[0], "ms": round(v[1], 3), "share": round(v[1] / total_k, 4)}
               for k, v in ktimes.items()}
 
@@ -673,19 +685,12 @@ def run_stack(args):
     total_k = sum(v[1] for v in ktimes.values()) or 1.0
     dom = max(ktimes.items(), key=lambda kv: kv[1][1])[0] if ktimes else None
     roof = None
-    if dom:
+    if dom and A.kernel_unit_bytes(dom, wl.H, wl.I, wl.I_s, wl.E)[0] is not None:
         launches, kms = ktimes[dom]
-        avg_s = kms / launches / 1e3
-        unit_bytes, unit, fixed = A.kernel_unit_bytes(dom, wl.H, wl.I, wl.I_s, wl.E)
-        if unit_bytes is not None:
-            units = touched_per_layer if unit.startswith("touched") else 1.0
-            alg = unit_bytes * units + fixed
-            achieved = alg / avg_s / 1e9
-            roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom, f"{args.workload}_T{T}"),
-                    "algorithmic_bytes_per_launch": int(alg), "unit_bytes": unit_bytes,
-                    "units_per_launch": round(units, 2), "units": unit, "avg_launch_us": round(avg_s * 1e6, 2),
-                    "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+        # one launch per layer: a "step" of the helper is one layer
+        roof = kernel_roofline(dom, launches, kms, launches, A.kernel_unit_bytes(dom, wl.H, wl.I, wl.I_s, wl.E),
+                               (None, None, None), T * wl.top_k, T, touched_per_layer, (peak, peak_kind), (None, None))
+        roof["traffic"] = ncu_traffic(dom, f"{args.workload}_T{T}")
     shares = {k: {"launches": v[0], "ms": round(v[1], 3), "share": round(v[1] / total_k, 4)}
               for k, v in ktimes.items()}
 

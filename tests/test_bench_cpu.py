@@ -1,0 +1,57 @@
+"""Host-side arithmetic of bench.py's dominant-kernel roofline (no GPU):
+algorithmic bytes or flops per launch over the mean launch time, with a
+step's work spread over the kernel's launches in a step."""
+
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from nvfp4_mixture_experts_counting_gb300 import accounting as A  # noqa: E402
+
+H, I, IS, E = 2560, 640, 640, 256
+HBM = (6786.0, "measured")
+FP4 = (11580.0, "measured x 6")
+
+
+def test_one_launch_per_step_hbm():
+    # 500 steps, one gate_up launch each, 24.8 ms in all: 49.6 us per launch
+    r = bench.kernel_roofline("k_dtc_gate_up", 500, 24.8, 500, A.kernel_unit_bytes("k_dtc_gate_up", H, I, IS, E),
+                              A.kernel_unit_flops("k_dtc_gate_up", H, I, IS, E), 128, 16, 102.75, HBM, FP4)
+    alg = 1_848_320 * 102.75 + 2 * IS * H * 2
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["algorithmic_bytes_per_launch"] == int(alg)
+    assert r["avg_launch_us"] == pytest.approx(49.6)
+    assert r["achieved"] == pytest.approx(alg / 49.6e-6 / 1e9, rel=1e-4)
+    assert r["frac"] == pytest.approx(r["achieved"] / HBM[0], rel=1e-3)
+
+
+def test_batched_launches_split_the_step():
+    # an offloaded forward: two gate_up launches per step, each half the work
+    one = bench.kernel_roofline("k_dtc_gate_up", 100, 5.0, 100, A.kernel_unit_bytes("k_dtc_gate_up", H, I, IS, E),
+                                (None, None, None), 128, 16, 100.0, HBM, FP4)
+    two = bench.kernel_roofline("k_dtc_gate_up", 200, 5.0, 100, A.kernel_unit_bytes("k_dtc_gate_up", H, I, IS, E),
+                                (None, None, None), 128, 16, 100.0, HBM, FP4)
+    assert two["units_per_launch"] == pytest.approx(one["units_per_launch"] / 2)
+    assert two["algorithmic_bytes_per_launch"] == pytest.approx(one["algorithmic_bytes_per_launch"] / 2, abs=1)
+    # half the bytes in half the time per launch: the same rate
+    assert two["achieved"] == pytest.approx(one["achieved"], rel=1e-4)
+
+
+def test_tensor_bound_flops_per_pair():
+    pairs = 4096 * 8
+    r = bench.kernel_roofline("k_pf_gate_up", 6, 6 * 0.157, 6, A.kernel_unit_bytes("k_pf_gate_up", H, I, IS, E),
+                              A.kernel_unit_flops("k_pf_gate_up", H, I, IS, E), pairs, 4096, 171.0, HBM, FP4)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["algorithmic_flops_per_launch"] == 2 * H * 2 * I * pairs
+    assert r["achieved"] == pytest.approx(2 * H * 2 * I * pairs / 157e-6 / 1e12, rel=1e-3)
+    assert r["peak"] == pytest.approx(FP4[0])
+
+
+def test_kernel_without_accounting_has_no_roofline():
+    assert bench.kernel_roofline("k_sort", 10, 1.0, 10, A.kernel_unit_bytes("k_sort", H, I, IS, E),
+                                 A.kernel_unit_flops("k_sort", H, I, IS, E), 128, 16, 100.0, HBM, FP4) is None
