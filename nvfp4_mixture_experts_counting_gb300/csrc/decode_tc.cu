@@ -8,7 +8,11 @@
 // tokens are N, so the SMs only issue TMA copies and MMAs while the weight
 // bytes stream; E2M1 values never pass through the CUDA cores.
 //
-//   k_dec_route      (decode_route.cu) routing and the activation codes
+//   k_dtc_router     router logits per K chunk on the tensor cores, the
+//                    activation codes, sigma and the x-norm bound (or, where
+//                    the chunks do not fit, k_dec_route in decode_route.cu)
+//   k_dec_topk       (decode_route.cu) one CTA per token: top-k, certificate,
+//                    the token's bits in the expert masks
 //   k_dtc_gate_up    work units: (touched expert, 64 gate + 64 up window rows)
 //                    against every token's resident activation codes, and
 //                    (shared expert, 64 + 64 bf16 rows) against bf16 x; the
@@ -341,11 +345,11 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   const int Us = Js;         // shared units: window tiles of 64 gate + 64 up rows
   const int row0 = a.win.row0, Iw = a.win.Iw;
   const uint32_t id_f4 = idesc_nvf4(128, npad), id_bf = idesc_bf16(128, npad);
-  // Two phases.  0: the shared expert's units (they need only x, so they run
-  // while the routing kernels still work), round-robin over the CTAs; 1:
-  // after the routing is known, a contiguous range of the routed units
-  // (touched expert, 64-row window tile) that balances the CTAs' whole
-  // loads.  Ring positions carry over.
+  // Two phases.  0: the shared expert's units, one whole-K unit per 64 + 64
+  // window rows on the first CTAs (they need only x, so they run while the
+  // routing kernels still work); 1: after the routing is known, the routed
+  // units (touched expert, 64-row window tile), handed out as below.  Ring
+  // positions carry over.
   int kk = 0, ui = 0, uu = 0, nt = 0, r0 = 0, R = 0;
   int qn = 0;  // phase-1 unit queue entries this thread has produced or consumed
   // When a whole forward has more routed units than CTAs it hands them out
@@ -355,7 +359,8 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   // them to the other roles through a queue of 8 entries (at most about 3
   // units are in flight in a CTA: the ring holds less than a unit and the
   // accumulators two).  With fewer units than CTAs (one token), and for
-  // offload batches, the static balanced split.
+  // offload batches, a contiguous range per CTA that balances the CTAs'
+  // whole loads (dtc_split).
   bool dyn_units = false;
   // the next unit of this role: the static range, or the queue
   auto next_unit = [&](int it, int phase, int* rr) -> bool {
