@@ -55,3 +55,32 @@ def test_tensor_bound_flops_per_pair():
 def test_kernel_without_accounting_has_no_roofline():
     assert bench.kernel_roofline("k_sort", 10, 1.0, 10, A.kernel_unit_bytes("k_sort", H, I, IS, E),
                                  A.kernel_unit_flops("k_sort", H, I, IS, E), 128, 16, 100.0, HBM, FP4) is None
+
+
+# ---- the algorithmic byte and flop counts, against hand-worked figures of
+# the bank format (E2M1 codes at 1/2 byte, one E4M3 scale per 16 elements,
+# one fp32 global per row; the down globals cover all H rows in any window)
+
+@pytest.mark.parametrize("H,I,full", [(256, 64, 29_184), (2560, 640, 2_780_160), (4096, 2048, 14_188_544)])
+def test_expert_bytes_full_bank(H, I, full):
+    assert A.expert_window_bytes(H, I) == full
+
+
+def test_expert_bytes_half_window_keeps_every_down_global():
+    # gate_up: 2 * 320 rows * (1280 + 160 + 4); down: 2560 rows * (160 + 20 + 4)
+    assert A.gate_up_window_bytes(2560, 320) == 924_160
+    assert A.down_window_bytes(2560, 320) == 471_040
+    assert A.expert_window_bytes(2560, 320) == 1_395_200
+
+
+def test_shared_expert_and_routed_flops():
+    # bf16 gate/up rows and down columns (9,830,400 B) plus the bf16 gate vector
+    assert A.shared_window_bytes(2560, 640) == 9_830_400 + 2560 * 2
+    # 2 flops per multiply-add: gate_up 2*H*2I and down 2*I*H per pair, 8 pairs a token
+    assert A.routed_flops(2560, 640, 8) == 78_643_200
+
+
+@pytest.mark.parametrize("T,touched,mb", [(1, 8, 34.7), (16, 102, 296.2)])
+def test_decode_layer_bytes(T, touched, mb):
+    # touched experts + shared expert + fp32 router + x in and bf16 out
+    assert A.layer_touched_bytes(2560, 256, 640, 640, T, touched) / 1e6 == pytest.approx(mb, abs=0.05)
