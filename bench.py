@@ -63,9 +63,19 @@ def parse_args():
     p.add_argument("--layers", type=int, default=0,
                    help="independently seeded layers rotated per step (default: 8 for decode, 2 for prefill)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="decode workload: leave out the prefill half of the metric (T=16384 and 4096)")
     p.add_argument("--slots-frac", type=float, default=0.37,
                    help="offload workload: HBM slots as a fraction of the experts (byte budget of full windows)")
     p.add_argument("--iloc", type=int, default=0, help="load and run the window [0, iloc) (0: all of I)")
+    p.add_argument("--compare", choices=["none", "ep"], default="none",
+                   help="ep: time each rank's compute of the intermediate split against expert "
+                        "parallelism, on this one GPU (a comparison, not the benchmark line)")
+    p.add_argument("--ranks", type=int, default=2, help="--compare ep: ranks to emulate")
+    p.add_argument("--split", choices=["replicas", "window"], default="replicas",
+                   help="N>1: replicas run their own tokens with no collective (default); window splits "
+                        "the intermediate axis over the ranks, which exchange their fp32 partials "
+                        "(NCCL all-gather) and sum them in rank order")
     return p.parse_args()
 
 
@@ -91,6 +101,17 @@ def load_peaks():
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 FP32_ALU_SOURCE = "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz (nominal)"
 FP4_PER_BF16 = 13.5 / 2.25  # nominal dense NVFP4 / BF16 tensor rates
+
+
+def load_bf16_peak():
+    """Dense bf16 tensor peak: the measured cuBLAS bf16 burst rate, else the
+    1.9 PFLOP/s fallback."""
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+    except Exception:
+        return 1900.0, "fallback bf16 1.9 PFLOP/s"
 
 
 def load_fp4_peak():
@@ -259,7 +280,7 @@ def cpu_threads() -> int:
 
 # ------------------------------------------------------------------ GPU arm
 
-def build_layers(wl, n_layers, max_tokens, dev, hbm_slot_bytes=0, I_loc=0):
+def build_layers(wl, n_layers, max_tokens, dev, hbm_slot_bytes=0, I_loc=0, i0=0):
     import torch
     from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
     cfg = ftmoe.make_config(H=wl.H, I=wl.I, E=wl.E, top_k=wl.top_k, I_shared=wl.I_s,
@@ -291,7 +312,7 @@ def build_layers(wl, n_layers, max_tokens, dev, hbm_slot_bytes=0, I_loc=0):
         sgu, sdn, sg = W.shared_weights(wl, l, device=dev)
         desc = ftmoe.bank_desc(rw, rb, q["gu_codes"], q["gu_scales"], q["gu_global"], q["dn_codes"],
                                q["dn_scales"], q["dn_global"], sgu, sdn, sg, on_device=True)
-        layer.load_bank(l, desc, 0, I_loc or None)
+        layer.load_bank(l, desc, i0, I_loc or None)
         del q
         torch.cuda.synchronize()
     return layer
@@ -328,6 +349,22 @@ def whole_job_tokens_per_s(ws: int, T: int, steps: int, ms_max: float) -> float:
     return ws * T * steps / (ms_max / 1e3)
 
 
+def window_of_rank(rank: int, ws: int, I: int):
+    """(i0, I_loc) of rank `rank` when the intermediate axis is split over
+    `ws` ranks: contiguous equal windows in rank order, each a multiple of 16
+    (the NVFP4 block), as the pages' TP patch splits I."""
+    if I % ws or (I // ws) % 16:
+        raise ValueError(f"I={I} does not split into {ws} windows of a multiple of 16")
+    w = I // ws
+    return rank * w, w
+
+
+def window_tokens_per_s(T: int, steps: int, ms_max: float) -> float:
+    """Window split: every rank works on the same T tokens, so the job's
+    tokens are T per step whatever the number of ranks."""
+    return T * steps / (ms_max / 1e3)
+
+
 def kernel_roofline(kernel: str, launches: int, kernel_ms: float, steps: int, unit_bytes_info, unit_flops_info,
                     pairs: int, T: int, touched_per_step: float, hbm_peak, fp4_peak):
     """The dominant kernel's achieved rate against its roofline: algorithmic
@@ -344,6 +381,8 @@ def kernel_roofline(kernel: str, launches: int, kernel_ms: float, steps: int, un
         achieved = unit_flops * units / avg_s / 1e12
         if path.startswith("nvfp4"):
             (pk, pk_src), bound = fp4_peak, "tensor"
+        elif path.startswith("bf16"):
+            (pk, pk_src), bound = load_bf16_peak(), "tensor"
         else:
             pk, pk_src, bound = FP32_ALU_TFLOPS, FP32_ALU_SOURCE, "alu"
         return {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1), "peak": round(pk, 1),
@@ -363,6 +402,128 @@ def kernel_roofline(kernel: str, launches: int, kernel_ms: float, steps: int, un
             "units_per_launch": round(units, 2), "units": unit,
             "avg_launch_us": round(avg_s * 1e6, 2),
             "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+
+
+def prefill_leg(T, K, Wm, rank, ws, local, cpu_baseline: bool):
+    """The prefill-shaped layer (Zipf-biased routing) timed the same way as
+    the headline: K steps after Wm warm-up steps, CUDA events on the launch
+    stream around the steps alone, two independently seeded layers rotated
+    (1.4 GB of banks, far larger than L2).  Returns the sub-report: tokens/s,
+    the routed GEMM's roofline against the NVFP4 peak, the layer's fraction
+    of the NVFP4 peak and of its combined roofline, kernel shares, clocks and
+    the oracle's rate on a token sample."""
+    import torch
+    from nvfp4_mixture_experts_counting_gb300 import accounting as A
+    from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
+    wl = W.WORKLOADS["prefill"]
+    L = 2
+    layer = build_layers(wl, L, T, "cuda")
+    xs = [W.hidden(wl, T, step=replica_step_seed(rank, s), device="cuda") for s in range(2)]
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        layer.forward(i % L, xs[i % 2], out, stream=stream)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    rerank0 = layer.stats(0).reranked_tokens
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    _barrier_and_sync(ws)
+    t_wall0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(K):
+        step(Wm + i)
+    ev1.record(stream)
+    _barrier_and_sync(ws)
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    reranked = layer.stats(0).reranked_tokens - rerank0
+    ms_max = _max_over_ranks(ws, ev0.elapsed_time(ev1))
+    value = whole_job_tokens_per_s(ws, T, K, ms_max)
+    t_step = ms_max / K / 1e3
+
+    KP = min(K, 10)
+    ftmoe.ftmoe_profile_enable(layer.handle, True)
+    ftmoe.ftmoe_profile_read(layer.handle)
+    for i in range(KP):
+        step(i)
+    torch.cuda.synchronize()
+    ktimes = ftmoe.ftmoe_profile_read(layer.handle)
+    ftmoe.ftmoe_profile_enable(layer.handle, False)
+
+    offs = torch.empty((wl.E + 1,), dtype=torch.int32, device="cuda")
+    aux = ftmoe.Aux(None, None, offs.data_ptr(), None, None)
+    touched = []
+    for li in range(L):
+        layer.forward(li, xs[li % 2], out, aux=aux, stream=stream)
+        o = offs.cpu()
+        touched.append(int(((o[1:] - o[:-1]) > 0).sum()))
+    mean_touched = sum(touched) / len(touched)
+
+    hbm, hbm_kind = load_peaks()
+    fp4, fp4_kind = load_fp4_peak()
+    bf16, _ = load_bf16_peak()
+    pairs = T * wl.top_k
+    total_k = sum(v[1] for v in ktimes.values()) or 1.0
+    roof = {}
+    for kname in ("k_pf_gate_up", "k_pf_down"):
+        if kname in ktimes:
+            launches, kms = ktimes[kname]
+            r = kernel_roofline(kname, launches, kms, KP, A.kernel_unit_bytes(kname, wl.H, wl.I, wl.I_s, wl.E),
+                                A.kernel_unit_flops(kname, wl.H, wl.I, wl.I_s, wl.E), pairs, T, mean_touched,
+                                (hbm, hbm_kind), (fp4, fp4_kind))
+            r["traffic"] = ncu_traffic(kname, f"prefill_T{T}")
+            roof[kname] = r
+    comb = A.combined_ideal_seconds(wl.H, wl.E, wl.I, wl.I_s, T, pairs, mean_touched, fp4, bf16, hbm)
+    routed = A.routed_flops(wl.H, wl.I, pairs)
+    cpu = None
+    if cpu_baseline and rank == 0:
+        th = cpu_threads()
+        n_tok = 4
+        try:
+            secs = sum(oracle_times("prefill", T, n_tok, 1, 1e9, th))
+            cpu = {"value": round(n_tok / secs, 4), "unit": "tokens/s", "cores": th, "kind": "oracle",
+                   "sample": f"{n_tok} tokens of one seeded T={T} batch of the prefill layer (their experts' "
+                             f"banks quantised beforehand, untimed); numpy fp64, BLAS threads={th}"}
+        except Exception as ex:
+            cpu = {"value": None, "unit": "tokens/s", "cores": th, "kind": "oracle", "sample": f"failed: {ex}"}
+    res = {
+        "workload": f"prefill layer: H={wl.H} I={wl.I} I_s={wl.I_s} E={wl.E} top_k={wl.top_k}, T={T}, "
+                    f"full I window, Zipf(1.1) router bias",
+        "value": round(value, 1), "unit": "tokens/s", "steps": K, "warmup": Wm,
+        "ms_per_step": round(ms_max / K, 4),
+        "l2": f"inputs larger than L2: {L} independently seeded layers rotated per step "
+              f"({L} x {A.expert_window_bytes(wl.H, wl.I) * wl.E / 1e6:.0f} MB of banks)",
+        "touched_experts_per_step": round(mean_touched, 2),
+        "reranked_tokens_per_step": round(reranked / K, 2),
+        "routed_fp4_tflops": round(routed / t_step / 1e12, 1),
+        "routed_frac_of_fp4_peak": round(routed / t_step / 1e12 / fp4, 4),
+        "fp4_peak_tflops": round(fp4, 1), "fp4_peak_source": fp4_kind,
+        "combined_roofline": {"frac": round(comb["bound_s"] / t_step, 4), "bound": comb["bound"],
+                              "ideal_us": round(comb["bound_s"] * 1e6, 2),
+                              "tensor_us": round(comb["tensor_s"] * 1e6, 2),
+                              "hbm_us": round(comb["hbm_s"] * 1e6, 2),
+                              "note": "routed FP4 flops at the NVFP4 peak + shared-expert flops at the bf16 "
+                                      "peak + 3 x router flops (three exact bf16 parts) at the bf16 peak, "
+                                      "against touched bytes at the HBM peak; frac = ideal / measured step"},
+        "roofline": roof.get("k_pf_gate_up"),
+        "roofline_down": roof.get("k_pf_down"),
+        "kernel_shares": {k: {"launches": v[0], "ms": round(v[1], 3), "share": round(v[1] / total_k, 4)}
+                          for k, v in ktimes.items()},
+        "gpu_launches": int(round(sum(v[0] for v in ktimes.values()) * K / KP)),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "cpu_baseline": cpu,
+    }
+    layer.close()
+    del xs, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_gpu(args):
@@ -385,21 +546,39 @@ def run_gpu(args):
     offload = args.workload == "offload"
     L = args.layers or (1 if offload else (8 if T <= 32 else 2))
     dev = "cuda"
-    I_loc = args.iloc or wl.I
+    split = args.split == "window"
+    if split:
+        if offload or args.iloc:
+            raise SystemExit("--split window runs the resident layer over its whole I")
+        i0, I_loc = window_of_rank(rank, ws, wl.I)
+    else:
+        i0, I_loc = 0, args.iloc or wl.I
     sI_loc = I_loc * wl.I_s // wl.I
     # offload: the slot budget is a fraction of the experts at full-window
     # bytes; a narrower window keeps the byte budget (more, smaller slots)
     slot_bytes = int(round(args.slots_frac * wl.E)) * A.expert_window_bytes(wl.H, wl.I) if offload else 0
-    layer = build_layers(wl, L, T, dev, hbm_slot_bytes=slot_bytes, I_loc=I_loc)
+    layer = build_layers(wl, L, T, dev, hbm_slot_bytes=slot_bytes, I_loc=I_loc, i0=i0)
     # offload: a fresh input every step (the slot cache must not see repeats);
     # otherwise 8 inputs in turn
     NX = (K + Wm) if offload else 8
-    xs = [W.hidden(wl, T, step=replica_step_seed(rank, s), device=dev) for s in range(NX)]
+    # replicas draw their own tokens; the ranks of a window split share them
+    xs = [W.hidden(wl, T, step=replica_step_seed(0 if split else rank, s), device=dev) for s in range(NX)]
     out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
+    part = torch.empty((T, wl.H), dtype=torch.float32, device=dev) if split else None
+    parts = torch.empty((ws, T, wl.H), dtype=torch.float32, device=dev) if split and ws > 1 else part
 
     def step(i, o=out, x=None):
-        layer.forward(i % L, xs[i % NX] if x is None else x, o, I_loc=I_loc, stream=stream)
+        xi = xs[i % NX] if x is None else x
+        if not split:
+            layer.forward(i % L, xi, o, i0=i0, I_loc=I_loc, stream=stream)
+            return
+        # this rank's window partial, every rank's partial gathered, summed in
+        # rank order and rounded once
+        layer.forward(i % L, xi, part, out_flags=ftmoe.OUT_FP32, i0=i0, I_loc=I_loc, stream=stream)
+        if ws > 1:
+            dist.all_gather_into_tensor(parts, part)
+        ftmoe.ftmoe_reduce_partials(parts, ws, T * wl.H, o, ftmoe.OUT_BF16, stream=stream)
 
     for i in range(Wm):
         step(i)
@@ -427,7 +606,7 @@ def run_gpu(args):
     st_after = layer.stats(0)
     reranked = st_after.reranked_tokens - rerank0
     ms_max = _max_over_ranks(ws, ms)
-    value = whole_job_tokens_per_s(ws, T, K, ms_max)
+    value = window_tokens_per_s(T, K, ms_max) if split else whole_job_tokens_per_s(ws, T, K, ms_max)
 
     # ---- per-kernel durations: a second pass of the same steps with CUDA
     # events around every kernel on the launch stream
@@ -446,7 +625,7 @@ def run_gpu(args):
     touched = {}
     for li in range(L):
         for xi in range(NX):
-            layer.forward(li, xs[xi], out, I_loc=I_loc, aux=aux, stream=stream)
+            layer.forward(li, xs[xi], out, i0=i0, I_loc=I_loc, aux=aux, stream=stream)
             o = offs.cpu()
             touched[(li, xi)] = int(((o[1:] - o[:-1]) > 0).sum())
     per_step_touched = [touched[((Wm + i) % L, (Wm + i) % NX)] for i in range(K)]
@@ -513,7 +692,7 @@ def run_gpu(args):
     e1.record(stream)
     _barrier_and_sync(ws)
     e2e_ms = _max_over_ranks(ws, e0.elapsed_time(e1))
-    e2e_value = whole_job_tokens_per_s(ws, T, K, e2e_ms)
+    e2e_value = window_tokens_per_s(T, K, e2e_ms) if split else whole_job_tokens_per_s(ws, T, K, e2e_ms)
 
     # ---- GPU launch count inside the timed region (the profiled pass counts
     # the launches of KP steps)
@@ -532,24 +711,36 @@ def run_gpu(args):
         except Exception as ex:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "tokens/s", "cores": th, "kind": "oracle", "sample": f"failed: {ex}"}
 
+    # the prefill half of the metric, on the default decode run
+    prefill = None
+    if args.workload == "decode" and not args.no_prefill and not split:
+        layer.close()
+        torch.cuda.empty_cache()
+        prefill = {f"T{Tp}": prefill_leg(Tp, Kp, 3, rank, ws, local, not args.no_cpu_baseline)
+                   for Tp, Kp in ((16384, 20), (4096, 40))}
+
     if rank == 0:
         cl = clocks.summary(t_wall0, t_wall1)
         line = {
-            "metric": "MoE-layer tokens/s at 1 GB300 (decode: % of HBM peak over touched bytes)",
+            "metric": "MoE-layer tokens/s at 1 GB300; % of HBM peak (decode) / NVFP4 tensor peak (prefill)",
             "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
-            "ms_per_step": round(ms_max / K, 5), "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
+            "scaling": "strong" if split else "weak",
             "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate); bf16 shared expert",
             "data": "synthetic, seeded",
             "config": {"workload": f"{args.workload} layer: H={wl.H} I={wl.I} I_s={wl.I_s} E={wl.E} "
                                    f"top_k={wl.top_k}, T={T}, "
-                                   + (f"window [0, {I_loc})" if I_loc != wl.I else "full I window")
+                                   + (f"window [{i0}, {i0 + I_loc}) per rank" if split else
+                                      f"window [0, {I_loc})" if I_loc != wl.I else "full I window")
                                    + (", Zipf(1.1) router bias" if wl.router_bias else "")
                                    + (f", offloaded banks, HBM slots for {args.slots_frac:.0%} of the experts"
                                       if offload else ""),
-                       "global_batch": T * ws, "layers_rotated": L,
+                       "global_batch": T if split else T * ws, "layers_rotated": L,
                        "l2": f"inputs larger than L2: {L} independently seeded layers rotated per step "
                              f"({L} x {A.expert_window_bytes(wl.H, I_loc) * wl.E / 1e6:.0f} MB of banks)",
-                       "parallelism": f"replicas x{ws} (token-parallel, no collective)"},
+                       "parallelism": (f"intermediate axis split over {ws} ranks: fp32 partials, NCCL "
+                                       f"all-gather, fixed rank-order sum" if split else
+                                       f"replicas x{ws} (token-parallel, no collective)")},
             "touched_experts_per_step": round(mean_touched, 2),
             **({"offload": {"slots": st_after.resident_slots, "residency": round(st_after.residency, 4),
                             "hit_rate": round((st_after.hits - st_before.hits) /
@@ -575,6 +766,7 @@ def run_gpu(args):
                     "d2h_bytes_per_step": T * wl.H * 2},
             "clocks": cl,
             "cpu_baseline": cpu,
+            **({"prefill": prefill} if prefill else {}),
         }
         print(json.dumps(line), flush=True)
     layer.close()
@@ -600,7 +792,7 @@ def run_reference(args):
     value = n / tot
     line = {
         "impl": "reference",
-        "metric": "MoE-layer tokens/s at 1 GB300 (decode: % of HBM peak over touched bytes)",
+        "metric": "MoE-layer tokens/s at 1 GB300; % of HBM peak (decode) / NVFP4 tensor peak (prefill)",
         "value": round(value, 4), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
         "ms_per_step": round(1e3 * tot / n, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic, seeded",
@@ -711,7 +903,7 @@ def run_stack(args):
 
     if rank == 0:
         line = {
-            "metric": "MoE-layer tokens/s at 1 GB300 (decode: % of HBM peak over touched bytes)",
+            "metric": "MoE-layer tokens/s at 1 GB300; % of HBM peak (decode) / NVFP4 tensor peak (prefill)",
             "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
             "ms_per_step": round(ms_max / K, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate); bf16 shared expert",
@@ -745,10 +937,85 @@ def run_stack(args):
         dist.destroy_process_group()
 
 
+def _kernel_ms_per_step(layer, fn, K):
+    """Summed CUDA-event times of the library's kernels per call of fn()."""
+    import torch
+    from nvfp4_mixture_experts_counting_gb300 import ftmoe
+    ftmoe.ftmoe_profile_enable(layer.handle, True)
+    ftmoe.ftmoe_profile_read(layer.handle)
+    for _ in range(K):
+        fn()
+    torch.cuda.synchronize()
+    kt = ftmoe.ftmoe_profile_read(layer.handle)
+    ftmoe.ftmoe_profile_enable(layer.handle, False)
+    return sum(v[1] for v in kt.values()) / K
+
+
+def run_compare(args):
+    """The two ways to put one MoE layer on G GPUs, each rank's compute timed
+    on this one GPU: the pages' intermediate split (rank r runs window r of
+    every expert: balanced by construction, one all-reduce of [T, H]) and
+    expert parallelism (rank r owns the experts e % G == r: its load follows
+    the routing, two all-to-alls of the dispatched rows, padded to T * top_k
+    rows for static shapes).  A step of either takes its slowest rank's time;
+    the collectives are reported as the bytes each rank sends, not timed
+    (this run has one GPU)."""
+    import numpy as np
+    import torch
+    from nvfp4_mixture_experts_counting_gb300 import build as B
+    B.build()
+    from nvfp4_mixture_experts_counting_gb300 import ftmoe, workloads as W
+    G, K = args.ranks, max(args.steps, 5)
+    out_lines = {}
+    for wname, T in (("decode", 16), ("prefill", 4096)):
+        wl = W.WORKLOADS[wname]
+        layer = build_layers(wl, 1, T, "cuda")
+        x = W.hidden(wl, T, step=7, device="cuda")
+        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+        aux_idx = torch.empty((T, wl.top_k), dtype=torch.int32, device="cuda")
+        layer.forward(0, x, out, aux=ftmoe.Aux(aux_idx.data_ptr(), None, None, None, None))
+        torch.cuda.synchronize()
+        idx = aux_idx.cpu().numpy()
+        full_ms = _kernel_ms_per_step(layer, lambda: layer.forward(0, x, out), K)
+        win, ep, pairs = [], [], []
+        for r in range(G):
+            i0, I_loc = window_of_rank(r, G, wl.I)
+            win.append(_kernel_ms_per_step(layer, lambda: layer.forward(0, x, out, i0=i0, I_loc=I_loc), K))
+            mask = (np.arange(wl.E) % G == r).astype(np.uint8)
+            ep.append(_kernel_ms_per_step(
+                layer, lambda: ftmoe.ftmoe_forward_experts(layer.handle, 0, x, T, out, ftmoe.OUT_BF16, mask), K))
+            pairs.append(int(np.isin(idx, np.nonzero(mask)[0]).sum()))
+        layer.close()
+        torch.cuda.empty_cache()
+        mean_pairs = T * wl.top_k / G
+        out_lines[f"{wname}_T{T}"] = {
+            "workload": f"{wname} layer: H={wl.H} I={wl.I} E={wl.E} top_k={wl.top_k}, T={T}"
+                        + (", Zipf(1.1) router bias" if wl.router_bias else ""),
+            "ranks": G,
+            "full_layer_kernel_ms": round(full_ms, 4),
+            "window_split": {"rank_kernel_ms": [round(v, 4) for v in win], "step_ms": round(max(win), 4),
+                             "allreduce_bytes_per_rank": T * wl.H * 2,
+                             "note": "rank r: window [r*I/G, (r+1)*I/G) of every expert and of the shared "
+                                     "expert, router and shared gate replicated"},
+            "expert_parallel": {"rank_kernel_ms": [round(v, 4) for v in ep], "step_ms": round(max(ep), 4),
+                                "rank_pairs": pairs, "pair_imbalance_max_over_mean": round(max(pairs) / mean_pairs, 3),
+                                "alltoall_bytes_per_rank_padded": 2 * T * wl.top_k * wl.H * 2,
+                                "note": "rank r: the routed slots of experts e % G == r (routing replicated); "
+                                        "the shared expert's time is not in these figures"},
+            "speedup_window_over_expert": round(max(ep) / max(win), 3),
+        }
+    line = {"mode": "window split vs expert parallel, per-rank kernel time on one GB300",
+            "unit": "ms", "steps": K, "comparison": out_lines,
+            "note": "kernel times are CUDA-event sums over the library's kernels per call; collectives not timed"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.compare == "ep":
+        run_compare(args)
     elif args.workload == "stack48":
         run_stack(args)
     else:

@@ -70,11 +70,17 @@ typedef enum {
   FTMOE_ERR_TOO_LARGE = -11        /* sizes exceed the fixed scratch of ftmoe_route_static */
 } ftmoe_status;
 
-/* out_flags of ftmoe_forward: the output type, optionally OR-ed with ACCUMULATE */
+/* out_flags of ftmoe_forward: the output type, optionally OR-ed with
+ * ACCUMULATE and with ACT_BF16 */
 enum {
   FTMOE_OUT_BF16 = 0,        /* out is bf16 [T, H] */
   FTMOE_OUT_FP32 = 1,        /* out is fp32 [T, H] */
-  FTMOE_OUT_ACCUMULATE = 0x100 /* fp32 only: out += this window's partial, one rounding per add */
+  FTMOE_OUT_ACCUMULATE = 0x100, /* fp32 only: out += this window's partial, one rounding per add */
+  FTMOE_ACT_BF16 = 0x200     /* W4A16 numerics: the routed experts take the bf16 x as it is and keep
+                                their intermediate in bf16, weights dequantised in registers (the
+                                weight-only 4-bit kernel the pages' review thread selects, [PR385]
+                                mirror, kernel-selection fix); CUDA cores, meant for decode sizes;
+                                resident mode only.  Default (flag clear): W4A4, activations NVFP4. */
 };
 
 typedef struct ftmoe_handle ftmoe_handle; /* opaque; library-owned */
@@ -142,11 +148,22 @@ typedef struct {
 } ftmoe_stats;
 
 /* Create a handle on CUDA device `device` for layers of the given shape.
+ * The shape is that of one MoE layer of the pages' model: E routed experts
+ * with top_k chosen per token, gate_up [2I, H] and down [H, I] per expert,
+ * a shared expert of intermediate I_shared gated by sigmoid(g . x)
+ * ([PR385] "What this adds", first and third bullets; [I62] "What it
+ * touches" for the [2I, H] / [H, I] shapes).  hbm_slot_bytes > 0 selects the
+ * offload backend the pages are about: banks in pinned host memory and a
+ * fraction of the experts resident in HBM slots ([PR385] "What this adds";
+ * [I62] "Why TP=2 loses today").
  * Allocates the workspace for config->max_tokens (offload mode: also the
  * copy stream; the HBM slot pool follows at the first ftmoe_load_bank, once
- * the record size is known).  Validates the config (INVALID_ARG, ALIGNMENT)
- * and the device (DEVICE).  On success *out owns everything until
- * ftmoe_destroy. */
+ * the record size is known), so that a forward allocates nothing and, in
+ * resident mode, can be captured in a CUDA graph ([I62] "The fix that
+ * fits": "CUDA graphs unaffected. Shapes stay static").  Validates the config
+ * (INVALID_ARG, ALIGNMENT) and the device (DEVICE).  On success *out owns
+ * everything until ftmoe_destroy; on failure *out is NULL and nothing is
+ * left allocated. */
 int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out);
 
 /* Load layer `layer`'s weights, keeping the intermediate window
@@ -166,6 +183,16 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* desc, int
 /* One forward of layer `layer` over T tokens (0 <= T <= max_tokens) for the
  * intermediate window [i0, i0 + I_loc), which must lie inside the loaded
  * window (SLICE_OUT_OF_RANGE) and be 16-aligned (ALIGNMENT).
+ * It computes the partial output that a tensor-parallel rank owning that
+ * window of every expert and of the shared expert would compute: the
+ * replicated router, softmax and top-k (renormalised when norm_topk_prob is
+ * set), the windowed gate_up rows, SwiGLU, the windowed down columns, and
+ * routed + sigmoid(gate) * shared formed before any reduction ([PR385] "What
+ * this adds", first to third bullets; [I62] "The fix that fits": the down
+ * projection yields partial sums, and its first comment: norm_topk_prob and
+ * a replicated router make the plain SUM of the partials exact).  The sums
+ * run in a fixed order with no atomics on values, so a repeated call gives
+ * the same bits ([PR385] "Correctness").
  *   x:   device, bf16 [T, H]
  *   out: device, [T, H] of the type out_flags names; must not alias x.
  *        With FTMOE_OUT_ACCUMULATE (fp32 only) the window's partial is added
@@ -201,7 +228,41 @@ int ftmoe_forward_stack(ftmoe_handle* h, const void* x, int T, void* out, ftmoe_
  * or H, T < 0. */
 int ftmoe_rms_renorm(const float* y, void* x, int T, int H, ftmoe_stream_t stream);
 
-/* Release everything the handle owns.  Safe on NULL. */
+/* The routed part of layer `layer` restricted to a subset of the experts:
+ *   out_t = sum over the slots j of token t whose expert is in the subset of
+ *           w_tj * Y_(t,j)   (no shared expert; routing over all experts)
+ * expert_mask: host [E], nonzero for the experts of the subset.  This is what
+ * one rank of an expert-parallel layer computes for the pairs dispatched to
+ * it when rank r owns the experts e with e % world == r, the alternative the
+ * pages weigh and reject for its all-to-all, its capture at static shapes and
+ * its load imbalance under skewed routing ([I62] "Why not expert parallelism
+ * proper"); summing the subsets of a partition of the experts and adding the
+ * gated shared expert gives the whole layer.  It exists to measure that
+ * alternative against the intermediate split on the same GPU.  Uses the
+ * whole loaded window; reads the routing back to the host once (one
+ * synchronisation); resident mode only; T <= 32 on the tensor-core decode
+ * shapes and T > 32 on the prefill shapes (INVALID_ARG otherwise). */
+int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags,
+                          const uint8_t* expert_mask, const ftmoe_aux* aux, ftmoe_stream_t stream);
+
+/* The combine of an intermediate-sharded layer: each of n_parts ranks (or
+ * windows) computed its fp32 partial of the same T tokens (ftmoe_forward
+ * with FTMOE_OUT_FP32 on its window), the partials were exchanged into one
+ * device buffer parts [n_parts][n] in rank order (n = T * H), and this sums
+ * every element over the ranks in rank order and rounds it once to the
+ * output type of out_flags (FTMOE_OUT_BF16, FTMOE_OUT_FP32, optionally
+ * FTMOE_OUT_ACCUMULATE).  The pages' TP patch combines the ranks' partials
+ * of routed + sigmoid(gate) * shared with one SUM per MoE layer ([PR385]
+ * "What this adds", third bullet; [I62] "The fix that fits": "No new
+ * collectives"); a fixed rank order keeps that sum identical run to run
+ * ([PR385] "Correctness").  parts must be 16-byte aligned.  Asynchronous. */
+int ftmoe_reduce_partials(const float* parts, int n_parts, int64_t n, void* out, int out_flags,
+                          ftmoe_stream_t stream);
+
+/* Release everything the handle owns (device workspace, banks, pinned host
+ * banks and HBM slots of the offload backend, its copy stream).  Safe on
+ * NULL.  Synchronises nothing: the caller makes sure no forward of this
+ * handle is still running on its streams. */
 int ftmoe_destroy(ftmoe_handle* h);
 
 /* Static description of a status code. */
@@ -210,14 +271,31 @@ const char* ftmoe_error_string(int code);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */
 const char* ftmoe_last_cuda_error(void);
 
-/* Per-layer counters (see ftmoe_stats).  The routing-dependent fields are
- * read back from the device, so this call synchronises the handle's device. */
+/* Per-layer counters (see ftmoe_stats): the touched experts and bytes of the
+ * last forward, and, for the offload backend, the slot residency, hits,
+ * misses and host-to-device bytes the pages measure the backend by ([PR385]
+ * "Measurements": residency and cache slots; [I62] "Why TP=2 loses today":
+ * slot counts per rank).  The routing-dependent fields are read back from
+ * the device, so this call synchronises the handle's device. */
 int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out);
 
 /* Synchronise `stream`, read the device status word that the kernels set on a
  * failed range check or an expired bounded wait, clear it, and return OK,
- * DEVICE_CHECK or TIMEOUT. */
+ * DEVICE_CHECK or TIMEOUT.  After TIMEOUT the handle's cross-CTA counters
+ * are cleared too, so the next forward starts clean.  The pages have no
+ * counterpart; it is how a failure inside a kernel reaches the caller
+ * without trapping the GPU. */
 int ftmoe_check_status(ftmoe_handle* h, ftmoe_stream_t stream);
+
+/* Test hook of the device-side failure path, off by default; the pages have
+ * no counterpart.  While enabled (enable = 1), one CTA of every forward's
+ * tensor-core decode down kernel never issues its first pipeline stage, so
+ * its bounded waits give up after wait_limit_ns (0: the default limit of one
+ * second): the kernel sets the status word's timeout bit, drains its copies,
+ * frees its tensor memory and returns, and its output tile is not written.
+ * ftmoe_check_status then returns FTMOE_ERR_TIMEOUT.  No GPU fault or trap
+ * is involved.  INVALID_ARG if the handle has no tensor-core decode path. */
+int ftmoe_test_withhold_stage(ftmoe_handle* h, int enable, int64_t wait_limit_ns);
 
 /* Per-kernel timing.  While enabled, every kernel the handle launches is
  * bracketed by two CUDA events recorded on its launch stream.  Reading
@@ -270,6 +348,50 @@ int ftmoe_quantize_weights(const float* w, int64_t rows, int K, uint8_t* codes, 
 int ftmoe_route_static(const void* x, int T, int H, const float* router_w, const float* router_bias, int E,
                        int top_k, int norm_topk_prob, int32_t* topk_idx, float* topk_w, int32_t* offsets,
                        int32_t* perm, int32_t* inv, ftmoe_stream_t stream);
+
+/* Device-side checks of the latest ftmoe_route_static call on the current
+ * device (the kernels' range checks: an expert index out of range is routed
+ * to expert 0 and marked here).  Synchronises `stream`, reads and clears the
+ * status word kept in the same fixed array, and returns OK, DEVICE_CHECK or
+ * TIMEOUT.  Allocates nothing.  The pages have no counterpart. */
+int ftmoe_route_static_status(ftmoe_stream_t stream);
+
+/* Bank formats that ftmoe_slice_format slices (the pages' loader handles
+ * several; [I62] "What it touches" and "Suggested staging").  Per expert, a
+ * matrix W [N, K] (gate_up: N = 2I, K = H; down: N = H, K = I) is held as:
+ *   NVFP4      arrays {codes [N][K/2], E4M3 scales [N][K/16], fp32 globals [N]}
+ *   FP8_BLOCK  arrays {E4M3 q [N][K], fp32 scale [ceil(N/128)][ceil(K/128)]},
+ *              W[n][k] = q[n][k] * scale[n/128][k/128]
+ *   Q4_0       array  {blocks [N][K/32][18]}: fp16 scale d, then 16 bytes of
+ *              4-bit codes (byte j: element j low nibble, j+16 high nibble),
+ *              value = d * (code - 8)
+ *   MXFP4      arrays {blocks_t [K/2][N], UE8M0 scales_t [K/32][N]}: stored
+ *              transposed, byte [j][n] holds elements (n, 2j) low and
+ *              (n, 2j+1) high, value = e2m1 * 2^(scale - 127) */
+typedef enum {
+  FTMOE_FMT_NVFP4 = 0,
+  FTMOE_FMT_FP8_BLOCK = 1,
+  FTMOE_FMT_Q4_0 = 2,
+  FTMOE_FMT_MXFP4 = 3
+} ftmoe_format;
+
+enum { FTMOE_MAT_GATE_UP = 0, FTMOE_MAT_DOWN = 1 };
+
+/* Slice E experts' gate_up or down matrix, held in `format`, to the
+ * intermediate window [i0, i0 + I_loc) ([I62] "What it touches": gate_up
+ * keeps two disjoint row ranges, gate rows [i0, i0+I_loc) then up rows
+ * [I+i0, I+i0+I_loc); down keeps the columns [i0, i0+I_loc); mxfp4, stored
+ * transposed, slices gate_up along its columns and down along its rows; the
+ * NVFP4 down row globals stay whole).  src[i] / dst[i] are device pointers
+ * to the format's arrays in the order listed above, for all E experts back
+ * to back; the sliced arrays have the same layout at I_loc in place of I
+ * (fp8_block: whole 128-row scale tiles of each part).  i0, I_loc, I and H
+ * must be multiples of the format's block size (16 NVFP4, 128 FP8_BLOCK,
+ * 32 Q4_0 and MXFP4: [I62] "Divisibility"), else FTMOE_ERR_ALIGNMENT; a
+ * window outside [0, I) is FTMOE_ERR_INVALID_ARG.  Asynchronous on
+ * `stream`; a load-time step, not part of the forward. */
+int ftmoe_slice_format(int format, int matrix, int E, int H, int I, int i0, int I_loc, const void* const* src,
+                       void* const* dst, ftmoe_stream_t stream);
 
 /* NVFP4-quantise bf16 activation rows with the global fixed at 1.0 (the
  * forward's own activation quantiser, exposed for testing):

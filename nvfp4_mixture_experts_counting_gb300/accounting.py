@@ -44,6 +44,33 @@ def routed_flops(H: int, I_loc: int, pairs: int) -> int:
     return pairs * (2 * H * 2 * I_loc + 2 * I_loc * H)
 
 
+def shared_flops(H: int, sI_loc: int, tokens: int) -> int:
+    """Multiply-adds x 2 of the bf16 shared expert: gate_up (2*sI_loc x H)
+    and down (H x sI_loc) per token."""
+    return tokens * (2 * H * 2 * sI_loc + 2 * sI_loc * H)
+
+
+def router_flops(H: int, E: int, tokens: int) -> int:
+    """Multiply-adds x 2 of the router logits, [T, H] x [H, E]."""
+    return tokens * 2 * H * E
+
+
+def combined_ideal_seconds(H: int, E: int, I_loc: int, sI_loc: int, T: int, pairs: int, touched: float,
+                           fp4_tflops: float, bf16_tflops: float, hbm_gbs: float,
+                           router_bf16_parts: int = 3) -> dict:
+    """The layer's time at its combined roofline: the routed FP4 flops at the
+    NVFP4 peak, plus the shared expert's flops at the bf16 peak, plus the
+    router's flops at the bf16 peak times the bf16 parts it is computed in
+    (an fp32 router row is three exact bf16 parts), against the touched
+    bytes at the HBM peak; the larger of the two is the bound."""
+    t_tensor = (routed_flops(H, I_loc, pairs) / (fp4_tflops * 1e12)
+                + shared_flops(H, sI_loc, T) / (bf16_tflops * 1e12)
+                + router_bf16_parts * router_flops(H, E, T) / (bf16_tflops * 1e12))
+    t_hbm = layer_touched_bytes(H, E, I_loc, sI_loc, T, int(round(touched))) / (hbm_gbs * 1e9)
+    return {"tensor_s": t_tensor, "hbm_s": t_hbm, "bound_s": max(t_tensor, t_hbm),
+            "bound": "tensor" if t_tensor >= t_hbm else "hbm"}
+
+
 def kernel_unit_bytes(kernel: str, H: int, I_loc: int, sI_loc: int, E: int = 0):
     """(bytes per unit, unit name, fixed bytes per launch) of a kernel's
     algorithmic HBM traffic; units are touched experts where named so."""
@@ -80,6 +107,13 @@ def kernel_unit_flops(kernel: str, H: int, I_loc: int, sI_loc: int, E: int = 0):
         return 2 * H * 2 * I_loc, "pair", "nvfp4 tensor"
     if kernel == "k_pf_down":
         return 2 * I_loc * H, "pair", "nvfp4 tensor"
+    if kernel == "k_pf_shared_gate_up":
+        return 2 * H * 2 * sI_loc, "token", "bf16 tensor"
+    if kernel == "k_pf_shared_down_combine":
+        return 2 * sI_loc * H, "token", "bf16 tensor"
+    if kernel == "k_pf_router":
+        # x times the three exact bf16 parts of every fp32 router row
+        return 3 * 2 * H * E, "token", "bf16 tensor"
     if kernel == "k_shared_gate_up":
         return 2 * H * 2 * sI_loc, "token", "fp32 CUDA cores"
     if kernel == "k_shared_down":

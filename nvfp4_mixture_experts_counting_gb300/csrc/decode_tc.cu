@@ -43,6 +43,10 @@ constexpr int kDtSmem = 220 * 1024;
 // keeps to half of the shared memory and of TMEM
 constexpr int kDdSmem = 112 * 1024;
 constexpr uint32_t kDdTmemCols = 256;
+// Arrival mark of a down CTA that gave up (a bounded wait ran out): the
+// low 16 bits of a tile's counter count arrivals, the high bits count
+// CTAs that gave up.
+constexpr int kDnGaveUp = 1 << 16;
 constexpr int kDtA = 16384;      // 128 weight rows x 128 bytes
 constexpr int kDtB = 4096;       // up to 32 token / pair rows x 128 bytes
 
@@ -690,6 +694,8 @@ __global__ void __launch_bounds__(kDdThreads, 2)
   float* part = reinterpret_cast<float*>(sm + L.part_off);  // [32 tokens][128 rows]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ht = blockIdx.x, g = blockIdx.y;
+  const uint64_t wlim = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs;
+  const bool withhold = a.withhold_first_stage && ht == 0 && g == 0;  // test of the failure path
   const bool has_shared = a.sh_down != nullptr && !a.skip_shared;
   const int G = gridDim.y - (has_shared ? 1 : 0);  // routed expert groups
   const bool shared = has_shared && g == G;
@@ -767,10 +773,12 @@ __global__ void __launch_bounds__(kDdThreads, 2)
       // the weights of the first NST K tiles stream before the dependency
       // wait (they do not depend on the gate_up kernel) ...
       const int pre = min(NST, n_items * nkt_u);
-      for (int k2 = 0; k2 < pre; ++k2) issue(k2, k2 / nkt_u, k2 % nkt_u, true, true, false);
+      // (a withheld first stage gets no arrival and no copy at all: every
+      // wait on it runs out)
+      for (int k2 = withhold ? 1 : 0; k2 < pre; ++k2) issue(k2, k2 / nkt_u, k2 % nkt_u, true, true, false);
       pdl_wait();  // the intermediates of the gate_up kernel
       // ... their activations after it, then the ring as usual
-      for (int k2 = 0; k2 < pre; ++k2) issue(k2, k2 / nkt_u, k2 % nkt_u, false, false, true);
+      for (int k2 = withhold ? 1 : 0; k2 < pre; ++k2) issue(k2, k2 / nkt_u, k2 % nkt_u, false, false, true);
       int kk = pre, rs = pre == NST ? 0 : pre;  // ring position, its stage and phase parity
       uint32_t rph = pre == NST ? 1 : 0;
       for (int it = kk / nkt_u; it < n_items && !*abort_flag; ++it) {
@@ -778,11 +786,11 @@ __global__ void __launch_bounds__(kDdThreads, 2)
           const int s = rs;
           const uint32_t ph = rph;
           if (++rs == NST) { rs = 0; rph ^= 1; }
-          if (kk >= NST && !mbar_wait(&empty[s], ph ^ 1, a.r.status)) { *abort_flag = 1; break; }
+          if (kk >= NST && !mbar_wait(&empty[s], ph ^ 1, a.r.status, wlim)) { *abort_flag = 1; break; }
           issue(s, it, kt, true, true, true);
         }
       }
-      for (int q = kk - NST > 0 ? kk - NST : 0; q < kk; ++q) mbar_wait(&full[q % NST], (q / NST) & 1, a.r.status);
+      for (int q = kk - NST > 0 ? kk - NST : 0; q < kk; ++q) mbar_wait(&full[q % NST], (q / NST) & 1, a.r.status, wlim);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -792,7 +800,7 @@ __global__ void __launch_bounds__(kDdThreads, 2)
       bool ok = true;
       for (int it = 0; it < n_items && !*abort_flag; ++it) {
         const int buf = it & 1;
-        if (it >= 2 && !mbar_wait(&acc_empty[buf], ((it >> 1) - 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+        if (it >= 2 && !mbar_wait(&acc_empty[buf], ((it >> 1) - 1) & 1, a.r.status, wlim)) { *abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t d = tmem + buf * npad;
         const int nkt_u = shared ? nkt_s : nkt_r;
@@ -800,7 +808,7 @@ __global__ void __launch_bounds__(kDdThreads, 2)
           const int s = rs;
           const uint32_t ph = rph;
           if (++rs == NST) { rs = 0; rph ^= 1; }
-          if (!mbar_wait(&sf_ready[s], ph, a.r.status)) { *abort_flag = 1; ok = false; break; }
+          if (!mbar_wait(&sf_ready[s], ph, a.r.status, wlim)) { *abort_flag = 1; ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(sm + s * L.stage);
           const uint64_t adesc = sdesc_k_sw128(sa), bdesc = sdesc_k_sw128(sa + kDtA);
@@ -819,7 +827,7 @@ __global__ void __launch_bounds__(kDdThreads, 2)
         tc_commit(&acc_full[buf]);
       }
       tc_commit(drain);
-      mbar_wait(drain, 0, a.r.status);
+      mbar_wait(drain, 0, a.r.status, wlim);
     }
   } else if (warp == 6) {
     // ---------------- scale factors: once a stage has landed, its weight
@@ -835,7 +843,7 @@ __global__ void __launch_bounds__(kDdThreads, 2)
           const int s = rs;
           const uint32_t ph = rph;
           if (++rs == NST) { rs = 0; rph ^= 1; }
-          if (!mbar_wait(&full[s], ph, a.r.status)) { *abort_flag = 1; break; }
+          if (!mbar_wait(&full[s], ph, a.r.status, wlim)) { *abort_flag = 1; break; }
           if (shared) {
             mbar_arrive(&sf_ready[s]);
             continue;
@@ -852,7 +860,7 @@ __global__ void __launch_bounds__(kDdThreads, 2)
         }
       }
       tc_commit(sf_drain);
-      mbar_wait(sf_drain, 0, a.r.status);
+      mbar_wait(sf_drain, 0, a.r.status, wlim);
     }
     __syncwarp();
   } else if (warp == 7) {
@@ -868,7 +876,7 @@ __global__ void __launch_bounds__(kDdThreads, 2)
       const int s0 = shared ? 0 : s_off[e], m = shared ? 0 : s_off[e + 1] - s0;
       // the row global is loaded before the accumulator wait
       const float gd = shared ? 0.f : reinterpret_cast<const float*>(s_rec[ti0 + it] + a.lay.dn_global)[hg];
-      if (!mbar_wait(&acc_full[buf], (it >> 1) & 1, a.r.status)) { *abort_flag = 1; break; }
+      if (!mbar_wait(&acc_full[buf], (it >> 1) & 1, a.r.status, wlim)) { *abort_flag = 1; break; }
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * npad;
       if (shared) {
@@ -884,14 +892,28 @@ __global__ void __launch_bounds__(kDdThreads, 2)
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
     // this group's partials gpart[g][tile][t][128], then the last CTA of
-    // the tile adds all groups in group order
-    if (!*abort_flag) {
+    // the tile adds all groups in group order.  Whether this CTA gave up is
+    // decided once (the flag may still be raised by another role), and every
+    // CTA arrives on the tile's counter, a CTA that gave up with a mark in
+    // the high half: the count always reaches the number of groups, so the
+    // last arriver always clears the counter for the next launch, and it
+    // writes the output only if no group of the tile gave up.
+    named_barrier(1, 128);
+    if (tid == 64) s_last = *abort_flag;
+    named_barrier(1, 128);
+    const bool gave_up = s_last != 0;
+    if (!gave_up) {
       float* gp = a.gpart + ((int64_t)g * gridDim.x + ht) * T * 128;
       for (int t = 0; t < T; ++t) gp[t * 128 + h] = part[t * 128 + h];
       __threadfence();
     }
     named_barrier(1, 128);
-    if (tid == 64) s_last = *abort_flag ? 0 : (atomicAdd(&a.dn_counter[ht], 1) == (int)gridDim.y - 1);
+    if (tid == 64) {
+      const int old = atomicAdd(&a.dn_counter[ht], gave_up ? (1 + kDnGaveUp) : 1);
+      const bool last = (old & (kDnGaveUp - 1)) == (int)gridDim.y - 1;
+      const bool clean = old < kDnGaveUp && !gave_up;
+      s_last = last ? (clean ? 1 : 2) : 0;
+    }
     named_barrier(1, 128);
   }
   tc_fence_before();
@@ -900,7 +922,11 @@ __global__ void __launch_bounds__(kDdThreads, 2)
     tc_fence_after();
     tmem_dealloc(tmem, kDdTmemCols);
   }
-  if (s_last) {
+  if (s_last == 2) {
+    // a group of this tile gave up (its timeout is in the status word): no
+    // output, only the counter cleared for the next launch
+    if (tid == 64) a.dn_counter[ht] = 0;
+  } else if (s_last == 1) {
     // every thread of the last CTA: items (token, 4 output rows), each the
     // sum over the groups in group order, with the groups' loads in flight
     // together

@@ -322,8 +322,11 @@ __global__ void k_combine(ExpertArgs a) {
     const int t = (int)(i / H), h = (int)(i % H);
     float acc = 0.f;
     for (int j = 0; j < k; ++j) {
-      const float y = a.y_tiles ? a.Y[(((int64_t)t * (H / 128) + h / 128) * k + j) * 128 + (h & 127)]
-                                : a.Y[(int64_t)r.inv[(int64_t)t * k + j] * H + h];
+      const int64_t yt = (((int64_t)t * (H / 128) + h / 128) * k + j) * 128 + (h & 127);
+      const float y =
+          a.y_tiles == 2 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(a.Y)[yt] << 16)
+          : a.y_tiles == 1 ? a.Y[yt]
+                           : a.Y[(int64_t)r.inv[(int64_t)t * k + j] * H + h];
       acc = fmaf(r.topk_w[(int64_t)t * k + j], y, acc);
     }
     if (a.sh_gate_up) acc = fmaf(r.sigma[t], a.S[i], acc);
@@ -450,6 +453,65 @@ cudaError_t launch_store_out(const float* y, void* out, int out_flags, int64_t n
   if (blocks > 4096) blocks = 4096;
   FTMOE_PROF_BEGIN("k_store_out", s);
   k_store_out<<<(int)blocks, 256, 0, s>>>(y, out, out_flags, n);
+  FTMOE_PROF_END(s);
+  return cudaGetLastError();
+}
+
+// out = sum over r of parts[r] (fp32 [n_parts][n], rank order), rounded once
+// to the output type (or added to an fp32 out): the combine of the window
+// partials that the ranks of an intermediate-sharded layer exchange.  Four
+// elements per thread; every element sums its partials in rank order.
+__global__ void k_reduce_partials(const float* __restrict__ parts, int n_parts, int64_t n, void* out,
+                                  int out_flags) {
+  // whole float4s while every partial starts 16-byte aligned (n % 4 == 0)
+  const int64_t n4 = (n & 3) == 0 ? n / 4 : 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (n + 3) / 4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < n4) {
+      for (int r = 0; r < n_parts; ++r) {
+        const float4 p = __ldg(reinterpret_cast<const float4*>(parts + (int64_t)r * n) + i);
+        v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+      }
+    } else {
+      for (int r = 0; r < n_parts; ++r)
+        for (int c = 0; c < 4 && 4 * i + c < n; ++c) v[c] += parts[(int64_t)r * n + 4 * i + c];
+    }
+    for (int c = 0; c < 4 && 4 * i + c < n; ++c) {
+      const int64_t j = 4 * i + c;
+      if ((out_flags & 0xff) == 0) reinterpret_cast<__nv_bfloat16*>(out)[j] = __float2bfloat16_rn(v[c]);
+      else if (out_flags & 0x100) reinterpret_cast<float*>(out)[j] += v[c];
+      else reinterpret_cast<float*>(out)[j] = v[c];
+    }
+  }
+}
+
+cudaError_t launch_reduce_partials(const float* parts, int n_parts, int64_t n, void* out, int out_flags,
+                                   cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = ((n + 3) / 4 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  FTMOE_PROF_BEGIN("k_reduce_partials", s);
+  k_reduce_partials<<<(int)blocks, 256, 0, s>>>(parts, n_parts, n, out, out_flags);
+  FTMOE_PROF_END(s);
+  return cudaGetLastError();
+}
+
+// w_out[p] = w[p] if pair p's expert is in the mask, else 0 (the combine of
+// an expert subset's pairs).
+__global__ void k_mask_weights(const int32_t* __restrict__ idx, const float* __restrict__ w,
+                               const uint8_t* __restrict__ mask, float* __restrict__ w_out, int64_t P) {
+  for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < P; p += (int64_t)gridDim.x * blockDim.x)
+    w_out[p] = mask[idx[p]] ? w[p] : 0.f;
+}
+
+cudaError_t launch_mask_weights(const int32_t* idx, const float* w, const uint8_t* mask, float* w_out, int64_t P,
+                                cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  int64_t blocks = (P + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  FTMOE_PROF_BEGIN("k_mask_weights", s);
+  k_mask_weights<<<(int)blocks, 256, 0, s>>>(idx, w, mask, w_out, P);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }

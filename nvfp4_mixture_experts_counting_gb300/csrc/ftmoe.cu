@@ -120,6 +120,7 @@ struct Layer {
   uint8_t* active_dev = nullptr;    // [E] experts of the current batch
   int last_T = 0;
   int last_I_loc = 0;
+  int last_touched = 0;  // offload mode: touched experts of the last forward (read on the host)
 };
 
 }  // namespace
@@ -173,6 +174,13 @@ struct ftmoe_handle {
   int dtc_groups = 0;
   uint32_t last_status = 0;
   EventProfiler* prof = nullptr;  // non-null while per-kernel timing is enabled
+  // expert-subset forwards (ftmoe_forward_experts), made at the first call
+  int32_t* ep_host = nullptr;   // pinned [2E + 4]: touched experts and count, then the subset list
+  uint8_t* ep_mask = nullptr;   // device [E]: experts of the subset
+  float* ep_w = nullptr;        // device [P]: routing weights with the other experts' slots zeroed
+  // test hook of the device-side failure path (ftmoe_test_withhold_stage)
+  int test_withhold = 0;
+  uint64_t test_wait_ns = 0;
 };
 
 namespace ftmoe {
@@ -319,6 +327,10 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
       {(void**)&h->off_y, c.hbm_slot_bytes > 0 ? T * c.H * 4 : 16},
       {(void**)&h->gu_split, (int64_t)(prop.multiProcessorCount + 1) * 4},
   };
+  // counts of the many-CTA counting sort (chunks of 4096 pairs)
+  h->r.sort_max_chunks = (int)((P + 4095) / 4096);
+  if (h->r.sort_max_chunks > 1)
+    parts.push_back({(void**)&h->r.sort_cnt, (int64_t)h->r.sort_max_chunks * c.E * 4});
   // tensor-core decode buffers
   const char* no_tc = getenv("FTMOE_NO_TC");
   if (c.H % 256 == 0 && c.I % 64 == 0 && c.E <= 1024 && !(no_tc && no_tc[0] == '1')) {
@@ -361,6 +373,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
   if (e == cudaSuccess) e = decode_set_smem_limits();
   if (e == cudaSuccess) e = prefill_set_smem_limits();
   if (e == cudaSuccess) e = decode_tc_set_smem_limits();
+  if (e == cudaSuccess) e = w16_set_smem_limits(8192, 8192);
   if (e == cudaSuccess && c.hbm_slot_bytes > 0) {
     h->offload = true;
     h->h2d_bytes.assign(c.num_layers, 0);
@@ -371,8 +384,7 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
   }
   if (e != cudaSuccess) {
     cuda_fail(e, "create");
-    cudaFree(h->ws);
-    delete h;
+    ftmoe_destroy(h);  // the workspace, and the copy stream, events and pinned buffer made so far
     return FTMOE_ERR_CUDA;
   }
   h->r.status = h->status;
@@ -388,6 +400,9 @@ int ftmoe_destroy(ftmoe_handle* h) {
   if (h->ev_compute) cudaEventDestroy(h->ev_compute);
   if (h->ev_copied) cudaEventDestroy(h->ev_copied);
   if (h->h_touched) cudaFreeHost(h->h_touched);
+  if (h->ep_host) cudaFreeHost(h->ep_host);
+  cudaFree(h->ep_mask);
+  cudaFree(h->ep_w);
   if (h->h_stage) cudaFreeHost(h->h_stage);
   cudaFree(h->slot_pool);
   delete h->prof;
@@ -607,6 +622,8 @@ static void decode_tc_args(ftmoe_handle* h, Layer& L, DecodeArgs& d) {
   d.dn_counter = h->dtc_counter;
   d.n_groups = h->dtc_groups;
   d.hq_cpitch = (int)align_up(d.win.I_loc / 2, 16);
+  d.withhold_first_stage = h->test_withhold;
+  d.wait_limit_ns = h->test_withhold ? h->test_wait_ns : 0;
   if (L.router_wcat && h->dtc_rpart && decode_tc_router_supported(h->cfg.H, h->cfg.E)) {
     d.wcat = L.router_wcat;
     d.wnorm = L.router_wnorm;
@@ -640,7 +657,11 @@ static PfArgs prefill_args(ftmoe_handle* h, Layer& L, const ExpertArgs& a, const
   p.hq = h->pf_hq;
   p.hq_sf = h->pf_hq_sf;
   p.hq_pitch = (int)align_up(a.win.I_loc / 2, 16);
+  // the pairs' outputs in the output's precision: bf16 for a bf16 output
+  // (half the bytes of the write and the read back), fp32 for an fp32 one,
+  // so that fp32 window partials still add up to the full layer
   p.Y = h->Y;
+  p.y_bf16 = (out_flags & 0xff) == FTMOE_OUT_BF16;
   p.status = h->status;
   if (tc_shared || tc_router) p.x = (const uint16_t*)x;
   if (tc_shared) {
@@ -700,7 +721,21 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
   const ftmoe_config& c = h->cfg;
   Layer& L = h->layers[layer];
   RouteArgs r = route_args(h, L, x, T);
-  ExpertArgs a = expert_args(h, L, r, T, out, out_flags, i0, I_loc);
+  ExpertArgs a = expert_args(h, L, r, T, out, out_flags & ~FTMOE_ACT_BF16, i0, I_loc);
+  if (out_flags & FTMOE_ACT_BF16) {
+    // W4A16: routing, shared gate_up, the routed experts on bf16 activations
+    // (Y in sorted order), shared down + combine
+    CK(launch_route(r, s));
+    CK(launch_experts(a, s, kPartSharedGateUp));
+    CK(launch_w16_routed(a, s));
+    a.y_tiles = 0;
+    CK(launch_experts(a, s, kPartTail));
+    int rc = copy_aux(h, r, T, aux, s);
+    if (rc) return rc;
+    L.last_T = T;
+    L.last_I_loc = I_loc;
+    return FTMOE_OK;
+  }
   const bool dtc = decode_tc_path(h, L, a, T);
   if (dtc || decode_supported(c.H, c.E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T, c.top_k)) {
     // decode sizes: routing, streamed gate_up, fused down + combine
@@ -734,7 +769,7 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     if (tc_shared) {
       CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
     } else {
-      a.y_tiles = 1;  // the tensor-core down kernel's layout of Y
+      a.y_tiles = p.y_bf16 ? 2 : 1;  // the tensor-core down kernel's layout of Y
       CK(launch_experts(a, s, kPartTail));
     }
   } else {
@@ -791,6 +826,8 @@ static int forward_offload(ftmoe_handle* h, int layer, const void* x, int T, voi
   CK(cudaStreamSynchronize(s));
   const int nt = h->h_touched[E];
   if (nt < 0 || nt > E) return FTMOE_ERR_DEVICE_CHECK;
+  // the device's count is overwritten by every batch below; keep the step's
+  L.last_touched = nt;
   const int S = h->cache.slots();
   const int nb = (nt + S - 1) / S;
   if (nb > h->max_batches) return FTMOE_ERR_INVALID_ARG;
@@ -863,7 +900,7 @@ static int forward_offload(ftmoe_handle* h, int layer, const void* x, int T, voi
     if (tc_shared) {
       CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
     } else {
-      a.y_tiles = 1;  // the tensor-core down kernel's layout of Y
+      a.y_tiles = p.y_bf16 ? 2 : 1;  // the tensor-core down kernel's layout of Y
       CK(launch_experts(a, s, kPartTail));
     }
   }
@@ -880,7 +917,8 @@ int ftmoe_forward(ftmoe_handle* h, int layer, const void* x, int T, void* out, i
   const ftmoe_config& c = h->cfg;
   if (T < 0 || T > c.max_tokens) return FTMOE_ERR_INVALID_ARG;
   const int otype = out_flags & 0xff;
-  if ((out_flags & ~0x1ff) || otype > FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  if ((out_flags & ~0x3ff) || otype > FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  if ((out_flags & FTMOE_ACT_BF16) && h->offload) return FTMOE_ERR_INVALID_ARG;
   if ((out_flags & FTMOE_OUT_ACCUMULATE) && otype != FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
   Layer& L = h->layers[layer];
   if (!L.loaded) return FTMOE_ERR_NOT_LOADED;
@@ -932,6 +970,109 @@ int ftmoe_rms_renorm(const float* y, void* x, int T, int H, ftmoe_stream_t strea
   return FTMOE_OK;
 }
 
+int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags,
+                          const uint8_t* expert_mask, const ftmoe_aux* aux, ftmoe_stream_t stream) {
+  if (!h || layer < 0 || layer >= h->cfg.num_layers || !expert_mask) return FTMOE_ERR_INVALID_ARG;
+  const ftmoe_config& c = h->cfg;
+  if (h->offload || T < 0 || T > c.max_tokens) return FTMOE_ERR_INVALID_ARG;
+  const int otype = out_flags & 0xff;
+  if ((out_flags & ~0x1ff) || otype > FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  if ((out_flags & FTMOE_OUT_ACCUMULATE) && otype != FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  Layer& L = h->layers[layer];
+  if (!L.loaded) return FTMOE_ERR_NOT_LOADED;
+  if (T == 0) return FTMOE_OK;
+  if (!x || !out || x == out) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return FTMOE_ERR_ALIGNMENT;
+  CK(cudaSetDevice(h->device));
+  ProfScope ps(h->prof);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int E = c.E;
+  if (!h->ep_host) {
+    if (cudaHostAlloc((void**)&h->ep_host, (size_t)(2 * E + 4) * 4, cudaHostAllocDefault) != cudaSuccess ||
+        cudaMalloc(&h->ep_mask, (size_t)E) != cudaSuccess ||
+        cudaMalloc(&h->ep_w, (size_t)(c.max_tokens > 0 ? c.max_tokens : 1) * c.top_k * 4) != cudaSuccess) {
+      cudaGetLastError();
+      return FTMOE_ERR_OOM;
+    }
+  }
+  const int i0 = L.li0, I_loc = L.lIw;
+  RouteArgs r = route_args(h, L, x, T);
+  ExpertArgs a = expert_args(h, L, r, T, out, out_flags, i0, I_loc);
+  const bool dec = T <= 32;
+  if (dec ? !decode_tc_path(h, L, a, T) : !prefill_path(h, L, T, I_loc, a.win.row0)) return FTMOE_ERR_INVALID_ARG;
+  DecodeArgs d{};
+  PfArgs p{};
+  PfMaps maps;
+  // routing over every expert, then the touched list on the host
+  if (dec) {
+    d = decode_args(h, a);
+    decode_tc_args(h, L, d);
+    CK(launch_decode_tc(d, s, 1));
+  } else {
+    const bool tc_router = L.router_wcat != nullptr;
+    p = prefill_args(h, L, a, x, out, out_flags, false, tc_router);
+    CK(prefill_make_maps(p, &maps));
+    if (tc_router) {
+      CK(launch_route(r, s, kRouteXq));
+      CK(launch_prefill_router(p, maps, h->num_sms, s));
+      CK(launch_route(r, s, kRouteTopk | kRouteSort));
+    } else {
+      CK(launch_route(r, s));
+    }
+  }
+  int32_t* ht = h->ep_host;
+  CK(cudaMemcpyAsync(ht, r.touched, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(ht + E, r.n_touched, 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  const int nt = ht[E];
+  if (nt < 0 || nt > E) return FTMOE_ERR_DEVICE_CHECK;
+  int32_t* list = ht + E + 1;   // [E] the subset's touched experts, in expert order
+  int32_t* count = list + E;    // their number
+  int n = 0;
+  for (int i = 0; i < nt; ++i)
+    if (expert_mask[ht[i]]) list[n++] = ht[i];
+  *count = n;
+  if (dec) {
+    // the expert kernels on the subset's list, without the shared expert
+    CK(cudaMemcpyAsync(r.touched, list, (size_t)(n > 0 ? n : 1) * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(r.n_touched, count, 4, cudaMemcpyHostToDevice, s));
+    d.skip_shared = 1;
+    if (n == 0) {
+      CK(cudaMemsetAsync(out, 0, (size_t)T * c.H * (otype == FTMOE_OUT_FP32 ? 4 : 2), s));
+    } else {
+      CK(launch_decode_tc(d, s, 2));
+    }
+  } else {
+    // the subset's experts only, then the combine of their slots (the other
+    // slots' weights zeroed), without the shared expert
+    CK(cudaMemcpyAsync(h->ep_mask, expert_mask, (size_t)E, cudaMemcpyHostToDevice, s));
+    p.active = h->ep_mask;
+    CK(launch_prefill_routed(p, maps, h->num_sms, s));
+    CK(launch_mask_weights(r.topk_idx, r.topk_w, h->ep_mask, h->ep_w, (int64_t)T * c.top_k, s));
+    a.r.topk_w = h->ep_w;
+    a.sh_gate_up = nullptr;
+    a.y_tiles = p.y_bf16 ? 2 : 1;
+    CK(launch_experts(a, s, kPartTail));
+  }
+  int rc = copy_aux(h, r, T, aux, s);
+  if (rc) return rc;
+  L.last_T = T;
+  L.last_I_loc = I_loc;
+  return FTMOE_OK;
+}
+
+int ftmoe_reduce_partials(const float* parts, int n_parts, int64_t n, void* out, int out_flags,
+                          ftmoe_stream_t stream) {
+  if (n_parts < 1 || n < 0 || !parts || !out) return FTMOE_ERR_INVALID_ARG;
+  const int otype = out_flags & 0xff;
+  if ((out_flags & ~0x1ff) || otype > FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  if ((out_flags & FTMOE_OUT_ACCUMULATE) && otype != FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(parts)) return FTMOE_ERR_ALIGNMENT;
+  if (n == 0) return FTMOE_OK;
+  CK(launch_reduce_partials(parts, n_parts, n, out, out_flags, (cudaStream_t)stream));
+  return FTMOE_OK;
+}
+
 int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out) {
   if (!h || !out || layer < 0 || layer >= h->cfg.num_layers) return FTMOE_ERR_INVALID_ARG;
   CK(cudaSetDevice(h->device));
@@ -940,7 +1081,7 @@ int ftmoe_get_stats(ftmoe_handle* h, int layer, ftmoe_stats* out) {
   Layer& L = h->layers[layer];
   int32_t nt = 0;
   CK(cudaMemcpy(&nt, h->r.n_touched, 4, cudaMemcpyDeviceToHost));
-  out->touched_experts = L.last_T > 0 ? nt : 0;
+  out->touched_experts = L.last_T > 0 ? (h->offload ? L.last_touched : nt) : 0;
   const int H = h->cfg.H, W = L.last_I_loc;
   const int64_t per_expert = (int64_t)2 * W * (H / 2 + H / 16 + 4) + (int64_t)H * (W / 2 + W / 16) + (int64_t)H * 4;
   out->touched_bytes = out->touched_experts * per_expert;
@@ -969,8 +1110,23 @@ int ftmoe_check_status(ftmoe_handle* h, ftmoe_stream_t stream) {
   CK(cudaMemcpy(&st, h->status, 4, cudaMemcpyDeviceToHost));
   CK(cudaMemset(h->status, 0, 4));
   h->last_status = st;
-  if (st & kStatusTimeout) return FTMOE_ERR_TIMEOUT;
+  if (st & kStatusTimeout) {
+    // a kernel gave up mid-launch: clear the cross-CTA counters it may have
+    // left behind, so the next forward starts from a clean state
+    if (h->dtc_counter) CK(cudaMemset(h->dtc_counter, 0, (size_t)(h->cfg.H / 128 + 1) * 4));
+    CK(cudaMemset(h->counter, 0, 16));
+    CK(cudaDeviceSynchronize());
+    return FTMOE_ERR_TIMEOUT;
+  }
   if (st & kStatusRange) return FTMOE_ERR_DEVICE_CHECK;
+  return FTMOE_OK;
+}
+
+int ftmoe_test_withhold_stage(ftmoe_handle* h, int enable, int64_t wait_limit_ns) {
+  if (!h || wait_limit_ns < 0) return FTMOE_ERR_INVALID_ARG;
+  if (enable && !h->dtc_enabled) return FTMOE_ERR_INVALID_ARG;  // the hook lives in the tensor-core decode kernel
+  h->test_withhold = enable ? 1 : 0;
+  h->test_wait_ns = (uint64_t)wait_limit_ns;
   return FTMOE_OK;
 }
 

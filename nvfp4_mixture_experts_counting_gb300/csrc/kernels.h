@@ -70,6 +70,10 @@ struct RouteArgs {
   unsigned long long* n_rerank;  // [1] cumulative count of re-ranked tokens (may be null)
   unsigned long long* touched_total;  // [1] cumulative touched experts over forwards (may be null)
   uint32_t* status;
+  // counting sort over many CTAs (large T): per (chunk of 4096 pairs,
+  // expert) counts, then first positions; null: the one-CTA sort
+  int32_t* sort_cnt;   // [sort_max_chunks][E]
+  int sort_max_chunks;
 };
 
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, uint8_t* codes,
@@ -96,8 +100,9 @@ struct ExpertArgs {
   uint16_t* hs;        // [T][s_I_loc] bf16 shared intermediate
   uint8_t* hq_codes;   // [P][I_loc/2]
   uint8_t* hq_scales;  // [P][I_loc/16]
-  float* Y;            // [P][H] fp32, rows in sorted order (y_tiles: [T][H/128][k][128], pair (t, slot))
-  int y_tiles;         // 1: Y was written by the tensor-core prefill down kernel, in its layout
+  float* Y;            // [P][H] fp32, rows in sorted order (y_tiles == 0); the tensor-core prefill
+                       // down kernel's [T][H/128][k][128] fp32 (y_tiles == 1) or bf16 (y_tiles == 2)
+  int y_tiles;
   float* S;            // [T][H] fp32
   void* out;
   int out_flags;
@@ -152,6 +157,12 @@ struct DecodeArgs {
   float* rpart;          // [n_rparts][T][E]
   int n_rparts;
   float kappa;           // bound of the tensor-core accumulation: kappa * ||x|| * ||w||
+  // test hook of the down kernel's failure path: CTA (0, 0) never issues its
+  // first stage, and its bounded waits give up after wait_limit_ns (0: the
+  // default limit), so its waits run out, it marks the status word and the
+  // tile's counter and leaves cleanly
+  int withhold_first_stage;
+  uint64_t wait_limit_ns;
 };
 
 int decode_hq_cpitch(int I_loc);
@@ -193,7 +204,8 @@ struct PfArgs {
   uint8_t* hq;                // [P_pad_max][hq_pitch] intermediate codes (I_loc/2 used)
   uint8_t* hq_sf;             // [P_pad_max/128][I_loc/64][512]
   int hq_pitch;
-  float* Y;                   // [T][H/128][k][128] fp32: pair (t, slot)'s output, per column tile
+  void* Y;                    // [T][H/128][k][128]: pair (t, slot)'s output, per column tile
+  int y_bf16;                 // Y in bf16 (the forward's output is bf16), else fp32
   int stage_y;                // down: Y goes out through shared memory (set by the launcher)
   uint32_t* status;
   // shared expert on the tensor cores, fused with the combine
@@ -234,6 +246,20 @@ cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m);
 cudaError_t prefill_set_smem_limits();
 cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw, int E, cudaStream_t s);
 cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
+
+// W4A16 routed experts (w4a16.cu): bf16 x, NVFP4 weights dequantised in
+// registers, bf16 intermediate in hq_codes ([P][I_loc] bf16), Y [P][H] in
+// sorted order (ExpertArgs y_tiles == 0)
+cudaError_t w16_set_smem_limits(int H, int I);
+cudaError_t launch_w16_routed(const ExpertArgs& a, cudaStream_t s);
+
+// w_out[p] = mask[idx[p]] ? w[p] : 0 over P pairs
+cudaError_t launch_mask_weights(const int32_t* idx, const float* w, const uint8_t* mask, float* w_out, int64_t P,
+                                cudaStream_t s);
+
+// out <- sum of n_parts fp32 partials [n_parts][n] in rank order (out_flags as a forward's)
+cudaError_t launch_reduce_partials(const float* parts, int n_parts, int64_t n, void* out, int out_flags,
+                                   cudaStream_t s);
 
 // y fp32 [T][H] -> bf16(y / sqrt(mean(y^2) + eps)) [T][H]
 cudaError_t launch_rms_renorm(const float* y, uint16_t* x, int T, int H, cudaStream_t s);

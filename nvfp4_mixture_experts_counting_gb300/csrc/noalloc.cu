@@ -120,3 +120,20 @@ extern "C" int ftmoe_route_static(const void* x, int T, int H, const float* rout
   if (launch_route(a, st) != cudaSuccess) { cudaGetLastError(); return FTMOE_ERR_CUDA; }
   return FTMOE_OK;
 }
+
+extern "C" int ftmoe_route_static_status(ftmoe_stream_t stream) {
+  unsigned char* s = nullptr;
+  int rc = scratch_for_current_device(&s);
+  if (rc) return rc;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) { cudaGetLastError(); return FTMOE_ERR_CUDA; }
+  uint32_t st = 0;
+  // a plain copy out of the library's own array: no allocation
+  if (cudaMemcpy(&st, s + kOffStatus, 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(s + kOffStatus, 0, 4) != cudaSuccess) {
+    cudaGetLastError();
+    return FTMOE_ERR_CUDA;
+  }
+  if (st & kStatusTimeout) return FTMOE_ERR_TIMEOUT;
+  if (st & kStatusRange) return FTMOE_ERR_DEVICE_CHECK;
+  return FTMOE_OK;
+}

@@ -51,11 +51,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;   // scale-factor columns start after the two accumulators
 
 __host__ __device__ inline int pf_smem_bytes(int E) { return 1024 + kPfOffTab + 3 * 4 * (E + 1); }
-// Down mode: each epilogue warp turns its 32 rows x 32 columns of Y through
-// shared memory (rows 36 floats apart), so that every store instruction
-// writes four whole 128-byte row segments.  It sits after the tables.
-constexpr int kPfStgRow = 36;
-constexpr int kPfStgBytes = kPfEpiWarps * 32 * kPfStgRow * 4;
+// Down mode: each epilogue warp turns its rows of Y through shared memory
+// (rows 144 bytes apart: 64 bf16 columns, or 32 fp32 columns at a time), so
+// that every store instruction writes four whole 128-byte row segments.  It
+// sits after the tables.
+constexpr int kPfStgRow = 144;
+constexpr int kPfStgBytes = kPfEpiWarps * 32 * kPfStgRow;
 __host__ __device__ inline int pf_stg_off(int E) { return (kPfOffTab + 3 * 4 * (E + 1) + 15) & ~15; }
 __host__ __device__ inline int pf_smem_bytes_staged(int E) { return 1024 + pf_stg_off(E) + kPfStgBytes; }
 
@@ -96,15 +97,11 @@ __device__ __forceinline__ int find_le(const int* tab, int n, int v) {
 // .32x128b.warpx4 places into TMEM lanes r % 32, columns r / 32).
 __host__ __device__ constexpr int sf_slot(int r) { return (r & 31) * 16 + ((r & 127) >> 5) * 4; }
 
-// SiLU with the fast exponential and division (the epilogue's result is
-// quantised to E2M1 right after; the approximation changes h by a few ulp).
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
-
-// NVFP4 quantisation of 16 activation values with global 1.0: scale =
-// E4M3(amax / 6), codes = E2M1(v * (1 / scale)).  Multiplying by the
-// reciprocal can move a value sitting exactly on an E2M1 rounding boundary
-// by one ulp, which the parity tolerance absorbs.
-__device__ __forceinline__ uint8_t quantize_act16_fast(const float v[16], uint8_t codes[8]) {
+// NVFP4 quantisation of 16 activation values with global 1.0, in the
+// quantiser's own order: scale = E4M3(fp32(amax / 6)), then each code =
+// E2M1(fp32(v / dec(scale))) with IEEE divisions, so the codes are those the
+// same fp32 values give in any other implementation of that order.
+__device__ __forceinline__ uint8_t quantize_act16(const float v[16], uint8_t codes[8]) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
@@ -115,9 +112,8 @@ __device__ __forceinline__ uint8_t quantize_act16_fast(const float v[16], uint8_
     for (int i = 0; i < 8; ++i) codes[i] = 0;
     return 0;
   }
-  const float r = __frcp_rn(d);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) codes[i] = e2m1x2_encode(v[2 * i] * r, v[2 * i + 1] * r);
+  for (int i = 0; i < 8; ++i) codes[i] = e2m1x2_encode(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d));
   return s;
 }
 
@@ -441,13 +437,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int i = 0; i < 16; i += 4) {
             const float4 gg = *reinterpret_cast<const float4*>(wglob + 16 * b + i);
             const float4 ug = *reinterpret_cast<const float4*>(wglob + 64 + 16 * b + i);
-            h[i] = silu_fast(__uint_as_float(g[i]) * gg.x) * (__uint_as_float(v[i]) * ug.x);
-            h[i + 1] = silu_fast(__uint_as_float(g[i + 1]) * gg.y) * (__uint_as_float(v[i + 1]) * ug.y);
-            h[i + 2] = silu_fast(__uint_as_float(g[i + 2]) * gg.z) * (__uint_as_float(v[i + 2]) * ug.z);
-            h[i + 3] = silu_fast(__uint_as_float(g[i + 3]) * gg.w) * (__uint_as_float(v[i + 3]) * ug.w);
+            h[i] = silu(__uint_as_float(g[i]) * gg.x) * (__uint_as_float(v[i]) * ug.x);
+            h[i + 1] = silu(__uint_as_float(g[i + 1]) * gg.y) * (__uint_as_float(v[i + 1]) * ug.y);
+            h[i + 2] = silu(__uint_as_float(g[i + 2]) * gg.z) * (__uint_as_float(v[i + 2]) * ug.z);
+            h[i + 3] = silu(__uint_as_float(g[i + 3]) * gg.w) * (__uint_as_float(v[i + 3]) * ug.w);
           }
           uint8_t codes[8];
-          const uint8_t sc = quantize_act16_fast(h, codes);
+          const uint8_t sc = quantize_act16(h, codes);
           sfw |= (uint32_t)sc << (8 * (b - 2 * hf));
           if (valid) {
             uint2 pk;
@@ -464,71 +460,149 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j) +
                   lane);
         __syncwarp();
-        if (a.stage_y) {
-          // rows [row_w, row_w + 32) of the unit are this warp's lanes; the
-          // first nvalid of them exist (the rest pad the expert's last tile)
-          const int row_w = nt * 128 + 32 * q;
-          const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
-          float* stg = reinterpret_cast<float*>(sm + pf_stg_off(E)) + (warp - 2) * 32 * kPfStgRow;
-          // Y is [token][H / 128 column tiles][slot][128]: the lane's row is
-          // pair p = t * k + slot, its tile-j segment at (t * H/128 + j) * k + slot
-          int yseg = 0;
-          if (lane < nvalid) {
-            const int pr = __ldg(a.perm + s_off[e] + row_w + lane);
-            yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
-          }
+        // Y is [token][H / 128 column tiles][slot][128]: a lane's row is
+        // pair p = t * k + slot, its tile-j segment at (t * H/128 + j) * k + slot;
+        // bf16 when the forward's output is bf16, else fp32
+        if (a.y_bf16) {
+          uint16_t* Yb = reinterpret_cast<uint16_t*>(a.Y);
+          if (a.stage_y) {
+            // rows [row_w, row_w + 32) of the unit are this warp's lanes; the
+            // first nvalid of them exist (the rest pad the expert's last tile)
+            const int row_w = nt * 128 + 32 * q;
+            const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
+            unsigned char* stg = sm + pf_stg_off(E) + (warp - 2) * 32 * kPfStgRow;
+            int yseg = 0;
+            if (lane < nvalid) {
+              const int pr = __ldg(a.perm + s_off[e] + row_w + lane);
+              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
+            }
+            const int cb = 64 * hf;  // the warp's 64 columns
+            uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kPfStgRow);
 #pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            const int cb = 64 * hf + 32 * cc;  // first of the chunk's 32 columns
-            uint32_t v0[16], v1[16];
-            tc_ld16(taddr + cb, v0);
-            tc_ld16(taddr + cb + 16, v1);
-            tc_wait16x2(v0, v1);
-            float* srow = stg + lane * kPfStgRow;
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t v0[16], v1[16];
+              tc_ld16(taddr + cb + 32 * cc, v0);
+              tc_ld16(taddr + cb + 32 * cc + 16, v1);
+              tc_wait16x2(v0, v1);
+              uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              const float4 g0 = *reinterpret_cast<const float4*>(wglob + cb + i);
-              const float4 g1 = *reinterpret_cast<const float4*>(wglob + cb + 16 + i);
-              *reinterpret_cast<float4*>(srow + i) =
-                  make_float4(__uint_as_float(v0[i]) * g0.x, __uint_as_float(v0[i + 1]) * g0.y,
-                              __uint_as_float(v0[i + 2]) * g0.z, __uint_as_float(v0[i + 3]) * g0.w);
-              *reinterpret_cast<float4*>(srow + 16 + i) =
-                  make_float4(__uint_as_float(v1[i]) * g1.x, __uint_as_float(v1[i + 1]) * g1.y,
-                              __uint_as_float(v1[i + 2]) * g1.z, __uint_as_float(v1[i + 3]) * g1.w);
+              for (int i = 0; i < 16; i += 2) {
+                const float2 g0 = *reinterpret_cast<const float2*>(wglob + cb + 32 * cc + i);
+                const float2 g1 = *reinterpret_cast<const float2*>(wglob + cb + 32 * cc + 16 + i);
+                const __nv_bfloat162 b0 =
+                    __floats2bfloat162_rn(__uint_as_float(v0[i]) * g0.x, __uint_as_float(v0[i + 1]) * g0.y);
+                const __nv_bfloat162 b1 =
+                    __floats2bfloat162_rn(__uint_as_float(v1[i]) * g1.x, __uint_as_float(v1[i + 1]) * g1.y);
+                pk[i / 2] = *reinterpret_cast<const uint32_t*>(&b0);
+                pk[8 + i / 2] = *reinterpret_cast<const uint32_t*>(&b1);
+              }
+              uint4* s4 = reinterpret_cast<uint4*>(srow + 16 * cc);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) s4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const int r = 4 * i + (lane >> 3), c4 = 4 * (lane & 7);
+              const int r = 4 * i + (lane >> 3), c8 = 8 * (lane & 7);
               const int seg = __shfl_sync(0xffffffffu, yseg, r);
               if (r < nvalid)
-                *reinterpret_cast<float4*>(a.Y + (int64_t)seg * 128 + cb + c4) =
-                    *reinterpret_cast<const float4*>(stg + r * kPfStgRow + c4);
+                *reinterpret_cast<uint4*>(Yb + (int64_t)seg * 128 + cb + c8) =
+                    *reinterpret_cast<const uint4*>(stg + r * kPfStgRow + 2 * c8);
             }
             __syncwarp();
+          } else {
+            int yseg = 0;
+            if (valid) {
+              const int pr = __ldg(a.perm + s_off[e] + local);
+              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
+            }
+            uint16_t* yrow = Yb + (int64_t)yseg * 128;
+#pragma unroll 1
+            for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+              uint32_t v[16];
+              tc_ld16(taddr + 16 * c, v);
+              tc_wait16(v);
+              if (valid) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                  const float2 gd = *reinterpret_cast<const float2*>(wglob + 16 * c + i);
+                  const __nv_bfloat162 b =
+                      __floats2bfloat162_rn(__uint_as_float(v[i]) * gd.x, __uint_as_float(v[i + 1]) * gd.y);
+                  pk[i / 2] = *reinterpret_cast<const uint32_t*>(&b);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(yrow + 16 * c);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              }
+            }
           }
         } else {
-          int yseg = 0;
-          if (valid) {
-            const int pr = __ldg(a.perm + s_off[e] + local);
-            yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
-          }
-          float* yrow = a.Y + (int64_t)yseg * 128;
+          float* Yf = reinterpret_cast<float*>(a.Y);
+          if (a.stage_y) {
+            // rows [row_w, row_w + 32) of the unit are this warp's lanes; the
+            // first nvalid of them exist (the rest pad the expert's last tile)
+            const int row_w = nt * 128 + 32 * q;
+            const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
+            float* stg = reinterpret_cast<float*>(sm + pf_stg_off(E) + (warp - 2) * 32 * kPfStgRow);
+            int yseg = 0;
+            if (lane < nvalid) {
+              const int pr = __ldg(a.perm + s_off[e] + row_w + lane);
+              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
+            }
 #pragma unroll 1
-          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
-            uint32_t v[16];
-            tc_ld16(taddr + 16 * c, v);
-            tc_wait16(v);
-            if (valid) {
+            for (int cc = 0; cc < 2; ++cc) {
+              const int cb = 64 * hf + 32 * cc;  // first of the chunk's 32 columns
+              uint32_t v0[16], v1[16];
+              tc_ld16(taddr + cb, v0);
+              tc_ld16(taddr + cb + 16, v1);
+              tc_wait16x2(v0, v1);
+              float* srow = stg + lane * (kPfStgRow / 4);
 #pragma unroll
               for (int i = 0; i < 16; i += 4) {
-                const float4 gd = *reinterpret_cast<const float4*>(wglob + 16 * c + i);
-                float4 o;
-                o.x = __uint_as_float(v[i]) * gd.x;
-                o.y = __uint_as_float(v[i + 1]) * gd.y;
-                o.z = __uint_as_float(v[i + 2]) * gd.z;
-                o.w = __uint_as_float(v[i + 3]) * gd.w;
-                *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
+                const float4 g0 = *reinterpret_cast<const float4*>(wglob + cb + i);
+                const float4 g1 = *reinterpret_cast<const float4*>(wglob + cb + 16 + i);
+                *reinterpret_cast<float4*>(srow + i) =
+                    make_float4(__uint_as_float(v0[i]) * g0.x, __uint_as_float(v0[i + 1]) * g0.y,
+                                __uint_as_float(v0[i + 2]) * g0.z, __uint_as_float(v0[i + 3]) * g0.w);
+                *reinterpret_cast<float4*>(srow + 16 + i) =
+                    make_float4(__uint_as_float(v1[i]) * g1.x, __uint_as_float(v1[i + 1]) * g1.y,
+                                __uint_as_float(v1[i + 2]) * g1.z, __uint_as_float(v1[i + 3]) * g1.w);
+              }
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3), c4 = 4 * (lane & 7);
+                const int seg = __shfl_sync(0xffffffffu, yseg, r);
+                if (r < nvalid)
+                  *reinterpret_cast<float4*>(Yf + (int64_t)seg * 128 + cb + c4) =
+                      *reinterpret_cast<const float4*>(stg + r * (kPfStgRow / 4) + c4);
+              }
+              __syncwarp();
+            }
+          } else {
+            int yseg = 0;
+            if (valid) {
+              const int pr = __ldg(a.perm + s_off[e] + local);
+              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
+            }
+            float* yrow = Yf + (int64_t)yseg * 128;
+#pragma unroll 1
+            for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+              uint32_t v[16];
+              tc_ld16(taddr + 16 * c, v);
+              tc_wait16(v);
+              if (valid) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                  const float4 gd = *reinterpret_cast<const float4*>(wglob + 16 * c + i);
+                  float4 o;
+                  o.x = __uint_as_float(v[i]) * gd.x;
+                  o.y = __uint_as_float(v[i + 1]) * gd.y;
+                  o.z = __uint_as_float(v[i + 2]) * gd.z;
+                  o.w = __uint_as_float(v[i + 3]) * gd.w;
+                  *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
+                }
               }
             }
           }
@@ -546,8 +620,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(v[2 * i]);
-              const float h1 = silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
+              const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(v[2 * i]);
+              const float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
               const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
               pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
             }
@@ -591,15 +665,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       } else {
         // combine for token t over output rows [128 j, 128 j + 128): the
         // slots' rows of Y in slot order, then sigma * the shared expert.
-        // Up to 8 slots keep their positions and weights in registers and
-        // have their Y loads in flight four slots at a time.
+        // Up to 8 slots keep their weights in registers and have their Y
+        // loads in flight together (fp32: four slots at a time).
         const int t = local;
         const int k = a.top_k;
         const float* w = a.topk_w + (int64_t)t * k;
         const float sig = valid ? a.sigma[t] : 0.f;
         const int64_t obase = (int64_t)t * H + 128 * j;
-        // the token's k slot segments of column tile j, contiguous
-        const float* yt = a.Y + ((int64_t)t * (H / 128) + j) * k * 128;
+        // the token's k slot segments of column tile j, contiguous (bf16 or fp32)
+        const int64_t yoff = ((int64_t)t * (H / 128) + j) * k * 128;
+        const uint16_t* ytb = reinterpret_cast<const uint16_t*>(a.Y) + yoff;
+        const float* ytf = reinterpret_cast<const float*>(a.Y) + yoff;
         float wj[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) wj[jj] = (valid && jj < k) ? __ldg(w + jj) : 0.f;
@@ -612,43 +688,81 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             float o[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = 0.f;
-            if (k <= 8) {
+            if (a.y_bf16) {
+              // each slot's 16 bf16 values of this chunk are two 16-byte loads;
+              // up to 8 slots have theirs in flight together
+              if (k <= 8) {
+                uint4 y[8][2];
 #pragma unroll
-              for (int j0 = 0; j0 < 8; j0 += 4) {
-                if (j0 < k) {
-                  float4 y[4][4];
+                for (int q2 = 0; q2 < 8; ++q2) {
+                  const uint4* yp = reinterpret_cast<const uint4*>(ytb + q2 * 128 + 16 * c);
+                  y[q2][0] = q2 < k ? __ldg(yp) : make_uint4(0, 0, 0, 0);
+                  y[q2][1] = q2 < k ? __ldg(yp + 1) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-                  for (int q2 = 0; q2 < 4; ++q2) {
-                    const float4* yp = reinterpret_cast<const float4*>(yt + (j0 + q2) * 128 + 16 * c);
+                for (int q2 = 0; q2 < 8; ++q2) {
+                  if (q2 < k) {
+                    const uint32_t u[8] = {y[q2][0].x, y[q2][0].y, y[q2][0].z, y[q2][0].w,
+                                           y[q2][1].x, y[q2][1].y, y[q2][1].z, y[q2][1].w};
 #pragma unroll
-                    for (int i4 = 0; i4 < 4; ++i4)
-                      y[q2][i4] = (j0 + q2 < k) ? __ldg(yp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  }
-#pragma unroll
-                  for (int q2 = 0; q2 < 4; ++q2) {
-                    if (j0 + q2 < k) {
-#pragma unroll
-                      for (int i4 = 0; i4 < 4; ++i4) {
-                        o[4 * i4] = fmaf(wj[j0 + q2], y[q2][i4].x, o[4 * i4]);
-                        o[4 * i4 + 1] = fmaf(wj[j0 + q2], y[q2][i4].y, o[4 * i4 + 1]);
-                        o[4 * i4 + 2] = fmaf(wj[j0 + q2], y[q2][i4].z, o[4 * i4 + 2]);
-                        o[4 * i4 + 3] = fmaf(wj[j0 + q2], y[q2][i4].w, o[4 * i4 + 3]);
-                      }
+                    for (int i = 0; i < 8; ++i) {
+                      o[2 * i] = fmaf(wj[q2], __uint_as_float(u[i] << 16), o[2 * i]);
+                      o[2 * i + 1] = fmaf(wj[q2], __uint_as_float(u[i] & 0xffff0000u), o[2 * i + 1]);
                     }
+                  }
+                }
+              } else {
+                for (int jj = 0; jj < k; ++jj) {
+                  const float wv = __ldg(w + jj);
+                  const uint4* yp = reinterpret_cast<const uint4*>(ytb + jj * 128 + 16 * c);
+                  const uint4 y0 = yp[0], y1 = yp[1];
+                  const uint32_t u[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    o[2 * i] = fmaf(wv, __uint_as_float(u[i] << 16), o[2 * i]);
+                    o[2 * i + 1] = fmaf(wv, __uint_as_float(u[i] & 0xffff0000u), o[2 * i + 1]);
                   }
                 }
               }
             } else {
-              for (int jj = 0; jj < k; ++jj) {
-                const float wv = __ldg(w + jj);
-                const float4* yp = reinterpret_cast<const float4*>(yt + jj * 128 + 16 * c);
+              if (k <= 8) {
 #pragma unroll
-                for (int i4 = 0; i4 < 4; ++i4) {
-                  const float4 y = yp[i4];
-                  o[4 * i4] = fmaf(wv, y.x, o[4 * i4]);
-                  o[4 * i4 + 1] = fmaf(wv, y.y, o[4 * i4 + 1]);
-                  o[4 * i4 + 2] = fmaf(wv, y.z, o[4 * i4 + 2]);
-                  o[4 * i4 + 3] = fmaf(wv, y.w, o[4 * i4 + 3]);
+                for (int j0 = 0; j0 < 8; j0 += 4) {
+                  if (j0 < k) {
+                    float4 y[4][4];
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                      const float4* yp = reinterpret_cast<const float4*>(ytf + (j0 + q2) * 128 + 16 * c);
+#pragma unroll
+                      for (int i4 = 0; i4 < 4; ++i4)
+                        y[q2][i4] = (j0 + q2 < k) ? __ldg(yp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                      if (j0 + q2 < k) {
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; ++i4) {
+                          o[4 * i4] = fmaf(wj[j0 + q2], y[q2][i4].x, o[4 * i4]);
+                          o[4 * i4 + 1] = fmaf(wj[j0 + q2], y[q2][i4].y, o[4 * i4 + 1]);
+                          o[4 * i4 + 2] = fmaf(wj[j0 + q2], y[q2][i4].z, o[4 * i4 + 2]);
+                          o[4 * i4 + 3] = fmaf(wj[j0 + q2], y[q2][i4].w, o[4 * i4 + 3]);
+                        }
+                      }
+                    }
+                  }
+                }
+              } else {
+                for (int jj = 0; jj < k; ++jj) {
+                  const float wv = __ldg(w + jj);
+                  const float4* yp = reinterpret_cast<const float4*>(ytf + jj * 128 + 16 * c);
+#pragma unroll
+                  for (int i4 = 0; i4 < 4; ++i4) {
+                    const float4 y = yp[i4];
+                    o[4 * i4] = fmaf(wv, y.x, o[4 * i4]);
+                    o[4 * i4 + 1] = fmaf(wv, y.y, o[4 * i4 + 1]);
+                    o[4 * i4 + 2] = fmaf(wv, y.z, o[4 * i4 + 2]);
+                    o[4 * i4 + 3] = fmaf(wv, y.w, o[4 * i4 + 3]);
+                  }
                 }
               }
             }

@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
 
 constexpr int kSortThreads = 1024;
 constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortChunk = 4096;  // pairs per CTA of the many-CTA sort
 
 // Exclusive scan of v over the CTA's 1024 threads; returns the prefix and
 // writes the total to *total.
@@ -474,6 +475,121 @@ __global__ void __launch_bounds__(kSortThreads) k_sort(RouteArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ counting sort over many CTAs
+
+// The same stable counting sort for large P, in three grids: each CTA c
+// counts its chunk of pairs [c * kSortChunk, ...) per expert; one CTA turns
+// the counts into the expert offsets and, per (chunk, expert), the first
+// sorted position of that chunk's pairs (chunks in order); each CTA then
+// scatters its chunk exactly as k_sort does (warps in order, lanes in order
+// within a warp), so every expert's pairs still come out in increasing pair
+// id.
+
+// Per-warp histogram of the warp's part of [c0, c1) into hist[warp][e].
+__device__ void sort_warp_hist(const RouteArgs& a, int E, int c0, int c1, int* hist) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kSortWarps * E; i += kSortThreads) hist[i] = 0;
+  __syncthreads();
+  const int CH = (c1 - c0 + kSortWarps - 1) / kSortWarps;
+  const int w0 = min(c1, c0 + warp * CH), w1 = min(c1, w0 + CH);
+  for (int p = w0 + lane; p < w1; p += 32) {
+    int e = __ldg(a.topk_idx + p);
+    if ((unsigned)e >= (unsigned)E) { set_status(a.status, kStatusRange); e = 0; }
+    atomicAdd(&hist[warp * E + e], 1);
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kSortThreads) k_sort_count(RouteArgs a) {
+  extern __shared__ int hist[];  // [kSortWarps][E]
+  const int E = a.E, P = a.T * a.top_k;
+  const int c0 = min(P, (int)blockIdx.x * kSortChunk), c1 = min(P, c0 + kSortChunk);
+  sort_warp_hist(a, E, c0, c1, hist);
+  for (int e = threadIdx.x; e < E; e += kSortThreads) {
+    int cnt = 0;
+    for (int w = 0; w < kSortWarps; ++w) cnt += hist[w * E + e];
+    a.sort_cnt[(int64_t)blockIdx.x * E + e] = cnt;
+  }
+}
+
+// One CTA: offsets, the touched list, and sort_cnt[c][e] replaced by the
+// first sorted position of chunk c's pairs of expert e.
+__global__ void __launch_bounds__(kSortThreads) k_sort_scan(RouteArgs a, int n_chunks) {
+  __shared__ int scratch[33];
+  const int E = a.E, P = a.T * a.top_k;
+  for (int base = 0; base < E; base += kSortThreads) {
+    const int e = base + threadIdx.x;
+    int cnt = 0;
+    if (e < E)
+      for (int c = 0; c < n_chunks; ++c) cnt += a.sort_cnt[(int64_t)c * E + e];
+    int total;
+    int off = block_exclusive_scan(cnt, scratch, &total);
+    const int prev_total = base == 0 ? 0 : a.offsets[base];
+    off += prev_total;
+    int tflag;
+    const int tpos = block_exclusive_scan((e < E && cnt > 0) ? 1 : 0, scratch, &tflag);
+    const int prev_touched = base == 0 ? 0 : a.n_touched[0];
+    if (e < E) {
+      a.offsets[e] = off;
+      if (cnt > 0) a.touched[prev_touched + tpos] = e;
+      int cur = off;
+      for (int c = 0; c < n_chunks; ++c) {
+        int* q = a.sort_cnt + (int64_t)c * E + e;
+        const int h = *q;
+        *q = cur;
+        cur += h;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      a.offsets[min(base + kSortThreads, E)] = prev_total + total;
+      a.n_touched[0] = prev_touched + tflag;
+    }
+    __threadfence_block();
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    a.offsets[E] = P;
+    if (a.touched_total) atomicAdd(a.touched_total, (unsigned long long)a.n_touched[0]);
+  }
+}
+
+__global__ void __launch_bounds__(kSortThreads) k_sort_scatter(RouteArgs a) {
+  extern __shared__ int hist[];  // [kSortWarps][E]: counts, then each warp's cursors
+  const int E = a.E, P = a.T * a.top_k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = min(P, (int)blockIdx.x * kSortChunk), c1 = min(P, c0 + kSortChunk);
+  sort_warp_hist(a, E, c0, c1, hist);
+  for (int e = threadIdx.x; e < E; e += kSortThreads) {
+    int cur = a.sort_cnt[(int64_t)blockIdx.x * E + e];
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int h = hist[w * E + e];
+      hist[w * E + e] = cur;
+      cur += h;
+    }
+  }
+  __syncthreads();
+  const int CH = (c1 - c0 + kSortWarps - 1) / kSortWarps;
+  const int w0 = min(c1, c0 + warp * CH), w1 = min(c1, w0 + CH);
+  for (int p0 = w0; p0 < w1; p0 += 32) {
+    const int p = p0 + lane;
+    const bool valid = p < w1;
+    int e = valid ? __ldg(a.topk_idx + p) : -1 - lane;
+    if (valid && (unsigned)e >= (unsigned)E) e = 0;
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(mask & ((1u << lane) - 1));
+    int pos = 0;
+    if (valid) pos = hist[warp * E + e] + rank;
+    __syncwarp();
+    if (valid) {
+      a.perm[pos] = p;
+      a.inv[p] = pos;
+      if (rank == 0) hist[warp * E + e] += __popc(mask);
+    }
+    __syncwarp();
+  }
+}
+
 // ------------------------------------------------------------------ launchers
 
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, uint8_t* codes,
@@ -523,10 +639,27 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int parts) {
   }
   if (parts & kRouteSort) {
     size_t smem = (size_t)kSortWarps * a.E * 4;
-    FTMOE_PROF_BEGIN("k_sort", s);
-    k_sort<<<1, kSortThreads, smem, s>>>(a);
-    FTMOE_PROF_END(s);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const int64_t P = (int64_t)a.T * a.top_k;
+    const int n_chunks = (int)((P + kSortChunk - 1) / kSortChunk);
+    if (a.sort_cnt && n_chunks > 1 && n_chunks <= a.sort_max_chunks) {
+      FTMOE_PROF_BEGIN("k_sort_count", s);
+      k_sort_count<<<n_chunks, kSortThreads, smem, s>>>(a);
+      FTMOE_PROF_END(s);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+      FTMOE_PROF_BEGIN("k_sort_scan", s);
+      k_sort_scan<<<1, kSortThreads, 0, s>>>(a, n_chunks);
+      FTMOE_PROF_END(s);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+      FTMOE_PROF_BEGIN("k_sort_scatter", s);
+      k_sort_scatter<<<n_chunks, kSortThreads, smem, s>>>(a);
+      FTMOE_PROF_END(s);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    } else {
+      FTMOE_PROF_BEGIN("k_sort", s);
+      k_sort<<<1, kSortThreads, smem, s>>>(a);
+      FTMOE_PROF_END(s);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
   }
   return cudaSuccess;
 }
@@ -544,6 +677,12 @@ cudaError_t route_set_smem_limits(int H, int E) {
     return e;
   if ((e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kTopkWarps * 1024 * 16)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_sort_count, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortWarps * 1024 * 4)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_sort_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSortWarps * 1024 * 4)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(k_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortWarps * 1024 * 4);
 }

@@ -60,13 +60,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete; false after the
 // time limit (status timeout bit set).  The clock is read only after many
 // unsuccessful polls, so a wait that ends soon costs nothing extra.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// `limit_ns` shortens the limit (tests of the failure path).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   for (int i = 0; i < 4096; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+    if ((i & 1023) == 0 && globaltimer() - t0 > limit_ns) {
       set_status(status, kStatusTimeout);
       return false;
     }

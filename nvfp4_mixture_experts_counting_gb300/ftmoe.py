@@ -18,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libftmoe.so")
 
 ABI_VERSION = 2
-OUT_BF16, OUT_FP32, OUT_ACCUMULATE = 0, 1, 0x100
+OUT_BF16, OUT_FP32, OUT_ACCUMULATE, ACT_BF16 = 0, 1, 0x100, 0x200
 
 STATUS = {
     0: "OK", -1: "INVALID_ARG", -2: "ALIGNMENT", -3: "NOT_LOADED", -4: "SLICE_OUT_OF_RANGE",
@@ -83,6 +83,13 @@ SIGNATURES = {
     "ftmoe_profile_read": ([C.c_void_p, C.POINTER(KernelTime), C.c_int, C.POINTER(C.c_int)], C.c_int),
     "ftmoe_route_static": ([C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "ftmoe_route_static_status": ([C.c_void_p], C.c_int),
+    "ftmoe_forward_experts": ([C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
+                               C.POINTER(Aux), C.c_void_p], C.c_int),
+    "ftmoe_reduce_partials": ([C.c_void_p, C.c_int, C.c_int64, C.c_void_p, C.c_int, C.c_void_p], C.c_int),
+    "ftmoe_test_withhold_stage": ([C.c_void_p, C.c_int, C.c_int64], C.c_int),
+    "ftmoe_slice_format": ([C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                            C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_void_p], C.c_int),
     "ftmoe_quantize_weights": ([C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p], C.c_int),
     "ftmoe_quantize_activations": ([C.c_void_p, C.c_int64, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p],
@@ -198,6 +205,45 @@ def ftmoe_route_static(x, T: int, H: int, router_w, router_bias, E: int, top_k: 
     _check(lib().ftmoe_route_static(_ptr(x), T, H, _ptr(router_w), _ptr(router_bias), E, top_k,
                                     int(norm_topk_prob), _ptr(topk_idx), _ptr(topk_w), _ptr(offsets),
                                     _ptr(perm), _ptr(inv), _stream(stream)), "ftmoe_route_static")
+
+
+def ftmoe_forward_experts(h: int, layer: int, x, T: int, out, out_flags: int, expert_mask,
+                          aux: Optional[Aux] = None, stream=None):
+    """The routed part of the layer over the experts whose mask byte (host
+    numpy uint8 [E]) is set: one expert-parallel rank's share."""
+    import numpy as np
+    m = np.ascontiguousarray(expert_mask, dtype=np.uint8)
+    _check(lib().ftmoe_forward_experts(h, layer, _ptr(x), T, _ptr(out), out_flags, m.ctypes.data,
+                                       C.byref(aux) if aux is not None else None, _stream(stream)),
+           "ftmoe_forward_experts")
+
+
+def ftmoe_reduce_partials(parts, n_parts: int, n: int, out, out_flags: int = OUT_BF16, stream=None):
+    """out <- sum over ranks of fp32 partials [n_parts][n], in rank order."""
+    _check(lib().ftmoe_reduce_partials(_ptr(parts), n_parts, n, _ptr(out), out_flags, _stream(stream)),
+           "ftmoe_reduce_partials")
+
+
+def ftmoe_route_static_status(stream=None) -> int:
+    """Status of the latest ftmoe_route_static call (0, DEVICE_CHECK or TIMEOUT)."""
+    return lib().ftmoe_route_static_status(_stream(stream))
+
+
+def ftmoe_test_withhold_stage(h: int, enable: bool, wait_limit_ns: int = 0):
+    _check(lib().ftmoe_test_withhold_stage(h, int(enable), wait_limit_ns), "ftmoe_test_withhold_stage")
+
+
+FMT = {"nvfp4": 0, "fp8_block": 1, "q4_0": 2, "mxfp4": 3}
+MAT_GATE_UP, MAT_DOWN = 0, 1
+
+
+def ftmoe_slice_format(fmt: str, matrix: int, E: int, H: int, I: int, i0: int, I_loc: int, src, dst, stream=None):
+    """Slice E experts' matrix in bank format `fmt` to a window; src / dst
+    are lists of device tensors (the format's arrays, in the header's order)."""
+    S = (C.c_void_p * 3)(*[_ptr(t) for t in src] + [None] * (3 - len(src)))
+    D = (C.c_void_p * 3)(*[_ptr(t) for t in dst] + [None] * (3 - len(dst)))
+    _check(lib().ftmoe_slice_format(FMT[fmt], matrix, E, H, I, i0, I_loc, S, D, _stream(stream)),
+           "ftmoe_slice_format")
 
 
 def ftmoe_quantize_weights(w, rows: int, K: int, codes, scales, globals_, stream=None):

@@ -123,6 +123,36 @@ def shared_weights(wl: Workload, layer: int = 0, device="cpu"):
     return gu.to(torch.bfloat16), dn.to(torch.bfloat16), g.to(torch.bfloat16)
 
 
+def format_matrix(fmt: str, N: int, K: int, seed: int) -> dict:
+    """Random bytes of a matrix [N, K] stored in one of the bank formats that
+    the loader slices (any byte pattern is a matrix of the format; NaN codes
+    are avoided), as numpy arrays named like the format's tensors:
+
+    * ``nvfp4``     codes [N, K/2], E4M3 scales [N, K/16], fp32 globals [N]
+    * ``fp8_block`` E4M3 q [N, K], fp32 scale [ceil(N/128), ceil(K/128)]
+    * ``q4_0``      blocks [N, K/32, 18] (fp16 scale, then 16 code bytes)
+    * ``mxfp4``     blocks_t [K/2, N], UE8M0 scales_t [K/32, N]"""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    if fmt == "nvfp4":
+        return {"codes": rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8),
+                "scales": rng.integers(0, 0x7F, size=(N, K // 16), dtype=np.uint8),
+                "globals": rng.random(N).astype(np.float32)}
+    if fmt == "fp8_block":
+        q = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+        q[(q & 0x7F) == 0x7F] = 0
+        return {"q": q, "scale": rng.random(((N + 127) // 128, (K + 127) // 128)).astype(np.float32)}
+    if fmt == "q4_0":
+        blocks = rng.integers(0, 256, size=(N, K // 32, 18), dtype=np.uint8)
+        d = (rng.random((N, K // 32)) * 0.01).astype(np.float16)
+        blocks[:, :, 0:2] = d.view(np.uint8).reshape(N, K // 32, 2)
+        return {"blocks": blocks}
+    if fmt == "mxfp4":
+        return {"blocks_t": rng.integers(0, 256, size=(K // 2, N), dtype=np.uint8),
+                "scales_t": rng.integers(100, 140, size=(K // 32, N), dtype=np.uint8)}
+    raise ValueError(fmt)
+
+
 def bf16_bits(t: torch.Tensor) -> torch.Tensor:
     """The raw 16-bit patterns of a bf16 tensor (as int16)."""
     return t.contiguous().view(torch.int16)

@@ -161,21 +161,32 @@ def check_window(I: int, i0: int, I_loc: int) -> None:
         raise ValueError("i0 and I_loc must be multiples of 16")
 
 
-def expert_pair_outputs(bank: ExpertBank, xq_rows: np.ndarray, I: int, i0: int, I_loc: int):
-    """Y rows [m, H] (fp64) of one expert for the dequantised activations of
-    its m pairs (``xq_rows`` [m, H] fp64).
+def expert_pair_outputs(bank: ExpertBank, xq_rows: np.ndarray, I: int, i0: int, I_loc: int,
+                        activations: str = "nvfp4"):
+    """Y rows [m, H] (fp64) of one expert for the activations of its m pairs
+    (``xq_rows`` [m, H] fp64: dequantised NVFP4 values, or the bf16 values
+    themselves in the bf16-activation mode).
 
-    G = W_gu[window rows] . xq in fp64; h = silu(G_gate) * G_up, rounded to
-    fp32 and quantised per 16-block along the window with global 1.0;
-    Y = W_dn[:, window] . hq  (gate/up rows and down columns per [I62]
+    G = W_gu[window rows] . xq in fp64; h = silu(G_gate) * G_up; then
+    * activations "nvfp4" (W4A4, the layer's reading): h rounded to fp32 and
+      quantised per 16-block along the window with global 1.0;
+    * activations "bf16" (W4A16, the weight-only 4-bit kernel the pages'
+      review thread selects for this backend, PR #385 mirror, kernel-selection
+      fix): h rounded to bf16, as the shared expert's intermediate;
+    Y = W_dn[:, window] . h  (gate/up rows and down columns per [I62]
     "What it touches"; SwiGLU on the gate/up pair)."""
     rows = slice_window_rows(I, i0, I_loc)
     w_gu = nvfp4.dequantize_rows(bank.gu_codes[rows], bank.gu_scales[rows], bank.gu_global[rows])
     G = xq_rows @ w_gu.T                                   # [m, 2*I_loc]
     h = silu(G[:, :I_loc]) * G[:, I_loc:]
-    h32 = h.astype(np.float32)
-    hc, hs = nvfp4.quantize_activation_rows(h32)
-    hq = nvfp4.dequantize_rows(hc, hs)                     # [m, I_loc]
+    if activations == "bf16":
+        hq = nvfp4.bf16_round(h)
+    elif activations == "nvfp4":
+        h32 = h.astype(np.float32)
+        hc, hs = nvfp4.quantize_activation_rows(h32)
+        hq = nvfp4.dequantize_rows(hc, hs)                 # [m, I_loc]
+    else:
+        raise ValueError("activations must be 'nvfp4' or 'bf16'")
     c0, c1 = i0 // 2, (i0 + I_loc) // 2
     b0, b1 = i0 // nvfp4.BLOCK, (i0 + I_loc) // nvfp4.BLOCK
     w_dn = nvfp4.dequantize_rows(bank.dn_codes[:, c0:c1], bank.dn_scales[:, b0:b1], bank.dn_global)
@@ -218,7 +229,9 @@ class LayerResult:
 def moe_layer(x, router_w, router_bias, get_expert: Callable[[int], ExpertBank],
               sh_gate_up, sh_down, sh_gate, *, I: int, I_s: int, top_k: int,
               i0: int = 0, I_loc: Optional[int] = None, norm_topk_prob: bool = True,
-              out_dtype: str = "bf16", tokens: Optional[np.ndarray] = None) -> LayerResult:
+              out_dtype: str = "bf16", tokens: Optional[np.ndarray] = None,
+              activations: str = "nvfp4", expert_mask: Optional[np.ndarray] = None,
+              include_shared: bool = True) -> LayerResult:
     """The whole layer for the window [i0, i0+I_loc) (default: all of I).
 
     ``x`` [T, H] holds bf16 values (any float dtype).  ``get_expert(e)``
@@ -229,7 +242,17 @@ def moe_layer(x, router_w, router_bias, get_expert: Callable[[int], ExpertBank],
     partition of I is the full layer ([I62] "The fix that fits").
 
     ``tokens`` restricts the per-token outputs to a subset (routing and the
-    permutation are still computed for all T); rows outside it are NaN."""
+    permutation are still computed for all T); rows outside it are NaN.
+
+    ``activations`` selects the expert contractions' activation format:
+    "nvfp4" (x and the intermediate NVFP4-quantised, the layer's reading) or
+    "bf16" (x as given and the intermediate rounded to bf16: weight-only
+    4-bit, see ``expert_pair_outputs``).
+
+    ``expert_mask`` (bool [E]) keeps only the slots whose expert is in it, and
+    ``include_shared`` drops the gated shared expert when False: with both,
+    the result is what one rank of an expert-parallel layer contributes when
+    it owns those experts ([I62] "Why not expert parallelism proper")."""
     if I_loc is None:
         I_loc = I - i0
     check_window(I, i0, I_loc)
@@ -246,19 +269,22 @@ def moe_layer(x, router_w, router_bias, get_expert: Callable[[int], ExpertBank],
     E = np.asarray(router_w).shape[0]
     offsets, perm, inv = counting_sort(idx, E)
     xc, xs = nvfp4.quantize_activation_rows(x32)
-    xq = nvfp4.dequantize_rows(xc, xs)
+    xq = nvfp4.dequantize_rows(xc, xs) if activations == "nvfp4" else x32.astype(np.float64)
 
     sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     want = np.zeros(T, dtype=bool)
     want[sel] = True
     Y = {}
+    keep = np.ones(E, dtype=bool) if expert_mask is None else np.asarray(expert_mask, dtype=bool)
     for e in range(E):
+        if not keep[e]:
+            continue
         pairs = perm[offsets[e]:offsets[e + 1]]
         pairs = [int(p) for p in pairs if want[int(p) // top_k]]
         if not pairs:
             continue
         toks = np.array([p // top_k for p in pairs])
-        ye = expert_pair_outputs(get_expert(e), xq[toks], I, i0, I_loc)
+        ye = expert_pair_outputs(get_expert(e), xq[toks], I, i0, I_loc, activations)
         for r, p in enumerate(pairs):
             Y[p] = ye[r]
     S, sigma = shared_expert(x32[sel], sh_gate_up, sh_down, sh_gate, I_s, si0, sil)
@@ -266,8 +292,9 @@ def moe_layer(x, router_w, router_bias, get_expert: Callable[[int], ExpertBank],
     for r, t in enumerate(sel):
         acc = np.zeros(H)
         for j in range(top_k):
-            acc = acc + w[t, j] * Y[int(t) * top_k + j]
-        out64[t] = acc + sigma[r] * S[r]
+            if keep[idx[t, j]]:
+                acc = acc + w[t, j] * Y[int(t) * top_k + j]
+        out64[t] = acc + sigma[r] * S[r] if include_shared else acc
     if out_dtype == "bf16":
         out = nvfp4.bf16_round(out64)
     elif out_dtype == "fp32":

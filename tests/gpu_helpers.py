@@ -64,6 +64,24 @@ class GpuBank:
             self._oracle_cache[e] = moe.quantize_expert(g.cpu().numpy(), d.cpu().numpy())
         return self._oracle_cache[e]
 
+    def prefetch_oracle_experts(self, experts, threads: int = 16):
+        """Quantise many experts with the oracle's encoder at once: the
+        masters are drawn on the GPU first (in this thread), the numpy
+        encoding then runs on a thread pool (numpy releases the GIL inside
+        its array loops)."""
+        from concurrent.futures import ThreadPoolExecutor
+        todo = [int(e) for e in experts if int(e) not in self._oracle_cache]
+        if not todo:
+            return
+        masters = {}
+        for e in todo:
+            g, d = W.expert_masters(self.wl, e, self.layer, device="cuda")
+            masters[e] = (g.cpu().numpy(), d.cpu().numpy())
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            banks = list(ex.map(lambda e: moe.quantize_expert(*masters[e]), todo))
+        for e, b in zip(todo, banks):
+            self._oracle_cache[e] = b
+
     def oracle_layer(self, x_bf16: torch.Tensor, i0=0, I_loc=None, out_dtype="bf16", tokens=None):
         wl = self.wl
         return moe.moe_layer(
@@ -107,6 +125,26 @@ def check_routing(aux: AuxBufs, ref: moe.LayerResult):
     # logits carry up to ~2^-19 * ||x|| * ||w|| (~1e-4) of error, which moves a
     # renormalised weight by at most twice that, relatively
     assert np.allclose(got["topk_w"], ref.topk_w, rtol=5e-4, atol=1e-6), "routing weights differ"
+
+
+def stratified_tokens(topk_idx: np.ndarray, n: int, seed: int, hot: int = 8, per_hot: int = 32) -> np.ndarray:
+    """A seeded sample of n tokens that holds, for each of the `hot` most
+    loaded experts, up to `per_hot` of the tokens routed to it (the experts
+    whose many full 128-row tiles a uniform sample would rarely reach), the
+    first and last token, and uniform draws for the rest."""
+    T = topk_idx.shape[0]
+    if n >= T:
+        return np.arange(T)
+    g = np.random.default_rng(seed)
+    load = np.bincount(topk_idx.reshape(-1), minlength=int(topk_idx.max()) + 1)
+    chosen = {0, T - 1}
+    for e in np.argsort(-load, kind="stable")[:hot]:
+        toks = np.nonzero((topk_idx == e).any(axis=1))[0]
+        if toks.size:
+            chosen.update(g.choice(toks, size=min(per_hot, toks.size), replace=False).tolist())
+    rest = np.setdiff1d(np.arange(T), np.fromiter(chosen, dtype=np.int64))
+    chosen.update(g.choice(rest, size=max(0, n - len(chosen)), replace=False).tolist())
+    return np.sort(np.fromiter(chosen, dtype=np.int64))
 
 
 def check_output(out: torch.Tensor, ref_out: np.ndarray, rows=None):

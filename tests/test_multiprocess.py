@@ -88,3 +88,77 @@ def test_single_rank_helpers_need_no_process_group():
     assert bench._max_over_ranks(1, 3.5) == 3.5
     assert bench.whole_job_tokens_per_s(1, 16, 1000, 156.0) == pytest.approx(16 * 1000 / 0.156)
     assert bench.replica_step_seed(0, 7) == 7 and bench.replica_step_seed(1, 7) != 7
+
+
+def _window_rank_main(rank, ws, port, q):
+    """One rank of the intermediate-axis split on CPU: its window's oracle
+    partial of the tiny layer, the partials exchanged with gloo, summed in
+    rank order."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from nvfp4_mixture_experts_counting_gb300 import workloads as W
+    from oracle import moe
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        wl = W.WORKLOADS["tiny"]
+        x = W.hidden(wl, 4).float().numpy()
+        rw = W.router_weight(wl).numpy()
+        sgu, sdn, sg = [t.float().numpy() for t in W.shared_weights(wl)]
+        banks = {}
+
+        def get(e):
+            if e not in banks:
+                g, d = W.expert_masters(wl, e)
+                banks[e] = moe.quantize_expert(g.numpy(), d.numpy())
+            return banks[e]
+
+        i0, I_loc = bench.window_of_rank(rank, ws, wl.I)
+        part = moe.moe_layer(x, rw, None, get, sgu, sdn, sg, I=wl.I, I_s=wl.I_s, top_k=wl.top_k,
+                             i0=i0, I_loc=I_loc, out_dtype="fp32").out64
+        gathered = [torch.empty(part.shape, dtype=torch.float64) for _ in range(ws)]
+        dist.all_gather(gathered, torch.from_numpy(part))
+        total = gathered[0].clone()
+        for r in range(1, ws):
+            total += gathered[r]
+        full = moe.moe_layer(x, rw, None, get, sgu, sdn, sg, I=wl.I, I_s=wl.I_s, top_k=wl.top_k,
+                             out_dtype="fp32").out64
+        q.put((rank, (i0, I_loc), float(np.max(np.abs(total.numpy() - full)) / np.max(np.abs(full)))))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("ws", [2, 4])
+def test_window_split_partials_sum_to_the_full_layer(ws):
+    """The pages' split across processes: rank r holds window r of every
+    expert and of the shared expert, with the router replicated; the SUM of
+    the ranks' partials is the whole layer (exact up to fp64 rounding: the
+    windows share no term)."""
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_window_rank_main, args=(r, ws, port, q)) for r in range(ws)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=180) for _ in range(ws))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    windows = [w for _, w, _ in res]
+    assert windows == [(r * 64 // ws, 64 // ws) for r in range(ws)]
+    for _, _, err in res:
+        assert err <= 1e-12
+
+
+def test_window_of_rank_covers_I_once():
+    sys.path.insert(0, ROOT)
+    import bench
+    for I, ws in ((640, 1), (640, 2), (640, 4), (2048, 2), (2048, 8)):
+        w = [bench.window_of_rank(r, ws, I) for r in range(ws)]
+        assert w[0][0] == 0 and sum(l for _, l in w) == I
+        assert all(a + l == b for (a, l), (b, _) in zip(w, w[1:]))
+    for ws in (3, 16):   # 640 / 3 is not whole; 640 / 16 = 40 is off the 16-block grid
+        with pytest.raises(ValueError):
+            bench.window_of_rank(0, ws, 640)

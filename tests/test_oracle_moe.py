@@ -185,6 +185,59 @@ def test_one_expert_reduces_to_dense_swiglu_mlp():
     assert np.all(res.topk_w == 1.0)
 
 
+def test_one_expert_bf16_activations_reduce_to_weight_only_mlp():
+    """The bf16-activation (W4A16) mode, E=1, k=1, zero shared expert: a
+    dense SwiGLU MLP on the dequantised weights with x unquantised and the
+    intermediate rounded to bf16 (torch fp64 matmuls, silu and bf16 cast)."""
+    rng = np.random.default_rng(26)
+    H, I = 64, 32
+    x = torch.from_numpy(rng.standard_normal((3, H)).astype(np.float32)).to(torch.bfloat16).float()
+    gu = (rng.standard_normal((2 * I, H)) * 0.1).astype(np.float32)
+    dn = (rng.standard_normal((H, I)) * 0.1).astype(np.float32)
+    bank = moe.quantize_expert(gu, dn)
+    res = moe.moe_layer(x.numpy(), np.ones((1, H), np.float32), None, lambda e: bank,
+                        np.zeros((2 * I, H)), np.zeros((H, I)), np.zeros(H),
+                        I=I, I_s=I, top_k=1, out_dtype="fp32", activations="bf16")
+    Wgu = torch.from_numpy(nvfp4.dequantize_rows(bank.gu_codes, bank.gu_scales, bank.gu_global))
+    Wdn = torch.from_numpy(nvfp4.dequantize_rows(bank.dn_codes, bank.dn_scales, bank.dn_global))
+    G = torch.nn.functional.linear(x.double(), Wgu)
+    h = (torch.nn.functional.silu(G[:, :I]) * G[:, I:]).to(torch.bfloat16).double()
+    y = torch.nn.functional.linear(h, Wdn)
+    assert np.allclose(res.out64, y.numpy(), rtol=1e-12, atol=1e-14)
+    # and it differs from the W4A4 layer (the activations are not quantised)
+    res4 = moe.moe_layer(x.numpy(), np.ones((1, H), np.float32), None, lambda e: bank,
+                         np.zeros((2 * I, H)), np.zeros((H, I)), np.zeros(H),
+                         I=I, I_s=I, top_k=1, out_dtype="fp32")
+    assert not np.allclose(res4.out64, res.out64, rtol=1e-3)
+
+
+def test_expert_subsets_add_up_to_the_layer():
+    """The routed parts over a partition of the experts (rank r owning the
+    experts e with e % G == r), plus the gated shared expert once, are the
+    whole layer; a subset's part has no term of another subset's expert."""
+    from nvfp4_mixture_experts_counting_gb300 import workloads as W
+    wl = W.WORKLOADS["tiny"]
+    x = W.hidden(wl, 6, step=4).float().numpy()
+    rw = W.router_weight(wl).numpy()
+    sgu, sdn, sg = [t.float().numpy() for t in W.shared_weights(wl)]
+    banks = {e: moe.quantize_expert(*[m.numpy() for m in W.expert_masters(wl, e)]) for e in range(wl.E)}
+    kw = dict(I=wl.I, I_s=wl.I_s, top_k=wl.top_k, out_dtype="fp32")
+    full = moe.moe_layer(x, rw, None, banks.__getitem__, sgu, sdn, sg, **kw)
+    shared_only = moe.moe_layer(x, rw, None, banks.__getitem__, sgu, sdn, sg,
+                                expert_mask=np.zeros(wl.E, bool), **kw).out64
+    for G in (2, 4):
+        parts = [moe.moe_layer(x, rw, None, banks.__getitem__, sgu, sdn, sg, include_shared=False,
+                               expert_mask=(np.arange(wl.E) % G == r), **kw).out64 for r in range(G)]
+        assert np.allclose(sum(parts) + shared_only, full.out64, rtol=1e-12, atol=1e-14)
+    # a token whose k experts all sit outside the subset gets exactly zero
+    mask = np.zeros(wl.E, bool)
+    mask[full.topk_idx[0]] = True
+    none = ~mask
+    part = moe.moe_layer(x, rw, None, banks.__getitem__, sgu, sdn, sg, include_shared=False,
+                         expert_mask=none, **kw).out64
+    assert np.all(part[0] == 0.0)
+
+
 def test_shared_expert_alone_matches_torch():
     rng = np.random.default_rng(17)
     H, I = 64, 32
@@ -298,7 +351,24 @@ def test_allreduce_bytes_match_pages():
         assert moe.allreduce_bytes(f["bs"], f["H"]) == f["bytes"]
 
 
-def test_rms_renorm():
+def test_rms_renorm_hand_worked_rows():
+    """Rows worked out by hand from x = bf16(y / sqrt(mean(y^2) + 1e-6)).
+
+    * four values of 1e-3: mean square 1e-6 equals eps, so x = 1e-3 /
+      sqrt(2e-6) = 0.70710678..., whose nearest bf16 is 362/512 = 0.70703125
+      (eps = 1e-5 would give 0.3015...);
+    * (3, -4, 0, 0): mean square 25/4, x = (1.2, -1.6, 0, 0) up to 8e-8, i.e.
+      bf16 154/128 and -205/128 (a sum over H - 1 = 3 would give 1.039...);
+    * (1e-4, 0, 0, 0): eps dominates, x0 = 1e-4 / sqrt(1.0025e-6) =
+      0.09987..., bf16 205/2048 (eps = 1e-5 would give 0.0316...);
+    * zeros stay zero (no 0/0)."""
+    y = np.array([[1e-3] * 4, [3.0, -4.0, 0.0, 0.0], [1e-4, 0.0, 0.0, 0.0], [0.0] * 4])
+    want = np.array([[362 / 512] * 4, [154 / 128, -205 / 128, 0.0, 0.0], [205 / 2048, 0.0, 0.0, 0.0],
+                     [0.0] * 4])
+    assert np.array_equal(moe.rms_renorm(y), want)
+
+
+def test_rms_renorm_matches_torch():
     rng = np.random.default_rng(18)
     y = rng.standard_normal((3, 256)) * 5
     r = moe.rms_renorm(y)

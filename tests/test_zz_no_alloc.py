@@ -74,6 +74,50 @@ def test_route_static_matches_forward_two_calls(routed_layer):
         assert np.allclose(got["topk_w"].cpu().numpy(), ref["topk_w"], rtol=1e-5, atol=1e-6)
 
 
+def _oracle_routing(x, rw, rb, top_k):
+    from oracle import moe
+    logits = moe.router_logits(x.float().cpu().numpy(), rw.cpu().numpy(), None if rb is None else rb.cpu().numpy())
+    idx, w = moe.select_topk(logits, top_k)
+    offs, perm, inv = moe.counting_sort(idx, rw.shape[0])
+    return dict(topk_idx=idx, topk_w=w, offsets=offs, perm=perm, inv=inv)
+
+
+@pytest.mark.parametrize("T,H,E,top_k,bias", [
+    (16, 2560, 256, 8, False),    # the decode layer
+    (16, 2560, 1024, 8, True),    # T * E at the scratch's limit, Zipf-biased router
+    (32, 8192, 256, 8, True),     # T * H and H at the limit
+    (1024, 256, 16, 4, True),     # T and T * E at the limit
+])
+def test_route_static_matches_oracle_at_the_limits(routed_layer, T, H, E, top_k, bias):
+    """Against the oracle directly: indices, offsets, perm and inv bit-exact,
+    weights within the tolerance of the fp32 softmax, at sizes up to the
+    fixed scratch's limits, with and without a router bias; the status
+    reader reports no failed check."""
+    wl = W.Workload("route_static", H=H, I=64, E=E, top_k=top_k, I_s=64, tokens=(T,), router_bias=bias)
+    x = W.hidden(wl, T, step=5, device=DEV)
+    rw = W.router_weight(wl, device=DEV)
+    rb = W.router_bias(wl, device=DEV)
+    got = _static_routing_raw(x, rw, rb, wl)
+    assert ftmoe.ftmoe_route_static_status() == 0
+    ref = _oracle_routing(x, rw, rb, top_k)
+    for k in ("topk_idx", "offsets", "perm", "inv"):
+        assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
+    assert np.allclose(got["topk_w"].cpu().numpy(), ref["topk_w"], rtol=5e-4, atol=1e-6)
+
+
+def _static_routing_raw(x, rw, rb, wl):
+    T = x.shape[0]
+    P = T * wl.top_k
+    idx = torch.full((T, wl.top_k), -1, dtype=torch.int32, device=DEV)
+    w = torch.zeros((T, wl.top_k), dtype=torch.float32, device=DEV)
+    offs = torch.full((wl.E + 1,), -1, dtype=torch.int32, device=DEV)
+    perm = torch.full((P,), -1, dtype=torch.int32, device=DEV)
+    inv = torch.full((P,), -1, dtype=torch.int32, device=DEV)
+    ftmoe.ftmoe_route_static(x, T, wl.H, rw, rb, wl.E, wl.top_k, wl.norm_topk_prob, idx, w, offs, perm, inv)
+    torch.cuda.synchronize()
+    return dict(topk_idx=idx, topk_w=w, offsets=offs, perm=perm, inv=inv)
+
+
 def test_route_static_rejects_oversized(routed_layer):
     wl, bank, _ = routed_layer
     lib = ftmoe.lib()
