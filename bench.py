@@ -982,8 +982,10 @@ def run_compare(args):
             i0, I_loc = window_of_rank(r, G, wl.I)
             win.append(_kernel_ms_per_step(layer, lambda: layer.forward(0, x, out, i0=i0, I_loc=I_loc), K))
             mask = (np.arange(wl.E) % G == r).astype(np.uint8)
+            si0, sI = window_of_rank(r, G, wl.I_s)
             ep.append(_kernel_ms_per_step(
-                layer, lambda: ftmoe.ftmoe_forward_experts(layer.handle, 0, x, T, out, ftmoe.OUT_BF16, mask), K))
+                layer, lambda: ftmoe.ftmoe_forward_experts(layer.handle, 0, x, T, out, ftmoe.OUT_BF16, mask,
+                                                           si0, sI), K))
             pairs.append(int(np.isin(idx, np.nonzero(mask)[0]).sum()))
         layer.close()
         torch.cuda.empty_cache()
@@ -1000,8 +1002,8 @@ def run_compare(args):
             "expert_parallel": {"rank_kernel_ms": [round(v, 4) for v in ep], "step_ms": round(max(ep), 4),
                                 "rank_pairs": pairs, "pair_imbalance_max_over_mean": round(max(pairs) / mean_pairs, 3),
                                 "alltoall_bytes_per_rank_padded": 2 * T * wl.top_k * wl.H * 2,
-                                "note": "rank r: the routed slots of experts e % G == r (routing replicated); "
-                                        "the shared expert's time is not in these figures"},
+                                "note": "rank r: the routed slots of experts e % G == r (routing replicated) "
+                                        "and window r of the shared expert"},
             "speedup_window_over_expert": round(max(ep) / max(win), 3),
         }
     line = {"mode": "window split vs expert parallel, per-rank kernel time on one GB300",

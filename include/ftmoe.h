@@ -228,22 +228,28 @@ int ftmoe_forward_stack(ftmoe_handle* h, const void* x, int T, void* out, ftmoe_
  * or H, T < 0. */
 int ftmoe_rms_renorm(const float* y, void* x, int T, int H, ftmoe_stream_t stream);
 
-/* The routed part of layer `layer` restricted to a subset of the experts:
+/* One rank's share of an expert-parallel layer: the routed slots of a
+ * subset of the experts, plus optionally a window of the shared expert:
  *   out_t = sum over the slots j of token t whose expert is in the subset of
- *           w_tj * Y_(t,j)   (no shared expert; routing over all experts)
- * expert_mask: host [E], nonzero for the experts of the subset.  This is what
- * one rank of an expert-parallel layer computes for the pairs dispatched to
- * it when rank r owns the experts e with e % world == r, the alternative the
- * pages weigh and reject for its all-to-all, its capture at static shapes and
- * its load imbalance under skewed routing ([I62] "Why not expert parallelism
- * proper"); summing the subsets of a partition of the experts and adding the
- * gated shared expert gives the whole layer.  It exists to measure that
- * alternative against the intermediate split on the same GPU.  Uses the
- * whole loaded window; reads the routing back to the host once (one
- * synchronisation); resident mode only; T <= 32 on the tensor-core decode
- * shapes and T > 32 on the prefill shapes (INVALID_ARG otherwise). */
+ *           w_tj * Y_(t,j)  +  sigmoid(g . x_t) * S_t over the shared window
+ * (routing over all experts; shared_I_loc == 0 leaves the shared expert out).
+ * expert_mask: host [E], nonzero for the experts of the subset.  Rank r of an
+ * expert-parallel layer owns the experts e with e % world == r, the
+ * alternative the pages weigh and reject for its all-to-all, its capture at
+ * static shapes and its load imbalance under skewed routing ([I62] "Why not
+ * expert parallelism proper"); giving rank r also window r of the shared
+ * expert keeps the shared work evenly split, and the shares over a partition
+ * of the experts and of the shared window add up to the whole layer.  It
+ * exists to measure that alternative against the intermediate split on the
+ * same GPU.  The routed experts use the whole loaded window; the shared
+ * window [shared_i0, shared_i0 + shared_I_loc) must lie in the loaded shared
+ * window (SLICE_OUT_OF_RANGE) and be 16-aligned (ALIGNMENT).  Reads the
+ * routing back to the host once (one synchronisation); resident mode only;
+ * T <= 32 on the tensor-core decode shapes and T > 32 on the prefill shapes
+ * (INVALID_ARG otherwise). */
 int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags,
-                          const uint8_t* expert_mask, const ftmoe_aux* aux, ftmoe_stream_t stream);
+                          const uint8_t* expert_mask, int shared_i0, int shared_I_loc, const ftmoe_aux* aux,
+                          ftmoe_stream_t stream);
 
 /* The combine of an intermediate-sharded layer: each of n_parts ranks (or
  * windows) computed its fp32 partial of the same T tokens (ftmoe_forward

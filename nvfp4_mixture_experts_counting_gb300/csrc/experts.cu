@@ -327,7 +327,10 @@ __global__ void k_combine(ExpertArgs a) {
           a.y_tiles == 2 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(a.Y)[yt] << 16)
           : a.y_tiles == 1 ? a.Y[yt]
                            : a.Y[(int64_t)r.inv[(int64_t)t * k + j] * H + h];
-      acc = fmaf(r.topk_w[(int64_t)t * k + j], y, acc);
+      // a slot of weight zero (an expert left out of the computed subset)
+      // adds nothing, whatever its stale Y holds
+      const float wv = r.topk_w[(int64_t)t * k + j];
+      if (wv != 0.f) acc = fmaf(wv, y, acc);
     }
     if (a.sh_gate_up) acc = fmaf(r.sigma[t], a.S[i], acc);
     if ((a.out_flags & 0xff) == 0) {

@@ -971,7 +971,8 @@ int ftmoe_rms_renorm(const float* y, void* x, int T, int H, ftmoe_stream_t strea
 }
 
 int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void* out, int out_flags,
-                          const uint8_t* expert_mask, const ftmoe_aux* aux, ftmoe_stream_t stream) {
+                          const uint8_t* expert_mask, int shared_i0, int shared_I_loc, const ftmoe_aux* aux,
+                          ftmoe_stream_t stream) {
   if (!h || layer < 0 || layer >= h->cfg.num_layers || !expert_mask) return FTMOE_ERR_INVALID_ARG;
   const ftmoe_config& c = h->cfg;
   if (h->offload || T < 0 || T > c.max_tokens) return FTMOE_ERR_INVALID_ARG;
@@ -980,6 +981,10 @@ int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void
   if ((out_flags & FTMOE_OUT_ACCUMULATE) && otype != FTMOE_OUT_FP32) return FTMOE_ERR_INVALID_ARG;
   Layer& L = h->layers[layer];
   if (!L.loaded) return FTMOE_ERR_NOT_LOADED;
+  if (shared_i0 % 16 || shared_I_loc % 16) return FTMOE_ERR_ALIGNMENT;
+  if (shared_I_loc < 0 || (shared_I_loc > 0 && (c.I_shared == 0 || shared_i0 < L.sli0 ||
+                                                shared_i0 + shared_I_loc > L.sli0 + L.slIw)))
+    return FTMOE_ERR_SLICE_OUT_OF_RANGE;
   if (T == 0) return FTMOE_OK;
   if (!x || !out || x == out) return FTMOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out)) return FTMOE_ERR_ALIGNMENT;
@@ -998,8 +1003,25 @@ int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void
   const int i0 = L.li0, I_loc = L.lIw;
   RouteArgs r = route_args(h, L, x, T);
   ExpertArgs a = expert_args(h, L, r, T, out, out_flags, i0, I_loc);
+  // the shared expert on its own window (or not at all)
+  const bool with_shared = shared_I_loc > 0;
+  if (with_shared) {
+    a.s_row0 = shared_i0 - L.sli0;
+    a.s_I_loc = shared_I_loc;
+  } else {
+    a.sh_gate_up = nullptr;
+    a.sh_down = nullptr;
+  }
   const bool dec = T <= 32;
-  if (dec ? !decode_tc_path(h, L, a, T) : !prefill_path(h, L, T, I_loc, a.win.row0)) return FTMOE_ERR_INVALID_ARG;
+  bool ok;
+  if (dec) {
+    ok = h->dtc_enabled && decode_tc_supported(c.H, E, I_loc, L.lIw, a.win.row0, a.s_I_loc, a.s_Iw, a.s_row0, T,
+                                               c.top_k, L.lay.gu_sf_bytes != 0);
+  } else {
+    ok = prefill_path(h, L, T, I_loc, a.win.row0) &&
+         (!with_shared || prefill_shared_supported(c.H, a.s_I_loc, a.s_Iw, a.s_row0, c.top_k));
+  }
+  if (!ok) return FTMOE_ERR_INVALID_ARG;
   DecodeArgs d{};
   PfArgs p{};
   PfMaps maps;
@@ -1010,7 +1032,7 @@ int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void
     CK(launch_decode_tc(d, s, 1));
   } else {
     const bool tc_router = L.router_wcat != nullptr;
-    p = prefill_args(h, L, a, x, out, out_flags, false, tc_router);
+    p = prefill_args(h, L, a, x, out, out_flags, with_shared, tc_router);
     CK(prefill_make_maps(p, &maps));
     if (tc_router) {
       CK(launch_route(r, s, kRouteXq));
@@ -1033,26 +1055,31 @@ int ftmoe_forward_experts(ftmoe_handle* h, int layer, const void* x, int T, void
     if (expert_mask[ht[i]]) list[n++] = ht[i];
   *count = n;
   if (dec) {
-    // the expert kernels on the subset's list, without the shared expert
-    CK(cudaMemcpyAsync(r.touched, list, (size_t)(n > 0 ? n : 1) * 4, cudaMemcpyHostToDevice, s));
-    CK(cudaMemcpyAsync(r.n_touched, count, 4, cudaMemcpyHostToDevice, s));
-    d.skip_shared = 1;
-    if (n == 0) {
+    // the expert kernels on the subset's list (and the shared window)
+    if (n == 0 && !with_shared) {
       CK(cudaMemsetAsync(out, 0, (size_t)T * c.H * (otype == FTMOE_OUT_FP32 ? 4 : 2), s));
     } else {
+      CK(cudaMemcpyAsync(r.touched, list, (size_t)(n > 0 ? n : 1) * 4, cudaMemcpyHostToDevice, s));
+      CK(cudaMemcpyAsync(r.n_touched, count, 4, cudaMemcpyHostToDevice, s));
+      d.skip_shared = with_shared ? 0 : 1;
       CK(launch_decode_tc(d, s, 2));
     }
   } else {
     // the subset's experts only, then the combine of their slots (the other
-    // slots' weights zeroed), without the shared expert
+    // slots' weights zeroed) with the shared window
     CK(cudaMemcpyAsync(h->ep_mask, expert_mask, (size_t)E, cudaMemcpyHostToDevice, s));
+    CK(launch_mask_weights(r.topk_idx, r.topk_w, h->ep_mask, h->ep_w, (int64_t)T * c.top_k, s));
+    if (with_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
     p.active = h->ep_mask;
     CK(launch_prefill_routed(p, maps, h->num_sms, s));
-    CK(launch_mask_weights(r.topk_idx, r.topk_w, h->ep_mask, h->ep_w, (int64_t)T * c.top_k, s));
-    a.r.topk_w = h->ep_w;
-    a.sh_gate_up = nullptr;
-    a.y_tiles = p.y_bf16 ? 2 : 1;
-    CK(launch_experts(a, s, kPartTail));
+    if (with_shared) {
+      p.topk_w = h->ep_w;
+      CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
+    } else {
+      a.r.topk_w = h->ep_w;
+      a.y_tiles = p.y_bf16 ? 2 : 1;
+      CK(launch_experts(a, s, kPartTail));
+    }
   }
   int rc = copy_aux(h, r, T, aux, s);
   if (rc) return rc;

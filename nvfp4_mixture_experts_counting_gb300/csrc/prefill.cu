@@ -701,7 +701,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
 #pragma unroll
                 for (int q2 = 0; q2 < 8; ++q2) {
-                  if (q2 < k) {
+                  // a slot of weight zero (left out of an expert subset)
+                  // adds nothing, whatever its stale Y holds
+                  if (q2 < k && wj[q2] != 0.f) {
                     const uint32_t u[8] = {y[q2][0].x, y[q2][0].y, y[q2][0].z, y[q2][0].w,
                                            y[q2][1].x, y[q2][1].y, y[q2][1].z, y[q2][1].w};
 #pragma unroll
@@ -714,6 +716,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               } else {
                 for (int jj = 0; jj < k; ++jj) {
                   const float wv = __ldg(w + jj);
+                  if (wv == 0.f) continue;
                   const uint4* yp = reinterpret_cast<const uint4*>(ytb + jj * 128 + 16 * c);
                   const uint4 y0 = yp[0], y1 = yp[1];
                   const uint32_t u[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
@@ -739,7 +742,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     }
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
-                      if (j0 + q2 < k) {
+                      if (j0 + q2 < k && wj[j0 + q2] != 0.f) {
 #pragma unroll
                         for (int i4 = 0; i4 < 4; ++i4) {
                           o[4 * i4] = fmaf(wj[j0 + q2], y[q2][i4].x, o[4 * i4]);
@@ -754,6 +757,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               } else {
                 for (int jj = 0; jj < k; ++jj) {
                   const float wv = __ldg(w + jj);
+                  if (wv == 0.f) continue;
                   const float4* yp = reinterpret_cast<const float4*>(ytf + jj * 128 + 16 * c);
 #pragma unroll
                   for (int i4 = 0; i4 < 4; ++i4) {

@@ -85,7 +85,7 @@ SIGNATURES = {
                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "ftmoe_route_static_status": ([C.c_void_p], C.c_int),
     "ftmoe_forward_experts": ([C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
-                               C.POINTER(Aux), C.c_void_p], C.c_int),
+                               C.c_int, C.c_int, C.POINTER(Aux), C.c_void_p], C.c_int),
     "ftmoe_reduce_partials": ([C.c_void_p, C.c_int, C.c_int64, C.c_void_p, C.c_int, C.c_void_p], C.c_int),
     "ftmoe_test_withhold_stage": ([C.c_void_p, C.c_int, C.c_int64], C.c_int),
     "ftmoe_slice_format": ([C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
@@ -208,13 +208,14 @@ def ftmoe_route_static(x, T: int, H: int, router_w, router_bias, E: int, top_k: 
 
 
 def ftmoe_forward_experts(h: int, layer: int, x, T: int, out, out_flags: int, expert_mask,
-                          aux: Optional[Aux] = None, stream=None):
-    """The routed part of the layer over the experts whose mask byte (host
-    numpy uint8 [E]) is set: one expert-parallel rank's share."""
+                          shared_i0: int = 0, shared_I_loc: int = 0, aux: Optional[Aux] = None, stream=None):
+    """One expert-parallel rank's share: the routed slots of the experts whose
+    mask byte (host numpy uint8 [E]) is set, plus the shared expert's window
+    [shared_i0, shared_i0 + shared_I_loc) (none when shared_I_loc is 0)."""
     import numpy as np
     m = np.ascontiguousarray(expert_mask, dtype=np.uint8)
-    _check(lib().ftmoe_forward_experts(h, layer, _ptr(x), T, _ptr(out), out_flags, m.ctypes.data,
-                                       C.byref(aux) if aux is not None else None, _stream(stream)),
+    _check(lib().ftmoe_forward_experts(h, layer, _ptr(x), T, _ptr(out), out_flags, m.ctypes.data, shared_i0,
+                                       shared_I_loc, C.byref(aux) if aux is not None else None, _stream(stream)),
            "ftmoe_forward_experts")
 
 

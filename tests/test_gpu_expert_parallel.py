@@ -46,12 +46,19 @@ def test_expert_shares_match_oracle_and_add_up(name, T, G):
     if T > 64:
         bank.prefetch_oracle_experts(range(wl.E))
     total = torch.zeros((T, wl.H), dtype=torch.float32, device=DEV)
+    with_shared = torch.zeros_like(total)
     for r in range(G):
         mask = (np.arange(wl.E) % G == r)
         share = torch.empty((T, wl.H), dtype=torch.float32, device=DEV)
         ftmoe.ftmoe_forward_experts(layer.handle, 0, x, T, share, ftmoe.OUT_FP32, mask.astype(np.uint8))
         bf = torch.empty((T, wl.H), dtype=torch.bfloat16, device=DEV)
         ftmoe.ftmoe_forward_experts(layer.handle, 0, x, T, bf, ftmoe.OUT_BF16, mask.astype(np.uint8))
+        # the same share with window r of the shared expert (a whole rank's
+        # work), where the window fits the tensor-core tiles (64-wide)
+        si0, sI = r * wl.I_s // G, wl.I_s // G
+        rank = torch.zeros((T, wl.H), dtype=torch.float32, device=DEV)
+        if sI % 64 == 0:
+            ftmoe.ftmoe_forward_experts(layer.handle, 0, x, T, rank, ftmoe.OUT_FP32, mask.astype(np.uint8), si0, sI)
         torch.cuda.synchronize()
         assert layer.check_status() == 0
         ref = _oracle(bank, x, expert_mask=mask, include_shared=False, out_dtype="fp32", tokens=rows)
@@ -59,12 +66,16 @@ def test_expert_shares_match_oracle_and_add_up(name, T, G):
         refb = _oracle(bank, x, expert_mask=mask, include_shared=False, tokens=rows)
         check_output(bf, refb.out, rows=rows)
         total += share
+        with_shared += rank
     routed = _oracle(bank, x, include_shared=False, out_dtype="fp32", tokens=rows)
     check_output(total, routed.out64, rows=rows)
-    # the shares plus the shared expert are the layer: against the full forward
+    if (wl.I_s // G) % 64:
+        layer.close()
+        return
+    # the ranks' shares, shared windows included, add up to the whole layer
     full = torch.empty((T, wl.H), dtype=torch.float32, device=DEV)
     layer.forward(0, x, full, out_flags=ftmoe.OUT_FP32)
-    shared_only = _oracle(bank, x, expert_mask=np.zeros(wl.E, bool), out_dtype="fp32", tokens=rows).out64
-    got = total.cpu().numpy()[rows] + shared_only[rows]
-    assert rel_l2(got, full.cpu().numpy()[rows]) <= 2e-3
+    torch.cuda.synchronize()
+    assert rel_l2(with_shared.cpu().numpy()[rows], full.cpu().numpy()[rows]) <= 1e-5
+    check_output(with_shared, _oracle(bank, x, out_dtype="fp32", tokens=rows).out64, rows=rows)
     layer.close()
