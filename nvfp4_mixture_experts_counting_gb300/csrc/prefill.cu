@@ -36,6 +36,12 @@ namespace {
 constexpr int kPfStages = 5;
 constexpr int kPfThreads = 352;    // producer, MMA, 8 epilogue warps, scale-factor copier
 constexpr int kPfEpiWarps = 8;
+// The routed gate_up's epilogue (globals, SwiGLU, NVFP4 quantisation of the
+// intermediate) is long chains of dependent arithmetic per value; with 8
+// warps it, not the copies or the tensor pipe, set the kernel's pace, so that
+// mode drains its accumulators with 16 warps, one 16-wide block each.
+__host__ __device__ constexpr int pf_epi_warps(int mode) { return mode == 0 ? 16 : kPfEpiWarps; }
+__host__ __device__ constexpr int pf_threads(int mode) { return 32 * (3 + pf_epi_warps(mode)); }
 constexpr int kTile = 16384;        // one 128 x 128-byte operand tile
 constexpr int kSfStage = 2048;      // four 512-byte scale blocks
 constexpr int kPfOffA = 0;
@@ -96,6 +102,11 @@ __device__ __forceinline__ int find_le(const int* tab, int n, int v) {
 // rows: rows r, r+32, r+64, r+96 share a 16-byte line (the order tcgen05.cp
 // .32x128b.warpx4 places into TMEM lanes r % 32, columns r / 32).
 __host__ __device__ constexpr int sf_slot(int r) { return (r & 31) * 16 + ((r & 127) >> 5) * 4; }
+
+// SiLU with the hardware exponential and reciprocal: the intermediate is
+// formed in fp32 (the oracle forms it in fp64), a few ulp either way; the
+// quantisation that follows keeps the quantiser's own order.
+__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
 // NVFP4 quantisation of 16 activation values with global 1.0, in the
 // quantiser's own order: scale = E4M3(fp32(amax / 6)), then each code =
@@ -226,10 +237,11 @@ __global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
 // A K step is 32 bytes of a row (64 E2M1 or 16 bf16 elements), a K tile 4
 // steps (one 128-byte swizzle row).
 template <int MODE>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(pf_threads(MODE), 1)
     k_pf_mma(const __grid_constant__ PfArgs a, const __grid_constant__ CUtensorMap mapA,
              const __grid_constant__ CUtensorMap mapB) {
   constexpr bool kF4 = MODE < 2;
+  constexpr int EW = pf_epi_warps(MODE), NT = pf_threads(MODE);
   extern __shared__ unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPfOffBar);
@@ -254,7 +266,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], kPfEpiWarps); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], EW); }
     mbar_init(drain, 1);
     for (int s = 0; s < kPfStages; ++s) mbar_init(&sf_ready[s], 1);
     mbar_init(sf_drain, 1);
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   if (kF4) {
-    for (int e = tid; e <= E; e += kPfThreads) {
+    for (int e = tid; e <= E; e += NT) {
       s_off[e] = a.offsets[e];
       s_pad[e] = a.pad_off[e];
     }
@@ -374,7 +386,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_commit(drain);
       mbar_wait(drain, 0, a.status);
     }
-  } else if (warp == 2 + kPfEpiWarps) {
+  } else if (warp == 2 + EW) {
     // ---------------- scale factors (NVFP4 modes): once a stage has landed,
     // its scale blocks go into that stage's TMEM columns
     if (kF4 && lane == 0) {
@@ -416,44 +428,37 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool valid = local < s_off[e + 1] - s_off[e];
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 128;
       if (MODE == 0) {
+        // warp (q, cb): pair rows 32q.. and the unit's 16-wide block cb, gate
+        // columns 16cb.. and up columns 64 + 16cb..; the rows' globals are
+        // read where they are (every lane the same sixteen)
+        const int cb = (warp - 2) >> 2;
         const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
-        {
-          // this unit's 64 gate and 64 up row globals into the warp's slot
-          const float* src = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * j +
-                             (lane < 16 ? 0 : Iw - 64);
-          reinterpret_cast<float4*>(wglob)[lane] = __ldg(reinterpret_cast<const float4*>(src) + lane);
-          __syncwarp();
-        }
+        const float* gglob = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * j + 16 * cb;
+        const float* uglob = gglob + Iw;
         const int pp = pp0 + 32 * q + lane;
-        uint32_t sfw = 0;
-#pragma unroll 1
-        for (int b = 2 * hf; b < 2 * hf + 2; ++b) {
-          uint32_t g[16], v[16];
-          tc_ld16(taddr + 16 * b, g);
-          tc_ld16(taddr + 64 + 16 * b, v);
-          tc_wait16x2(g, v);
-          float h[16];
+        uint32_t g[16], v[16];
+        tc_ld16(taddr + 16 * cb, g);
+        tc_ld16(taddr + 64 + 16 * cb, v);
+        tc_wait16x2(g, v);
+        float h[16];
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 gg = *reinterpret_cast<const float4*>(wglob + 16 * b + i);
-            const float4 ug = *reinterpret_cast<const float4*>(wglob + 64 + 16 * b + i);
-            h[i] = silu(__uint_as_float(g[i]) * gg.x) * (__uint_as_float(v[i]) * ug.x);
-            h[i + 1] = silu(__uint_as_float(g[i + 1]) * gg.y) * (__uint_as_float(v[i + 1]) * ug.y);
-            h[i + 2] = silu(__uint_as_float(g[i + 2]) * gg.z) * (__uint_as_float(v[i + 2]) * ug.z);
-            h[i + 3] = silu(__uint_as_float(g[i + 3]) * gg.w) * (__uint_as_float(v[i + 3]) * ug.w);
-          }
-          uint8_t codes[8];
-          const uint8_t sc = quantize_act16(h, codes);
-          sfw |= (uint32_t)sc << (8 * (b - 2 * hf));
-          if (valid) {
-            uint2 pk;
-            pk.x = codes[0] | (codes[1] << 8) | (codes[2] << 16) | ((uint32_t)codes[3] << 24);
-            pk.y = codes[4] | (codes[5] << 8) | (codes[6] << 16) | ((uint32_t)codes[7] << 24);
-            *reinterpret_cast<uint2*>(a.hq + (int64_t)pp * a.hq_pitch + 32 * j + 8 * b) = pk;
-          }
+        for (int i = 0; i < 16; i += 4) {
+          const float4 gg = __ldg(reinterpret_cast<const float4*>(gglob + i));
+          const float4 ug = __ldg(reinterpret_cast<const float4*>(uglob + i));
+          h[i] = silu_fast(__uint_as_float(g[i]) * gg.x) * (__uint_as_float(v[i]) * ug.x);
+          h[i + 1] = silu_fast(__uint_as_float(g[i + 1]) * gg.y) * (__uint_as_float(v[i + 1]) * ug.y);
+          h[i + 2] = silu_fast(__uint_as_float(g[i + 2]) * gg.z) * (__uint_as_float(v[i + 2]) * ug.z);
+          h[i + 3] = silu_fast(__uint_as_float(g[i + 3]) * gg.w) * (__uint_as_float(v[i + 3]) * ug.w);
         }
-        *reinterpret_cast<uint16_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4 +
-                                     2 * hf) = valid ? (uint16_t)sfw : (uint16_t)0;
+        uint8_t codes[8];
+        const uint8_t sc = quantize_act16(h, codes);
+        if (valid) {
+          uint2 pk;
+          pk.x = codes[0] | (codes[1] << 8) | (codes[2] << 16) | ((uint32_t)codes[3] << 24);
+          pk.y = codes[4] | (codes[5] << 8) | (codes[6] << 16) | ((uint32_t)codes[7] << 24);
+          *reinterpret_cast<uint2*>(a.hq + (int64_t)pp * a.hq_pitch + 32 * j + 8 * cb) = pk;
+        }
+        a.hq_sf[((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4 + cb] = valid ? sc : 0;
       } else if (MODE == 1) {
         const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
         reinterpret_cast<float4*>(wglob)[lane] =
@@ -815,6 +820,250 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ routed gate_up, 128 x 256 tiles
+
+// The routed gate_up with 256 weight rows per tile: two consecutive 64 + 64
+// (gate, up) window tiles against one 128-row pair tile, one MMA of N = 256
+// per K step.  An SM takes in its operands at a bounded rate (about 50-60
+// GB/s whatever the copy kind, multicast included), so operand bytes per
+// product set the pace: a stage brings 48 KB of codes for twice the products
+// of a 128 x 128 tile's 32 KB.  Four stages of 54 KB; one accumulator of 256
+// TMEM columns, drained into registers by 16 epilogue warps (two 16-wide
+// blocks each) before they compute, so the next tile's MMAs start early.
+// Roles otherwise as in k_pf_mma.
+namespace {
+constexpr int kGuStages = 4;
+constexpr int kGuTileB = 32768;    // 256 x 128-byte weight tile
+constexpr int kGuSfb = 4096;       // two tiles' four 512-byte scale blocks
+constexpr int kGuEpi = 16;
+constexpr int kGuThreads = 32 * (3 + kGuEpi);
+constexpr int kGuOffA = 0;
+constexpr int kGuOffB = kGuStages * kTile;
+constexpr int kGuOffSfa = kGuOffB + kGuStages * kGuTileB;
+constexpr int kGuOffSfb = kGuOffSfa + kGuStages * kSfStage;
+constexpr int kGuOffBar = kGuOffSfb + kGuStages * kGuSfb;
+constexpr int kGuOffTab = kGuOffBar + 256;
+constexpr uint32_t kGuSfCol0 = 256;  // after the accumulator; 48 columns per stage
+__host__ __device__ inline int gu256_smem_bytes(int E) { return 1024 + kGuOffTab + 3 * 4 * (E + 1); }
+}  // namespace
+
+__global__ void __launch_bounds__(kGuThreads, 1)
+    k_pf_gu256(const __grid_constant__ PfArgs a, const __grid_constant__ CUtensorMap mapA,
+               const __grid_constant__ CUtensorMap mapB) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kGuOffBar);
+  uint64_t* empty = full + kGuStages;
+  uint64_t* acc_full = empty + kGuStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint64_t* sf_ready = drain + 1;  // [kGuStages]
+  uint64_t* sf_drain = sf_ready + kGuStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int E = a.E, H = a.H;
+  int* s_off = reinterpret_cast<int*>(sm + kGuOffTab);
+  int* s_pad = s_off + (E + 1);
+  int* s_up = s_pad + (E + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int I_loc = a.win.I_loc, row0 = a.win.row0, Iw = a.win.Iw;
+  const int nks_all = H / 64;            // 64-element K steps
+  const int nkt = (nks_all + 3) / 4;     // 128-byte K tiles
+  const int J2 = I_loc / 128;            // 256-row weight tiles per pair tile
+
+  if (tid == 0) {
+    for (int s = 0; s < kGuStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kGuEpi);
+    mbar_init(drain, 1);
+    for (int s = 0; s < kGuStages; ++s) mbar_init(&sf_ready[s], 1);
+    mbar_init(sf_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  for (int e = tid; e <= E; e += kGuThreads) {
+    s_off[e] = a.offsets[e];
+    s_pad[e] = a.pad_off[e];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) warp_excl_scan(E, [&](int e) { return ((s_pad[e + 1] - s_pad[e]) >> 7) * J2; }, s_up);
+  __syncthreads();
+  const uint32_t tmem = *tmem_slot;
+  const int n_units = s_up[E];
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int k = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+        const int e = find_le(s_up, E, u), r = u - s_up[e];
+        const int nt = r / J2, jj = r % J2;
+        const int pp0 = s_pad[e] + nt * 128;
+        const int z = a.rec_z ? a.rec_z[e] : e;
+        const uint8_t* rec = a.bank + a.lay.bytes * z;
+        const int t0 = row0 / 64 + 2 * jj;  // first of the unit's two 64 + 64-row window tiles
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kGuStages;
+          if (k >= kGuStages && !mbar_wait(&empty[s], ((k / kGuStages) - 1) & 1, a.status)) {
+            *abort_flag = 1;
+            break;
+          }
+          const int nks = min(4, nks_all - 4 * kt);
+          unsigned char* sa = sm + kGuOffA + s * kTile;
+          unsigned char* sb = sm + kGuOffB + s * kGuTileB;
+          unsigned char* sfa = sm + kGuOffSfa + s * kSfStage;
+          unsigned char* sfb = sm + kGuOffSfb + s * kGuSfb;
+          mbar_arrive_expect_tx(&full[s], kTile + kGuTileB + 3 * nks * 512);
+          tma_load_2d(sa, &mapA, kt * 128, pp0, &full[s]);
+          for (int h = 0; h < 2; ++h) {
+            // B rows: gate tile, then its up tile, for each of the two tiles
+            tma_load_3d(sb + h * kTile, &mapB, kt * 128, 64 * (t0 + h), z, &full[s]);
+            tma_load_3d(sb + h * kTile + kTile / 2, &mapB, kt * 128, Iw + 64 * (t0 + h), z, &full[s]);
+            bulk_g2s(sfb + h * kSfStage, rec + a.lay.gu_sf + ((int64_t)(t0 + h) * nks_all + 4 * kt) * 512,
+                     nks * 512, &full[s]);
+          }
+          bulk_g2s(sfa, a.xg_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
+        }
+      }
+      // nothing may still be landing when the CTA exits
+      for (int q = k - kGuStages > 0 ? k - kGuStages : 0; q < k; ++q)
+        mbar_wait(&full[q % kGuStages], (q / kGuStages) & 1, a.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: one accumulator, N = 256
+    if (lane == 0) {
+      const uint32_t idesc = idesc_nvf4(128, 256);
+      int k = 0, ui = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
+        if (ui >= 1 && !mbar_wait(acc_empty, (ui - 1) & 1, a.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        bool ok = true;
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kGuStages;
+          if (!mbar_wait(&sf_ready[s], (k / kGuStages) & 1, a.status)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nks = min(4, nks_all - 4 * kt);
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + kGuOffA + s * kTile));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + kGuOffB + s * kGuTileB));
+          const uint32_t sfa_col = tmem + kGuSfCol0 + s * 48, sfb_col = sfa_col + 16;
+          for (int ks = 0; ks < nks; ++ks)
+            tc_mma_nvf4(tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, sfa_col + 4 * ks, sfb_col + 8 * ks,
+                        (kt | ks) != 0);
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.status);
+    }
+  } else if (warp == 2 + kGuEpi) {
+    // ---------------- scale factors: per K step, the pair tile's block into
+    // 4 columns, the two weight tiles' blocks into the next 8 (rows 0-127,
+    // then 128-255)
+    if (lane == 0) {
+      int k = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kGuStages;
+          if (!mbar_wait(&full[s], (k / kGuStages) & 1, a.status)) { *abort_flag = 1; break; }
+          tc_fence_after();
+          const int nks = min(4, nks_all - 4 * kt);
+          const uint32_t sfa_col = tmem + kGuSfCol0 + s * 48, sfb_col = sfa_col + 16;
+          const uint32_t sfa_smem = smem_u32(sm + kGuOffSfa + s * kSfStage);
+          const uint32_t sfb_smem = smem_u32(sm + kGuOffSfb + s * kGuSfb);
+          for (int ks = 0; ks < nks; ++ks) {
+            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
+            tc_cp_sf(sfb_col + 8 * ks, sdesc_sf(sfb_smem + 512 * ks));
+            tc_cp_sf(sfb_col + 8 * ks + 4, sdesc_sf(sfb_smem + kSfStage + 512 * ks));
+          }
+          tc_commit(&sf_ready[s]);
+        }
+      }
+      tc_commit(sf_drain);
+      mbar_wait(sf_drain, 0, a.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: warp (q, part) holds TMEM lanes 32q.. (pair
+    // rows) and two 16-wide blocks of window tile t0 + (part >> 1): gate
+    // columns 16b.. and up columns 64 + 16b.. for b = 2 (part & 1) + {0, 1}
+    const int q = warp & 3, part = (warp - 2) >> 2;
+    const int hf = part >> 1, b0 = 2 * (part & 1);
+    int ui = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
+      if (!mbar_wait(acc_full, ui & 1, a.status)) { *abort_flag = 1; break; }
+      tc_fence_after();
+      const int e = find_le(s_up, E, u), r = u - s_up[e];
+      const int nt = r / J2, jj = r % J2;
+      const int pp0 = s_pad[e] + nt * 128;
+      const int local = nt * 128 + 32 * q + lane;
+      const bool valid = local < s_off[e + 1] - s_off[e];
+      const int tw = 2 * jj + hf;  // the warp's window tile, counted from the forward's window start
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + 128 * hf;
+      // the warp's slice into registers, then the accumulator is free
+      uint32_t g[2][16], v[2][16];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        tc_ld16(taddr + 16 * (b0 + i), g[i]);
+        tc_ld16(taddr + 64 + 16 * (b0 + i), v[i]);
+      }
+      tc_wait16x2(g[0], v[0]);
+      tc_wait16x2(g[1], v[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
+      const float* gglob = reinterpret_cast<const float*>(rec + a.lay.gu_global) + row0 + 64 * tw;
+      const float* uglob = gglob + Iw;
+      const int pp = pp0 + 32 * q + lane;
+      uint32_t sfw = 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int b = b0 + i;
+        float h[16];
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
+          const float4 gg = __ldg(reinterpret_cast<const float4*>(gglob + 16 * b + c));
+          const float4 ug = __ldg(reinterpret_cast<const float4*>(uglob + 16 * b + c));
+          h[c] = silu_fast(__uint_as_float(g[i][c]) * gg.x) * (__uint_as_float(v[i][c]) * ug.x);
+          h[c + 1] = silu_fast(__uint_as_float(g[i][c + 1]) * gg.y) * (__uint_as_float(v[i][c + 1]) * ug.y);
+          h[c + 2] = silu_fast(__uint_as_float(g[i][c + 2]) * gg.z) * (__uint_as_float(v[i][c + 2]) * ug.z);
+          h[c + 3] = silu_fast(__uint_as_float(g[i][c + 3]) * gg.w) * (__uint_as_float(v[i][c + 3]) * ug.w);
+        }
+        uint8_t codes[8];
+        const uint8_t sc = quantize_act16(h, codes);
+        sfw |= (uint32_t)sc << (8 * i);
+        if (valid) {
+          uint2 pk;
+          pk.x = codes[0] | (codes[1] << 8) | (codes[2] << 16) | ((uint32_t)codes[3] << 24);
+          pk.y = codes[4] | (codes[5] << 8) | (codes[6] << 16) | ((uint32_t)codes[7] << 24);
+          *reinterpret_cast<uint2*>(a.hq + (int64_t)pp * a.hq_pitch + 32 * tw + 8 * b) = pk;
+        }
+      }
+      *reinterpret_cast<uint16_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + tw) * 512 + lane * 16 + q * 4 +
+                                   b0) = valid ? (uint16_t)sfw : (uint16_t)0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 int64_t pf_pad_max(int64_t P, int E) {
@@ -921,6 +1170,9 @@ cudaError_t prefill_set_smem_limits() {
   if ((e = cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) !=
       cudaSuccess)
     return e;
+  if ((e = cudaFuncSetAttribute(k_pf_gu256, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) !=
+      cudaSuccess)
+    return e;
   if ((e = cudaFuncSetAttribute(k_pf_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_pf_mma<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
@@ -946,7 +1198,10 @@ cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms,
   }
   const int smem = pf_smem_bytes(a.E);
   FTMOE_PROF_BEGIN("k_pf_gate_up", s);
-  k_pf_mma<0><<<num_sms, kPfThreads, smem, s>>>(a, m.xg, m.gu);
+  if (a.win.I_loc % 128 == 0 && gu256_smem_bytes(a.E) <= 227 * 1024)
+    k_pf_gu256<<<num_sms, kGuThreads, gu256_smem_bytes(a.E), s>>>(a, m.xg, m.gu);
+  else
+    k_pf_mma<0><<<num_sms, pf_threads(0), smem, s>>>(a, m.xg, m.gu);
   FTMOE_PROF_END(s);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   // the down epilogue stages Y through shared memory where it fits
