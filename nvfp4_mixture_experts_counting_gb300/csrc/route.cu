@@ -270,16 +270,43 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
       nc += __popc(m);
     }
   }
-  if (lane == 0) s_nc[warp] = nc;
+  // Only a candidate whose interval meets another candidate's needs its
+  // compensated logit: one whose interval is apart from every other
+  // candidate's already ranks right against all of them by its fp32 logit
+  // (and an expert outside the candidates ranks below every chosen one).
+  // The list of those that need it reuses the warp's working logits.
+  int* need = reinterpret_cast<int*>(lw);
+  int nn = 0;
+  __syncwarp();
+  if (!certified) {
+    for (int base = 0; base < nc; base += 32) {
+      const int c = base + lane;
+      bool nd = false;
+      if (c < nc) {
+        const int e = cand[c];
+        const float l = lg[e], r = er[e];
+        for (int c2 = 0; c2 < nc && !nd; ++c2) {
+          const int e2 = cand[c2];
+          if (c2 != c && fabsf(l - lg[e2]) <= r + er[e2]) nd = true;
+        }
+        l64[c] = df32{l, 0.f};  // the fp32 logit, unless computed again below
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, nd);
+      if (nd) need[nn + __popc(m & ((1u << lane) - 1))] = c;
+      nn += __popc(m);
+    }
+  }
+  if (lane == 0) s_nc[warp] = nn;
   __syncthreads();
   {
-    // every warp computes compensated logits of the CTA's candidates in turn
+    // every warp computes compensated logits of the CTA's needed candidates in turn
     int total = 0;
     for (int w = 0; w < kTopkWarps; ++w) total += s_nc[w];
     for (int item = warp; item < total; item += kTopkWarps) {
-      int w = 0, c = item;
-      while (c >= s_nc[w]) { c -= s_nc[w]; ++w; }
+      int w = 0, i = item;
+      while (i >= s_nc[w]) { i -= s_nc[w]; ++w; }
       const int tw = blockIdx.x * kTopkWarps + w;
+      const int c = reinterpret_cast<const int*>(sm)[w * E + i];
       const int e = reinterpret_cast<const int*>(sm)[kTopkWarps * E + w * E + c];
       const df32 v = logit_df32(a.x + (int64_t)tw * a.H, a.router_w + (int64_t)e * a.H, a.H,
                                 a.router_bias ? a.router_bias[e] : 0.f, lane);
