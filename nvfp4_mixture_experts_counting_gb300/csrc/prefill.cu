@@ -1079,6 +1079,207 @@ bool prefill_supported(int H, int E, int I_loc, int Iw, int row0) {
   return pf_smem_bytes(E) <= 227 * 1024;
 }
 
+// ------------------------------------------------------------------ bf16 products, 128 x 256 tiles
+
+// The shared expert's gate_up (mode 2) and the router logits (mode 4) with
+// 256 weight rows per tile.  One thread issues a tile's MMAs, and at N = 128
+// its four MMAs per stage plus the stage's wait and commit take longer than
+// the tensor pipe needs for them; at N = 256 the same issue work moves twice
+// the products.  No scale factors, so two 256-column accumulators fit in
+// TMEM and the epilogue of one tile overlaps the next tile's MMAs.
+namespace {
+constexpr int kBwStages = 4;
+constexpr int kBwTileB = 32768;  // 256 x 128-byte weight tile
+constexpr int kBwOffA = 0;
+constexpr int kBwOffB = kBwStages * kTile;
+constexpr int kBwOffBar = kBwOffB + kBwStages * kBwTileB;
+constexpr int kBwThreads = 32 * (2 + kPfEpiWarps);
+constexpr int kBwSmem = 1024 + kBwOffBar + 256;
+}  // namespace
+
+template <int MODE>
+__global__ void __launch_bounds__(kBwThreads, 1)
+    k_pf_bf16w(const __grid_constant__ PfArgs a, const __grid_constant__ CUtensorMap mapA,
+               const __grid_constant__ CUtensorMap mapB) {
+  static_assert(MODE == 2 || MODE == 4, "bf16 modes only");
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kBwOffBar);
+  uint64_t* empty = full + kBwStages;
+  uint64_t* acc_full = empty + kBwStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.H;
+  const int nks_all = MODE == 2 ? 2 * H / 32 : 6 * H / 32;  // 32-byte K steps (16 bf16)
+  const int nkt = (nks_all + 3) / 4;
+  const int J = MODE == 2 ? a.s_I_loc / 128 : a.E / 256;  // weight tiles per row tile
+  const int n_units = ((a.T + 127) / 128) * J;
+
+  if (tid == 0) {
+    for (int s = 0; s < kBwStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], kPfEpiWarps); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int k = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+        const int nt = u / J, j = u % J;
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kBwStages;
+          if (k >= kBwStages && !mbar_wait(&empty[s], ((k / kBwStages) - 1) & 1, a.status)) {
+            *abort_flag = 1;
+            break;
+          }
+          unsigned char* sa = sm + kBwOffA + s * kTile;
+          unsigned char* sb = sm + kBwOffB + s * kBwTileB;
+          mbar_arrive_expect_tx(&full[s], kTile + kBwTileB);
+          tma_load_2d(sa, &mapA, MODE == 4 ? (kt * 128) % (2 * H) : kt * 128, nt * 128, &full[s]);
+          if (MODE == 2) {
+            // gate rows, then the matching up rows, for each of the two 64-row tiles
+            for (int h = 0; h < 2; ++h) {
+              tma_load_2d(sb + h * kTile, &mapB, kt * 128, a.s_row0 + 128 * j + 64 * h, &full[s]);
+              tma_load_2d(sb + h * kTile + kTile / 2, &mapB, kt * 128, a.s_Iw + a.s_row0 + 128 * j + 64 * h,
+                          &full[s]);
+            }
+          } else {
+            tma_load_2d(sb, &mapB, kt * 128, 256 * j, &full[s]);
+            tma_load_2d(sb + kTile, &mapB, kt * 128, 256 * j + 128, &full[s]);
+          }
+        }
+      }
+      for (int q = k - kBwStages > 0 ? k - kBwStages : 0; q < k; ++q)
+        mbar_wait(&full[q % kBwStages], (q / kBwStages) & 1, a.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: two 256-column accumulators
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, 256);
+      int k = 0, ui = 0;
+      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
+        const int buf = ui & 1;
+        if (ui >= 2 && !mbar_wait(&acc_empty[buf], ((ui >> 1) - 1) & 1, a.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * 256;
+        bool ok = true;
+        for (int kt = 0; kt < nkt; ++kt, ++k) {
+          const int s = k % kBwStages;
+          if (!mbar_wait(&full[s], (k / kBwStages) & 1, a.status)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nks = min(4, nks_all - 4 * kt);
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + kBwOffA + s * kTile));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + kBwOffB + s * kBwTileB));
+          for (int ks = 0; ks < nks; ++ks) tc_mma_bf16(d, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kt | ks) != 0);
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.status);
+    }
+  } else {
+    // ---------------- epilogue: warp (q, hf) reads TMEM lanes 32q.. and the
+    // accumulator's columns [128 hf, 128 hf + 128)
+    const int q = warp & 3, hf = (warp - 2) >> 2;
+    int ui = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
+      const int buf = ui & 1;
+      if (!mbar_wait(&acc_full[buf], (ui >> 1) & 1, a.status)) { *abort_flag = 1; break; }
+      tc_fence_after();
+      const int nt = u / J, j = u % J;
+      const int t = nt * 128 + 32 * q + lane;
+      const bool valid = t < a.T;
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 256 + 128 * hf;
+      if (MODE == 2) {
+        // h = silu(gate) * up for intermediate columns [128 j + 64 hf, +64):
+        // gate in the half's first 64 columns, up in its last 64
+        uint16_t* hrow = a.hs + (int64_t)t * a.s_I_loc + 128 * j + 64 * hf;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          uint32_t g[16], v[16];
+          tc_ld16(taddr + 16 * b, g);
+          tc_ld16(taddr + 64 + 16 * b, v);
+          tc_wait16x2(g, v);
+          if (valid) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(v[2 * i]);
+              const float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+              pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(hrow + 16 * b);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else {
+        // logits of token t for experts [256 j + 128 hf, +128) and their bounds
+        const float xn = valid ? a.xnorm[t] : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tc_ld16(taddr + 16 * c, v);
+          tc_wait16(v);
+          if (valid) {
+            const int e0 = 256 * j + 128 * hf + 16 * c;
+            float* lrow = a.logits + (int64_t)t * a.E + e0;
+            float* erow = a.err + (int64_t)t * a.E + e0;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 wn = __ldg(reinterpret_cast<const float4*>(a.wnorm + e0 + i));
+              float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (a.router_bias) b = __ldg(reinterpret_cast<const float4*>(a.router_bias + e0 + i));
+              float4 l, er;
+              l.x = __uint_as_float(v[i]) + b.x;
+              l.y = __uint_as_float(v[i + 1]) + b.y;
+              l.z = __uint_as_float(v[i + 2]) + b.z;
+              l.w = __uint_as_float(v[i + 3]) + b.w;
+              er.x = a.kappa * xn * wn.x + 2.4e-7f * fabsf(l.x) + 1e-30f;
+              er.y = a.kappa * xn * wn.y + 2.4e-7f * fabsf(l.y) + 1e-30f;
+              er.z = a.kappa * xn * wn.z + 2.4e-7f * fabsf(l.z) + 1e-30f;
+              er.w = a.kappa * xn * wn.w + 2.4e-7f * fabsf(l.w) + 1e-30f;
+              *reinterpret_cast<float4*>(lrow + i) = l;
+              *reinterpret_cast<float4*>(erow + i) = er;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 static cudaError_t encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                           const uint32_t* box) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1175,6 +1376,10 @@ cudaError_t prefill_set_smem_limits() {
     return e;
   if ((e = cudaFuncSetAttribute(k_pf_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
+  if ((e = cudaFuncSetAttribute(k_pf_bf16w<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwSmem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_pf_bf16w<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwSmem)) != cudaSuccess)
+    return e;
   if ((e = cudaFuncSetAttribute(k_pf_mma<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(k_pf_mma<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1253,14 +1458,20 @@ cudaError_t launch_router_split(const float* w, int E, int H, uint16_t* wcat, fl
 
 cudaError_t launch_prefill_router(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
   FTMOE_PROF_BEGIN("k_pf_router", s);
-  k_pf_mma<4><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.x, m.wr);
+  if (a.E % 256 == 0)
+    k_pf_bf16w<4><<<num_sms, kBwThreads, kBwSmem, s>>>(a, m.x, m.wr);
+  else
+    k_pf_mma<4><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.x, m.wr);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_shared_gate_up(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
   FTMOE_PROF_BEGIN("k_pf_shared_gate_up", s);
-  k_pf_mma<2><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.x, m.sgu);
+  if (a.s_I_loc % 128 == 0)
+    k_pf_bf16w<2><<<num_sms, kBwThreads, kBwSmem, s>>>(a, m.x, m.sgu);
+  else
+    k_pf_mma<2><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.x, m.sgu);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
