@@ -104,6 +104,14 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// 32 bytes of read-only global data at a 32-byte-aligned address, one
+// 256-bit load.
+__device__ __forceinline__ void ldg_nc_32B(const void* p, uint32_t* r) {
+  asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "l"(p));
+}
+
 // ---------------------------------------------------------------- double-fp32
 
 // A number hi + lo held as two fp32 values.  Built from error-free

@@ -694,27 +694,30 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = 0.f;
             if (a.y_bf16) {
-              // each slot's 16 bf16 values of this chunk are two 16-byte loads;
-              // up to 8 slots have theirs in flight together
+              // each slot's 16 bf16 values of this chunk are one 32-byte
+              // load (the warp's lanes read 32 different rows, so a load's
+              // cost is its rows, not its bytes); up to 8 slots have theirs
+              // in flight together
               if (k <= 8) {
-                uint4 y[8][2];
+                uint32_t y[8][8];
 #pragma unroll
                 for (int q2 = 0; q2 < 8; ++q2) {
-                  const uint4* yp = reinterpret_cast<const uint4*>(ytb + q2 * 128 + 16 * c);
-                  y[q2][0] = q2 < k ? __ldg(yp) : make_uint4(0, 0, 0, 0);
-                  y[q2][1] = q2 < k ? __ldg(yp + 1) : make_uint4(0, 0, 0, 0);
+                  if (q2 < k) {
+                    ldg_nc_32B(ytb + q2 * 128 + 16 * c, y[q2]);
+                  } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[q2][i] = 0u;
+                  }
                 }
 #pragma unroll
                 for (int q2 = 0; q2 < 8; ++q2) {
                   // a slot of weight zero (left out of an expert subset)
                   // adds nothing, whatever its stale Y holds
                   if (q2 < k && wj[q2] != 0.f) {
-                    const uint32_t u[8] = {y[q2][0].x, y[q2][0].y, y[q2][0].z, y[q2][0].w,
-                                           y[q2][1].x, y[q2][1].y, y[q2][1].z, y[q2][1].w};
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                      o[2 * i] = fmaf(wj[q2], __uint_as_float(u[i] << 16), o[2 * i]);
-                      o[2 * i + 1] = fmaf(wj[q2], __uint_as_float(u[i] & 0xffff0000u), o[2 * i + 1]);
+                      o[2 * i] = fmaf(wj[q2], __uint_as_float(y[q2][i] << 16), o[2 * i]);
+                      o[2 * i + 1] = fmaf(wj[q2], __uint_as_float(y[q2][i] & 0xffff0000u), o[2 * i + 1]);
                     }
                   }
                 }
@@ -737,24 +740,23 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
 #pragma unroll
                 for (int j0 = 0; j0 < 8; j0 += 4) {
                   if (j0 < k) {
-                    float4 y[4][4];
+                    // a slot's 16 fp32 values are two 32-byte loads
+                    uint32_t y[4][16];
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
-                      const float4* yp = reinterpret_cast<const float4*>(ytf + (j0 + q2) * 128 + 16 * c);
+                      if (j0 + q2 < k) {
+                        ldg_nc_32B(ytf + (j0 + q2) * 128 + 16 * c, y[q2]);
+                        ldg_nc_32B(ytf + (j0 + q2) * 128 + 16 * c + 8, y[q2] + 8);
+                      } else {
 #pragma unroll
-                      for (int i4 = 0; i4 < 4; ++i4)
-                        y[q2][i4] = (j0 + q2 < k) ? __ldg(yp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int i = 0; i < 16; ++i) y[q2][i] = 0u;
+                      }
                     }
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
                       if (j0 + q2 < k && wj[j0 + q2] != 0.f) {
 #pragma unroll
-                        for (int i4 = 0; i4 < 4; ++i4) {
-                          o[4 * i4] = fmaf(wj[j0 + q2], y[q2][i4].x, o[4 * i4]);
-                          o[4 * i4 + 1] = fmaf(wj[j0 + q2], y[q2][i4].y, o[4 * i4 + 1]);
-                          o[4 * i4 + 2] = fmaf(wj[j0 + q2], y[q2][i4].z, o[4 * i4 + 2]);
-                          o[4 * i4 + 3] = fmaf(wj[j0 + q2], y[q2][i4].w, o[4 * i4 + 3]);
-                        }
+                        for (int i = 0; i < 16; ++i) o[i] = fmaf(wj[j0 + q2], __uint_as_float(y[q2][i]), o[i]);
                       }
                     }
                   }
