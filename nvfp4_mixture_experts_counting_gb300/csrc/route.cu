@@ -214,11 +214,23 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(RouteArgs a) {
   float* lw = reinterpret_cast<float*>(sm) + warp * E;                // working logits
   int* cand = reinterpret_cast<int*>(sm) + kTopkWarps * E + warp * E;  // candidate list
   df32* l64 = reinterpret_cast<df32*>(sm + (size_t)kTopkWarps * E * 8) + warp * E;
+  // the token's logits and bounds, copied once: every later read is in
+  // shared memory (the selection's reads depend on the previous round's
+  // winner, so from global memory each would wait a full load latency)
+  float* lg = reinterpret_cast<float*>(sm + (size_t)kTopkWarps * E * 16) + warp * E;
+  float* er = reinterpret_cast<float*>(sm + (size_t)kTopkWarps * E * 20) + warp * E;
   const int t = blockIdx.x * kTopkWarps + warp;
   const bool have = t < a.T;
-  const float* lg = a.logits + (int64_t)(have ? t : 0) * E;
-  const float* er = a.err + (int64_t)(have ? t : 0) * E;
-  for (int e = lane; e < E; e += 32) lw[e] = lg[e];
+  {
+    const float* lgg = a.logits + (int64_t)(have ? t : 0) * E;
+    const float* erg = a.err + (int64_t)(have ? t : 0) * E;
+    for (int e = lane; e < E; e += 32) {
+      const float l = lgg[e];
+      lw[e] = l;
+      lg[e] = l;
+      er[e] = erg[e];
+    }
+  }
   __syncwarp();
 
   int chosen[32];
@@ -658,7 +670,7 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int parts) {
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   if (parts & kRouteTopk) {
-    size_t smem = (size_t)kTopkWarps * a.E * (4 + 4 + 8);
+    size_t smem = (size_t)kTopkWarps * a.E * (4 + 4 + 8 + 4 + 4);
     FTMOE_PROF_BEGIN("k_topk", s);
     k_topk<<<(a.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, smem, s>>>(a);
     FTMOE_PROF_END(s);
@@ -703,7 +715,7 @@ cudaError_t route_set_smem_limits(int H, int E) {
                                 kRouterTT * 8192 * 2)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kTopkWarps * 1024 * 16)) != cudaSuccess)
+                                kTopkWarps * 1024 * 24)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_sort_count, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortWarps * 1024 * 4)) !=
       cudaSuccess)
