@@ -419,13 +419,32 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
     int ui = 0;
     for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
       const int buf = ui & 1;
-      if (!mbar_wait(&acc_full[buf], (ui >> 1) & 1, a.status)) { *abort_flag = 1; break; }
-      tc_fence_after();
       const int e = find_le(s_up, E, u), r = u - s_up[e];
       const int nt = r / J, j = r % J;
       const int pp0 = s_pad[e] + nt * 128;
       const int local = nt * 128 + 32 * q + lane;
       const bool valid = local < s_off[e + 1] - s_off[e];
+      // the unit's loads that do not need the accumulator are issued before
+      // its wait, so their latency overlaps the unit's MMAs: the down
+      // rows' globals and the lane's pair index (mode 1), the token's
+      // routing weights and sigma (mode 3)
+      float4 pre_g = make_float4(0.f, 0.f, 0.f, 0.f);
+      int pre_pr = 0;
+      float pre_w[8], pre_sig = 0.f;
+      if (MODE == 1) {
+        const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
+        pre_g = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j) +
+                      lane);
+        if (valid) pre_pr = __ldg(a.perm + s_off[e] + local);
+      }
+      if (MODE == 3) {
+        const float* w = a.topk_w + (int64_t)local * a.top_k;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) pre_w[jj] = (valid && jj < a.top_k) ? __ldg(w + jj) : 0.f;
+        pre_sig = valid ? a.sigma[local] : 0.f;
+      }
+      if (!mbar_wait(&acc_full[buf], (ui >> 1) & 1, a.status)) { *abort_flag = 1; break; }
+      tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 128;
       if (MODE == 0) {
         // warp (q, cb): pair rows 32q.. and the unit's 16-wide block cb, gate
@@ -460,10 +479,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         }
         a.hq_sf[((int64_t)(pp0 >> 7) * (I_loc / 64) + j) * 512 + lane * 16 + q * 4 + cb] = valid ? sc : 0;
       } else if (MODE == 1) {
-        const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
-        reinterpret_cast<float4*>(wglob)[lane] =
-            __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j) +
-                  lane);
+        reinterpret_cast<float4*>(wglob)[lane] = pre_g;
         __syncwarp();
         // Y is [token][H / 128 column tiles][slot][128]: a lane's row is
         // pair p = t * k + slot, its tile-j segment at (t * H/128 + j) * k + slot;
@@ -477,10 +493,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
             const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
             unsigned char* stg = sm + pf_stg_off(E) + (warp - 2) * 32 * kPfStgRow;
             int yseg = 0;
-            if (lane < nvalid) {
-              const int pr = __ldg(a.perm + s_off[e] + row_w + lane);
-              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
-            }
+            if (lane < nvalid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
             const int cb = 64 * hf;  // the warp's 64 columns
             uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kPfStgRow);
 #pragma unroll 1
@@ -517,10 +530,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
             __syncwarp();
           } else {
             int yseg = 0;
-            if (valid) {
-              const int pr = __ldg(a.perm + s_off[e] + local);
-              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
-            }
+            if (valid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
             uint16_t* yrow = Yb + (int64_t)yseg * 128;
 #pragma unroll 1
             for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
@@ -551,10 +561,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
             const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
             float* stg = reinterpret_cast<float*>(sm + pf_stg_off(E) + (warp - 2) * 32 * kPfStgRow);
             int yseg = 0;
-            if (lane < nvalid) {
-              const int pr = __ldg(a.perm + s_off[e] + row_w + lane);
-              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
-            }
+            if (lane < nvalid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
               const int cb = 64 * hf + 32 * cc;  // first of the chunk's 32 columns
@@ -587,10 +594,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
             }
           } else {
             int yseg = 0;
-            if (valid) {
-              const int pr = __ldg(a.perm + s_off[e] + local);
-              yseg = ((pr / a.top_k) * (H / 128) + j) * a.top_k + pr % a.top_k;
-            }
+            if (valid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
             float* yrow = Yf + (int64_t)yseg * 128;
 #pragma unroll 1
             for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
@@ -675,7 +679,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         const int t = local;
         const int k = a.top_k;
         const float* w = a.topk_w + (int64_t)t * k;
-        const float sig = valid ? a.sigma[t] : 0.f;
+        const float sig = pre_sig;
         const int64_t obase = (int64_t)t * H + 128 * j;
         // the token's k slot segments of column tile j, contiguous (bf16 or fp32)
         const int64_t yoff = ((int64_t)t * (H / 128) + j) * k * 128;
@@ -683,7 +687,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         const float* ytf = reinterpret_cast<const float*>(a.Y) + yoff;
         float wj[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) wj[jj] = (valid && jj < k) ? __ldg(w + jj) : 0.f;
+        for (int jj = 0; jj < 8; ++jj) wj[jj] = pre_w[jj];
 #pragma unroll 1
         for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
           uint32_t v[16];
