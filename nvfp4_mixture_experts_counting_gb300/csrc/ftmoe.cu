@@ -685,6 +685,10 @@ static PfArgs prefill_args(ftmoe_handle* h, Layer& L, const ExpertArgs& a, const
     p.logits = r.logits;
     p.err = r.err;
     p.kappa = kRouterKappa;
+    // Y is not written before the routed down kernel, so the router's
+    // K-split partials may use it
+    p.rpart = h->Y;
+    p.rpart_cap = (int64_t)(c.max_tokens > 0 ? c.max_tokens : 1) * c.top_k * c.H;
   }
   return p;
 }

@@ -227,6 +227,12 @@ struct PfArgs {
   float* logits;              // [T][E]
   float* err;                 // [T][E] bound on |logit - exact|
   float kappa;                // err = kappa * ||x|| * ||w|| + 2^-22 |logit|
+  // few tokens: the router's K range split over r_ksplit CTAs per tile, whose
+  // partial sums ([r_ksplit][T][E] fp32, in a buffer of rpart_cap floats
+  // that routing does not otherwise use) a second kernel adds in order
+  float* rpart;
+  int64_t rpart_cap;
+  int r_ksplit;
 };
 struct PfMaps {
   CUtensorMap xg, gu, hq, dn;   // routed operands

@@ -1122,7 +1122,10 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   const int nks_all = MODE == 2 ? 2 * H / 32 : 6 * H / 32;  // 32-byte K steps (16 bf16)
   const int nkt = (nks_all + 3) / 4;
   const int J = MODE == 2 ? a.s_I_loc / 128 : a.E / 256;  // weight tiles per row tile
-  const int n_units = ((a.T + 127) / 128) * J;
+  // router with few tokens: each (row tile, weight tile) split into KS
+  // contiguous K ranges, one unit each
+  const int KS = MODE == 4 && a.r_ksplit > 1 ? a.r_ksplit : 1;
+  const int n_units = ((a.T + 127) / 128) * J * KS;
 
   if (tid == 0) {
     for (int s = 0; s < kBwStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -1146,8 +1149,9 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     if (lane == 0) {
       int k = 0;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-        const int nt = u / J, j = u % J;
-        for (int kt = 0; kt < nkt; ++kt, ++k) {
+        const int mn = u / KS, ks = u % KS;
+        const int nt = mn / J, j = mn % J;
+        for (int kt = ks * nkt / KS; kt < (ks + 1) * nkt / KS; ++kt, ++k) {
           const int s = k % kBwStages;
           if (k >= kBwStages && !mbar_wait(&empty[s], ((k / kBwStages) - 1) & 1, a.status)) {
             *abort_flag = 1;
@@ -1183,8 +1187,9 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         if (ui >= 2 && !mbar_wait(&acc_empty[buf], ((ui >> 1) - 1) & 1, a.status)) { *abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t d = tmem + buf * 256;
+        const int ks = u % KS, kt0 = ks * nkt / KS;
         bool ok = true;
-        for (int kt = 0; kt < nkt; ++kt, ++k) {
+        for (int kt = kt0; kt < (ks + 1) * nkt / KS; ++kt, ++k) {
           const int s = k % kBwStages;
           if (!mbar_wait(&full[s], (k / kBwStages) & 1, a.status)) {
             *abort_flag = 1;
@@ -1195,7 +1200,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
           const int nks = min(4, nks_all - 4 * kt);
           const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + kBwOffA + s * kTile));
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + kBwOffB + s * kBwTileB));
-          for (int ks = 0; ks < nks; ++ks) tc_mma_bf16(d, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kt | ks) != 0);
+          for (int q = 0; q < nks; ++q) tc_mma_bf16(d, adesc + 2 * q, bdesc + 2 * q, idesc, (kt != kt0) || q != 0);
           tc_commit(&empty[s]);
         }
         if (!ok) break;
@@ -1213,7 +1218,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       const int buf = ui & 1;
       if (!mbar_wait(&acc_full[buf], (ui >> 1) & 1, a.status)) { *abort_flag = 1; break; }
       tc_fence_after();
-      const int nt = u / J, j = u % J;
+      const int mn = u / KS, ks = u % KS;
+      const int nt = mn / J, j = mn % J;
       const int t = nt * 128 + 32 * q + lane;
       const bool valid = t < a.T;
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 256 + 128 * hf;
@@ -1239,6 +1245,22 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             uint4* dst = reinterpret_cast<uint4*>(hrow + 16 * b);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else if (KS > 1) {
+        // this K range's partial sums for experts [256 j + 128 hf, +128)
+        float* prow = a.rpart + ((int64_t)ks * a.T + t) * a.E + 256 * j + 128 * hf;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tc_ld16(taddr + 16 * c, v);
+          tc_wait16(v);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(prow + 16 * c + i) =
+                  make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                              __uint_as_float(v[i + 3]));
           }
         }
       } else {
@@ -1462,12 +1484,52 @@ cudaError_t launch_router_split(const float* w, int E, int H, uint16_t* wcat, fl
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_router(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
+// Router logits from the K-split partials: l = sum over the ranges in range
+// order + bias, and the bound of the tensor-core sums plus that of the
+// KS - 1 fp32 additions (each at most 2^-24 of the sum of the partials'
+// magnitudes, which sum to at most ||[x x x]|| ||[W1 W2 W3]|| <= 1.75
+// ||x|| ||w|| upper bounds).
+__global__ void __launch_bounds__(256) k_router_finish(PfArgs a, int KS) {
+  const int E = a.E;
+  const int64_t n = (int64_t)a.T * E;
+  const float add = (float)(KS - 1) * 1.05e-7f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / E), e = (int)(i % E);
+    float l = 0.f;
+    for (int ks = 0; ks < KS; ++ks) l += __ldg(a.rpart + (int64_t)ks * n + i);
+    if (a.router_bias) l += __ldg(a.router_bias + e);
+    const float xw = a.xnorm[t] * __ldg(a.wnorm + e);
+    a.logits[i] = l;
+    a.err[i] = a.kappa * xw + add * xw + 2.4e-7f * fabsf(l) + 1e-30f;
+  }
+}
+
+cudaError_t launch_prefill_router(const PfArgs& a0, const PfMaps& m, int num_sms, cudaStream_t s) {
+  PfArgs a = a0;
+  a.r_ksplit = 1;
+  if (a.E % 256 == 0 && a.rpart) {
+    // enough units for the SMs: split each tile's K range while there are
+    // fewer tiles than SMs (at most 16 ranges, and as many as the buffer holds)
+    const int tiles = ((a.T + 127) / 128) * (a.E / 256);
+    const int nkt = (6 * a.H / 32 + 3) / 4;
+    int ks = num_sms / tiles;
+    if (ks > 16) ks = 16;
+    if (ks > nkt) ks = nkt;
+    while (ks > 1 && (int64_t)ks * a.T * a.E > a.rpart_cap) --ks;
+    a.r_ksplit = ks < 1 ? 1 : ks;
+  }
   FTMOE_PROF_BEGIN("k_pf_router", s);
-  if (a.E % 256 == 0)
+  if (a.E % 256 == 0) {
     k_pf_bf16w<4><<<num_sms, kBwThreads, kBwSmem, s>>>(a, m.x, m.wr);
-  else
+    if (a.r_ksplit > 1 && cudaPeekAtLastError() == cudaSuccess) {
+      const int64_t n = (int64_t)a.T * a.E;
+      int blocks = (int)((n + 255) / 256);
+      if (blocks > num_sms * 8) blocks = num_sms * 8;
+      k_router_finish<<<blocks, 256, 0, s>>>(a, a.r_ksplit);
+    }
+  } else {
     k_pf_mma<4><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.x, m.wr);
+  }
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
