@@ -176,16 +176,32 @@ __global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
     for (int e = threadIdx.x; e <= E; e += blockDim.x) a.pad_off[e] = s_pad[e];
   const int total = s_pad[E], hc = H / 2, nks = H / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  // codes: one warp per padded row (rows past an expert's pairs stay as
-  // they are: their MMA rows are never read)
-  for (int pp = blockIdx.x * nw + warp; pp < total; pp += gridDim.x * nw) {
-    const int e = find_le(s_pad, E, pp);
-    const int local = pp - s_pad[e], m = s_off[e + 1] - s_off[e];
-    if (local < m) {
-      const int t = a.perm[s_off[e] + local] / a.top_k;
-      const uint4* src = reinterpret_cast<const uint4*>(a.xq_codes + (int64_t)t * hc);
-      uint4* dst = reinterpret_cast<uint4*>(a.xg + (int64_t)pp * hc);
-      for (int i = lane; i < hc / 16; i += 32) dst[i] = src[i];
+  // codes: eight lanes per padded row, four rows per warp at a time, each
+  // lane's loads of its row in flight together (rows past an expert's pairs
+  // stay as they are: their MMA rows are never read)
+  {
+    const int sub = lane >> 3, l8 = lane & 7, n16 = hc / 16;
+    for (int p0 = (blockIdx.x * nw + warp) * 4; p0 < total; p0 += gridDim.x * nw * 4) {
+      const int pp = p0 + sub;
+      int t = -1;
+      if (pp < total) {
+        const int e = find_le(s_pad, E, pp);
+        const int local = pp - s_pad[e];
+        if (local < s_off[e + 1] - s_off[e]) t = __ldg(a.perm + s_off[e] + local) / a.top_k;
+      }
+      if (t >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.xq_codes + (int64_t)t * hc);
+        uint4* dst = reinterpret_cast<uint4*>(a.xg + (int64_t)pp * hc);
+        for (int i0 = l8; i0 < n16; i0 += 8 * 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (i0 + 8 * c < n16) v[c] = __ldg(src + i0 + 8 * c);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (i0 + 8 * c < n16) dst[i0 + 8 * c] = v[c];
+        }
+      }
     }
   }
   // scales: a 128-row tile per 128 threads, a thread per row: its token's
