@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define FTMOE_ABI_VERSION 2
+#define FTMOE_ABI_VERSION 3
 
 typedef void* ftmoe_stream_t; /* a cudaStream_t */
 
@@ -133,6 +133,14 @@ typedef struct {
   int32_t* inv;       /* [T*top_k] sorted position of each pair id */
   float* logits;      /* [T, E] router logits (bias included) as the fast pass computed them,
                          before any re-rank of uncertain tokens */
+  /* Each pair's quantised intermediate h = SiLU(G_gate) * G_up (NVFP4, global
+     1.0, 16-blocks along the window), rows in sorted-position order:
+     h_codes [T*top_k, I_loc/2] (two E2M1 codes a byte, low nibble first),
+     h_scales [T*top_k, I_loc/16] (E4M3).  Written by ftmoe_forward's
+     tensor-core prefill path only (resident banks, T > 32 and the shapes it
+     takes); other paths and calls leave them untouched. */
+  uint8_t* h_codes;
+  uint8_t* h_scales;
 } ftmoe_aux;
 
 typedef struct {

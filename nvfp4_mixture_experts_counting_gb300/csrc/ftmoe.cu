@@ -770,6 +770,7 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     if (tc_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
     else CK(launch_experts(a, s, kPartSharedGateUp));
     CK(launch_prefill_routed(p, maps, h->num_sms, s));
+    if (aux) CK(launch_prefill_export_h(p, aux->h_codes, aux->h_scales, h->num_sms, s));
     if (tc_shared) {
       CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
     } else {

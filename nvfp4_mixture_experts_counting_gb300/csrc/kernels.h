@@ -252,6 +252,7 @@ cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m);
 cudaError_t prefill_set_smem_limits();
 cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw, int E, cudaStream_t s);
 cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill_export_h(const PfArgs& a, uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t s);
 
 // W4A16 routed experts (w4a16.cu): bf16 x, NVFP4 weights dequantised in
 // registers, bf16 intermediate in hq_codes ([P][I_loc] bf16), Y [P][H] in

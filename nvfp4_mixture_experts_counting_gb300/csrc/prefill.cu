@@ -1462,6 +1462,31 @@ cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms,
   return cudaGetLastError();
 }
 
+// Each pair's intermediate codes and scales in sorted-position order, from
+// the padded pair rows the gate_up epilogue wrote (a scale lives in its
+// row tile's 512-byte block of the 64-wide window tile, at sf_slot(row)).
+// One warp per sorted position.
+__global__ void __launch_bounds__(256) k_pf_export_h(PfArgs a, uint8_t* codes, uint8_t* scales) {
+  const int P = a.T * a.top_k, I_loc = a.win.I_loc, hc = I_loc / 2, nb = I_loc / 16;
+  const int lane = threadIdx.x & 31;
+  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < P; p += (gridDim.x * blockDim.x) >> 5) {
+    const int e = find_le(a.offsets, a.E - 1, p);
+    const int pp = a.pad_off[e] + p - a.offsets[e];
+    if (codes)
+      for (int i = lane; i < hc; i += 32) codes[(int64_t)p * hc + i] = a.hq[(int64_t)pp * a.hq_pitch + i];
+    if (scales)
+      for (int kb = lane; kb < nb; kb += 32)
+        scales[(int64_t)p * nb + kb] =
+            a.hq_sf[((int64_t)(pp >> 7) * (I_loc / 64) + kb / 4) * 512 + sf_slot(pp) + (kb & 3)];
+  }
+}
+
+cudaError_t launch_prefill_export_h(const PfArgs& a, uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t s) {
+  if (!codes && !scales) return cudaSuccess;
+  k_pf_export_h<<<num_sms * 4, 256, 0, s>>>(a, codes, scales);
+  return cudaGetLastError();
+}
+
 bool prefill_router_supported(int H, int E) { return E % 128 == 0 && E <= kPfMaxE && H % 64 == 0; }
 
 // Exact split of each fp32 router row into three bf16 parts (w - W1 and

@@ -17,7 +17,7 @@ from typing import Optional
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libftmoe.so")
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 OUT_BF16, OUT_FP32, OUT_ACCUMULATE, ACT_BF16 = 0, 1, 0x100, 0x200
 
 STATUS = {
@@ -50,7 +50,8 @@ class BankDesc(C.Structure):
 
 class Aux(C.Structure):
     _fields_ = [("topk_idx", C.c_void_p), ("topk_w", C.c_void_p), ("offsets", C.c_void_p),
-                ("perm", C.c_void_p), ("inv", C.c_void_p), ("logits", C.c_void_p)]
+                ("perm", C.c_void_p), ("inv", C.c_void_p), ("logits", C.c_void_p),
+                ("h_codes", C.c_void_p), ("h_scales", C.c_void_p)]
 
 
 class Stats(C.Structure):

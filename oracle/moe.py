@@ -161,6 +161,19 @@ def check_window(I: int, i0: int, I_loc: int) -> None:
         raise ValueError("i0 and I_loc must be multiples of 16")
 
 
+def expert_pair_intermediate(bank: ExpertBank, xq_rows: np.ndarray, I: int, i0: int, I_loc: int):
+    """The W4A4 intermediate of one expert's m pairs: G = W_gu[window rows] .
+    xq in fp64, h = silu(G_gate) * G_up, rounded to fp32 and quantised per
+    16-block along the window with global 1.0.  Returns (codes uint8
+    [m, I_loc/2], scales uint8 [m, I_loc/16]); the same steps as
+    expert_pair_outputs' "nvfp4" mode."""
+    rows = slice_window_rows(I, i0, I_loc)
+    w_gu = nvfp4.dequantize_rows(bank.gu_codes[rows], bank.gu_scales[rows], bank.gu_global[rows])
+    G = xq_rows @ w_gu.T                                   # [m, 2*I_loc]
+    h = silu(G[:, :I_loc]) * G[:, I_loc:]
+    return nvfp4.quantize_activation_rows(h.astype(np.float32))
+
+
 def expert_pair_outputs(bank: ExpertBank, xq_rows: np.ndarray, I: int, i0: int, I_loc: int,
                         activations: str = "nvfp4"):
     """Y rows [m, H] (fp64) of one expert for the activations of its m pairs

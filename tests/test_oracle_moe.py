@@ -185,6 +185,27 @@ def test_one_expert_reduces_to_dense_swiglu_mlp():
     assert np.all(res.topk_w == 1.0)
 
 
+def test_pair_intermediate_is_the_dense_mlps_quantised_h():
+    """expert_pair_intermediate against the same torch step by step as the
+    dense SwiGLU pin above (torch fp64 matmul and silu, then the oracle's
+    quantiser), on a window of a wider expert: the rows it takes are the
+    window's gate and up rows."""
+    rng = np.random.default_rng(17)
+    H, I, i0, I_loc = 64, 64, 16, 32
+    x = torch.from_numpy(rng.standard_normal((5, H)).astype(np.float32)).to(torch.bfloat16).float()
+    gu = (rng.standard_normal((2 * I, H)) * 0.1).astype(np.float32)
+    dn = (rng.standard_normal((H, I)) * 0.1).astype(np.float32)
+    bank = moe.quantize_expert(gu, dn)
+    xc, xs = nvfp4.quantize_activation_rows(x.numpy())
+    xq = nvfp4.dequantize_rows(xc, xs)
+    hc, hs = moe.expert_pair_intermediate(bank, xq, I, i0, I_loc)
+    Wgu = torch.from_numpy(nvfp4.dequantize_rows(bank.gu_codes, bank.gu_scales, bank.gu_global))
+    G = torch.nn.functional.linear(torch.from_numpy(xq), Wgu)  # all 2I rows
+    h = (torch.nn.functional.silu(G[:, i0:i0 + I_loc]) * G[:, I + i0:I + i0 + I_loc]).float()
+    rc, rs = nvfp4.quantize_activation_rows(h.numpy())
+    assert np.array_equal(hc, rc) and np.array_equal(hs, rs)
+
+
 def test_one_expert_bf16_activations_reduce_to_weight_only_mlp():
     """The bf16-activation (W4A16) mode, E=1, k=1, zero shared expert: a
     dense SwiGLU MLP on the dequantised weights with x unquantised and the
