@@ -34,14 +34,17 @@ namespace ftmoe {
 namespace {
 
 constexpr int kPfStages = 5;
-constexpr int kPfThreads = 352;    // producer, MMA, 8 epilogue warps, scale-factor copier
+constexpr int kPfThreads = 384;    // two producers, MMA, 8 epilogue warps, scale-factor copier
 constexpr int kPfEpiWarps = 8;
 // The routed gate_up's epilogue (globals, SwiGLU, NVFP4 quantisation of the
 // intermediate) is long chains of dependent arithmetic per value; with 8
 // warps it, not the copies or the tensor pipe, set the kernel's pace, so that
 // mode drains its accumulators with 16 warps, one 16-wide block each.
 __host__ __device__ constexpr int pf_epi_warps(int mode) { return mode == 0 ? 16 : kPfEpiWarps; }
-__host__ __device__ constexpr int pf_threads(int mode) { return 32 * (3 + pf_epi_warps(mode)); }
+// warps: 0 and 3 + epilogue warps the TMA producers (alternate stages), 1
+// MMA, 2 .. 1 + epilogue warps the epilogue, 2 + epilogue warps the
+// scale-factor copies
+__host__ __device__ constexpr int pf_threads(int mode) { return 32 * (4 + pf_epi_warps(mode)); }
 constexpr int kTile = 16384;        // one 128 x 128-byte operand tile
 constexpr int kSfStage = 2048;      // four 512-byte scale blocks
 constexpr int kPfOffA = 0;
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if ((warp == 0 || warp == 3 + EW) && lane == 0) {
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
   }
@@ -313,8 +316,12 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
   const uint32_t tmem = *tmem_slot;
   const int n_units = s_up[E];
 
-  if (warp == 0) {
-    // ---------------- TMA producer
+  if (warp == 0 || warp == 3 + EW) {
+    // ---------------- TMA producers: warp 0 issues the even stages, the
+    // other producer the odd ones (a thread's per-stage work -- the wait
+    // for the stage to come free, the barrier's expected bytes, the copies
+    // one after another -- is longer than the MMA thread's)
+    const int pw = warp == 0 ? 0 : 1;
     if (lane == 0) {
       int k = 0;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
@@ -324,6 +331,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         const int z = kF4 && a.rec_z ? a.rec_z[e] : e;  // record index in the bank / slot pool
         const uint8_t* rec = kF4 ? a.bank + a.lay.bytes * z : nullptr;
         for (int kt = 0; kt < nkt; ++kt, ++k) {
+          if ((k & 1) != pw) continue;
           const int s = k % kPfStages;
           if (k >= kPfStages && !mbar_wait(&empty[s], ((k / kPfStages) - 1) & 1, a.status)) {
             *abort_flag = 1;
@@ -357,9 +365,9 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
           }
         }
       }
-      // nothing may still be landing when the CTA exits
+      // nothing this warp issued may still be landing when the CTA exits
       for (int q = k - kPfStages > 0 ? k - kPfStages : 0; q < k; ++q)
-        mbar_wait(&full[q % kPfStages], (q / kPfStages) & 1, a.status);
+        if ((q & 1) == pw) mbar_wait(&full[q % kPfStages], (q / kPfStages) & 1, a.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -427,7 +435,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
       mbar_wait(sf_drain, 0, a.status);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp < 2 + EW) {
     // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ...;
     // the two warps of a lane quarter split the columns in halves
     const int q = warp & 3, hf = (warp - 2) >> 2;
