@@ -680,7 +680,9 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int parts) {
     size_t smem = (size_t)kSortWarps * a.E * 4;
     const int64_t P = (int64_t)a.T * a.top_k;
     const int n_chunks = (int)((P + kSortChunk - 1) / kSortChunk);
-    if (a.sort_cnt && n_chunks > 1 && n_chunks <= a.sort_max_chunks) {
+    // the many-CTA sort (three launches) pays off above four chunks; below,
+    // the one-CTA sort's single launch is faster
+    if (a.sort_cnt && n_chunks > 4 && n_chunks <= a.sort_max_chunks) {
       FTMOE_PROF_BEGIN("k_sort_count", s);
       k_sort_count<<<n_chunks, kSortThreads, smem, s>>>(a);
       FTMOE_PROF_END(s);
