@@ -43,9 +43,32 @@ def stack3():
     return wl, banks, layer
 
 
+@pytest.fixture(scope="module")
+def stack3_decode():
+    """Three layers of the decode workload's shape (H=2560, I=640, E=256,
+    k=8): the tensor-core decode kernels, with each layer's RMS renorm
+    launched programmatically ahead of the next layer's router."""
+    wl = W.WORKLOADS["decode"]
+    NL = 3
+    banks = [GpuBank(wl, layer=l) for l in range(NL)]
+    layer = make_layer(wl, max_tokens=32, num_layers=NL)
+    for l, b in enumerate(banks):
+        layer.load_bank(l, b.desc())
+    return wl, banks, layer
+
+
 @pytest.mark.parametrize("T", [1, 16, 40])
 def test_stack_layer_by_layer(stack3, T):
-    wl, banks, layer = stack3
+    _stack_layer_by_layer(stack3, T)
+
+
+@pytest.mark.parametrize("T", [1, 16, 32])
+def test_decode_shape_stack_layer_by_layer(stack3_decode, T):
+    _stack_layer_by_layer(stack3_decode, T)
+
+
+def _stack_layer_by_layer(stack, T):
+    wl, banks, layer = stack
     NL = len(banks)
     x = W.hidden(wl, T, step=11, device=DEV)
     out = torch.empty((T, wl.H), dtype=torch.bfloat16, device=DEV)
@@ -56,6 +79,12 @@ def test_stack_layer_by_layer(stack3, T):
         y = torch.empty((T, wl.H), dtype=torch.bfloat16 if last else torch.float32, device=DEV)
         layer.forward(l, xl, y, out_flags=ftmoe.OUT_BF16 if last else ftmoe.OUT_FP32)
         torch.cuda.synchronize()
+        topk = moe.select_topk(moe.router_logits(xl.float().cpu().numpy().astype(np.float64),
+                                                 banks[l].router_w.cpu().numpy().astype(np.float64),
+                                                 None if banks[l].router_bias is None
+                                                 else banks[l].router_bias.cpu().numpy().astype(np.float64)),
+                               wl.top_k)[0]
+        banks[l].prefetch_oracle_experts(np.unique(topk))
         ref = banks[l].oracle_layer(xl, out_dtype="bf16" if last else "fp32")
         check_output(y, ref.out if last else ref.out64)
         if not last:
@@ -74,7 +103,15 @@ def test_stack_layer_by_layer(stack3, T):
 
 def test_stack_graph_replay_matches_direct_call(stack3):
     """The stack captured in a CUDA graph and replayed gives the same bits."""
-    wl, banks, layer = stack3
+    _graph_replay(stack3)
+
+
+def test_decode_shape_stack_graph_replay_matches_direct_call(stack3_decode):
+    _graph_replay(stack3_decode)
+
+
+def _graph_replay(stack):
+    wl, banks, layer = stack
     x = W.hidden(wl, 16, step=12, device=DEV)
     direct = torch.empty((16, wl.H), dtype=torch.bfloat16, device=DEV)
     layer.forward_stack(x, direct)
