@@ -852,6 +852,42 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
 
 // ------------------------------------------------------------------ routed gate_up, 128 x 256 tiles
 
+// Scale columns stored from registers (tcgen05.st, this warp's 32 TMEM
+// lanes).  A block-scaled MMA reads A row m's scales from lane m, column
+// base + m/32, and B row n's from lane n % 32 of every lane quarter, column
+// base + n/32: a warp of quarter q stores, per K step, its A rows' word
+// (atom word q of row `lane`) into all 4 columns of the step, and the whole
+// 16-byte atom row `lane` of each B block.
+// 16 columns: column 4k + j = a[k].
+__device__ __forceinline__ void tc_st_sfa4(uint32_t taddr, const uint32_t (&a)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%2,%2,%2,%2,%3,%3,%3,%3,%4,%4,%4,%4};" ::"r"(taddr),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3])
+      : "memory");
+}
+
+// 8 columns: b0's four words, then b1's.
+__device__ __forceinline__ void tc_st_sfb2(uint32_t taddr, uint4 b0, uint4 b1) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(b0.x),
+               "r"(b0.y), "r"(b0.z), "r"(b0.w), "r"(b1.x), "r"(b1.y), "r"(b1.z), "r"(b1.w)
+               : "memory");
+}
+
+// Wait for this thread's TMEM stores.
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Per-warpgroup register budgets (all four warps of the warpgroup execute
+// it).  The increases draw on what the decreases released within the
+// block's launch-time registers, so the shares must add up to them.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // The routed gate_up with 256 weight rows per tile: two consecutive 64 + 64
 // (gate, up) window tiles against one 128-row pair tile, one MMA of N = 256
 // per K step.  An SM takes in its operands at a bounded rate (about 50-60
@@ -860,13 +896,27 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
 // of a 128 x 128 tile's 32 KB.  Four stages of 54 KB; one accumulator of 256
 // TMEM columns, drained into registers by 16 epilogue warps (two 16-wide
 // blocks each) before they compute, so the next tile's MMAs start early.
-// Roles otherwise as in k_pf_mma.
+//
+// Scale factors go into TMEM by tcgen05.st from four warps, one per lane
+// quarter, not by tcgen05.cp: a copy costs about 43 ns of the SM's tensor
+// pipe per instruction, and a stage needs twelve, in the same pipe as the
+// stage's MMAs.  The 24 warps are six warpgroups: 0 = producer, MMA and two
+// idle warps, 1 = the scale warps, 2-5 = the epilogue.  Launched at 80
+// registers a thread; warpgroups 0 and 1 give theirs down to 48 so the
+// epilogue's rise to 96 (what its drain of 64 accumulator values needs)
+// comes out of the same launch budget: 2 x 128 x 48 + 4 x 128 x 96 =
+// 768 x 80.
 namespace {
 constexpr int kGuStages = 4;
 constexpr int kGuTileB = 32768;    // 256 x 128-byte weight tile
 constexpr int kGuSfb = 4096;       // two tiles' four 512-byte scale blocks
 constexpr int kGuEpi = 16;
-constexpr int kGuThreads = 32 * (3 + kGuEpi);
+constexpr int kGuSfW0 = 4;         // first scale warp (warpgroup 1)
+constexpr int kGuEpiW0 = 8;        // first epilogue warp (warpgroups 2-5)
+constexpr int kGuThreads = 32 * (kGuEpiW0 + kGuEpi);
+constexpr int kGuLaunchRegs = 80, kGuLowRegs = 48, kGuEpiRegs = 96;
+static_assert(kGuThreads * kGuLaunchRegs == 2 * 128 * kGuLowRegs + kGuEpi * 32 * kGuEpiRegs,
+              "the warpgroups' register shares add up to the launch's registers");
 constexpr int kGuOffA = 0;
 constexpr int kGuOffB = kGuStages * kTile;
 constexpr int kGuOffSfa = kGuOffB + kGuStages * kGuTileB;
@@ -906,12 +956,12 @@ __global__ void __launch_bounds__(kGuThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kGuEpi);
     mbar_init(drain, 1);
-    for (int s = 0; s < kGuStages; ++s) mbar_init(&sf_ready[s], 1);
+    for (int s = 0; s < kGuStages; ++s) mbar_init(&sf_ready[s], 4);
     mbar_init(sf_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if ((warp == 0 || warp == 2) && lane == 0) {
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
   }
@@ -927,9 +977,12 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   __syncthreads();
   const uint32_t tmem = *tmem_slot;
   const int n_units = s_up[E];
-
-  if (warp == 0) {
-    // ---------------- TMA producer
+  if (warp < kGuEpiW0) {
+  setmaxnreg_dec<kGuLowRegs>();
+  if (warp == 0 || warp == 2) {
+    // ---------------- TMA producers: warp 0 issues the even stages, warp 2
+    // the odd ones
+    const int pw = warp == 0 ? 0 : 1;
     if (lane == 0) {
       int k = 0;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
@@ -940,6 +993,7 @@ __global__ void __launch_bounds__(kGuThreads, 1)
         const uint8_t* rec = a.bank + a.lay.bytes * z;
         const int t0 = row0 / 64 + 2 * jj;  // first of the unit's two 64 + 64-row window tiles
         for (int kt = 0; kt < nkt; ++kt, ++k) {
+          if ((k & 1) != pw) continue;
           const int s = k % kGuStages;
           if (k >= kGuStages && !mbar_wait(&empty[s], ((k / kGuStages) - 1) & 1, a.status)) {
             *abort_flag = 1;
@@ -962,9 +1016,9 @@ __global__ void __launch_bounds__(kGuThreads, 1)
           bulk_g2s(sfa, a.xg_sf + ((int64_t)(pp0 >> 7) * nks_all + 4 * kt) * 512, nks * 512, &full[s]);
         }
       }
-      // nothing may still be landing when the CTA exits
+      // nothing this warp issued may still be landing when the CTA exits
       for (int q = k - kGuStages > 0 ? k - kGuStages : 0; q < k; ++q)
-        mbar_wait(&full[q % kGuStages], (q / kGuStages) & 1, a.status);
+        if ((q & 1) == pw) mbar_wait(&full[q % kGuStages], (q / kGuStages) & 1, a.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: one accumulator, N = 256
@@ -998,38 +1052,50 @@ __global__ void __launch_bounds__(kGuThreads, 1)
       tc_commit(drain);
       mbar_wait(drain, 0, a.status);
     }
-  } else if (warp == 2 + kGuEpi) {
-    // ---------------- scale factors: per K step, the pair tile's block into
-    // 4 columns, the two weight tiles' blocks into the next 8 (rows 0-127,
-    // then 128-255)
-    if (lane == 0) {
-      int k = 0;
-      for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-        for (int kt = 0; kt < nkt; ++kt, ++k) {
-          const int s = k % kGuStages;
-          if (!mbar_wait(&full[s], (k / kGuStages) & 1, a.status)) { *abort_flag = 1; break; }
-          tc_fence_after();
-          const int nks = min(4, nks_all - 4 * kt);
-          const uint32_t sfa_col = tmem + kGuSfCol0 + s * 48, sfb_col = sfa_col + 16;
-          const uint32_t sfa_smem = smem_u32(sm + kGuOffSfa + s * kSfStage);
-          const uint32_t sfb_smem = smem_u32(sm + kGuOffSfb + s * kGuSfb);
-          for (int ks = 0; ks < nks; ++ks) {
-            tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
-            tc_cp_sf(sfb_col + 8 * ks, sdesc_sf(sfb_smem + 512 * ks));
-            tc_cp_sf(sfb_col + 8 * ks + 4, sdesc_sf(sfb_smem + kSfStage + 512 * ks));
-          }
-          tc_commit(&sf_ready[s]);
+  } else if (warp >= kGuSfW0 && warp < kGuSfW0 + 4) {
+    // ---------------- scale factors: warp q = warp % 4 stores, for each K
+    // step, its 32 pair rows' scale word into the step's 4 A columns and
+    // the 16-byte atom row `lane` of both weight-row blocks into its 8 B
+    // columns, once the stage has landed
+    const int q = warp & 3;
+    int k = 0;
+    for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+      bool ok = true;
+      for (int kt = 0; kt < nkt; ++kt, ++k) {
+        const int s = k % kGuStages;
+        bool landed = true;
+        if (lane == 0) landed = mbar_wait(&full[s], (k / kGuStages) & 1, a.status);
+        if (!__shfl_sync(0xffffffffu, landed, 0)) {
+          if (lane == 0) *abort_flag = 1;
+          ok = false;
+          break;
         }
+        // every lane's own acquire of the completed phase (returns at once)
+        mbar_wait(&full[s], (k / kGuStages) & 1, a.status);
+        const uint32_t* fa = reinterpret_cast<const uint32_t*>(sm + kGuOffSfa + s * kSfStage) + 4 * lane + q;
+        const uint4* fb = reinterpret_cast<const uint4*>(sm + kGuOffSfb + s * kGuSfb) + lane;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + kGuSfCol0 + s * 48;
+        uint32_t va[4];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) va[ks] = fa[128 * ks];
+        tc_st_sfa4(tq, va);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) tc_st_sfb2(tq + 16 + 8 * ks, fb[32 * ks], fb[kSfStage / 16 + 32 * ks]);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[s]);
       }
-      tc_commit(sf_drain);
-      mbar_wait(sf_drain, 0, a.status);
+      if (!ok) break;
     }
-    __syncwarp();
+  }
   } else {
+  setmaxnreg_inc<kGuEpiRegs>();
+  {
     // ---------------- epilogue: warp (q, part) holds TMEM lanes 32q.. (pair
     // rows) and two 16-wide blocks of window tile t0 + (part >> 1): gate
     // columns 16b.. and up columns 64 + 16b.. for b = 2 (part & 1) + {0, 1}
-    const int q = warp & 3, part = (warp - 2) >> 2;
+    const int q = warp & 3, part = (warp - kGuEpiW0) >> 2;
     const int hf = part >> 1, b0 = 2 * (part & 1);
     int ui = 0;
     for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
@@ -1085,6 +1151,7 @@ __global__ void __launch_bounds__(kGuThreads, 1)
       *reinterpret_cast<uint16_t*>(a.hq_sf + ((int64_t)(pp0 >> 7) * (I_loc / 64) + tw) * 512 + lane * 16 + q * 4 +
                                    b0) = valid ? (uint16_t)sfw : (uint16_t)0;
     }
+  }
   }
   tc_fence_before();
   __syncthreads();
@@ -1443,6 +1510,22 @@ cudaError_t launch_repack_sf(uint8_t* bank, const RecLayout& lay, int H, int Iw,
   return cudaGetLastError();
 }
 
+// The 128 x 256 gate_up kernel divides its launch registers between
+// warpgroups; it runs only when compiled at exactly the registers a thread
+// that the division adds up to (a larger increase than the launch holds
+// would wait forever), else the 128 x 128 kernel takes the routed gate_up.
+static bool gu256_launchable() {
+  static int state = 0;  // 0 unknown, 1 yes, 2 no
+  if (state == 0) {
+    cudaFuncAttributes attr;
+    const bool ok = cudaFuncGetAttributes(&attr, k_pf_gu256) == cudaSuccess && attr.numRegs == kGuLaunchRegs &&
+                    attr.maxThreadsPerBlock >= kGuThreads;
+    if (!ok) (void)cudaGetLastError();
+    state = ok ? 1 : 2;
+  }
+  return state == 1;
+}
+
 cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
   cudaError_t err;
   {
@@ -1455,7 +1538,7 @@ cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms,
   }
   const int smem = pf_smem_bytes(a.E);
   FTMOE_PROF_BEGIN("k_pf_gate_up", s);
-  if (a.win.I_loc % 128 == 0 && gu256_smem_bytes(a.E) <= 227 * 1024)
+  if (a.win.I_loc % 128 == 0 && gu256_smem_bytes(a.E) <= 227 * 1024 && gu256_launchable())
     k_pf_gu256<<<num_sms, kGuThreads, gu256_smem_bytes(a.E), s>>>(a, m.xg, m.gu);
   else
     k_pf_mma<0><<<num_sms, pf_threads(0), smem, s>>>(a, m.xg, m.gu);
