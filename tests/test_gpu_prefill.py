@@ -164,6 +164,28 @@ def test_prefill_halves_sum_to_full(prefill):
         check_output(half, ref.out64)
 
 
+def test_prefill_offset_windows_on_the_256_row_kernel(prefill):
+    """Windows [0, 256) and [256, 640) of the full bank: both widths are
+    multiples of 128, so the routed gate_up runs on 128 x 256 weight tiles,
+    the second starting 256 rows into each expert's gate and up blocks.
+    Each window matches the oracle's partial on every token, and the two
+    add up to the full layer."""
+    wl, bank, layer = prefill
+    T = 1024
+    x = W.hidden(wl, T, step=4, device=DEV)
+    full, _ = _run(wl, layer, x, out_dtype=torch.float32)
+    acc = torch.zeros_like(full)
+    for i0, il in ((0, 256), (256, 384)):
+        part = torch.empty_like(full)
+        layer.forward(0, x, part, out_flags=ftmoe.OUT_FP32, i0=i0, I_loc=il)
+        torch.cuda.synchronize()
+        assert layer.check_status() == 0
+        ref = bank.oracle_layer(x, i0=i0, I_loc=il, out_dtype="fp32")
+        check_output(part, ref.out64)
+        acc += part
+    assert rel_l2(acc.cpu().numpy(), full.cpu().numpy()) <= 1e-6
+
+
 # ------------------------------------------------------------------ tensor-core router
 
 
