@@ -890,18 +890,20 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 
 // The routed gate_up with 256 weight rows per tile: two consecutive 64 + 64
 // (gate, up) window tiles against one 128-row pair tile, one MMA of N = 256
-// per K step.  An SM takes in its operands at a bounded rate (about 50-60
-// GB/s whatever the copy kind, multicast included), so operand bytes per
-// product set the pace: a stage brings 48 KB of codes for twice the products
-// of a 128 x 128 tile's 32 KB.  Four stages of 54 KB; one accumulator of 256
+// per K step.  The operand ring's turn-around (TMA latency, the scale and
+// MMA hops: about 2.1 us for four stages, about 100 GB/s per SM) bounds an
+// SM's intake, so operand bytes per product set the pace: a stage brings
+// 48 KB of codes for twice the products of a 128 x 128 tile's 32 KB.  Four
+// stages of 54 KB; one accumulator of 256
 // TMEM columns, drained into registers by 16 epilogue warps (two 16-wide
 // blocks each) before they compute, so the next tile's MMAs start early.
 //
 // Scale factors go into TMEM by tcgen05.st from four warps, one per lane
 // quarter, not by tcgen05.cp: a copy costs about 43 ns of the SM's tensor
 // pipe per instruction, and a stage needs twelve, in the same pipe as the
-// stage's MMAs.  The 24 warps are six warpgroups: 0 = producer, MMA and two
-// idle warps, 1 = the scale warps, 2-5 = the epilogue.  Launched at 80
+// stage's MMAs.  The 24 warps are six warpgroups: 0 = the TMA producers
+// (warps 0 and 2, alternate stages), the MMA thread (warp 1) and an idle
+// warp, 1 = the scale warps, 2-5 = the epilogue.  Launched at 80
 // registers a thread; warpgroups 0 and 1 give theirs down to 48 so the
 // epilogue's rise to 96 (what its drain of 64 accumulator values needs)
 // comes out of the same launch budget: 2 x 128 x 48 + 4 x 128 x 96 =
@@ -938,8 +940,7 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint64_t* sf_ready = drain + 1;  // [kGuStages]
-  uint64_t* sf_drain = sf_ready + kGuStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_ready + kGuStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int E = a.E, H = a.H;
   int* s_off = reinterpret_cast<int*>(sm + kGuOffTab);
@@ -957,7 +958,6 @@ __global__ void __launch_bounds__(kGuThreads, 1)
     mbar_init(acc_empty, kGuEpi);
     mbar_init(drain, 1);
     for (int s = 0; s < kGuStages; ++s) mbar_init(&sf_ready[s], 4);
-    mbar_init(sf_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
