@@ -109,7 +109,7 @@ def kernel_unit_flops(kernel: str, H: int, I_loc: int, sI_loc: int, E: int = 0):
         return 2 * I_loc * H, "pair", "nvfp4 tensor"
     if kernel == "k_pf_shared_gate_up":
         return 2 * H * 2 * sI_loc, "token", "bf16 tensor"
-    if kernel == "k_pf_shared_down_combine":
+    if kernel == "k_pf_shared_down":
         return 2 * sI_loc * H, "token", "bf16 tensor"
     if kernel == "k_pf_router":
         # x times the three exact bf16 parts of every fp32 router row

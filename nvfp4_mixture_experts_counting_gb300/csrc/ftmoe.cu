@@ -676,6 +676,7 @@ static PfArgs prefill_args(ftmoe_handle* h, Layer& L, const ExpertArgs& a, const
     p.sigma = r.sigma;
     p.out = out;
     p.out_flags = out_flags;
+    p.S = h->S;  // the any-T path's buffer, unused by the prefill path otherwise
   }
   if (tc_router) {
     p.wcat = L.router_wcat;

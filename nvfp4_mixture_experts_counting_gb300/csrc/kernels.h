@@ -219,6 +219,7 @@ struct PfArgs {
   const float* sigma;         // [T]
   void* out;
   int out_flags;
+  float* S;                   // [T][H] fp32 shared-expert output, when the combine runs as its own kernel
   // router logits on the tensor cores: W = W1 + W2 + W3 exactly (bf16 parts)
   const uint16_t* wcat;       // [E][3H] bf16: W1 | W2 | W3
   const float* wnorm;         // [E] upper bound of ||w_e||_2

@@ -111,6 +111,14 @@ __host__ __device__ constexpr int sf_slot(int r) { return (r & 31) * 16 + ((r & 
 // quantisation that follows keeps the quantiser's own order.
 __device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
+// 32 bytes to a 32-byte-aligned global address, one 256-bit store (a whole
+// sector per lane when the lanes write different rows).
+__device__ __forceinline__ void stg_32B(void* p, const uint32_t (&r)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+               "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // NVFP4 quantisation of 16 activation values with global 1.0, in the
 // quantiser's own order: scale = E4M3(fp32(amax / 6)), then each code =
 // E2M1(fp32(v / dec(scale))) with IEEE divisions, so the codes are those the
@@ -240,16 +248,13 @@ __global__ void __launch_bounds__(256) k_pf_prep(PfArgs a) {
 // ------------------------------------------------------------------ grouped GEMM
 
 // One kernel body, four problems (all D = A * B^T, A = 128 token or pair
-// rows, B = 128 weight rows, K-major operands in 128-byte swizzled tiles):
+// rows, B = 128 weight rows, K-major operands in 128-byte swizzled tiles);
+// each is also, or only, served by a 128 x 256 kernel where the shapes allow:
 //   MODE 0  routed gate_up, NVFP4, grouped by expert; epilogue: row globals,
 //           SwiGLU, NVFP4 quantisation of the intermediate (padded order)
 //   MODE 1  routed down, NVFP4, grouped; epilogue: down row global -> Y
 //   MODE 2  shared gate_up, bf16, one group of T tokens; epilogue: SwiGLU,
 //           rounded to bf16 -> hs
-//   MODE 3  shared down, bf16; epilogue: the combine
-//           out_t = sum_j w_tj * Y[inv(t, j)] + sigma_t * S_t in slot order
-//           (PR #385 "feat(qwen4_exp): tensor parallelism for
-//           Qwen3.8-Flash-Next (offload backend)", "What this adds")
 //   MODE 4  router logits, bf16: x . (W1 + W2 + W3) with K = 3H (the three
 //           exact bf16 parts of the fp32 router rows, x repeated along K);
 //           epilogue: bias and the error bound the top-k certificate uses
@@ -278,7 +283,8 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
   int* s_up = s_pad + (E + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int I_loc = a.win.I_loc, row0 = a.win.row0, Iw = a.win.Iw;
-  const int kbytes = MODE == 0 ? H / 2 : MODE == 1 ? I_loc / 2 : MODE == 2 ? 2 * H : MODE == 3 ? 2 * a.s_I_loc : 6 * H;
+  static_assert(MODE != 3, "the shared down runs on k_pf_bf16w<3>, the combine on k_pf_combine");
+  const int kbytes = MODE == 0 ? H / 2 : MODE == 1 ? I_loc / 2 : MODE == 2 ? 2 * H : 6 * H;
   const int nks_all = kbytes / 32;
   const int nkt = (nks_all + 3) / 4;
   const int J = MODE == 0 ? I_loc / 64 : MODE == 2 ? a.s_I_loc / 64 : MODE == 4 ? a.E / 128 : H / 128;  // weight tiles per row tile
@@ -358,8 +364,6 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
           } else if (MODE == 2) {
             tma_load_2d(sb, &mapB, kt * 128, a.s_row0 + 64 * j, &full[s]);
             tma_load_2d(sb + kTile / 2, &mapB, kt * 128, a.s_Iw + a.s_row0 + 64 * j, &full[s]);
-          } else if (MODE == 3) {
-            tma_load_2d(sb, &mapB, 2 * a.s_row0 + kt * 128, 128 * j, &full[s]);
           } else {
             tma_load_2d(sb, &mapB, kt * 128, 128 * j, &full[s]);
           }
@@ -450,22 +454,14 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
       const bool valid = local < s_off[e + 1] - s_off[e];
       // the unit's loads that do not need the accumulator are issued before
       // its wait, so their latency overlaps the unit's MMAs: the down
-      // rows' globals and the lane's pair index (mode 1), the token's
-      // routing weights and sigma (mode 3)
+      // rows' globals and the lane's pair index (mode 1)
       float4 pre_g = make_float4(0.f, 0.f, 0.f, 0.f);
       int pre_pr = 0;
-      float pre_w[8], pre_sig = 0.f;
       if (MODE == 1) {
         const uint8_t* rec = a.bank + a.lay.bytes * (a.rec_z ? a.rec_z[e] : e);
         pre_g = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(rec + a.lay.dn_global) + 128 * j) +
                       lane);
         if (valid) pre_pr = __ldg(a.perm + s_off[e] + local);
-      }
-      if (MODE == 3) {
-        const float* w = a.topk_w + (int64_t)local * a.top_k;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) pre_w[jj] = (valid && jj < a.top_k) ? __ldg(w + jj) : 0.f;
-        pre_sig = valid ? a.sigma[local] : 0.f;
       }
       if (!mbar_wait(&acc_full[buf], (ui >> 1) & 1, a.status)) { *abort_flag = 1; break; }
       tc_fence_after();
@@ -692,147 +688,6 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
               er.w = a.kappa * xn * wn.w + 2.4e-7f * fabsf(l.w) + 1e-30f;
               *reinterpret_cast<float4*>(lrow + i) = l;
               *reinterpret_cast<float4*>(erow + i) = er;
-            }
-          }
-        }
-      } else {
-        // combine for token t over output rows [128 j, 128 j + 128): the
-        // slots' rows of Y in slot order, then sigma * the shared expert.
-        // Up to 8 slots keep their weights in registers and have their Y
-        // loads in flight together (fp32: four slots at a time).
-        const int t = local;
-        const int k = a.top_k;
-        const float* w = a.topk_w + (int64_t)t * k;
-        const float sig = pre_sig;
-        const int64_t obase = (int64_t)t * H + 128 * j;
-        // the token's k slot segments of column tile j, contiguous (bf16 or fp32)
-        const int64_t yoff = ((int64_t)t * (H / 128) + j) * k * 128;
-        const uint16_t* ytb = reinterpret_cast<const uint16_t*>(a.Y) + yoff;
-        const float* ytf = reinterpret_cast<const float*>(a.Y) + yoff;
-        float wj[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) wj[jj] = pre_w[jj];
-#pragma unroll 1
-        for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
-          uint32_t v[16];
-          tc_ld16(taddr + 16 * c, v);
-          tc_wait16(v);
-          if (valid) {
-            float o[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = 0.f;
-            if (a.y_bf16) {
-              // each slot's 16 bf16 values of this chunk are one 32-byte
-              // load (the warp's lanes read 32 different rows, so a load's
-              // cost is its rows, not its bytes); up to 8 slots have theirs
-              // in flight together
-              if (k <= 8) {
-                uint32_t y[8][8];
-#pragma unroll
-                for (int q2 = 0; q2 < 8; ++q2) {
-                  if (q2 < k) {
-                    ldg_nc_32B(ytb + q2 * 128 + 16 * c, y[q2]);
-                  } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) y[q2][i] = 0u;
-                  }
-                }
-#pragma unroll
-                for (int q2 = 0; q2 < 8; ++q2) {
-                  // a slot of weight zero (left out of an expert subset)
-                  // adds nothing, whatever its stale Y holds
-                  if (q2 < k && wj[q2] != 0.f) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                      o[2 * i] = fmaf(wj[q2], __uint_as_float(y[q2][i] << 16), o[2 * i]);
-                      o[2 * i + 1] = fmaf(wj[q2], __uint_as_float(y[q2][i] & 0xffff0000u), o[2 * i + 1]);
-                    }
-                  }
-                }
-              } else {
-                for (int jj = 0; jj < k; ++jj) {
-                  const float wv = __ldg(w + jj);
-                  if (wv == 0.f) continue;
-                  const uint4* yp = reinterpret_cast<const uint4*>(ytb + jj * 128 + 16 * c);
-                  const uint4 y0 = yp[0], y1 = yp[1];
-                  const uint32_t u[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    o[2 * i] = fmaf(wv, __uint_as_float(u[i] << 16), o[2 * i]);
-                    o[2 * i + 1] = fmaf(wv, __uint_as_float(u[i] & 0xffff0000u), o[2 * i + 1]);
-                  }
-                }
-              }
-            } else {
-              if (k <= 8) {
-#pragma unroll
-                for (int j0 = 0; j0 < 8; j0 += 4) {
-                  if (j0 < k) {
-                    // a slot's 16 fp32 values are two 32-byte loads
-                    uint32_t y[4][16];
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                      if (j0 + q2 < k) {
-                        ldg_nc_32B(ytf + (j0 + q2) * 128 + 16 * c, y[q2]);
-                        ldg_nc_32B(ytf + (j0 + q2) * 128 + 16 * c + 8, y[q2] + 8);
-                      } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) y[q2][i] = 0u;
-                      }
-                    }
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                      if (j0 + q2 < k && wj[j0 + q2] != 0.f) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = fmaf(wj[j0 + q2], __uint_as_float(y[q2][i]), o[i]);
-                      }
-                    }
-                  }
-                }
-              } else {
-                for (int jj = 0; jj < k; ++jj) {
-                  const float wv = __ldg(w + jj);
-                  if (wv == 0.f) continue;
-                  const float4* yp = reinterpret_cast<const float4*>(ytf + jj * 128 + 16 * c);
-#pragma unroll
-                  for (int i4 = 0; i4 < 4; ++i4) {
-                    const float4 y = yp[i4];
-                    o[4 * i4] = fmaf(wv, y.x, o[4 * i4]);
-                    o[4 * i4 + 1] = fmaf(wv, y.y, o[4 * i4 + 1]);
-                    o[4 * i4 + 2] = fmaf(wv, y.z, o[4 * i4 + 2]);
-                    o[4 * i4 + 3] = fmaf(wv, y.w, o[4 * i4 + 3]);
-                  }
-                }
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = fmaf(sig, __uint_as_float(v[i]), o[i]);
-            const int64_t oi = obase + 16 * c;
-            if ((a.out_flags & 0xff) == 0) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const __nv_bfloat162 hb = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-                pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
-              }
-              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + oi);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            } else {
-              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi);
-              const bool accum = (a.out_flags & 0x100) != 0;
-#pragma unroll
-              for (int i4 = 0; i4 < 4; ++i4) {
-                float4 val = make_float4(o[4 * i4], o[4 * i4 + 1], o[4 * i4 + 2], o[4 * i4 + 3]);
-                if (accum) {
-                  const float4 prev = dst[i4];
-                  val.x += prev.x;
-                  val.y += prev.y;
-                  val.z += prev.z;
-                  val.w += prev.w;
-                }
-                dst[i4] = val;
-              }
             }
           }
         }
@@ -1198,7 +1053,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kBwThreads, 1)
     k_pf_bf16w(const __grid_constant__ PfArgs a, const __grid_constant__ CUtensorMap mapA,
                const __grid_constant__ CUtensorMap mapB) {
-  static_assert(MODE == 2 || MODE == 4, "bf16 modes only");
+  static_assert(MODE == 2 || MODE == 3 || MODE == 4, "bf16 modes only");
   extern __shared__ unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kBwOffBar);
@@ -1210,9 +1065,9 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
-  const int nks_all = MODE == 2 ? 2 * H / 32 : 6 * H / 32;  // 32-byte K steps (16 bf16)
+  const int nks_all = MODE == 2 ? 2 * H / 32 : MODE == 3 ? 2 * a.s_I_loc / 32 : 6 * H / 32;  // 32-byte K steps
   const int nkt = (nks_all + 3) / 4;
-  const int J = MODE == 2 ? a.s_I_loc / 128 : a.E / 256;  // weight tiles per row tile
+  const int J = MODE == 2 ? a.s_I_loc / 128 : MODE == 3 ? H / 256 : a.E / 256;  // weight tiles per row tile
   // router with few tokens: each (row tile, weight tile) split into KS
   // contiguous K ranges, one unit each
   const int KS = MODE == 4 && a.r_ksplit > 1 ? a.r_ksplit : 1;
@@ -1259,6 +1114,10 @@ __global__ void __launch_bounds__(kBwThreads, 1)
               tma_load_2d(sb + h * kTile + kTile / 2, &mapB, kt * 128, a.s_Iw + a.s_row0 + 128 * j + 64 * h,
                           &full[s]);
             }
+          } else if (MODE == 3) {
+            // output rows [256 j, 256 j + 256) of the shared down, the window's columns
+            tma_load_2d(sb, &mapB, 2 * a.s_row0 + kt * 128, 256 * j, &full[s]);
+            tma_load_2d(sb + kTile, &mapB, 2 * a.s_row0 + kt * 128, 256 * j + 128, &full[s]);
           } else {
             tma_load_2d(sb, &mapB, kt * 128, 256 * j, &full[s]);
             tma_load_2d(sb + kTile, &mapB, kt * 128, 256 * j + 128, &full[s]);
@@ -1338,6 +1197,37 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
+      } else if (MODE == 3) {
+        // the shared expert's output for columns [256 j + 128 hf, +128), in
+        // Y's precision (bf16 when the forward's output is bf16), each lane's
+        // 16 values of a chunk in whole 32-byte stores
+        const int64_t so = (int64_t)t * H + 256 * j + 128 * hf;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tc_ld16(taddr + 16 * c, v);
+          tc_wait16(v);
+          if (valid) {
+            if (a.y_bf16) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const __nv_bfloat162 hb = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
+              }
+              stg_32B(reinterpret_cast<uint16_t*>(a.S) + so + 16 * c, pk);
+            } else {
+              uint32_t lo[8], hi[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                lo[i] = v[i];
+                hi[i] = v[8 + i];
+              }
+              stg_32B(a.S + so + 16 * c, lo);
+              stg_32B(a.S + so + 16 * c + 8, hi);
+            }
+          }
+        }
       } else if (KS > 1) {
         // this K range's partial sums for experts [256 j + 128 hf, +128)
         float* prow = a.rpart + ((int64_t)ks * a.T + t) * a.E + 256 * j + 128 * hf;
@@ -1396,6 +1286,133 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// The combine, after the shared down wrote S (in Y's precision):
+//   out_t = sum_j w_tj * Y[t, slot j] + sigma_t * S_t
+// the slots in order (a slot of weight zero adds nothing, whatever its stale
+// Y holds), then the shared term, in fp32 (the pages' combine: PR #385
+// "feat(qwen4_exp): tensor parallelism for Qwen3.8-Flash-Next (offload
+// backend)", "What this adds").  A thread takes 8 consecutive columns of a
+// token: each slot's piece is one 16-byte load (bf16 Y), and a warp's loads
+// cover whole runs of the token's slot segments, so the reads stream
+// instead of gathering 32 rows per load.
+__global__ void __launch_bounds__(256) k_pf_combine(PfArgs a) {
+  const int H = a.H, k = a.top_k;
+  const int64_t n8 = (int64_t)a.T * (H / 8);
+  for (int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i8 < n8;
+       i8 += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = i8 * 8;
+    const int t = (int)(i / H), h = (int)(i % H);
+    // slot 0's 8 values; slot j's are 128 further
+    const int64_t y0 = ((int64_t)t * (H / 128) + h / 128) * k * 128 + (h & 127);
+    const float* w = a.topk_w + (int64_t)t * k;
+    float o[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) o[c] = 0.f;
+    if (k <= 8) {
+      float wj[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) wj[q] = q < k ? __ldg(w + q) : 0.f;
+      if (a.y_bf16) {
+        const uint16_t* Yb = reinterpret_cast<const uint16_t*>(a.Y);
+        uint4 y[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          y[q] = q < k ? __ldg(reinterpret_cast<const uint4*>(Yb + y0 + q * 128)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q < k && wj[q] != 0.f) {
+            const uint32_t u[4] = {y[q].x, y[q].y, y[q].z, y[q].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              o[2 * c] = fmaf(wj[q], __uint_as_float(u[c] << 16), o[2 * c]);
+              o[2 * c + 1] = fmaf(wj[q], __uint_as_float(u[c] & 0xffff0000u), o[2 * c + 1]);
+            }
+          }
+        }
+      } else {
+        const float* Yf = reinterpret_cast<const float*>(a.Y);
+#pragma unroll
+        for (int q0 = 0; q0 < 8; q0 += 4) {
+          float4 y[4][2];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (q0 + q < k) {
+              y[q][0] = __ldg(reinterpret_cast<const float4*>(Yf + y0 + (q0 + q) * 128));
+              y[q][1] = __ldg(reinterpret_cast<const float4*>(Yf + y0 + (q0 + q) * 128 + 4));
+            } else {
+              y[q][0] = y[q][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (q0 + q < k && wj[q0 + q] != 0.f) {
+              const float v8[8] = {y[q][0].x, y[q][0].y, y[q][0].z, y[q][0].w,
+                                   y[q][1].x, y[q][1].y, y[q][1].z, y[q][1].w};
+#pragma unroll
+              for (int c = 0; c < 8; ++c) o[c] = fmaf(wj[q0 + q], v8[c], o[c]);
+            }
+          }
+        }
+      }
+    } else {
+      for (int q = 0; q < k; ++q) {
+        const float wv = __ldg(w + q);
+        if (wv == 0.f) continue;
+        if (a.y_bf16) {
+          const uint4 yv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.Y) + y0 + q * 128));
+          const uint32_t u[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            o[2 * c] = fmaf(wv, __uint_as_float(u[c] << 16), o[2 * c]);
+            o[2 * c + 1] = fmaf(wv, __uint_as_float(u[c] & 0xffff0000u), o[2 * c + 1]);
+          }
+        } else {
+          const float* yp = reinterpret_cast<const float*>(a.Y) + y0 + q * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) o[c] = fmaf(wv, __ldg(yp + c), o[c]);
+        }
+      }
+    }
+    const float sg = __ldg(a.sigma + t);
+    float sv[8];
+    if (a.y_bf16) {
+      const uint4 sb = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.S) + i));
+      const uint32_t u[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        sv[2 * c] = __uint_as_float(u[c] << 16);
+        sv[2 * c + 1] = __uint_as_float(u[c] & 0xffff0000u);
+      }
+    } else {
+      const float4 s0 = __ldg(reinterpret_cast<const float4*>(a.S + i));
+      const float4 s1 = __ldg(reinterpret_cast<const float4*>(a.S + i) + 1);
+      sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
+      sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) o[c] = fmaf(sg, sv[c], o[c]);
+    if ((a.out_flags & 0xff) == 0) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(o[2 * c], o[2 * c + 1]);
+        pk[c] = *reinterpret_cast<const uint32_t*>(&hb);
+      }
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + i);
+      float4 v0 = make_float4(o[0], o[1], o[2], o[3]), v1 = make_float4(o[4], o[5], o[6], o[7]);
+      if (a.out_flags & 0x100) {
+        const float4 p0 = dst[0], p1 = dst[1];
+        v0.x += p0.x; v0.y += p0.y; v0.z += p0.z; v0.w += p0.w;
+        v1.x += p1.x; v1.y += p1.y; v1.z += p1.z; v1.w += p1.w;
+      }
+      dst[0] = v0;
+      dst[1] = v1;
+    }
   }
 }
 
@@ -1499,7 +1516,7 @@ cudaError_t prefill_set_smem_limits() {
     return e;
   if ((e = cudaFuncSetAttribute(k_pf_bf16w<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwSmem)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_pf_mma<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_pf_bf16w<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwSmem)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(k_pf_mma<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
@@ -1676,9 +1693,20 @@ cudaError_t launch_prefill_shared_gate_up(const PfArgs& a, const PfMaps& m, int 
   return cudaGetLastError();
 }
 
+// The shared down on 128 x 256 tiles into S (H is a multiple of 256 on the
+// prefill path), then the combine streaming Y, S and the output.
 cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
-  FTMOE_PROF_BEGIN("k_pf_shared_down_combine", s);
-  k_pf_mma<3><<<num_sms, kPfThreads, pf_smem_bytes(1), s>>>(a, m.hs, m.sdn);
+  if (!a.S || a.H % 256) return cudaErrorInvalidValue;
+  FTMOE_PROF_BEGIN("k_pf_shared_down", s);
+  k_pf_bf16w<3><<<num_sms, kBwThreads, kBwSmem, s>>>(a, m.hs, m.sdn);
+  FTMOE_PROF_END(s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t n8 = (int64_t)a.T * (a.H / 8);
+  int64_t blocks = (n8 + 255) / 256;
+  if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+  FTMOE_PROF_BEGIN("k_pf_combine", s);
+  k_pf_combine<<<(int)blocks, 256, 0, s>>>(a);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
