@@ -206,7 +206,6 @@ struct PfArgs {
   int hq_pitch;
   void* Y;                    // [T][H/128][k][128]: pair (t, slot)'s output, per column tile
   int y_bf16;                 // Y in bf16 (the forward's output is bf16), else fp32
-  int stage_y;                // down: Y goes out through shared memory (set by the launcher)
   uint32_t* status;
   // shared expert on the tensor cores, fused with the combine
   const uint16_t* x;          // [T][H] bf16

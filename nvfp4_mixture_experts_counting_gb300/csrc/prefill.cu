@@ -47,27 +47,24 @@ __host__ __device__ constexpr int pf_epi_warps(int mode) { return mode == 0 ? 16
 __host__ __device__ constexpr int pf_threads(int mode) { return 32 * (4 + pf_epi_warps(mode)); }
 constexpr int kTile = 16384;        // one 128 x 128-byte operand tile
 constexpr int kSfStage = 2048;      // four 512-byte scale blocks
-constexpr int kPfOffA = 0;
-constexpr int kPfOffB = kPfStages * kTile;
-constexpr int kPfOffSfa = 2 * kPfStages * kTile;
-constexpr int kPfOffSfb = kPfOffSfa + kPfStages * kSfStage;
-constexpr int kPfOffBar = kPfOffSfb + kPfStages * kSfStage;
-constexpr int kPfOffGlob = kPfOffBar + 256;  // per epilogue warp: 128 row globals
-constexpr int kPfOffTab = kPfOffGlob + kPfEpiWarps * 512;
+// shared-memory layout of the 128 x 128 kernels (NS stages)
+template <int NS>
+struct PfLay {
+  static constexpr int A = 0;
+  static constexpr int B = NS * kTile;
+  static constexpr int Sfa = 2 * NS * kTile;
+  static constexpr int Sfb = Sfa + NS * kSfStage;
+  static constexpr int Bar = Sfb + NS * kSfStage;
+  static constexpr int Glob = Bar + 256;  // per epilogue warp: 128 row globals
+  static constexpr int Tab = Glob + kPfEpiWarps * 512;
+};
+constexpr int kPfOffTab = PfLay<kPfStages>::Tab;
 constexpr int kPfMaxE = 1024;
 constexpr int kPfMaxK = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;   // scale-factor columns start after the two accumulators
 
 __host__ __device__ inline int pf_smem_bytes(int E) { return 1024 + kPfOffTab + 3 * 4 * (E + 1); }
-// Down mode: each epilogue warp turns its rows of Y through shared memory
-// (rows 144 bytes apart: 64 bf16 columns, or 32 fp32 columns at a time), so
-// that every store instruction writes four whole 128-byte row segments.  It
-// sits after the tables.
-constexpr int kPfStgRow = 144;
-constexpr int kPfStgBytes = kPfEpiWarps * 32 * kPfStgRow;
-__host__ __device__ inline int pf_stg_off(int E) { return (kPfOffTab + 3 * 4 * (E + 1) + 15) & ~15; }
-__host__ __device__ inline int pf_smem_bytes_staged(int E) { return 1024 + pf_stg_off(E) + kPfStgBytes; }
 
 // Exclusive scan over n values val(i) by one warp: out[i] = sum_{j<i} val(j),
 // out[n] = the total.
@@ -264,21 +261,23 @@ template <int MODE>
 __global__ void __launch_bounds__(pf_threads(MODE), 1)
     k_pf_mma(const __grid_constant__ PfArgs a, const __grid_constant__ CUtensorMap mapA,
              const __grid_constant__ CUtensorMap mapB) {
+  constexpr int NS = kPfStages;
+  using L = PfLay<NS>;
   constexpr bool kF4 = MODE < 2;
   constexpr int EW = pf_epi_warps(MODE), NT = pf_threads(MODE);
   extern __shared__ unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPfOffBar);
-  uint64_t* empty = full + kPfStages;
-  uint64_t* acc_full = empty + kPfStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::Bar);
+  uint64_t* empty = full + NS;
+  uint64_t* acc_full = empty + NS;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint64_t* sf_ready = drain + 1;  // [kPfStages] stage landed and its scale blocks are in TMEM
-  uint64_t* sf_drain = sf_ready + kPfStages;
+  uint64_t* sf_ready = drain + 1;  // [NS] stage landed and its scale blocks are in TMEM
+  uint64_t* sf_drain = sf_ready + NS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int E = kF4 ? a.E : 1, H = a.H;
-  int* s_off = reinterpret_cast<int*>(sm + kPfOffTab);
+  int* s_off = reinterpret_cast<int*>(sm + L::Tab);
   int* s_pad = s_off + (E + 1);
   int* s_up = s_pad + (E + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -290,10 +289,10 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
   const int J = MODE == 0 ? I_loc / 64 : MODE == 2 ? a.s_I_loc / 64 : MODE == 4 ? a.E / 128 : H / 128;  // weight tiles per row tile
 
   if (tid == 0) {
-    for (int s = 0; s < kPfStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], EW); }
     mbar_init(drain, 1);
-    for (int s = 0; s < kPfStages; ++s) mbar_init(&sf_ready[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&sf_ready[s], 1);
     mbar_init(sf_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -338,16 +337,16 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         const uint8_t* rec = kF4 ? a.bank + a.lay.bytes * z : nullptr;
         for (int kt = 0; kt < nkt; ++kt, ++k) {
           if ((k & 1) != pw) continue;
-          const int s = k % kPfStages;
-          if (k >= kPfStages && !mbar_wait(&empty[s], ((k / kPfStages) - 1) & 1, a.status)) {
+          const int s = k % NS;
+          if (k >= NS && !mbar_wait(&empty[s], ((k / NS) - 1) & 1, a.status)) {
             *abort_flag = 1;
             break;
           }
           const int nks = min(4, nks_all - 4 * kt);
-          unsigned char* sa = sm + kPfOffA + s * kTile;
-          unsigned char* sb = sm + kPfOffB + s * kTile;
-          unsigned char* sfa = sm + kPfOffSfa + s * kSfStage;
-          unsigned char* sfb = sm + kPfOffSfb + s * kSfStage;
+          unsigned char* sa = sm + L::A + s * kTile;
+          unsigned char* sb = sm + L::B + s * kTile;
+          unsigned char* sfa = sm + L::Sfa + s * kSfStage;
+          unsigned char* sfb = sm + L::Sfb + s * kSfStage;
           mbar_arrive_expect_tx(&full[s], 2 * kTile + (kF4 ? 2 * nks * 512 : 0));
           tma_load_2d(sa, &mapA, MODE == 4 ? (kt * 128) % (2 * H) : kt * 128, pp0, &full[s]);
           if (MODE == 0) {
@@ -370,8 +369,8 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         }
       }
       // nothing this warp issued may still be landing when the CTA exits
-      for (int q = k - kPfStages > 0 ? k - kPfStages : 0; q < k; ++q)
-        if ((q & 1) == pw) mbar_wait(&full[q % kPfStages], (q / kPfStages) & 1, a.status);
+      for (int q = k - NS > 0 ? k - NS : 0; q < k; ++q)
+        if ((q & 1) == pw) mbar_wait(&full[q % NS], (q / NS) & 1, a.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -385,18 +384,18 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         const uint32_t d = tmem + buf * 128;
         bool ok = true;
         for (int kt = 0; kt < nkt; ++kt, ++k) {
-          const int s = k % kPfStages;
+          const int s = k % NS;
           // NVFP4: the scale-factor warp completes sf_ready[s] once the stage
           // has landed and its scale blocks are in TMEM
-          if (!mbar_wait(kF4 ? &sf_ready[s] : &full[s], (k / kPfStages) & 1, a.status)) {
+          if (!mbar_wait(kF4 ? &sf_ready[s] : &full[s], (k / NS) & 1, a.status)) {
             *abort_flag = 1;
             ok = false;
             break;
           }
           tc_fence_after();
           const int nks = min(4, nks_all - 4 * kt);
-          const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + kPfOffA + s * kTile));
-          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + kPfOffB + s * kTile));
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(sm + L::A + s * kTile));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sm + L::B + s * kTile));
           if (kF4) {
             const uint32_t sfa_col = tmem + kSfCol0 + s * 32, sfb_col = sfa_col + 16;
             for (int ks = 0; ks < nks; ++ks)
@@ -421,13 +420,13 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
       int k = 0;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
         for (int kt = 0; kt < nkt; ++kt, ++k) {
-          const int s = k % kPfStages;
-          if (!mbar_wait(&full[s], (k / kPfStages) & 1, a.status)) { *abort_flag = 1; break; }
+          const int s = k % NS;
+          if (!mbar_wait(&full[s], (k / NS) & 1, a.status)) { *abort_flag = 1; break; }
           tc_fence_after();
           const int nks = min(4, nks_all - 4 * kt);
           const uint32_t sfa_col = tmem + kSfCol0 + s * 32, sfb_col = sfa_col + 16;
-          const uint32_t sfa_smem = smem_u32(sm + kPfOffSfa + s * kSfStage);
-          const uint32_t sfb_smem = smem_u32(sm + kPfOffSfb + s * kSfStage);
+          const uint32_t sfa_smem = smem_u32(sm + L::Sfa + s * kSfStage);
+          const uint32_t sfb_smem = smem_u32(sm + L::Sfb + s * kSfStage);
           for (int ks = 0; ks < nks; ++ks) {
             tc_cp_sf(sfa_col + 4 * ks, sdesc_sf(sfa_smem + 512 * ks));
             tc_cp_sf(sfb_col + 4 * ks, sdesc_sf(sfb_smem + 512 * ks));
@@ -443,7 +442,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
     // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ...;
     // the two warps of a lane quarter split the columns in halves
     const int q = warp & 3, hf = (warp - 2) >> 2;
-    float* wglob = reinterpret_cast<float*>(sm + kPfOffGlob) + (warp - 2) * 128;
+    float* wglob = reinterpret_cast<float*>(sm + L::Glob) + (warp - 2) * 128;
     int ui = 0;
     for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ++ui) {
       const int buf = ui & 1;
@@ -506,49 +505,7 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
         // bf16 when the forward's output is bf16, else fp32
         if (a.y_bf16) {
           uint16_t* Yb = reinterpret_cast<uint16_t*>(a.Y);
-          if (a.stage_y) {
-            // rows [row_w, row_w + 32) of the unit are this warp's lanes; the
-            // first nvalid of them exist (the rest pad the expert's last tile)
-            const int row_w = nt * 128 + 32 * q;
-            const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
-            unsigned char* stg = sm + pf_stg_off(E) + (warp - 2) * 32 * kPfStgRow;
-            int yseg = 0;
-            if (lane < nvalid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
-            const int cb = 64 * hf;  // the warp's 64 columns
-            uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kPfStgRow);
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-              uint32_t v0[16], v1[16];
-              tc_ld16(taddr + cb + 32 * cc, v0);
-              tc_ld16(taddr + cb + 32 * cc + 16, v1);
-              tc_wait16x2(v0, v1);
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; i += 2) {
-                const float2 g0 = *reinterpret_cast<const float2*>(wglob + cb + 32 * cc + i);
-                const float2 g1 = *reinterpret_cast<const float2*>(wglob + cb + 32 * cc + 16 + i);
-                const __nv_bfloat162 b0 =
-                    __floats2bfloat162_rn(__uint_as_float(v0[i]) * g0.x, __uint_as_float(v0[i + 1]) * g0.y);
-                const __nv_bfloat162 b1 =
-                    __floats2bfloat162_rn(__uint_as_float(v1[i]) * g1.x, __uint_as_float(v1[i + 1]) * g1.y);
-                pk[i / 2] = *reinterpret_cast<const uint32_t*>(&b0);
-                pk[8 + i / 2] = *reinterpret_cast<const uint32_t*>(&b1);
-              }
-              uint4* s4 = reinterpret_cast<uint4*>(srow + 16 * cc);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) s4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = 4 * i + (lane >> 3), c8 = 8 * (lane & 7);
-              const int seg = __shfl_sync(0xffffffffu, yseg, r);
-              if (r < nvalid)
-                *reinterpret_cast<uint4*>(Yb + (int64_t)seg * 128 + cb + c8) =
-                    *reinterpret_cast<const uint4*>(stg + r * kPfStgRow + 2 * c8);
-            }
-            __syncwarp();
-          } else {
+          {
             int yseg = 0;
             if (valid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
             uint16_t* yrow = Yb + (int64_t)yseg * 128;
@@ -566,53 +523,13 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
                       __floats2bfloat162_rn(__uint_as_float(v[i]) * gd.x, __uint_as_float(v[i + 1]) * gd.y);
                   pk[i / 2] = *reinterpret_cast<const uint32_t*>(&b);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(yrow + 16 * c);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                stg_32B(yrow + 16 * c, pk);
               }
             }
           }
         } else {
           float* Yf = reinterpret_cast<float*>(a.Y);
-          if (a.stage_y) {
-            // rows [row_w, row_w + 32) of the unit are this warp's lanes; the
-            // first nvalid of them exist (the rest pad the expert's last tile)
-            const int row_w = nt * 128 + 32 * q;
-            const int nvalid = min(32, s_off[e + 1] - s_off[e] - row_w);
-            float* stg = reinterpret_cast<float*>(sm + pf_stg_off(E) + (warp - 2) * 32 * kPfStgRow);
-            int yseg = 0;
-            if (lane < nvalid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-              const int cb = 64 * hf + 32 * cc;  // first of the chunk's 32 columns
-              uint32_t v0[16], v1[16];
-              tc_ld16(taddr + cb, v0);
-              tc_ld16(taddr + cb + 16, v1);
-              tc_wait16x2(v0, v1);
-              float* srow = stg + lane * (kPfStgRow / 4);
-#pragma unroll
-              for (int i = 0; i < 16; i += 4) {
-                const float4 g0 = *reinterpret_cast<const float4*>(wglob + cb + i);
-                const float4 g1 = *reinterpret_cast<const float4*>(wglob + cb + 16 + i);
-                *reinterpret_cast<float4*>(srow + i) =
-                    make_float4(__uint_as_float(v0[i]) * g0.x, __uint_as_float(v0[i + 1]) * g0.y,
-                                __uint_as_float(v0[i + 2]) * g0.z, __uint_as_float(v0[i + 3]) * g0.w);
-                *reinterpret_cast<float4*>(srow + 16 + i) =
-                    make_float4(__uint_as_float(v1[i]) * g1.x, __uint_as_float(v1[i + 1]) * g1.y,
-                                __uint_as_float(v1[i + 2]) * g1.z, __uint_as_float(v1[i + 3]) * g1.w);
-              }
-              __syncwarp();
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int r = 4 * i + (lane >> 3), c4 = 4 * (lane & 7);
-                const int seg = __shfl_sync(0xffffffffu, yseg, r);
-                if (r < nvalid)
-                  *reinterpret_cast<float4*>(Yf + (int64_t)seg * 128 + cb + c4) =
-                      *reinterpret_cast<const float4*>(stg + r * (kPfStgRow / 4) + c4);
-              }
-              __syncwarp();
-            }
-          } else {
+          {
             int yseg = 0;
             if (valid) yseg = ((pre_pr / a.top_k) * (H / 128) + j) * a.top_k + pre_pr % a.top_k;
             float* yrow = Yf + (int64_t)yseg * 128;
@@ -622,16 +539,14 @@ __global__ void __launch_bounds__(pf_threads(MODE), 1)
               tc_ld16(taddr + 16 * c, v);
               tc_wait16(v);
               if (valid) {
+                uint32_t lo[8], hi[8];
 #pragma unroll
-                for (int i = 0; i < 16; i += 4) {
-                  const float4 gd = *reinterpret_cast<const float4*>(wglob + 16 * c + i);
-                  float4 o;
-                  o.x = __uint_as_float(v[i]) * gd.x;
-                  o.y = __uint_as_float(v[i + 1]) * gd.y;
-                  o.z = __uint_as_float(v[i + 2]) * gd.z;
-                  o.w = __uint_as_float(v[i + 3]) * gd.w;
-                  *reinterpret_cast<float4*>(yrow + 16 * c + i) = o;
+                for (int i = 0; i < 8; ++i) {
+                  lo[i] = __float_as_uint(__uint_as_float(v[i]) * wglob[16 * c + i]);
+                  hi[i] = __float_as_uint(__uint_as_float(v[8 + i]) * wglob[16 * c + 8 + i]);
                 }
+                stg_32B(yrow + 16 * c, lo);
+                stg_32B(yrow + 16 * c + 8, hi);
               }
             }
           }
@@ -1504,8 +1419,7 @@ cudaError_t prefill_set_smem_limits() {
   const int bytes = pf_smem_bytes(kPfMaxE);
   if ((e = cudaFuncSetAttribute(k_pf_mma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) !=
-      cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_pf_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_pf_gu256, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) !=
       cudaSuccess)
@@ -1561,11 +1475,8 @@ cudaError_t launch_prefill_routed(const PfArgs& a, const PfMaps& m, int num_sms,
     k_pf_mma<0><<<num_sms, pf_threads(0), smem, s>>>(a, m.xg, m.gu);
   FTMOE_PROF_END(s);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  // the down epilogue stages Y through shared memory where it fits
-  PfArgs ad = a;
-  ad.stage_y = pf_smem_bytes_staged(a.E) <= 227 * 1024;
   FTMOE_PROF_BEGIN("k_pf_down", s);
-  k_pf_mma<1><<<num_sms, kPfThreads, ad.stage_y ? pf_smem_bytes_staged(a.E) : smem, s>>>(ad, m.hq, m.dn);
+  k_pf_mma<1><<<num_sms, pf_threads(1), smem, s>>>(a, m.hq, m.dn);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
 }
