@@ -159,6 +159,10 @@ struct ftmoe_handle {
   int64_t slot_rec_bytes = 0;
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev_compute = nullptr, ev_copied = nullptr;
+  // prefill: the shared expert's GEMMs on a side stream, forked at the start
+  // of a forward and joined before the combine
+  cudaStream_t side_stream = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int32_t* h_touched = nullptr;   // pinned [E + 1]: touched experts, then their count
   unsigned char* h_stage = nullptr;  // pinned per-batch tables
   size_t stage_bytes = 0;
@@ -374,6 +378,9 @@ int ftmoe_create(const ftmoe_config* config, int device, ftmoe_handle** out) {
   if (e == cudaSuccess) e = prefill_set_smem_limits();
   if (e == cudaSuccess) e = decode_tc_set_smem_limits();
   if (e == cudaSuccess) e = w16_set_smem_limits(8192, 8192);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess && c.hbm_slot_bytes > 0) {
     h->offload = true;
     h->h2d_bytes.assign(c.num_layers, 0);
@@ -397,6 +404,9 @@ int ftmoe_destroy(ftmoe_handle* h) {
   cudaSetDevice(h->device);
   for (auto& L : h->layers) free_layer(L);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+  if (h->side_stream) cudaStreamDestroy(h->side_stream);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_compute) cudaEventDestroy(h->ev_compute);
   if (h->ev_copied) cudaEventDestroy(h->ev_copied);
   if (h->h_touched) cudaFreeHost(h->h_touched);
@@ -754,13 +764,28 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     }
   } else if (prefill_path(h, L, T, I_loc, a.win.row0)) {
     // prefill sizes: router logits, the routed GEMMs and the shared expert
-    // (its down product fused with the combine) on the tensor cores where
-    // the shapes fit them
+    // on the tensor cores where the shapes fit them.  The shared expert needs
+    // only x, so its two GEMMs (gate_up, then down into S) run on the side
+    // stream while the routing and the routed GEMMs run here, and the
+    // combine waits for both; the fork's event also orders them after this
+    // stream's earlier work (the previous combine read S).  While the
+    // per-kernel profiler is on, everything stays on one stream.
     const bool tc_shared = a.sh_gate_up && prefill_shared_supported(c.H, a.s_I_loc, a.s_Iw, a.s_row0, c.top_k);
     const bool tc_router = L.router_wcat != nullptr;
     PfArgs p = prefill_args(h, L, a, x, out, out_flags, tc_shared, tc_router);
     PfMaps maps;
     CK(prefill_make_maps(p, &maps));
+    const bool fork = tc_shared && !g_prof;
+    cudaStream_t ss = fork ? h->side_stream : s;
+    if (fork) {
+      CK(cudaEventRecord(h->ev_fork, s));
+      CK(cudaStreamWaitEvent(ss, h->ev_fork, 0));
+    }
+    if (tc_shared) {
+      CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, ss));
+      CK(launch_prefill_shared_down(p, maps, h->num_sms, ss));
+    }
+    if (fork) CK(cudaEventRecord(h->ev_join, ss));
     if (tc_router) {
       CK(launch_route(r, s, kRouteXq));
       CK(launch_prefill_router(p, maps, h->num_sms, s));
@@ -768,12 +793,12 @@ static int forward_impl(ftmoe_handle* h, int layer, const void* x, int T, void* 
     } else {
       CK(launch_route(r, s));
     }
-    if (tc_shared) CK(launch_prefill_shared_gate_up(p, maps, h->num_sms, s));
-    else CK(launch_experts(a, s, kPartSharedGateUp));
+    if (!tc_shared) CK(launch_experts(a, s, kPartSharedGateUp));
     CK(launch_prefill_routed(p, maps, h->num_sms, s));
     if (aux) CK(launch_prefill_export_h(p, aux->h_codes, aux->h_scales, h->num_sms, s));
     if (tc_shared) {
-      CK(launch_prefill_shared_down_combine(p, maps, h->num_sms, s));
+      if (fork) CK(cudaStreamWaitEvent(s, h->ev_join, 0));
+      CK(launch_prefill_combine(p, h->num_sms, s));
     } else {
       a.y_tiles = p.y_bf16 ? 2 : 1;  // the tensor-core down kernel's layout of Y
       CK(launch_experts(a, s, kPartTail));

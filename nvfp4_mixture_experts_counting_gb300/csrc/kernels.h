@@ -247,6 +247,8 @@ bool prefill_router_supported(int H, int E);
 cudaError_t launch_router_split(const float* w, int E, int H, uint16_t* wcat, float* wnorm, cudaStream_t s);
 cudaError_t launch_prefill_router(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill_shared_gate_up(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill_shared_down(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill_combine(const PfArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s);
 cudaError_t prefill_make_maps(const PfArgs& a, PfMaps* m);
 cudaError_t prefill_set_smem_limits();

@@ -1605,14 +1605,17 @@ cudaError_t launch_prefill_shared_gate_up(const PfArgs& a, const PfMaps& m, int 
 }
 
 // The shared down on 128 x 256 tiles into S (H is a multiple of 256 on the
-// prefill path), then the combine streaming Y, S and the output.
-cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
+// prefill path).
+cudaError_t launch_prefill_shared_down(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
   if (!a.S || a.H % 256) return cudaErrorInvalidValue;
   FTMOE_PROF_BEGIN("k_pf_shared_down", s);
   k_pf_bf16w<3><<<num_sms, kBwThreads, kBwSmem, s>>>(a, m.hs, m.sdn);
   FTMOE_PROF_END(s);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// The combine, streaming Y, S and the output.
+cudaError_t launch_prefill_combine(const PfArgs& a, int num_sms, cudaStream_t s) {
   const int64_t n8 = (int64_t)a.T * (a.H / 8);
   int64_t blocks = (n8 + 255) / 256;
   if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
@@ -1620,6 +1623,11 @@ cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m,
   k_pf_combine<<<(int)blocks, 256, 0, s>>>(a);
   FTMOE_PROF_END(s);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_shared_down_combine(const PfArgs& a, const PfMaps& m, int num_sms, cudaStream_t s) {
+  cudaError_t e = launch_prefill_shared_down(a, m, num_sms, s);
+  return e != cudaSuccess ? e : launch_prefill_combine(a, num_sms, s);
 }
 
 }  // namespace ftmoe
