@@ -80,6 +80,18 @@ def test_shared_expert_and_routed_flops():
     assert A.routed_flops(2560, 640, 8) == 78_643_200
 
 
+def test_prefill_kernel_flops_per_unit():
+    # per pair: gate_up 2*2560*1280, down 2*640*2560; per token: the shared
+    # expert's gate_up 2*2560*1280 and down 2*640*2560, the router x times
+    # three bf16 parts of 256 rows of 2560
+    f = lambda k: A.kernel_unit_flops(k, 2560, 640, 640, 256)[:2]
+    assert f("k_pf_gate_up") == (6_553_600, "pair")
+    assert f("k_pf_down") == (3_276_800, "pair")
+    assert f("k_pf_shared_gate_up") == (6_553_600, "token")
+    assert f("k_pf_shared_down") == (3_276_800, "token")
+    assert f("k_pf_router") == (3_932_160, "token")
+
+
 @pytest.mark.parametrize("T,touched,mb", [(1, 8, 34.7), (16, 102, 296.2)])
 def test_decode_layer_bytes(T, touched, mb):
     # touched experts + shared expert + fp32 router + x in and bf16 out
