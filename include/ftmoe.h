@@ -208,8 +208,11 @@ int ftmoe_load_bank(ftmoe_handle* h, int layer, const ftmoe_bank_desc* desc, int
  *        into one buffer gives the full layer in a fixed order.
  *   aux: NULL or optional routing outputs (see ftmoe_aux).
  * Routing always uses the full replicated router.  Asynchronous on `stream`;
- * resident mode does no host synchronisation and may be captured in a CUDA
- * graph.  Offload mode reads the step's routing back to the host once per
+ * at prefill sizes the shared expert's products run on a stream of the
+ * handle that waits for `stream`'s earlier work and that `stream` waits for
+ * before the combine, so the call's work stays ordered within `stream`.
+ * Resident mode does no host synchronisation and may be captured in a CUDA
+ * graph (the capture follows the fork and the join).  Offload mode reads the step's routing back to the host once per
  * call (one synchronisation) to plan its slot copies; a forward touching more
  * experts than there are slots runs its experts in batches of at most the
  * slot count; offload needs the tensor-core shapes (H a multiple of 256,
