@@ -186,6 +186,29 @@ def test_prefill_offset_windows_on_the_256_row_kernel(prefill):
     assert rel_l2(acc.cpu().numpy(), full.cpu().numpy()) <= 1e-6
 
 
+def test_prefill_graph_replay_matches_direct_call(prefill):
+    """A prefill forward captured in a CUDA graph (the shared expert's
+    products forked onto the handle's side stream and joined before the
+    combine) and replayed gives the direct call's bits."""
+    wl, bank, layer = prefill
+    T = 1024
+    x = W.hidden(wl, T, step=6, device=DEV)
+    direct = torch.empty((T, wl.H), dtype=torch.bfloat16, device=DEV)
+    layer.forward(0, x, direct, out_flags=ftmoe.OUT_BF16)
+    torch.cuda.synchronize()
+    out = torch.empty_like(direct)
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        layer.forward(0, x, out, out_flags=ftmoe.OUT_BF16, stream=cs)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert layer.check_status() == 0
+    assert torch.equal(out.view(torch.int16), direct.view(torch.int16))
+
+
 # ------------------------------------------------------------------ tensor-core router
 
 
