@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router_logits(RouteArgs a
 
 // ------------------------------------------------------------------ top-k
 
-constexpr int kTopkWarps = 8;
+constexpr int kTopkWarps = 4;
 
 // Key order: larger logit first, then lower expert index.
 __device__ __forceinline__ bool before(float la, int ea, float lb, int eb) {
